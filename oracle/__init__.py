@@ -1,0 +1,142 @@
+"""CPU oracle for exact attention forward — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import this package. The CUDA product path never imports it and
+shares no code with it.
+
+* ``attn_rows`` / ``attn_full``: the fp64 plain-definition oracle (``attn_oracle.c``,
+  compiled here with the system C compiler, OpenMP over rows).
+* ``bruteforce.attn_materialised``: an independent numpy implementation that
+  materialises S and P, used to pin the C oracle on tiny inputs.
+
+Definition followed: "Flash Attention optimization" skill page, workflow 1 step 2
+(standard attention softmax(q kᵀ/√d_k)·v) and workflow 2 steps 2-3 (layout, causal,
+fewer K/V heads, window); "What is memory-efficient attention for long context on
+8x H100?", section 2 (the tiled method is exact).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FP16, BF16 = 0, 1
+
+
+def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
+    """Compile ``src`` into the shared library ``out`` (skipped when up to date)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cc = os.environ.get("CC", "gcc")
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [cc, "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_attn_rows.restype = ctypes.c_int
+    lib.oracle_attn_rows.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                     ctypes.c_int, i64, ctypes.c_double, p, i64, p, p]
+    lib.oracle_widen.restype = None
+    lib.oracle_widen.argtypes = [p, ctypes.c_int, p, i64]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_max_threads.argtypes = []
+    return lib
+
+
+def load(path: str = None):
+    """Return the ctypes handle of the oracle library (built on first use)."""
+    global _lib
+    if path is not None:
+        return _bind(path)
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+        return _lib
+
+
+def _dtype_code(dtype) -> int:
+    if dtype in ("fp16", FP16):
+        return FP16
+    if dtype in ("bf16", BF16):
+        return BF16
+    raise ValueError(f"unsupported dtype {dtype!r}")
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """Thin marshalling over one compiled oracle library (default: attn_oracle.c)."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
+
+    def widen(self, bits: np.ndarray, dtype) -> np.ndarray:
+        bits = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(bits.shape, dtype=np.float64)
+        self.lib.oracle_widen(_ptr(bits), _dtype_code(dtype), _ptr(out), bits.size)
+        return out
+
+    def attn_rows(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale, rows):
+        """O rows (n x d, float64) and LSE (n,) for flat row ids (b*Hq + h)*L + i.
+
+        q_bits: uint16 [B, L, Hq, d]; k_bits / v_bits: uint16 [B, L, Hkv, d].
+        """
+        q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+        k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+        v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+        B, L, Hq, d = q_bits.shape
+        Hkv = k_bits.shape[2]
+        if k_bits.shape != (B, L, Hkv, d) or v_bits.shape != k_bits.shape:
+            raise ValueError("K/V shape mismatch")
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, d), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.oracle_attn_rows(
+            _ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _dtype_code(dtype), B, L, Hq, Hkv, d,
+            int(bool(causal)), int(window_left), float(scale), _ptr(rows), rows.size,
+            _ptr(o), _ptr(lse))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_rows rejected its arguments (rc={rc})")
+        return o, lse
+
+    def attn_full(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale):
+        """Full O [B, L, Hq, d] and LSE [B, Hq, L] in float64."""
+        B, L, Hq, d = q_bits.shape
+        rows = np.arange(B * Hq * L, dtype=np.int64)
+        o, lse = self.attn_rows(q_bits, k_bits, v_bits, dtype, causal, window_left, scale,
+                                rows)
+        # rows are ordered (b, h, i); O is stored [b, i, h, :]
+        o = o.reshape(B, Hq, L, d).transpose(0, 2, 1, 3).copy()
+        return o, lse.reshape(B, Hq, L)
+
+
+_default = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

@@ -1,0 +1,58 @@
+"""Materialised-matrix attention in numpy float64 — TEST INFRASTRUCTURE.
+
+A second, separate statement of standard attention ("Flash Attention optimization"
+skill page, workflow 1 step 2: weights = softmax(q kᵀ/√d_k), out = weights · v),
+written the unfused way: S = scale·Q Kᵀ is formed in full, masked with -inf, turned
+into P = exp(S - rowmax) / rowsum and multiplied by V. It is used only on tiny
+inputs to pin the C oracle, which never materialises S. The two share no code.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def visibility(L: int, causal: bool, window_left: int) -> np.ndarray:
+    """Boolean L x L matrix: True where key j is visible from query row i."""
+    i = np.arange(L)[:, None]
+    j = np.arange(L)[None, :]
+    vis = np.ones((L, L), dtype=bool)
+    if causal:
+        vis &= j <= i
+    if window_left >= 0:
+        vis &= j >= i - window_left
+    return vis
+
+
+def attn_materialised(q, k, v, causal=False, window_left=-1, scale=1.0, return_p=False):
+    """q: [B, L, Hq, d]; k, v: [B, L, Hkv, d] (float64). Returns O, LSE[, P].
+
+    P has shape [B, Hq, L, L]; rows with no visible key give O = 0, LSE = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    group = Hq // Hkv
+    vis = visibility(L, causal, window_left)
+    o = np.zeros((B, L, Hq, d))
+    lse = np.full((B, Hq, L), -np.inf)
+    p_all = np.zeros((B, Hq, L, L)) if return_p else None
+    for b in range(B):
+        for h in range(Hq):
+            g = h // group
+            s = scale * (q[b, :, h, :] @ k[b, :, g, :].T)
+            s = np.where(vis, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            has = np.isfinite(m[:, 0])
+            m_safe = np.where(np.isfinite(m), m, 0.0)
+            e = np.where(vis, np.exp(s - m_safe), 0.0)
+            l = e.sum(axis=1, keepdims=True)
+            p = np.where(has[:, None], e / np.where(l > 0, l, 1.0), 0.0)
+            o[b, :, h, :] = p @ v[b, :, g, :]
+            lse[b, h, has] = m[has, 0] + np.log(l[has, 0])
+            if return_p:
+                p_all[b, h] = p
+    if return_p:
+        return o, lse, p_all
+    return o, lse

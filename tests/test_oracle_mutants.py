@@ -1,0 +1,53 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each mutant is a copy of ``oracle/attn_oracle.c`` with one plausible error (a
+dropped term, an off-by-one mask, a wrong head mapping, a transposed operand, a
+wrong exponent bias ...), compiled on the CPU into a temporary library. The test
+passes when at least one pin from ``oracle_pins`` fails on that mutant, which shows
+the pins would notice the same mistake in the real oracle.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ORACLE_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+MUTANTS = {
+    "drop_scale": ("s[j - j_lo] = scale * dot;", "s[j - j_lo] = dot;"),
+    "causal_excludes_diagonal": ("j_hi = i + 1;", "j_hi = i;"),
+    "window_one_short": ("j_lo = i - window_left;", "j_lo = i - window_left + 1;"),
+    "gqa_modulo_mapping": ("int64_t g = h / (Hq / Hkv);", "int64_t g = h % Hkv;"),
+    "lse_drops_max": ("*lse = m + log(l);", "*lse = log(l);"),
+    "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "fp16_exponent_bias": ("e - 25);", "e - 24);"),
+    "fp16_subnormal_scale": ("ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
+    "no_normalisation": ("double p = exp(s[j - j_lo] - m) / l;",
+                         "double p = exp(s[j - j_lo] - m);"),
+    "key_indexed_by_query_row": ("k + ((b * L + j) * Hkv + g) * d;",
+                                 "k + ((b * L + (j + i) % L) * Hkv + g) * d;"),
+    "values_read_from_keys": ("const uint16_t *vj = v + ", "const uint16_t *vj = k + "),
+    "bf16_low_half": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
+    "max_not_subtracted_in_weights": ("double p = exp(s[j - j_lo] - m) / l;",
+                                      "double p = exp(s[j - j_lo]) / l;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    src = tmp_path / f"mutant_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.load(oracle.build(str(src), str(tmp_path / f"lib_{name}.so"), force=True))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in ORACLE_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutant {name}"
