@@ -1,0 +1,204 @@
+"""exact_io_aware_19_gb300 — exact, IO-aware attention forward on GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libattn.so`` (declared in
+``include/attn.h``). Every step of the computation runs in the library's CUDA
+kernels; this module only checks tensors, allocates outputs with PyTorch and
+passes raw pointers and the current CUDA stream. There is no fallback: if the
+library is missing or the device is not a GB300, calls raise.
+
+    o, lse = attn_fwd(q, k, v, causal=True)             # q: [B, L, Hq, d] fp16/bf16
+    o, lse = attn_fwd(q, k, v, causal=True, window_left=4096, out_fp32=True)
+
+Definition: standard attention softmax(scale · q kᵀ) v of the "Flash Attention
+optimization" skill page (workflow 1 step 2), with the causal / MQA-GQA / window
+options of its workflow 2 steps 2-3, computed exactly the way section 2 of "What is
+memory-efficient attention for long context on 8x H100?" describes.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "sync_status", "AttnError",
+           "library_path", "load_library", "set_wait_limit_ns", "debug_wait_probe",
+           "STATUS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libattn.so")
+
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_WORKSPACE", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+FP16, BF16 = 0, 1
+OUT_SAME, OUT_FP32 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+_workspaces = {}
+
+
+class AttnError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, code: int, detail: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{self.name}: {detail}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _bind(lib):
+    p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.attn_fwd.restype = i
+    lib.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p, sz, p]
+    lib.attn_fwd_workspace_size.restype = sz
+    lib.attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.attn_fwd_sync_status.restype = i
+    lib.attn_fwd_sync_status.argtypes = [p, p]
+    lib.attn_set_wait_limit_ns.restype = None
+    lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.attn_debug_wait_probe.restype = i
+    lib.attn_debug_wait_probe.argtypes = [p, sz, ctypes.c_uint64, p]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_last_error_detail.restype = ctypes.c_char_p
+    lib.attn_last_error_detail.argtypes = []
+    lib.attn_abi_version.restype = i
+    lib.attn_abi_version.argtypes = []
+    return lib
+
+
+def load_library(path: Optional[str] = None):
+    """Load libattn.so (built by ``exact_io_aware_19_gb300.build``). Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            path = path or _LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -m exact_io_aware_19_gb300.build` "
+                    "(or __graft_entry__.build()); there is no fallback implementation")
+            lib = _bind(ctypes.CDLL(path))
+            if path != _LIB_PATH:
+                return lib
+            _lib = lib
+        return _lib
+
+
+def _check(code: int):
+    if code != 0:
+        lib = load_library()
+        raise AttnError(code, lib.attn_last_error_detail().decode(errors="replace"))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FP16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"q, k, v must be float16 or bfloat16, got {t.dtype}")
+
+
+def workspace_size(B, L, Hq, Hkv, d, causal=False, window_left=-1) -> int:
+    return int(load_library().attn_fwd_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)),
+                                                      int(window_left)))
+
+
+def _default_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=f"cuda:{key}")
+        _workspaces[key] = ws
+    return ws
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
+                  workspace=None, stream=None) -> None:
+    """Write attention of (q, k, v) into preallocated ``o`` (q's dtype or float32) and
+    ``lse`` (float32 [B, Hq, L] or None). Asynchronous on ``stream``."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, L, H, d]")
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, L, Hkv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, L, Hkv, d] = {(B, L, Hkv, d)}")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if tuple(o.shape) != (B, L, Hq, d):
+        raise ValueError("o must be [B, L, Hq, d]")
+    if o.dtype == torch.float32:
+        out = OUT_FP32
+    elif o.dtype == q.dtype:
+        out = OUT_SAME
+    else:
+        raise TypeError("o must have q's dtype or float32")
+    if lse is not None:
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, L) or \
+                not lse.is_contiguous() or not lse.is_cuda:
+            raise ValueError("lse must be a contiguous CUDA float32 tensor [B, Hq, L]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = workspace_size(B, L, Hq, Hkv, d, causal, window_left)
+    if workspace is None:
+        workspace = _default_workspace(q.device, need)
+    code = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                        lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
+                        int(bool(causal)), int(window_left), float(scale), dt, out,
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream))
+    _check(code)
+
+
+def attn_fwd(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=False,
+             return_lse=True, workspace=None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Exact attention forward. Returns (o, lse); lse is float32 [B, Hq, L] or None.
+
+    ``scale`` defaults to 1/sqrt(d). ``window_left = w >= 0`` (with ``causal``)
+    restricts row i to keys i-w .. i.
+    """
+    B, L, Hq, d = q.shape
+    o = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if return_lse else None
+    attn_fwd_into(q, k, v, o, lse, causal=causal, window_left=window_left, scale=scale,
+                  workspace=workspace, stream=stream)
+    return o, lse
+
+
+def sync_status(workspace: Optional[torch.Tensor] = None, device=None, stream=None) -> None:
+    """Synchronise and raise AttnError if a device-side error was recorded."""
+    lib = load_library()
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        workspace = _default_workspace(dev, 256)
+    _check(lib.attn_fwd_sync_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    load_library().attn_set_wait_limit_ns(int(limit_ns))
+
+
+def debug_wait_probe(workspace: torch.Tensor, limit_ns: int, stream=None) -> None:
+    lib = load_library()
+    _check(lib.attn_debug_wait_probe(workspace.data_ptr(), workspace.numel(), int(limit_ns),
+                                     _stream_handle(stream)))

@@ -1,0 +1,293 @@
+// attn_api.cu — the C ABI declared in include/attn.h: argument validation, TMA
+// tensor maps, grid sizing and launch. Host code only; no device allocation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "attn.h"
+#include "attn_launch.h"
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = 256;  // status word (16 B), padded
+constexpr unsigned long long kDefaultWaitLimitNs = 4000000000ull;
+constexpr int kUnitRows = 256;           // query rows per kernel work unit
+
+thread_local std::string g_detail;
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+attn_status_t fail(attn_status_t s, const std::string& msg) {
+  g_detail = msg;
+  return s;
+}
+
+attn_status_t cuda_fail(const char* what, cudaError_t e) {
+  return fail(ATTN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                                 cudaGetErrorString(e) + ")");
+}
+
+struct DeviceInfo {
+  int sms = 0, major = 0, minor = 0;
+};
+
+bool device_info(int dev, DeviceInfo* out, cudaError_t* err) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    DeviceInfo d;
+    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) {
+      *err = e;
+      return false;
+    }
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    } else if (status == cudaSuccess) {
+      status = cudaErrorSymbolNotFound;
+    }
+  });
+  *err = status;
+  return fn;
+}
+
+// Tensor map over a [B, L, H, d] 16-bit tensor. Dimensions are listed innermost
+// first with increasing strides (d, H, L, B); the box is 64 elements (128 bytes,
+// one swizzle span) of d, 1 head, 128 rows, 1 batch.
+bool make_tensor_map(CUtensorMap* map, const void* ptr, bool bf16, int B, int L, int H, int d,
+                     std::string* why) {
+  cudaError_t err;
+  auto encode = encode_fn(&err);
+  if (encode == nullptr) {
+    *why = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorName(err);
+    return false;
+  }
+  const cuuint64_t e = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * e, (cuuint64_t)H * d * e, (cuuint64_t)L * H * d * e};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      4, const_cast<void*>(ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The pointer must be device (or managed) memory of device `dev`.
+bool is_device_ptr(const void* p, int dev, std::string* why, const char* name) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *why = std::string(name) + ": cudaPointerGetAttributes failed";
+    return false;
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) {
+    *why = std::string(name) + " is not device memory";
+    return false;
+  }
+  if (at.type == cudaMemoryTypeDevice && at.device != dev) {
+    *why = std::string(name) + " lives on device " + std::to_string(at.device) +
+           ", current device is " + std::to_string(dev);
+    return false;
+  }
+  return true;
+}
+
+// Shape checks shared by attn_fwd and attn_fwd_workspace_size.
+attn_status_t check_shape(int B, int L, int Hq, int Hkv, int d, int causal, int window_left) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, L, Hq and Hkv must all be >= 1");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  if (d < 1) return fail(ATTN_ERR_INVALID_ARG, "d must be >= 1");
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "d must be 64 or 128");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (window_left < -1) return fail(ATTN_ERR_INVALID_ARG, "window_left must be >= -1");
+  if (window_left >= 0 && !causal)
+    return fail(ATTN_ERR_UNSUPPORTED, "a left window is only supported with causal = 1");
+  const long long rows = (long long)B * Hq * L;
+  if (rows >= (1LL << 31)) return fail(ATTN_ERR_INVALID_ARG, "B * Hq * L must be < 2^31");
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal, int window_left) {
+  if (check_shape(B, L, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
+  return kWorkspaceBytes;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int L, int Hq, int Hkv, int d, int causal, int window_left, float scale,
+                       attn_dtype_t dtype, attn_out_t out_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  g_detail.clear();
+  attn_status_t st = check_shape(B, L, Hq, Hkv, d, causal, window_left);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "bad dtype");
+  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
+  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
+  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  if (workspace_bytes < kWorkspaceBytes)
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_workspace_size()");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  std::string why;
+  const void* ptrs[6] = {q, k, v, o, workspace, lse};
+  const char* names[6] = {"q", "k", "v", "o", "workspace", "lse"};
+  for (int i = 0; i < 6; ++i)
+    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
+      return fail(ATTN_ERR_INVALID_ARG, why);
+
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why) ||
+      !make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) ||
+      !make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why))
+    return fail(ATTN_ERR_CUDA, why);
+
+  ex19::LaunchArgs a;
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  ex19::FwdParams& p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.status = static_cast<uint32_t*>(workspace);
+  p.B = B;
+  p.L = L;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f ? 1 : 0;
+  p.units_per_bh = (L + kUnitRows - 1) / kUnitRows;
+  p.num_units = B * Hq * p.units_per_bh;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.grid = p.num_units < info.sms ? p.num_units : info.sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+
+  const bool out_f32 = out_dtype == ATTN_OUT_FP32;
+  e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd_sync_status(void* workspace, void* stream) {
+  g_detail.clear();
+  if (!workspace || !aligned(workspace, 16))
+    return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null and 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+  uint32_t word[4] = {0, 0, 0, 0};
+  e = cudaMemcpyAsync(word, workspace, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail("reading the status word", e);
+  if (word[0] == 0) return ATTN_OK;
+  e = cudaMemsetAsync(workspace, 0, sizeof word, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail("clearing the status word", e);
+  char buf[160];
+  std::snprintf(buf, sizeof buf, "device status %u at site 0x%05x, CTA %u, unit %u", word[0],
+                word[1], word[2], word[3]);
+  attn_status_t code = (word[0] <= ATTN_ERR_TIMEOUT) ? static_cast<attn_status_t>(word[0])
+                                                      : ATTN_ERR_CUDA;
+  return fail(code, buf);
+}
+
+void attn_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns ? (unsigned long long)limit_ns : kDefaultWaitLimitNs);
+}
+
+attn_status_t attn_debug_wait_probe(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                    void* stream) {
+  g_detail.clear();
+  if (!workspace || !aligned(workspace, 16) || workspace_bytes < kWorkspaceBytes)
+    return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null, 16-byte aligned and large enough");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300)");
+  std::string why;
+  if (!is_device_ptr(workspace, dev, &why, "workspace")) return fail(ATTN_ERR_INVALID_ARG, why);
+  e = ex19::launch_wait_probe(static_cast<uint32_t*>(workspace), limit_ns,
+                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("probe launch", e);
+  return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported";
+    case ATTN_ERR_WORKSPACE: return "bad workspace";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* attn_last_error_detail(void) { return g_detail.c_str(); }
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+}  // extern "C"

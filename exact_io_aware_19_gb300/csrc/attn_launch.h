@@ -1,0 +1,24 @@
+// attn_launch.h — host-side entry points of the per-head-dim kernel instantiations.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn_params.h"
+
+namespace ex19 {
+
+struct LaunchArgs {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  FwdParams p;
+  int grid;
+  cudaStream_t stream;
+};
+
+// Each returns the CUDA error of configuring / enqueuing the kernel.
+cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
+cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
+cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace ex19

@@ -1,0 +1,233 @@
+// sm103_ptx.cuh — inline-PTX building blocks for the sm_103a attention kernel:
+// mbarriers with bounded waits, TMA tile loads, TMEM allocation, tcgen05 MMA /
+// commit / fences, and the shared-memory and instruction descriptors of tcgen05.
+//
+// Descriptor encodings follow the PTX ISA (tcgen05 "shared memory descriptor" and
+// "instruction descriptor" for .kind::f16); the field positions are the ones
+// written in each encoder below.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+namespace ex19 {
+
+// ---------------------------------------------------------------- status words
+// The device status word (in the caller's workspace): [0] = attn_status_t code of
+// the first error, [1] = where it happened (role << 16 | site), [2] = CTA, [3] = unit.
+enum : uint32_t { kStatusTimeout = 5 };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------- mbarriers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// One non-blocking probe: true once the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Shared control block of one CTA for bounded waits.
+struct WaitCtl {
+  volatile uint32_t* abort_flag;  // shared memory: set once any role gives up
+  uint32_t* status;               // global status word (may be null)
+  uint64_t limit_ns;              // per-wait limit
+  uint32_t unit;                  // current work unit, for the report
+};
+
+__device__ __forceinline__ void record_error(const WaitCtl& c, uint32_t code, uint32_t where) {
+  *c.abort_flag = 1u;
+  if (c.status != nullptr) {
+    if (atomicCAS(c.status, 0u, code) == 0u) {
+      c.status[1] = where;
+      c.status[2] = blockIdx.x;
+      c.status[3] = c.unit;
+      __threadfence();
+    }
+  }
+}
+
+// Slow path of a bounded wait: polls until phase `parity` of `bar` completes, the
+// limit runs out (recording a timeout) or, when `honor_abort`, another role of
+// the CTA has aborted. Returns true only when the phase completed.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                            uint32_t where, bool honor_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_test(bar, parity)) return true;
+    if (honor_abort && *c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > c.limit_ns) {
+      record_error(c, kStatusTimeout, where);
+      return false;
+    }
+  }
+}
+
+// Waits for phase `parity` of `bar`; false (never an endless wait) on timeout or abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                                  uint32_t where) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, where, true);
+}
+
+// Same, but keeps waiting after an abort: used to let in-flight copies and MMAs
+// finish before the CTA releases its TMEM and exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                                uint32_t where) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, where, false);
+}
+
+// Whole-warp wait: every lane polls, then the warp agrees (all lanes must see the
+// phase complete), so the .sync.aligned tcgen05 instructions that follow are
+// always executed by the full warp or by none of it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                               uint32_t where) {
+  const bool ok = mbar_wait_bounded(bar, parity, c, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------------------- TMA
+// 4-D tiled bulk-tensor load into shared memory, completing on `bar` with the
+// copied byte count. Coordinates are element indices, innermost first; the
+// innermost coordinate times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------------ TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05 MMA
+// D[tmem] (+)= A[smem desc] · B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] · B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ descriptors
+// Shared-memory matrix descriptor, 128-byte swizzle:
+//   bits  0-13 start address >> 4      bits 16-29 leading-dimension byte offset >> 4
+//   bits 32-45 stride byte offset >> 4 bits 46-47 descriptor version (1)
+//   bits 49-51 base offset (0: atoms are 1024-byte aligned)
+//   bits 61-63 layout (2 = 128-byte swizzle)
+// K-major operand: rows of 128 bytes, 8-row atoms `sbo` apart (lbo unused).
+// MN-major operand: 64-element row segments, `lbo` = distance between 64-wide
+// segments along MN, `sbo` = distance between groups of 8 rows along K.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, .kind::f16, dense, fp32 accumulator:
+//   bits 4-5 D format (1 = f32)   bits 7-9 A format, 10-12 B format (0 = f16, 1 = bf16)
+//   bit 15 A major (0 = K)        bit 16 B major (0 = K, 1 = MN)
+//   bits 17-22 N >> 3             bits 24-28 M >> 4
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// -------------------------------------------------------------------- arithmetic
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace ex19

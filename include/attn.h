@@ -1,0 +1,132 @@
+/*
+ * attn.h — C ABI of the exact attention-forward library (libattn.so, sm_103a).
+ *
+ * Operation. Exact scaled-dot-product attention forward, the standard attention of
+ * the "Flash Attention optimization" skill page (hermes-agent, mlops-flash-attention),
+ * workflow 1 step 2: out = softmax(q kᵀ · scale) · v, with the options of workflow 2
+ * steps 2-3: layout [batch, seq, heads, dim], causal masking, fewer K/V heads than
+ * query heads (MQA/GQA), and a left sliding window. It is computed the IO-aware way
+ * described in "What is memory-efficient attention for long context on 8x H100?"
+ * (aivaro.ru, answers 650), section 2: Q/K/V are processed in blocks held on chip
+ * with an online softmax, so the L x L score matrix never reaches HBM and the extra
+ * memory is O(L·d) (only inputs, outputs and a fixed-size workspace).
+ *
+ * For batch b, query head h, row i, with g = h / (Hq / Hkv) and the visible keys
+ *   J_i = { j < L : (causal => j <= i) and (window_left >= 0 => j >= i - window_left) }:
+ *   O[b, i, h, :] = sum_{j in J_i} softmax_j(scale · q[b,i,h,:]·k[b,j,g,:]) · v[b, j, g, :]
+ *   LSE[b, h, i]  = ln sum_{j in J_i} exp(scale · q[b,i,h,:]·k[b,j,g,:])
+ *
+ * Layouts (all contiguous, row-major, element strides implied by the sizes):
+ *   q, o : [B, L, Hq, d]      k, v : [B, L, Hkv, d]      lse : [B, Hq, L] float32
+ *
+ * Ownership. The caller owns every buffer. The library never allocates device
+ * memory; it keeps only host-side caches (device properties, driver entry point).
+ * All pointers passed to attn_fwd are DEVICE pointers of the current CUDA device.
+ *
+ * Asynchrony. attn_fwd enqueues one kernel on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream) and returns without synchronising. Argument errors are
+ * returned before anything is enqueued. Errors detected on the device (a bounded
+ * wait that ran out) are recorded in the workspace status word and reported by
+ * attn_fwd_sync_status.
+ *
+ * Threading. Calls are thread-safe; concurrent calls must use distinct workspaces.
+ */
+#ifndef EXACT_ATTN_H
+#define EXACT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or option is invalid          */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (d, arch ...) */
+    ATTN_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required        */
+    ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (detail string kept)     */
+    ATTN_ERR_TIMEOUT = 5      /* a device-side bounded wait ran out; the kernel stopped     */
+} attn_status_t;
+
+typedef enum {
+    ATTN_FP16 = 0, /* IEEE binary16 inputs (and outputs with ATTN_OUT_SAME) */
+    ATTN_BF16 = 1  /* bfloat16 inputs (and outputs with ATTN_OUT_SAME)      */
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OUT_SAME = 0, /* O in the input dtype, rounded to nearest even */
+    ATTN_OUT_FP32 = 1  /* O in float32 (no final rounding to 16 bits)   */
+} attn_out_t;
+
+/*
+ * Bytes of device workspace attn_fwd needs for this problem (a status word; the
+ * size does not depend on the problem today, but callers should query it).
+ * Returns 0 for sizes attn_fwd would reject.
+ */
+size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
+                               int window_left);
+
+/*
+ * Attention forward (see the header comment for the definition).
+ *   q, k, v     device pointers, 16-byte aligned, layouts above, dtype `dtype`
+ *   o           device pointer, 16-byte aligned, [B, L, Hq, d] of `dtype` or float32
+ *   lse         device pointer to [B, Hq, L] float32, 4-byte aligned, or NULL to skip
+ *   B, L        batch and sequence length, both >= 1; B*Hq*L < 2^31
+ *   Hq, Hkv     query / key-value heads, Hkv >= 1, Hq % Hkv == 0
+ *   d           head dimension: 64 or 128
+ *   causal      0 or 1 (causal: key j visible from query i only when j <= i)
+ *   window_left -1 for none, or w >= 0 (keys i-w .. i); requires causal = 1
+ *   scale       finite multiplier of q·k (1/sqrt(d) is the usual choice)
+ *   workspace   device pointer, 16-byte aligned, >= attn_fwd_workspace_size bytes;
+ *               must not be used by another call that is still running
+ *   stream      cudaStream_t to enqueue on
+ * Returns ATTN_OK when the kernel was enqueued; otherwise nothing was enqueued and
+ * the outputs are untouched. Requires a device of compute capability 10.3.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int L, int Hq, int Hkv, int d, int causal, int window_left,
+                       float scale, attn_dtype_t dtype, attn_out_t out_dtype,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, reads the workspace status word written by earlier
+ * attn_fwd calls on it, clears it, and returns it (ATTN_OK when no device-side
+ * error was recorded). A CUDA error while synchronising returns ATTN_ERR_CUDA.
+ */
+attn_status_t attn_fwd_sync_status(void *workspace, void *stream);
+
+/*
+ * Sets the limit, in nanoseconds, of every device-side wait in kernels launched
+ * afterwards by this process (default 4e9 = 4 s; 0 restores the default). A wait
+ * that runs out records ATTN_ERR_TIMEOUT in the workspace and makes every role of
+ * the kernel stop and release its resources.
+ */
+void attn_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Launches a one-warp kernel that waits, with the same bounded wait the attention
+ * kernel uses, on a barrier that nothing completes, for `limit_ns` nanoseconds, and
+ * records ATTN_ERR_TIMEOUT in `workspace`. It exists so the timeout path can be
+ * tested without stalling the real kernel. Same argument rules as attn_fwd.
+ */
+attn_status_t attn_debug_wait_probe(void *workspace, size_t workspace_bytes,
+                                    uint64_t limit_ns, void *stream);
+
+/* Static description of a status code. */
+const char *attn_status_string(attn_status_t s);
+
+/* Detail of the last non-OK status returned to the calling thread ("" if none). */
+const char *attn_last_error_detail(void);
+
+/* ATTN_ABI_VERSION of the loaded library. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTN_H */

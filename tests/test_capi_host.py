@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library loads, exports every function that
+include/attn.h declares, and rejects bad arguments before touching the GPU.
+
+Arguments here are fake (but aligned) pointers: every case below must be rejected
+by validation that runs before the first CUDA call, so nothing is enqueued.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import exact_io_aware_19_gb300 as ex
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_19_gb300 import build
+    build.build()
+    return ex.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_fwd_workspace_size", "attn_fwd_sync_status",
+                     "attn_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(ex.library_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert lib.attn_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code, text in [(0, b"ok"), (1, b"invalid argument"), (2, b"unsupported"),
+                       (3, b"bad workspace"), (4, b"CUDA error"), (5, b"device wait timed out")]:
+        assert lib.attn_status_string(code) == text
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+def test_workspace_size(lib):
+    assert lib.attn_fwd_workspace_size(1, 131072, 4, 4, 64, 1, -1) == 256
+    assert lib.attn_fwd_workspace_size(1, 1, 32, 8, 128, 1, 4096) == 256
+    for bad in [(0, 16, 4, 4, 64, 1, -1), (1, 0, 4, 4, 64, 1, -1), (1, 16, 3, 2, 64, 1, -1),
+                (1, 16, 4, 4, 96, 1, -1), (1, 16, 4, 4, 64, 0, 5), (1, 16, 4, 4, 64, 1, -2),
+                (1, 16, 4, 4, 64, 2, -1), (1 << 16, 1 << 16, 1, 1, 64, 0, -1)]:
+        assert lib.attn_fwd_workspace_size(*bad) == 0, bad
+
+
+A = 1 << 20  # a fake, 16-byte aligned address; never dereferenced
+
+
+def call(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, L=256, Hq=4, Hkv=4, d=64, causal=1, wl=-1,
+             scale=0.125, dtype=0, out=0, ws=A, wsb=256, stream=None)
+    a.update(kw)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"],
+                        a["Hkv"], a["d"], a["causal"], a["wl"], a["scale"], a["dtype"], a["out"],
+                        a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(L=0), 1), (dict(L=-5), 1), (dict(Hq=0), 1), (dict(Hkv=0), 1),
+    (dict(Hq=6, Hkv=4), 1), (dict(d=0), 1), (dict(d=96), 2), (dict(d=256), 2),
+    (dict(causal=2), 1), (dict(wl=-2), 1), (dict(causal=0, wl=8), 2),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(dtype=2), 1), (dict(out=5), 1),
+    (dict(q=None), 1), (dict(o=None), 1), (dict(k=A + 8), 1), (dict(o=A + 2), 1),
+    (dict(lse=A + 2), 1), (dict(ws=None), 3), (dict(ws=A + 4), 3), (dict(wsb=16), 3),
+    (dict(B=1 << 12, L=1 << 16, Hq=8, Hkv=8), 1),
+])
+def test_invalid_arguments_are_rejected_before_launch(lib, kw, code):
+    assert call(lib, **kw) == code
+    assert lib.attn_last_error_detail()  # a reason is kept
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
+    assert call(lib) == 4
+    assert lib.attn_debug_wait_probe(A, 256, 1000, None) == 4
+
+
+def test_sync_status_and_probe_reject_bad_workspace(lib):
+    assert lib.attn_fwd_sync_status(None, None) == 3
+    assert lib.attn_fwd_sync_status(A + 4, None) == 3
+    assert lib.attn_debug_wait_probe(None, 256, 1000, None) == 3
+    assert lib.attn_debug_wait_probe(A, 8, 1000, None) == 3
+
+
+def test_python_binding_rejects_cpu_tensors():
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        ex.attn_fwd(q, q, q)

@@ -1,0 +1,156 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small shapes run in full and span several 128-row tiles plus ragged tails; the five
+workloads run at their full sizes in the launch configuration the benchmark uses,
+compared in full where the oracle finishes in seconds and on a stratified row
+sample otherwise.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from parity_util import compare, gpu_run
+
+pytestmark = pytest.mark.gpu
+
+SMALL_L = [1, 2, 127, 128, 129, 255, 256, 257, 300, 640]
+MASKS = [(False, -1), (True, -1), (True, 0), (True, 1), (True, 100), (True, 300)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("L", SMALL_L)
+def test_small_shapes_all_masks(d, dtype, L):
+    for n, ((causal, wl), (hq, hkv)) in enumerate(
+            itertools.product(MASKS, [(2, 2), (4, 1)])):
+        q, k, v = si.random_qkv(2, L, hq, hkv, d, dtype=dtype, seed=1000 * L + 10 * n + d)
+        compare(q, k, v, dtype, causal, wl, 1.0 / math.sqrt(d),
+                label=f"L={L} d={d} {dtype} mask={(causal, wl)} heads={hq}/{hkv}")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.125, 0.5, 2.0])
+def test_scale_values(scale):
+    q, k, v = si.random_qkv(1, 384, 2, 1, 64, seed=77)
+    for causal in (False, True):
+        compare(q, k, v, "fp16", causal, -1, scale, label=f"scale={scale} causal={causal}")
+
+
+def test_gqa_group_sizes():
+    for hq, hkv in [(8, 8), (8, 4), (8, 2), (8, 1)]:
+        q, k, v = si.random_qkv(1, 513, hq, hkv, 128, dtype="bf16", seed=hq * 10 + hkv)
+        compare(q, k, v, "bf16", True, -1, 1 / math.sqrt(128), label=f"gqa {hq}/{hkv}")
+
+
+def _workload(w, rows=None):
+    q, k, v = si.make_qkv(w)
+    return compare(q, k, v, w.dtype, w.causal, w.window_left, w.scale, rows=rows, label=w.name)
+
+
+def test_causal_b1_h4_L2048_full():
+    _workload(si.CAUSAL_B1_H4_L2048_D64)
+
+
+def test_noncausal_b2_h8_L512_full():
+    _workload(si.NONCAUSAL_B2_H8_D64_L512)
+
+
+def test_pages_accuracy_check_fp16_output():
+    """The skill page's own bar (workflow 1 step 4): fp16 output within 1e-3 of
+    standard attention at 1x8x512x64, scale 1/8, non-causal."""
+    w = si.NONCAUSAL_B2_H8_D64_L512
+    q, k, v = si.make_qkv(w)
+    q, k, v = q[:1].contiguous(), k[:1].contiguous(), v[:1].contiguous()
+    o, _ = gpu_run(q, k, v, False, -1, 0.125, out_fp32=False)
+    import oracle
+    o_ref, _ = oracle.default().attn_full(si.bits16(q), si.bits16(k), si.bits16(v), "fp16",
+                                          False, -1, 0.125)
+    assert np.abs(o.double().cpu().numpy() - o_ref).max() < 1e-3
+
+
+def test_noncausal_b2_h8_L2048_full():
+    _workload(si.NONCAUSAL_B2_H8_D64_L2048)
+
+
+@pytest.mark.parametrize("L", si.SWEEP_LENGTHS)
+def test_causal_sweep(L):
+    w = si.CAUSAL_SWEEP_B1_H4_D64.with_length(L)
+    _workload(w, rows=None if L <= 4096 else si.sample_rows(w))
+
+
+def test_causal_gqa_hq32_hkv8_d128_L131072_sampled():
+    w = si.CAUSAL_GQA_B1_H32_KV8_D128
+    _workload(w, rows=si.sample_rows(w, n_random=128))
+
+
+def test_window4096_b4_h16_d128_L32768_sampled():
+    w = si.WINDOW_B4_H16_D128
+    _workload(w, rows=si.sample_rows(w, n_random=256))
+
+
+def test_repeatable_bits():
+    q, k, v = si.random_qkv(2, 1000, 4, 2, 64, seed=5, device="cuda")
+    import exact_io_aware_19_gb300 as ex
+    o1, l1 = ex.attn_fwd(q, k, v, causal=True)
+    o2, l2 = ex.attn_fwd(q, k, v, causal=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Guard bands around O and LSE keep their canary values (no stray writes)."""
+    import exact_io_aware_19_gb300 as ex
+    B, L, H, d = 1, 333, 3, 128
+    q, k, v = si.random_qkv(B, L, H, H, d, dtype="bf16", seed=9, device="cuda")
+    pad = 4096
+    for out_dt in (torch.bfloat16, torch.float32):
+        n = B * L * H * d
+        obuf = torch.full((n + 2 * pad,), -7.0, dtype=out_dt, device="cuda")
+        lbuf = torch.full((B * H * L + 2 * pad,), -7.0, dtype=torch.float32, device="cuda")
+        o = obuf[pad:pad + n].view(B, L, H, d)
+        lse = lbuf[pad:pad + B * H * L].view(B, H, L)
+        ex.attn_fwd_into(q, k, v, o, lse, causal=True)
+        ex.sync_status()
+        assert (obuf[:pad] == -7).all() and (obuf[pad + n:] == -7).all()
+        assert (lbuf[:pad] == -7).all() and (lbuf[pad + B * H * L:] == -7).all()
+        assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_no_device_allocation_inside_the_call():
+    import exact_io_aware_19_gb300 as ex
+    q, k, v = si.random_qkv(1, 4096, 4, 4, 64, seed=3, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 4, 4096, dtype=torch.float32, device="cuda")
+    ex.attn_fwd_into(q, k, v, o, lse, causal=True)  # warm (workspace cached)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        ex.attn_fwd_into(q, k, v, o, lse, causal=True)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert free1 == free0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """The one-warp probe waits on a barrier nothing completes; the wait gives up
+    after 2 ms, the status word says ATTN_ERR_TIMEOUT, and the GPU keeps working."""
+    import exact_io_aware_19_gb300 as ex
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ex.debug_wait_probe(ws, 2_000_000)
+    with pytest.raises(ex.AttnError) as e:
+        ex.sync_status(ws)
+    assert e.value.code == 5
+    ex.sync_status(ws)  # cleared
+    q, k, v = si.random_qkv(1, 200, 2, 2, 64, seed=1)
+    compare(q, k, v, "fp16", True, -1, 0.125, label="after timeout")
+
+
+def test_wrong_device_type_rejected():
+    import exact_io_aware_19_gb300 as ex
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.float32, device="cuda")
+    with pytest.raises(TypeError):
+        ex.attn_fwd(q, q, q)
