@@ -149,6 +149,12 @@ attn_status_t check_shape(int B, int L, int Hq, int Hkv, int d, int causal, int 
 
 }  // namespace
 
+namespace ex19 {
+// Lets other translation units of the library set the detail string that
+// attn_last_error_detail() returns to the calling thread.
+void set_last_error_detail(const std::string& msg) { g_detail = msg; }
+}  // namespace ex19
+
 extern "C" {
 
 size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal, int window_left) {

@@ -93,6 +93,31 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * attn_fwd without a caller-provided workspace, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is forbidden or unsafe (inside an
+ * allocator or memory-pool callback, under another framework's allocator that owns
+ * all device memory, or on a path that must never enter the allocator). The pages
+ * have no counterpart; this is an interface addition of this library.
+ *
+ * The call allocates nothing. Its scratch (the kernel's 16-byte status word) lives
+ * in a fixed 256-byte device array inside the library that every GPU loading the
+ * library keeps until the process exits. Arguments and results are those of
+ * attn_fwd. Rules:
+ *   - Problems needing more scratch than 256 bytes return ATTN_ERR_WORKSPACE (none
+ *     do today).
+ *   - All calls on a device share the array, and each call clears its status word
+ *     first: calls that overlap on the GPU (other streams, other threads) race.
+ *   - The first call on a device looks up the array's address (and may load the
+ *     library's device code); make it before any stream capture starts.
+ *   - A device-side timeout is recorded only in that shared word, which no entry
+ *     point reads; use attn_fwd with a workspace when that report is needed.
+ */
+attn_status_t attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int B, int L, int Hq, int Hkv, int d, int causal,
+                               int window_left, float scale, attn_dtype_t dtype,
+                               attn_out_t out_dtype, void *stream);
+
+/*
  * Synchronises `stream`, reads the workspace status word written by earlier
  * attn_fwd calls on it, clears it, and returns it (ATTN_OK when no device-side
  * error was recorded). A CUDA error while synchronising returns ATTN_ERR_CUDA.
