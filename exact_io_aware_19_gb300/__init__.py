@@ -25,7 +25,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "sync_status", "AttnError",
-           "library_path", "load_library", "set_wait_limit_ns", "debug_wait_probe",
+           "library_path", "load_library", "set_wait_limit_ns", "debug_wait_probe", "debug_exp2",
            "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +66,8 @@ def _bind(lib):
     lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.attn_debug_wait_probe.restype = i
     lib.attn_debug_wait_probe.argtypes = [p, sz, ctypes.c_uint64, p]
+    lib.attn_debug_exp2.restype = i
+    lib.attn_debug_exp2.argtypes = [p, p, p, i, p]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i]
     lib.attn_last_error_detail.restype = ctypes.c_char_p
@@ -196,6 +198,16 @@ def sync_status(workspace: Optional[torch.Tensor] = None, device=None, stream=No
 
 def set_wait_limit_ns(limit_ns: int) -> None:
     load_library().attn_set_wait_limit_ns(int(limit_ns))
+
+
+def debug_exp2(x: torch.Tensor):
+    """(2^x by the kernel's polynomial path, 2^x by MUFU ex2) for a CUDA float32 tensor."""
+    lib = load_library()
+    x = x.contiguous()
+    yp, ym = torch.empty_like(x), torch.empty_like(x)
+    _check(lib.attn_debug_exp2(x.data_ptr(), yp.data_ptr(), ym.data_ptr(), x.numel(),
+                               _stream_handle(None)))
+    return yp, ym
 
 
 def debug_wait_probe(workspace: torch.Tensor, limit_ns: int, stream=None) -> None:

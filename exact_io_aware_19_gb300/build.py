@@ -43,8 +43,26 @@ def _inputs():
         glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "attn.h"), __file__]
 
 
+STAMP = os.path.join(BUILD, "flags.txt")
+
+
+def _defines():
+    """Tuning defines taken from the environment: EX19_POLY_PAIRS (pairs of every 8
+    softmax columns whose exp2 runs on the FMA-pipe polynomial; default 0),
+    EX19_SEPARATE_P (d = 64 fp16 keeps P in its own TMEM columns; default 1),
+    EX19_SOFTMAX_F2 (paired fp32 FMA / adds in the softmax; default 0),
+    EX19_MAX3 (3-input max instruction in the row max; default 0)."""
+    out = []
+    for name in ("EX19_POLY_PAIRS", "EX19_SEPARATE_P", "EX19_SOFTMAX_F2", "EX19_MAX3"):
+        if os.environ.get(name):
+            out.append("-D%s=%d" % (name, int(os.environ[name])))
+    return out
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+        return False
+    if open(STAMP).read() != " ".join(_defines()):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(p) <= t for p in _inputs())
@@ -56,7 +74,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + _defines()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
@@ -77,6 +95,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as fh:
+        fh.write(" ".join(_defines()))
     return LIB
 
 

@@ -280,6 +280,28 @@ attn_status_t attn_debug_wait_probe(void* workspace, size_t workspace_bytes, uin
   return ATTN_OK;
 }
 
+attn_status_t attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, void* stream) {
+  g_detail.clear();
+  if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be >= 0");
+  if (n == 0) return ATTN_OK;
+  if (!x || !y_poly || !y_mufu) return fail(ATTN_ERR_INVALID_ARG, "pointers must be non-null");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300)");
+  std::string why;
+  const void* ptrs[3] = {x, y_poly, y_mufu};
+  const char* names[3] = {"x", "y_poly", "y_mufu"};
+  for (int i = 0; i < 3; ++i)
+    if (!is_device_ptr(ptrs[i], dev, &why, names[i])) return fail(ATTN_ERR_INVALID_ARG, why);
+  e = ex19::launch_exp2_probe(x, y_poly, y_mufu, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("exp2 probe launch", e);
+  return ATTN_OK;
+}
+
 const char* attn_status_string(attn_status_t s) {
   switch (s) {
     case ATTN_OK: return "ok";

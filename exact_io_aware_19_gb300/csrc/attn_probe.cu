@@ -23,6 +23,29 @@ __global__ void wait_probe_kernel(uint32_t* status, unsigned long long limit_ns)
 }
 
 
+// Element-wise 2^x by the polynomial path and by MUFU ex2, for accuracy tests.
+__global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float a = x[i];
+  const float b = (i + 1 < n) ? x[i + 1] : 0.f;
+  float p0, p1;
+  exp2_poly_pair(a, b, p0, p1);
+  y_poly[i] = p0;
+  y_mufu[i] = ex2_approx(a);
+  if (i + 1 < n) {
+    y_poly[i + 1] = p1;
+    y_mufu[i + 1] = ex2_approx(b);
+  }
+}
+
+cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
+                              cudaStream_t stream) {
+  const int pairs = (n + 1) / 2;
+  exp2_probe_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y_poly, y_mufu, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream) {
   wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();

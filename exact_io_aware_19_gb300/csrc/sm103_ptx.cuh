@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "exp2_poly.h"
+
 namespace ex19 {
 
 // ---------------------------------------------------------------- status words
@@ -222,6 +224,57 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of fp32 (one 64-bit register) and the sm_100+ paired FMA / add.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x0, 2^x1 on the FMA and ALU pipes instead of MUFU: x = j + f with j = rint(x)
+// (1.5·2^23 rounding trick) and f in [-1/2, 1/2]; 2^f from the fitted polynomial
+// of exp2_poly.h; j is added to the exponent field. Inputs are clamped to
+// [-125, +inf) so the result stays a normal number (or a negligible 2^-125).
+__device__ __forceinline__ void exp2_poly_pair(float x0, float x1, float& y0, float& y1) {
+  x0 = fmaxf(x0, -125.f);
+  x1 = fmaxf(x1, -125.f);
+  const uint64_t xx = f2_pack(x0, x1);
+  const uint64_t t = f2_add(xx, f2_pack(12582912.f, 12582912.f));
+  const uint64_t jf = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t f = f2_fma(jf, f2_pack(-1.f, -1.f), xx);
+  uint64_t p = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  p = f2_fma(p, f, f2_pack(kExp2C1, kExp2C1));
+  p = f2_fma(p, f, f2_pack(kExp2C0, kExp2C0));
+  float t0, t1, p0, p1;
+  f2_unpack(t, t0, t1);
+  f2_unpack(p, p0, p1);
+  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
 __device__ __forceinline__ float lg2_approx(float x) {

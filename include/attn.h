@@ -141,6 +141,16 @@ void attn_set_wait_limit_ns(uint64_t limit_ns);
 attn_status_t attn_debug_wait_probe(void *workspace, size_t workspace_bytes,
                                     uint64_t limit_ns, void *stream);
 
+/*
+ * Evaluates 2^x[i] for i < n with the two exp2 paths of the attention kernel:
+ * the FMA-pipe polynomial (y_poly) and the MUFU instruction (y_mufu). Device
+ * float32 arrays; used by the accuracy tests of the polynomial. The polynomial
+ * (degree 3, fitted by fit_exp2_poly.py) is valid for x <= 128; inputs below -125
+ * are clamped to -125.
+ */
+attn_status_t attn_debug_exp2(const float *x, float *y_poly, float *y_mufu, int n,
+                              void *stream);
+
 /* Static description of a status code. */
 const char *attn_status_string(attn_status_t s);
 

@@ -154,3 +154,23 @@ def test_wrong_device_type_rejected():
     q = torch.zeros(1, 8, 1, 64, dtype=torch.float32, device="cuda")
     with pytest.raises(TypeError):
         ex.attn_fwd(q, q, q)
+
+
+def test_exp2_polynomial_error_bound():
+    """The FMA-pipe exp2 (fitted degree-3 polynomial + exponent insertion) stays within
+    its fitted relative-error bound against float64 2^x, and MUFU ex2 stays near 2^x."""
+    import re
+    import exact_io_aware_19_gb300 as ex
+    hdr = open(ex.__file__.replace("__init__.py", "csrc/exp2_poly.h")).read()
+    bound = float(re.search(r"kExp2PolyMaxRelErr = ([0-9.e+-]+)f", hdr).group(1))
+    x = torch.cat([torch.linspace(-124.0, 8.0, 1 << 20),
+                   torch.tensor([0.0, -0.5, 0.5, 1.0, -1.0])])
+    yp, ym = ex.debug_exp2(x.cuda())
+    ref = torch.exp2(x.double())
+    rel_p = ((yp.double().cpu() - ref) / ref).abs().max().item()
+    rel_m = ((ym.double().cpu() - ref) / ref).abs().max().item()
+    assert rel_p <= bound * 1.05 + 2e-7, (rel_p, bound)
+    assert rel_m <= 1e-6
+    # clamping: far below the range gives a tiny positive number, never inf/nan
+    yp, _ = ex.debug_exp2(torch.tensor([-1000.0, -200.0, -126.0], device="cuda"))
+    assert torch.isfinite(yp).all() and (yp >= 0).all() and (yp < 1e-37).all()
