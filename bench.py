@@ -45,6 +45,7 @@ L2_BYTES = 129 * 1024 * 1024
 # taken on. A changed kernel reports null until it is captured again.
 TRAFFIC_BY_SOURCE = {
     "57cbef3a389c5a7c": 883_172_096 + 68_679_424,  # first tcgen05 version
+    "73ba059d1a6a1b4f": 893_060_352 + 65_744_896,  # separate P region, two-pass softmax
 }
 
 

@@ -50,10 +50,12 @@ def _defines():
     """Tuning defines taken from the environment: EX19_POLY_PAIRS (pairs of every 8
     softmax columns whose exp2 runs on the FMA-pipe polynomial; default 0),
     EX19_SEPARATE_P (d = 64 fp16 keeps P in its own TMEM columns; default 1),
-    EX19_SOFTMAX_F2 (paired fp32 FMA / adds in the softmax; default 0),
-    EX19_MAX3 (3-input max instruction in the row max; default 0)."""
+    EX19_SOFTMAX_F2 (paired fp32 FMA / adds in the softmax; default 1),
+    EX19_MAX3 (3-input max instruction in the row max; default 0),
+    EX19_SUSPEND_NS (sleep hint of the mbarrier polls in ns; default 1e6, 0 = none)."""
     out = []
-    for name in ("EX19_POLY_PAIRS", "EX19_SEPARATE_P", "EX19_SOFTMAX_F2", "EX19_MAX3"):
+    for name in ("EX19_POLY_PAIRS", "EX19_SEPARATE_P", "EX19_SOFTMAX_F2", "EX19_MAX3",
+                 "EX19_SUSPEND_NS"):
         if os.environ.get(name):
             out.append("-D%s=%d" % (name, int(os.environ[name])))
     return out

@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "attn_params.h"
 #include "sm103_ptx.cuh"
@@ -47,14 +48,27 @@ constexpr int kThreads = 320;        // 8 softmax warps + producer warp + MMA wa
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..)
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows > 2^8
+constexpr float kRescaleThreshold = 8.0f;
+#ifndef EX19_SEPARATE_P
+#define EX19_SEPARATE_P 1  // d = 64 fp16: P in its own TMEM columns (S released early)
+#endif
+#ifndef EX19_SOFTMAX_F2
+#define EX19_SOFTMAX_F2 1  // softmax FMA / adds as paired fp32 (sm_100+ float2 builtins)
+#endif
+#ifndef EX19_MAX3
+#define EX19_MAX3 0  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
+#endif
+#ifndef EX19_POLY_PAIRS
+#define EX19_POLY_PAIRS 0  // exp2 polynomial offload: pairs out of every 8 (0 = all on MUFU)
+#endif  // log2 units: rescale O only when m grows > 2^8
 
 // Wait sites (for the status word): role << 16 | site
 enum : uint32_t {
   kSiteProdEmpty = 0x10001, kSiteProdQFree = 0x10002,
   kSiteMmaQFull = 0x20001, kSiteMmaKFull = 0x20002, kSiteMmaVFull = 0x20003,
   kSiteMmaPFull = 0x20004, kSiteMmaOFree = 0x20005, kSiteMmaDrain = 0x20006,
-  kSiteSmxSFull = 0x30001, kSiteSmxOFull = 0x30002,
+  kSiteMmaSFree = 0x20007,
+  kSiteSmxSFull = 0x30001, kSiteSmxOFull = 0x30002, kSiteSmxPvDone = 0x30003,
   kSiteDrainLoads = 0x40001,
 };
 
@@ -67,8 +81,9 @@ struct Geometry {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kTilesPerUnit * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-  // barriers: full[S], empty[S], q_full, q_free, s_full[2], p_full[2], o_full[2], o_free[2], drain
-  static constexpr int kNumBars = 2 * kSlots + 11;
+  // barriers: full[S], empty[S], q_full, q_free, s_full[2], p_full[2], o_full[2], o_free[2],
+  // drain, s_free[2], pv_done[2]
+  static constexpr int kNumBars = 2 * kSlots + 15;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
@@ -128,6 +143,43 @@ __device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
 
 __device__ __forceinline__ bool has_block(const TileSpan& s, int j) { return j >= s.lo && j < s.hi; }
 
+// Maximum of a 128-value row: 8 independent chains (16 values each), then a tree.
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float m[8];
+#if EX19_MAX3
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = max3f(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+    for (int k = 24; k < 120; k += 16) a = max3f(a, s[k + i], s[k + 8 + i]);  // 24 .. 112
+    m[i] = fmaxf(a, s[120 + i]);
+  }
+  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+#else
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = s[i];
+#pragma unroll
+    for (int k = 8; k < 128; k += 8) a = fmaxf(a, s[k + i]);
+    m[i] = a;
+  }
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+#endif
+}
+
+// Minimum of a 128-value row (used when the scale is negative).
+__device__ __forceinline__ float row_min128(const float (&s)[128]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = s[i];
+#pragma unroll
+    for (int k = 8; k < 128; k += 8) a = fminf(a, s[k + i]);
+    m[i] = a;
+  }
+  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   if (bf16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -157,6 +209,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // bf16 P is split into hi + lo halves (two P·V MMAs) so that rounding P to 8
   // significant bits does not dominate the output error; fp16 P has 11 bits.
   constexpr bool kSplitP = BF16;
+  // Of every 8 column pairs, this many take exp2 from the FMA-pipe polynomial
+  // instead of MUFU (fp16 only: the bf16 path keeps P to ~16 bits).
+  constexpr int kPolyPairs = BF16 ? 0 : EX19_POLY_PAIRS;
+  // TMEM columns. With P over S (d = 128, or bf16 whose split P needs 128 columns):
+  // S_t = [128t, 128t+128), P_t aliased over S_t, O_t = [256+128t, ...). With a
+  // separate P region (d = 64 fp16): S_t = [128t, ...), P_t = [256+64t, 256+64t+64),
+  // O_t = [384+64t, 384+64t+64) — all 512 columns.
+  constexpr bool kSeparateP = (D == 64) && !BF16 && (EX19_SEPARATE_P != 0);
+  constexpr uint32_t kColS0 = 0, kStrideS = 128;
+  constexpr uint32_t kColP0 = kSeparateP ? 256 : 0, kStrideP = kSeparateP ? 64 : 128;
+  constexpr uint32_t kColO0 = kSeparateP ? 384 : 256, kStrideO = kSeparateP ? 64 : 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -174,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_o_full = [&](int t) { return bars + 8u * (2 * S + 6 + t); };
   auto bar_o_free = [&](int t) { return bars + 8u * (2 * S + 8 + t); };
   const uint32_t bar_drain = bars + 8u * (2 * S + 10);
+  auto bar_s_free = [&](int t) { return bars + 8u * (2 * S + 11 + t); };
+  auto bar_pv_done = [&](int t) { return bars + 8u * (2 * S + 13 + t); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
 
@@ -194,6 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_o_free(t), kBM);
     }
     mbar_init(bar_drain, 1);
+    for (int t = 0; t < kTilesPerUnit; ++t) {
+      mbar_init(bar_s_free(t), kBM);
+      mbar_init(bar_pv_done(t), 1);
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -270,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, q_cnt = 0;
       uint32_t p_cnt[kTilesPerUnit] = {0, 0};
       uint32_t o_cnt[kTilesPerUnit] = {0, 0};
+      uint32_t ns[kTilesPerUnit] = {0, 0};  // S MMAs issued per tile (separate-P order)
       bool ok = true;
       Unit u;
       for (int k = 0; ok && unit_of(p, k, u); ++k) {
@@ -278,6 +348,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_cnt;
         if (!ok) break;
         tc_fence_after();
+        if constexpr (kSeparateP) {
+          // Issue order per block j: S_t(j+1) for both tiles as soon as each tile's
+          // softmax has read S_t(j), then O_t += P_t(j)·V_j as each P_t(j) lands.
+          // S, P and O live in separate TMEM columns, so S(j+1) overlaps the
+          // softmax of block j.
+          const uint32_t it0 = it;
+          bool first_pv[kTilesPerUnit] = {true, true};
+          auto slot_of = [&](uint32_t idx) { return idx % S; };
+          auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
+          auto issue_s = [&](const int t, int j) __attribute__((always_inline)) -> bool {
+            if (ns[t] > 0 &&
+                !mbar_wait_bounded(bar_s_free(t), (ns[t] - 1) & 1u, wc, kSiteMmaSFree))
+              return false;
+            tc_fence_after();
+            const uint32_t kidx = it0 + 2u * (j - u.lo);
+            const uint32_t q_addr = sQ + t * G::kTileBytes;
+            const uint32_t k_addr = sKV + slot_of(kidx) * G::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+              mma_ss(tmem_base + kColS0 + kStrideS * t, sdesc_sw128(q_addr + off, 16, 1024),
+                     sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_s_full(t));
+            ++ns[t];
+            return true;
+          };
+          auto issue_pv2 = [&](const int t, int j) __attribute__((always_inline)) -> bool {
+            if (!mbar_wait_bounded(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull)) return false;
+            ++p_cnt[t];
+            if (first_pv[t] &&
+                !mbar_wait_bounded(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree))
+              return false;
+            tc_fence_after();
+            const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
+            const uint32_t v_addr = sKV + slot_of(vidx) * G::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
+              mma_ts(tmem_base + kColO0 + kStrideO * t, tmem_base + kColP0 + kStrideP * t + kk * 8,
+                     bdesc, idesc_o, (first_pv[t] && kk == 0) ? 0u : 1u);
+            }
+            mma_commit(bar_pv_done(t));
+            first_pv[t] = false;
+            return true;
+          };
+          {  // S of the first block
+            const uint32_t kidx = it0;
+            ok = mbar_wait_bounded(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < kTilesPerUnit; ++t)
+              if (ok && has_block(u.t[t], u.lo)) ok = issue_s(t, u.lo);
+            if (ok) mma_commit(bar_empty(slot_of(kidx)));
+          }
+          for (int j = u.lo; ok && j < u.hi; ++j) {
+            if (j + 1 < u.hi) {
+              const uint32_t kidx = it0 + 2u * (j + 1 - u.lo);
+              ok = mbar_wait_bounded(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
+              tc_fence_after();
+#pragma unroll
+              for (int t = 0; t < kTilesPerUnit; ++t)
+                if (ok && has_block(u.t[t], j + 1)) ok = issue_s(t, j + 1);
+              if (!ok) break;
+              mma_commit(bar_empty(slot_of(kidx)));
+            }
+            const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
+            ok = mbar_wait_bounded(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull);
+#pragma unroll
+            for (int t = 0; t < kTilesPerUnit; ++t) {
+              if (ok && has_block(u.t[t], j)) {
+                ok = issue_pv2(t, j);
+                if (ok && j == u.t[t].hi - 1) {
+                  mma_commit(bar_o_full(t));  // tile t's last block of this unit
+                  ++o_cnt[t];
+                }
+              }
+            }
+            if (!ok) break;
+            mma_commit(bar_empty(slot_of(vidx)));
+          }
+          if (!ok) break;
+          it = it0 + 2u * (u.hi - u.lo);
+          mma_commit(bar_q_free);
+          continue;
+        }
         int pend[kTilesPerUnit] = {-1, -1};          // block whose S_t waits for its P·V
         uint32_t pend_vslot[kTilesPerUnit] = {0, 0};
         uint32_t pend_vpar[kTilesPerUnit] = {0, 0};
@@ -286,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool have_prev_v = false;
 
         // O_t (+)= P_t · V for the pending block of tile t.
-        auto issue_pv = [&](int t) -> bool {
+        auto issue_pv = [&](const int t) __attribute__((always_inline)) -> bool {
           if (!mbar_wait_bounded(bar_full(pend_vslot[t]), pend_vpar[t], wc, kSiteMmaVFull))
             return false;
           if (!mbar_wait_bounded(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull)) return false;
@@ -296,20 +452,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               return false;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + 256 + 128 * t;
-          const uint32_t p_tmem = tmem_base + 128 * t;
+          const uint32_t d_tmem = tmem_base + kColO0 + kStrideO * t;
+          const uint32_t p_tmem = tmem_base + kColP0 + kStrideP * t;
           const uint32_t v_addr = sKV + pend_vslot[t] * G::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             // 16 keys per MMA: 8 TMEM columns of packed P, 16 rows (2 KiB) of V.
+            // Split P keeps each 64-key half as [hi 32 columns | lo 32 columns].
+            const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
             const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
-            mma_ts(d_tmem, p_tmem + kk * 8, bdesc, idesc_o, (first_pv[t] && kk == 0) ? 0u : 1u);
+            mma_ts(d_tmem, p_tmem + pcol, bdesc, idesc_o, (first_pv[t] && kk == 0) ? 0u : 1u);
           }
           if (kSplitP) {
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk) {
+              const uint32_t pcol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
               const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
-              mma_ts(d_tmem, p_tmem + 64 + kk * 8, bdesc, idesc_o, 1u);
+              mma_ts(d_tmem, p_tmem + pcol, bdesc, idesc_o, 1u);
             }
           }
           first_pv[t] = false;
@@ -325,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait_bounded(bar_full(kslot), kpar, wc, kSiteMmaKFull);
           if (!ok) break;
           tc_fence_after();
+#pragma unroll
           for (int t = 0; t < kTilesPerUnit; ++t) {
             const bool flushed = pend[t] >= 0;
             if (flushed && !(ok = issue_pv(t))) break;
@@ -335,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-                mma_ss(tmem_base + 128 * t, sdesc_sw128(q_addr + off, 16, 1024),
+                mma_ss(tmem_base + kColS0 + kStrideS * t, sdesc_sw128(q_addr + off, 16, 1024),
                        sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
               }
               mma_commit(bar_s_full(t));
@@ -353,8 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           prev_vslot = vslot;
           have_prev_v = true;
         }
-        for (int t = 0; ok && t < kTilesPerUnit; ++t) {
-          if (pend[t] >= 0) {
+#pragma unroll
+        for (int t = 0; t < kTilesPerUnit; ++t) {
+          if (ok && pend[t] >= 0) {
             if (!(ok = issue_pv(t))) break;
             mma_commit(bar_o_full(t));
             ++o_cnt[t];
@@ -374,33 +535,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem_base + lane_off + 128 * t;
-    const uint32_t tO = tmem_base + lane_off + 256 + 128 * t;
+    const uint32_t tS = tmem_base + lane_off + kColS0 + kStrideS * t;
+    const uint32_t tP = tmem_base + lane_off + kColP0 + kStrideP * t;
+    const uint32_t tO = tmem_base + lane_off + kColO0 + kStrideO * t;
     const float C = p.score_log2;
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;  // blocks / units this tile has processed (all units)
     bool ok = true;
     Unit u;
     for (int k = 0; ok && unit_of(p, k, u); ++k) {
       wc.unit = k;
-      const TileSpan span = u.t[t];
+      const TileSpan span = (t == 0) ? u.t[0] : u.t[1];  // no dynamic index: stays in registers
       if (span.lo >= span.hi) continue;
       const int row = span.row0 + r_in_tile;
       float m_ref = -INFINITY;  // reference max (base-2 units) the P values are relative to
       float l = 0.f;            // running sum of P
       for (int j = span.lo; j < span.hi; ++j) {
         ok = mbar_wait_warp(bar_s_full(t), s_cnt & 1u, wc, kSiteSmxSFull);
-        ++s_cnt;
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld_x128(tS, sr);
-        float s[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        if (p.negate_scores) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = -s[c];
-        }
         const int key0 = j * kBN;
         const bool masked = (key0 + kBN > p.L) || (p.causal && key0 + kBN - 1 > span.row0) ||
                             (p.window_left >= 0 && key0 < span.row0 + kBM - 1 - p.window_left);
@@ -412,53 +564,148 @@ __global__ void __launch_bounds__(kThreads, 1)
           vis_hi = max(0, min(kBN, hi_key - key0));
           vis_lo = max(0, min(kBN, lo_key - key0));
         }
-        float mx = -INFINITY;
-        if (!masked) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= vis_lo && c < vis_hi) mx = fmaxf(mx, s[c]);
-        }
-        const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
+        // x = Cs · s with Cs = ±C, so that x carries the sign of the scale.
+        const bool neg = p.negate_scores != 0;
+        const float Cs = neg ? -C : C;
         float alpha = 1.f;
         bool rescale = false;
-        if (bm > m_ref + kRescaleThreshold) {
-          alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
-          m_ref = bm;
-          rescale = true;
-        }
-        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float sum0 = 0.f, sum1 = 0.f;
-        // P in 32-column chunks: 16 packed registers per chunk, stored to TMEM
-        // over the S columns already read (P hi at column c/2, P lo at 64 + c/2).
+        bool stop = false;
+        // The block body, instantiated twice: blocks that cross no mask boundary
+        // (almost all of them) carry no per-element selects at all. S is read from
+        // TMEM twice: all 128 columns for the row maximum, then 64 at a time for the
+        // exponentials, which keeps the live registers of a thread well under 168.
+        auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
+          constexpr bool M = decltype(masked_tag)::value;
+          float mx;  // max over visible columns of Cs·s / C (i.e. of ±s)
+          {
+            float m8[8];
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t pk[16];
-          uint32_t pk_lo[16];
+            for (int h = 0; h < 2; ++h) {
+              uint32_t sr[64];
+              tmem_ld_x64(tS + 64 * h, sr);
+              float sv[64];
 #pragma unroll
-          for (int c = c0; c < c0 + 32; c += 2) {
-            float p0 = ex2_approx(fmaf(s[c], C, -mu));
-            float p1 = ex2_approx(fmaf(s[c + 1], C, -mu));
-            if (masked) {
-              p0 = (c >= vis_lo && c < vis_hi) ? p0 : 0.f;
-              p1 = (c + 1 >= vis_lo && c + 1 < vis_hi) ? p1 : 0.f;
+              for (int c = 0; c < 64; ++c) {
+                sv[c] = neg ? -__uint_as_float(sr[c]) : __uint_as_float(sr[c]);
+                if constexpr (M) {
+                  if (64 * h + c < vis_lo || 64 * h + c >= vis_hi) sv[c] = -INFINITY;
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float a = (h == 0) ? sv[i] : fmaxf(m8[i], sv[i]);
+#pragma unroll
+                for (int c = 8; c < 64; c += 8) a = fmaxf(a, sv[c + i]);
+                m8[i] = a;
+              }
             }
-            sum0 += p0;
-            sum1 += p1;
-            const uint32_t hi = pack2(p0, p1, BF16);
-            pk[(c - c0) >> 1] = hi;
-            if constexpr (kSplitP)
-              pk_lo[(c - c0) >> 1] =
-                  pack2(p0 - low_as_float(hi, BF16), p1 - high_as_float(hi, BF16), BF16);
+            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
           }
-          tmem_st_x16(tS + (c0 >> 1), pk);
-          if constexpr (kSplitP) tmem_st_x16(tS + 64 + (c0 >> 1), pk_lo);
+          const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
+          if (bm > m_ref + kRescaleThreshold) {
+            alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
+            m_ref = bm;
+            rescale = true;
+          }
+          const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+          if constexpr (kSeparateP) {
+            // P_t and O_t are read by this tile's previous P·V: wait until it is done.
+            if (s_cnt > 0) {
+              if (!mbar_wait_warp(bar_pv_done(t), (s_cnt - 1) & 1u, wc, kSiteSmxPvDone)) {
+                stop = true;
+                return;
+              }
+              tc_fence_after();
+            }
+          }
+#if EX19_SOFTMAX_F2
+          const float2 c2 = make_float2(Cs, Cs);
+          const float2 nmu2 = make_float2(-mu, -mu);
+          float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#else
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+#endif
+          // Second pass, 64 columns at a time; P in 32-column chunks of 16 packed
+          // registers, stored to TMEM (P hi at column c/2 of the P region, P lo at
+          // 64 + c/2).
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t sr[64];
+            tmem_ld_x64(tS + 64 * h, sr);
+            if constexpr (kSeparateP) {
+              if (h == 1) {  // S is fully in registers: the next S MMA may overwrite it
+                tc_fence_before();
+                mbar_arrive(bar_s_free(t));
+              }
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+              uint32_t pk[16];
+              uint32_t pk_lo[16];
+#pragma unroll
+              for (int c = c0; c < c0 + 32; c += 2) {
+                const int cc = 64 * h + c;  // column within the block
+#if EX19_SOFTMAX_F2
+                const float2 x = __ffma2_rn(
+                    make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nmu2);
+                const float x0 = x.x, x1 = x.y;
+#else
+                const float x0 = fmaf(__uint_as_float(sr[c]), Cs, -mu);
+                const float x1 = fmaf(__uint_as_float(sr[c + 1]), Cs, -mu);
+#endif
+                float p0, p1;
+                if (kPolyPairs > 0 && ((cc >> 1) & 7) < kPolyPairs) {
+                  exp2_poly_pair(x0, x1, p0, p1);  // on the FMA/ALU pipes
+                } else {
+                  p0 = ex2_approx(x0);  // on MUFU
+                  p1 = ex2_approx(x1);
+                }
+                if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
+                  p0 = (cc >= vis_lo && cc < vis_hi) ? p0 : 0.f;
+                  p1 = (cc + 1 >= vis_lo && cc + 1 < vis_hi) ? p1 : 0.f;
+                }
+#if EX19_SOFTMAX_F2
+                acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
+#else
+                acc[c & 3] += p0;
+                acc[(c + 1) & 3] += p1;
+#endif
+                const uint32_t hi = pack2(p0, p1, BF16);
+                pk[(c - c0) >> 1] = hi;
+                if constexpr (kSplitP)
+                  pk_lo[(c - c0) >> 1] =
+                      pack2(p0 - low_as_float(hi, BF16), p1 - high_as_float(hi, BF16), BF16);
+              }
+              if constexpr (kSplitP) {
+                // P over S, half h: hi at columns 64h .. 64h+31, lo at 64h+32 .. 64h+63,
+                // i.e. inside the S columns this thread has already read.
+                tmem_st_x16(tP + 64 * h + (c0 >> 1), pk);
+                tmem_st_x16(tP + 64 * h + 32 + (c0 >> 1), pk_lo);
+              } else {
+                tmem_st_x16(tP + 32 * h + (c0 >> 1), pk);  // P at columns 0 .. 63
+              }
+            }
+          }
+#if EX19_SOFTMAX_F2
+          const float rowsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+#else
+          const float rowsum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#endif
+          l = l * alpha + rowsum;
+        };
+        if (masked)
+          block_body(std::true_type{});
+        else
+          block_body(std::false_type{});
+        if (stop) {
+          ok = false;
+          break;
         }
-        l = l * alpha + (sum0 + sum1);
-        // O rescale (the previous P·V of this tile is complete: S_t(j) was issued
-        // after it and s_full tracks all earlier MMAs).
+        ++s_cnt;
+        // O rescale. The previous P·V of this tile is complete: with P over S,
+        // S_t(j) was issued after it and s_full tracks all earlier MMAs; with a
+        // separate P region, pv_done was waited just above.
         if (__any_sync(0xffffffffu, rescale && j != span.lo)) {
           const float a = (rescale && j != span.lo) ? alpha : 1.f;
 #pragma unroll
@@ -480,9 +727,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++o_cnt;
       if (!ok) break;
       tc_fence_after();
-      const bool live = row < p.L;
+      // Opaque copies: keep the compiler from hoisting the epilogue's 64-bit
+      // addresses above the block loop, where they would hold registers the
+      // softmax needs.
+      int eb = u.b, eh = u.h, erow = row;
+      asm volatile("" : "+r"(eb), "+r"(eh), "+r"(erow));
+      const bool live = erow < p.L;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const size_t o_row = ((static_cast<size_t>(u.b) * p.L + row) * p.Hq + u.h) * D;
+      const size_t o_row = ((static_cast<size_t>(eb) * p.L + erow) * p.Hq + eh) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t orow[32];
@@ -513,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (live && p.lse != nullptr) {
         const float lse = (l > 0.f) ? (m_ref + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
-        p.lse[(static_cast<size_t>(u.b) * p.Hq + u.h) * p.L + row] = lse;
+        p.lse[(static_cast<size_t>(eb) * p.Hq + eh) * p.L + erow] = lse;
       }
       tc_fence_before();
       mbar_arrive(bar_o_free(t));

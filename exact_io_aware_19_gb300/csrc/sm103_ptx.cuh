@@ -59,6 +59,27 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Probe with a suspend-time hint: a thread whose phase is not complete sleeps in
+// hardware until the phase completes or `hint_ns` passes, instead of spinning and
+// taking issue slots from the warps that do the work.
+#ifndef EX19_SUSPEND_NS
+#define EX19_SUSPEND_NS 1000000  // 1 ms: also the worst-case reaction time to an abort (0: no hint)
+#endif
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity) {
+#if EX19_SUSPEND_NS == 0
+  return mbar_test(bar, parity);
+#endif
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(EX19_SUSPEND_NS))
+      : "memory");
+  return ok != 0;
+}
+
 // Shared control block of one CTA for bounded waits.
 struct WaitCtl {
   volatile uint32_t* abort_flag;  // shared memory: set once any role gives up
@@ -86,7 +107,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
                                             uint32_t where, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test_sleep(bar, parity)) return true;
     if (honor_abort && *c.abort_flag) return false;
     if (globaltimer_ns() - t0 > c.limit_ns) {
       record_error(c, kStatusTimeout, where);
