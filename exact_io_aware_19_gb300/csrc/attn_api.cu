@@ -16,7 +16,11 @@
 
 namespace {
 
-constexpr size_t kWorkspaceBytes = 256;  // status word (16 B), padded
+#ifndef EX19_TRACE
+#define EX19_TRACE 0
+#endif
+// status word (16 B), padded; trace builds append the timeline probe buffer
+constexpr size_t kWorkspaceBytes = EX19_TRACE ? 256 + 16384 : 256;
 constexpr unsigned long long kDefaultWaitLimitNs = 4000000000ull;
 constexpr int kUnitRows = 256;           // query rows per kernel work unit
 
@@ -224,6 +228,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.units_per_bh = (L + kUnitRows - 1) / kUnitRows;
   p.num_units = B * Hq * p.units_per_bh;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.trace = EX19_TRACE ? reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + 256)
+                       : nullptr;
   a.grid = p.num_units < info.sms ? p.num_units : info.sms;
   a.stream = static_cast<cudaStream_t>(stream);
 

@@ -55,6 +55,15 @@ constexpr float kRescaleThreshold = 8.0f;
 #ifndef EX19_SOFTMAX_F2
 #define EX19_SOFTMAX_F2 1  // softmax FMA / adds as paired fp32 (sm_100+ float2 builtins)
 #endif
+#ifndef EX19_TRACE
+#define EX19_TRACE 0  // 1: CTA 0 stamps clock64 at each step of its first unit (debug)
+#endif
+#ifndef EX19_MMA_EVENT
+#define EX19_MMA_EVENT 0  // d = 64 fp16: event-driven MMA issue (1) or fixed order per block (0)
+#endif
+#ifndef EX19_MMA_IDLE_NS
+#define EX19_MMA_IDLE_NS 0  // nanosleep of the MMA issuer after a poll round with no progress
+#endif
 #ifndef EX19_MAX3
 #define EX19_MAX3 0  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
 #endif
@@ -67,7 +76,7 @@ enum : uint32_t {
   kSiteProdEmpty = 0x10001, kSiteProdQFree = 0x10002,
   kSiteMmaQFull = 0x20001, kSiteMmaKFull = 0x20002, kSiteMmaVFull = 0x20003,
   kSiteMmaPFull = 0x20004, kSiteMmaOFree = 0x20005, kSiteMmaDrain = 0x20006,
-  kSiteMmaSFree = 0x20007,
+  kSiteMmaSFree = 0x20007, kSiteMmaPoll = 0x20008,
   kSiteSmxSFull = 0x30001, kSiteSmxOFull = 0x30002, kSiteSmxPvDone = 0x30003,
   kSiteDrainLoads = 0x40001,
 };
@@ -88,6 +97,16 @@ struct Geometry {
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
 };
+
+// Timeline probe (trace builds): u64 slots [softmax tile 0 | tile 1 | MMA | producer],
+// kTraceBlocks blocks each, kTraceEv events per block.
+constexpr int kTraceBlocks = 48, kTraceEv = 10;
+__device__ __forceinline__ void trace_mark(const FwdParams& p, int role, int k, int jr, int ev) {
+#if EX19_TRACE
+  if (p.trace != nullptr && blockIdx.x == 0 && k == 0 && jr >= 0 && jr < kTraceBlocks)
+    p.trace[(role * kTraceBlocks + jr) * kTraceEv + ev] = clock64();
+#endif
+}
 
 // Rows and key blocks of one query tile of a unit.
 struct TileSpan {
@@ -309,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++q_cnt;
         for (int j = u.lo; ok && j < u.hi; ++j) {
+          trace_mark(p, 3, k, j - u.lo, 0);
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t slot = it % S;
             ok = mbar_wait_bounded(bar_empty(slot), ((it / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
@@ -319,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
                           c * 64, u.g, j * kBN, u.b);
             ++it;
+            trace_mark(p, 3, k, j - u.lo, 1 + kv);
           }
         }
       }
@@ -349,6 +370,110 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         if constexpr (kSeparateP) {
+#if EX19_MMA_EVENT
+          // Event-driven issue: each tile advances on its own. S_t(j) goes out as
+          // soon as K_j has landed and the tile's softmax has read S_t(j-1)
+          // (s_free); O_t += P_t(j)·V_j as soon as V_j has landed and P_t(j) is
+          // written (p_full). A K/V slot is released once every tile that uses its
+          // block has issued the MMA that reads it. S, P and O live in separate
+          // TMEM columns, so S_t(j+1) overlaps the softmax of block j, and one
+          // tile's softmax never waits for the other tile's.
+          const uint32_t it0 = it;
+          bool first_pv[kTilesPerUnit] = {true, true};
+          int s_next[kTilesPerUnit], pv_next[kTilesPerUnit], t_end[kTilesPerUnit];
+#pragma unroll
+          for (int t = 0; t < kTilesPerUnit; ++t) {
+            const bool live = u.t[t].lo < u.t[t].hi;
+            s_next[t] = pv_next[t] = live ? u.t[t].lo : u.lo;
+            t_end[t] = live ? u.t[t].hi : u.lo;
+          }
+          auto slot_of = [&](uint32_t idx) { return idx % S; };
+          auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
+          int k_rel = u.lo, v_rel = u.lo;  // next blocks whose K / V slot is released
+          bool idle = false;
+          uint64_t idle_since = 0;
+          while (true) {
+            bool progress = false;
+#pragma unroll
+            for (int t = 0; t < kTilesPerUnit; ++t) {
+              if (s_next[t] < t_end[t]) {
+                const int j = s_next[t];
+                const uint32_t kidx = it0 + 2u * (j - u.lo);
+                if (mbar_poll(bar_full(slot_of(kidx)), par_of(kidx)) &&
+                    (ns[t] == 0 || mbar_poll(bar_s_free(t), (ns[t] - 1) & 1u))) {
+                  tc_fence_after();
+                  const uint32_t q_addr = sQ + t * G::kTileBytes;
+                  const uint32_t k_addr = sKV + slot_of(kidx) * G::kTileBytes;
+#pragma unroll
+                  for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem_base + kColS0 + kStrideS * t, sdesc_sw128(q_addr + off, 16, 1024),
+                           sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                  }
+                  mma_commit(bar_s_full(t));
+                  ++ns[t];
+                  ++s_next[t];
+                  progress = true;
+                }
+              }
+              if (pv_next[t] < s_next[t]) {
+                const int j = pv_next[t];
+                const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
+                if (mbar_poll(bar_full(slot_of(vidx)), par_of(vidx)) &&
+                    mbar_poll(bar_p_full(t), p_cnt[t] & 1u) &&
+                    (!first_pv[t] || mbar_poll(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u))) {
+                  tc_fence_after();
+                  const uint32_t v_addr = sKV + slot_of(vidx) * G::kTileBytes;
+#pragma unroll
+                  for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
+                    mma_ts(tmem_base + kColO0 + kStrideO * t,
+                           tmem_base + kColP0 + kStrideP * t + kk * 8, bdesc, idesc_o,
+                           (first_pv[t] && kk == 0) ? 0u : 1u);
+                  }
+                  mma_commit(bar_pv_done(t));
+                  ++p_cnt[t];
+                  first_pv[t] = false;
+                  ++pv_next[t];
+                  if (pv_next[t] == t_end[t]) {
+                    mma_commit(bar_o_full(t));  // tile t's last block of this unit
+                    ++o_cnt[t];
+                  }
+                  progress = true;
+                }
+              }
+            }
+            while (k_rel < u.hi && (!has_block(u.t[0], k_rel) || s_next[0] > k_rel) &&
+                   (!has_block(u.t[1], k_rel) || s_next[1] > k_rel)) {
+              mma_commit(bar_empty(slot_of(it0 + 2u * (k_rel - u.lo))));
+              ++k_rel;
+            }
+            while (v_rel < u.hi && (!has_block(u.t[0], v_rel) || pv_next[0] > v_rel) &&
+                   (!has_block(u.t[1], v_rel) || pv_next[1] > v_rel)) {
+              mma_commit(bar_empty(slot_of(it0 + 2u * (v_rel - u.lo) + 1u)));
+              ++v_rel;
+            }
+            if (pv_next[0] == t_end[0] && pv_next[1] == t_end[1] && v_rel == u.hi) break;
+            if (progress) {
+              idle = false;
+              continue;
+            }
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (EX19_MMA_IDLE_NS > 0) __nanosleep(EX19_MMA_IDLE_NS);  // yield issue slots
+            const uint64_t now = globaltimer_ns();
+            if (!idle) {
+              idle = true;
+              idle_since = now;
+            } else if (now - idle_since > wc.limit_ns) {
+              record_error(wc, kStatusTimeout, kSiteMmaPoll);
+              ok = false;
+              break;
+            }
+          }
+#else
           // Issue order per block j: S_t(j+1) for both tiles as soon as each tile's
           // softmax has read S_t(j), then O_t += P_t(j)·V_j as each P_t(j) lands.
           // S, P and O live in separate TMEM columns, so S(j+1) overlaps the
@@ -404,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) mma_commit(bar_empty(slot_of(kidx)));
           }
           for (int j = u.lo; ok && j < u.hi; ++j) {
+            trace_mark(p, 2, k, j - u.lo, 0);
             if (j + 1 < u.hi) {
               const uint32_t kidx = it0 + 2u * (j + 1 - u.lo);
               ok = mbar_wait_bounded(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
@@ -414,12 +540,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               mma_commit(bar_empty(slot_of(kidx)));
             }
+            trace_mark(p, 2, k, j - u.lo, 1);
             const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
             ok = mbar_wait_bounded(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull);
+            trace_mark(p, 2, k, j - u.lo, 2);
 #pragma unroll
             for (int t = 0; t < kTilesPerUnit; ++t) {
               if (ok && has_block(u.t[t], j)) {
                 ok = issue_pv2(t, j);
+                trace_mark(p, 2, k, j - u.lo, 3 + t);
                 if (ok && j == u.t[t].hi - 1) {
                   mma_commit(bar_o_full(t));  // tile t's last block of this unit
                   ++o_cnt[t];
@@ -429,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             mma_commit(bar_empty(slot_of(vidx)));
           }
+#endif
           if (!ok) break;
           it = it0 + 2u * (u.hi - u.lo);
           mma_commit(bar_q_free);
@@ -549,8 +679,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = span.row0 + r_in_tile;
       float m_ref = -INFINITY;  // reference max (base-2 units) the P values are relative to
       float l = 0.f;            // running sum of P
+      const bool tr = EX19_TRACE && quarter == 0 && lane == 0;
       for (int j = span.lo; j < span.hi; ++j) {
+        const int jr = j - span.lo;
+        if (tr) trace_mark(p, t, k, jr, 0);
         ok = mbar_wait_warp(bar_s_full(t), s_cnt & 1u, wc, kSiteSmxSFull);
+        if (tr) trace_mark(p, t, k, jr, 1);
         if (!ok) break;
         tc_fence_after();
         const int key0 = j * kBN;
@@ -619,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
           }
+          if (tr) trace_mark(p, t, k, jr, 4);
 #if EX19_SOFTMAX_F2
           const float2 c2 = make_float2(Cs, Cs);
           const float2 nmu2 = make_float2(-mu, -mu);
@@ -633,6 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 2; ++h) {
             uint32_t sr[64];
             tmem_ld_x64(tS + 64 * h, sr);
+            if (tr) trace_mark(p, t, k, jr, 5 + 2 * h);
             if constexpr (kSeparateP) {
               if (h == 1) {  // S is fully in registers: the next S MMA may overwrite it
                 tc_fence_before();
@@ -686,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_x16(tP + 32 * h + (c0 >> 1), pk);  // P at columns 0 .. 63
               }
             }
+            if (tr) trace_mark(p, t, k, jr, 6 + 2 * h);
           }
 #if EX19_SOFTMAX_F2
           const float rowsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
@@ -720,6 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar_p_full(t));
+        if (tr) trace_mark(p, t, k, jr, 9);
       }
       if (!ok) break;
       // ---- epilogue: O / l and LSE for this tile

@@ -59,6 +59,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe (never suspends): used by the MMA issuer, which polls several
+// barriers in turn and must not sleep on one while another is ready.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Probe with a suspend-time hint: a thread whose phase is not complete sleeps in
 // hardware until the phase completes or `hint_ns` passes, instead of spinning and
 // taking issue slots from the warps that do the work.
