@@ -53,13 +53,13 @@ def _defines():
     EX19_SOFTMAX_F2 (paired fp32 FMA / adds in the softmax; default 1),
     EX19_MAX3 (3-input max instruction in the row max; default 0),
     EX19_SUSPEND_NS (sleep hint of the mbarrier polls in ns; default 1e6, 0 = none),
-    EX19_MMA_IDLE_NS (nanosleep of the MMA issuer after an idle poll round; default 0),
-    EX19_MMA_EVENT (d = 64 fp16 event-driven MMA issue instead of a fixed order; default 0),
-    EX19_TRACE (CTA 0 records a clock64 timeline of its first unit in the workspace; default 0)."""
+    EX19_TRACE (CTA 0 records a clock64 timeline of its first unit in the workspace; default 0),
+    EX19_ONEPASS (the softmax reads S from TMEM once instead of twice; default 1),
+    EX19_SPIN (bounded waits spin on mbarrier.test_wait instead of try_wait; default 0)."""
     out = []
     for name in ("EX19_POLY_PAIRS", "EX19_SEPARATE_P", "EX19_SOFTMAX_F2", "EX19_MAX3",
-                 "EX19_SUSPEND_NS", "EX19_MMA_IDLE_NS", "EX19_MMA_EVENT",
-                 "EX19_TRACE"):
+                 "EX19_SUSPEND_NS",
+                 "EX19_TRACE", "EX19_ONEPASS", "EX19_SPIN"):
         if os.environ.get(name):
             out.append("-D%s=%d" % (name, int(os.environ[name])))
     return out

@@ -58,11 +58,8 @@ constexpr float kRescaleThreshold = 8.0f;
 #ifndef EX19_TRACE
 #define EX19_TRACE 0  // 1: CTA 0 stamps clock64 at each step of its first unit (debug)
 #endif
-#ifndef EX19_MMA_EVENT
-#define EX19_MMA_EVENT 0  // d = 64 fp16: event-driven MMA issue (1) or fixed order per block (0)
-#endif
-#ifndef EX19_MMA_IDLE_NS
-#define EX19_MMA_IDLE_NS 0  // nanosleep of the MMA issuer after a poll round with no progress
+#ifndef EX19_ONEPASS
+#define EX19_ONEPASS 1  // S read from TMEM once (1) or twice, max then exponentials (0)
 #endif
 #ifndef EX19_MAX3
 #define EX19_MAX3 0  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
@@ -76,7 +73,7 @@ enum : uint32_t {
   kSiteProdEmpty = 0x10001, kSiteProdQFree = 0x10002,
   kSiteMmaQFull = 0x20001, kSiteMmaKFull = 0x20002, kSiteMmaVFull = 0x20003,
   kSiteMmaPFull = 0x20004, kSiteMmaOFree = 0x20005, kSiteMmaDrain = 0x20006,
-  kSiteMmaSFree = 0x20007, kSiteMmaPoll = 0x20008,
+  kSiteMmaSFree = 0x20007,
   kSiteSmxSFull = 0x30001, kSiteSmxOFull = 0x30002, kSiteSmxPvDone = 0x30003,
   kSiteDrainLoads = 0x40001,
 };
@@ -354,311 +351,177 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kBN, false);
-      constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, kBM, D, true);
-      uint32_t it = 0, q_cnt = 0;
-      uint32_t p_cnt[kTilesPerUnit] = {0, 0};
-      uint32_t o_cnt[kTilesPerUnit] = {0, 0};
-      uint32_t ns[kTilesPerUnit] = {0, 0};  // S MMAs issued per tile (separate-P order)
-      bool ok = true;
-      Unit u;
-      for (int k = 0; ok && unit_of(p, k, u); ++k) {
-        wc.unit = k;
-        ok = mbar_wait_bounded(bar_q_full, q_cnt & 1u, wc, kSiteMmaQFull);
-        ++q_cnt;
-        if (!ok) break;
-        tc_fence_after();
-        if constexpr (kSeparateP) {
-#if EX19_MMA_EVENT
-          // Event-driven issue: each tile advances on its own. S_t(j) goes out as
-          // soon as K_j has landed and the tile's softmax has read S_t(j-1)
-          // (s_free); O_t += P_t(j)·V_j as soon as V_j has landed and P_t(j) is
-          // written (p_full). A K/V slot is released once every tile that uses its
-          // block has issued the MMA that reads it. S, P and O live in separate
-          // TMEM columns, so S_t(j+1) overlaps the softmax of block j, and one
-          // tile's softmax never waits for the other tile's.
-          const uint32_t it0 = it;
-          bool first_pv[kTilesPerUnit] = {true, true};
-          int s_next[kTilesPerUnit], pv_next[kTilesPerUnit], t_end[kTilesPerUnit];
+    // The whole warp runs the issue loop with warp-uniform control flow and
+    // waits (so addresses and descriptors sit in uniform registers); one lane,
+    // picked by elect.sync, issues each tcgen05 instruction.
+    constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kBN, false);
+    constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, kBM, D, true);
+    // Descriptor bases. The start-address field holds (address >> 4) in its low
+    // 14 bits; every operand address is below 256 KiB, so adding (offset >> 4)
+    // to a base never carries out of that field.
+    const uint64_t dq = sdesc_sw128(sQ, 16, 1024);               // Q tiles, K-major
+    const uint64_t dk = sdesc_sw128(sKV, 16, 1024);              // K slots, K-major
+    const uint64_t dv = sdesc_sw128(sKV, G::kChunkBytes, 1024);  // V slots, MN-major
+    uint32_t it = 0, q_cnt = 0;
+    uint32_t p_cnt[kTilesPerUnit] = {0, 0};
+    uint32_t o_cnt[kTilesPerUnit] = {0, 0};
+    uint32_t ns[kTilesPerUnit] = {0, 0};  // S MMAs issued per tile
+    bool ok = true;
+    Unit u;
+    auto slot_of = [&](uint32_t idx) { return idx % S; };
+    auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
+    // S_t = Q_t · K_jᵀ from K slot `slot` (D/16 MMAs of K = 16), then commit s_full.
+    auto issue_s = [&](const int t, uint32_t slot) __attribute__((always_inline)) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+        mma_ss_elect(tmem_base + kColS0 + kStrideS * t,
+                     dq + ((t * G::kTileBytes + off) >> 4),
+                     dk + ((slot * G::kTileBytes + off) >> 4), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(bar_s_full(t));
+      ++ns[t];
+    };
+    // O_t (+)= P_t · V_j from V slot `slot`. 16 keys per MMA: 8 TMEM columns of
+    // packed P, 16 rows (2 KiB) of V. Split P keeps each 64-key half as
+    // [hi 32 columns | lo 32 columns].
+    auto issue_pv = [&](const int t, uint32_t slot, bool first) __attribute__((always_inline)) {
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
+        mma_ts_elect(tmem_base + kColO0 + kStrideO * t, tmem_base + kColP0 + kStrideP * t + pcol,
+                     dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o,
+                     (first && kk == 0) ? 0u : 1u);
+      }
+      if constexpr (kSplitP) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t pcol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
+          mma_ts_elect(tmem_base + kColO0 + kStrideO * t, tmem_base + kColP0 + kStrideP * t + pcol,
+                       dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o, 1u);
+        }
+      }
+    };
+    for (int k = 0; ok && unit_of(p, k, u); ++k) {
+      wc.unit = k;
+      ok = mbar_wait_warp(bar_q_full, q_cnt & 1u, wc, kSiteMmaQFull);
+      ++q_cnt;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t it0 = it;
+      bool first_pv[kTilesPerUnit] = {true, true};
+      if constexpr (kSeparateP) {
+        // Per block j: S_t(j+1) for both tiles as soon as each tile's softmax has
+        // read S_t(j) (s_free), then O_t += P_t(j)·V_j as each P_t(j) lands.
+        // S, P and O live in separate TMEM columns, so S(j+1) overlaps the
+        // softmax of block j.
+        auto s_for_block = [&](int j) __attribute__((always_inline)) -> bool {
+          const uint32_t kidx = it0 + 2u * (j - u.lo);
+          if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull))
+            return false;
 #pragma unroll
           for (int t = 0; t < kTilesPerUnit; ++t) {
-            const bool live = u.t[t].lo < u.t[t].hi;
-            s_next[t] = pv_next[t] = live ? u.t[t].lo : u.lo;
-            t_end[t] = live ? u.t[t].hi : u.lo;
-          }
-          auto slot_of = [&](uint32_t idx) { return idx % S; };
-          auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
-          int k_rel = u.lo, v_rel = u.lo;  // next blocks whose K / V slot is released
-          bool idle = false;
-          uint64_t idle_since = 0;
-          while (true) {
-            bool progress = false;
-#pragma unroll
-            for (int t = 0; t < kTilesPerUnit; ++t) {
-              if (s_next[t] < t_end[t]) {
-                const int j = s_next[t];
-                const uint32_t kidx = it0 + 2u * (j - u.lo);
-                if (mbar_poll(bar_full(slot_of(kidx)), par_of(kidx)) &&
-                    (ns[t] == 0 || mbar_poll(bar_s_free(t), (ns[t] - 1) & 1u))) {
-                  tc_fence_after();
-                  const uint32_t q_addr = sQ + t * G::kTileBytes;
-                  const uint32_t k_addr = sKV + slot_of(kidx) * G::kTileBytes;
-#pragma unroll
-                  for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem_base + kColS0 + kStrideS * t, sdesc_sw128(q_addr + off, 16, 1024),
-                           sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                  }
-                  mma_commit(bar_s_full(t));
-                  ++ns[t];
-                  ++s_next[t];
-                  progress = true;
-                }
-              }
-              if (pv_next[t] < s_next[t]) {
-                const int j = pv_next[t];
-                const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
-                if (mbar_poll(bar_full(slot_of(vidx)), par_of(vidx)) &&
-                    mbar_poll(bar_p_full(t), p_cnt[t] & 1u) &&
-                    (!first_pv[t] || mbar_poll(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u))) {
-                  tc_fence_after();
-                  const uint32_t v_addr = sKV + slot_of(vidx) * G::kTileBytes;
-#pragma unroll
-                  for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
-                    mma_ts(tmem_base + kColO0 + kStrideO * t,
-                           tmem_base + kColP0 + kStrideP * t + kk * 8, bdesc, idesc_o,
-                           (first_pv[t] && kk == 0) ? 0u : 1u);
-                  }
-                  mma_commit(bar_pv_done(t));
-                  ++p_cnt[t];
-                  first_pv[t] = false;
-                  ++pv_next[t];
-                  if (pv_next[t] == t_end[t]) {
-                    mma_commit(bar_o_full(t));  // tile t's last block of this unit
-                    ++o_cnt[t];
-                  }
-                  progress = true;
-                }
-              }
-            }
-            while (k_rel < u.hi && (!has_block(u.t[0], k_rel) || s_next[0] > k_rel) &&
-                   (!has_block(u.t[1], k_rel) || s_next[1] > k_rel)) {
-              mma_commit(bar_empty(slot_of(it0 + 2u * (k_rel - u.lo))));
-              ++k_rel;
-            }
-            while (v_rel < u.hi && (!has_block(u.t[0], v_rel) || pv_next[0] > v_rel) &&
-                   (!has_block(u.t[1], v_rel) || pv_next[1] > v_rel)) {
-              mma_commit(bar_empty(slot_of(it0 + 2u * (v_rel - u.lo) + 1u)));
-              ++v_rel;
-            }
-            if (pv_next[0] == t_end[0] && pv_next[1] == t_end[1] && v_rel == u.hi) break;
-            if (progress) {
-              idle = false;
-              continue;
-            }
-            if (*abort_flag) {
-              ok = false;
-              break;
-            }
-            if (EX19_MMA_IDLE_NS > 0) __nanosleep(EX19_MMA_IDLE_NS);  // yield issue slots
-            const uint64_t now = globaltimer_ns();
-            if (!idle) {
-              idle = true;
-              idle_since = now;
-            } else if (now - idle_since > wc.limit_ns) {
-              record_error(wc, kStatusTimeout, kSiteMmaPoll);
-              ok = false;
-              break;
-            }
-          }
-#else
-          // Issue order per block j: S_t(j+1) for both tiles as soon as each tile's
-          // softmax has read S_t(j), then O_t += P_t(j)·V_j as each P_t(j) lands.
-          // S, P and O live in separate TMEM columns, so S(j+1) overlaps the
-          // softmax of block j.
-          const uint32_t it0 = it;
-          bool first_pv[kTilesPerUnit] = {true, true};
-          auto slot_of = [&](uint32_t idx) { return idx % S; };
-          auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
-          auto issue_s = [&](const int t, int j) __attribute__((always_inline)) -> bool {
+            if (!has_block(u.t[t], j)) continue;
             if (ns[t] > 0 &&
-                !mbar_wait_bounded(bar_s_free(t), (ns[t] - 1) & 1u, wc, kSiteMmaSFree))
+                !mbar_wait_warp(bar_s_free(t), (ns[t] - 1) & 1u, wc, kSiteMmaSFree))
               return false;
             tc_fence_after();
-            const uint32_t kidx = it0 + 2u * (j - u.lo);
-            const uint32_t q_addr = sQ + t * G::kTileBytes;
-            const uint32_t k_addr = sKV + slot_of(kidx) * G::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-              mma_ss(tmem_base + kColS0 + kStrideS * t, sdesc_sw128(q_addr + off, 16, 1024),
-                     sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bar_s_full(t));
-            ++ns[t];
-            return true;
-          };
-          auto issue_pv2 = [&](const int t, int j) __attribute__((always_inline)) -> bool {
-            if (!mbar_wait_bounded(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull)) return false;
-            ++p_cnt[t];
-            if (first_pv[t] &&
-                !mbar_wait_bounded(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree))
-              return false;
-            tc_fence_after();
-            const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
-            const uint32_t v_addr = sKV + slot_of(vidx) * G::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
-              mma_ts(tmem_base + kColO0 + kStrideO * t, tmem_base + kColP0 + kStrideP * t + kk * 8,
-                     bdesc, idesc_o, (first_pv[t] && kk == 0) ? 0u : 1u);
-            }
-            mma_commit(bar_pv_done(t));
-            first_pv[t] = false;
-            return true;
-          };
-          {  // S of the first block
-            const uint32_t kidx = it0;
-            ok = mbar_wait_bounded(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
-            tc_fence_after();
-#pragma unroll
-            for (int t = 0; t < kTilesPerUnit; ++t)
-              if (ok && has_block(u.t[t], u.lo)) ok = issue_s(t, u.lo);
-            if (ok) mma_commit(bar_empty(slot_of(kidx)));
+            issue_s(t, slot_of(kidx));
           }
-          for (int j = u.lo; ok && j < u.hi; ++j) {
-            trace_mark(p, 2, k, j - u.lo, 0);
-            if (j + 1 < u.hi) {
-              const uint32_t kidx = it0 + 2u * (j + 1 - u.lo);
-              ok = mbar_wait_bounded(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
-              tc_fence_after();
-#pragma unroll
-              for (int t = 0; t < kTilesPerUnit; ++t)
-                if (ok && has_block(u.t[t], j + 1)) ok = issue_s(t, j + 1);
-              if (!ok) break;
-              mma_commit(bar_empty(slot_of(kidx)));
-            }
-            trace_mark(p, 2, k, j - u.lo, 1);
-            const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
-            ok = mbar_wait_bounded(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull);
-            trace_mark(p, 2, k, j - u.lo, 2);
-#pragma unroll
-            for (int t = 0; t < kTilesPerUnit; ++t) {
-              if (ok && has_block(u.t[t], j)) {
-                ok = issue_pv2(t, j);
-                trace_mark(p, 2, k, j - u.lo, 3 + t);
-                if (ok && j == u.t[t].hi - 1) {
-                  mma_commit(bar_o_full(t));  // tile t's last block of this unit
-                  ++o_cnt[t];
-                }
-              }
-            }
-            if (!ok) break;
-            mma_commit(bar_empty(slot_of(vidx)));
-          }
-#endif
-          if (!ok) break;
-          it = it0 + 2u * (u.hi - u.lo);
-          mma_commit(bar_q_free);
-          continue;
-        }
-        int pend[kTilesPerUnit] = {-1, -1};          // block whose S_t waits for its P·V
-        uint32_t pend_vslot[kTilesPerUnit] = {0, 0};
-        uint32_t pend_vpar[kTilesPerUnit] = {0, 0};
-        bool first_pv[kTilesPerUnit] = {true, true};
-        uint32_t prev_vslot = 0;
-        bool have_prev_v = false;
-
-        // O_t (+)= P_t · V for the pending block of tile t.
-        auto issue_pv = [&](const int t) __attribute__((always_inline)) -> bool {
-          if (!mbar_wait_bounded(bar_full(pend_vslot[t]), pend_vpar[t], wc, kSiteMmaVFull))
-            return false;
-          if (!mbar_wait_bounded(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull)) return false;
-          ++p_cnt[t];
-          if (first_pv[t]) {
-            if (!mbar_wait_bounded(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree))
-              return false;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + kColO0 + kStrideO * t;
-          const uint32_t p_tmem = tmem_base + kColP0 + kStrideP * t;
-          const uint32_t v_addr = sKV + pend_vslot[t] * G::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            // 16 keys per MMA: 8 TMEM columns of packed P, 16 rows (2 KiB) of V.
-            // Split P keeps each 64-key half as [hi 32 columns | lo 32 columns].
-            const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
-            const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
-            mma_ts(d_tmem, p_tmem + pcol, bdesc, idesc_o, (first_pv[t] && kk == 0) ? 0u : 1u);
-          }
-          if (kSplitP) {
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint32_t pcol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
-              const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, G::kChunkBytes, 1024);
-              mma_ts(d_tmem, p_tmem + pcol, bdesc, idesc_o, 1u);
-            }
-          }
-          first_pv[t] = false;
-          pend[t] = -1;
+          mma_commit_elect(bar_empty(slot_of(kidx)));
           return true;
         };
-
+        ok = s_for_block(u.lo);
         for (int j = u.lo; ok && j < u.hi; ++j) {
-          const uint32_t kslot = it % S, kpar = (it / S) & 1u;
-          ++it;
-          const uint32_t vslot = it % S, vpar = (it / S) & 1u;
-          ++it;
-          ok = mbar_wait_bounded(bar_full(kslot), kpar, wc, kSiteMmaKFull);
-          if (!ok) break;
-          tc_fence_after();
+          trace_mark(p, 2, k, j - u.lo, 0);
+          if (j + 1 < u.hi && !(ok = s_for_block(j + 1))) break;
+          trace_mark(p, 2, k, j - u.lo, 1);
+          const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
+          ok = mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull);
+          trace_mark(p, 2, k, j - u.lo, 2);
 #pragma unroll
           for (int t = 0; t < kTilesPerUnit; ++t) {
-            const bool flushed = pend[t] >= 0;
-            if (flushed && !(ok = issue_pv(t))) break;
-            if (has_block(u.t[t], j)) {
-              // S_t = Q_t · K_jᵀ  (D/16 MMAs of K = 16)
-              const uint32_t q_addr = sQ + t * G::kTileBytes;
-              const uint32_t k_addr = sKV + kslot * G::kTileBytes;
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-                mma_ss(tmem_base + kColS0 + kStrideS * t, sdesc_sw128(q_addr + off, 16, 1024),
-                       sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(bar_s_full(t));
-              pend[t] = j;
-              pend_vslot[t] = vslot;
-              pend_vpar[t] = vpar;
-            } else if (flushed) {
-              mma_commit(bar_o_full(t));  // that was tile t's last block
+            if (!ok || !has_block(u.t[t], j)) continue;
+            ok = mbar_wait_warp(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull);
+            ++p_cnt[t];
+            if (ok && first_pv[t])
+              ok = mbar_wait_warp(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, slot_of(vidx), first_pv[t]);
+            mma_commit_elect(bar_pv_done(t));
+            first_pv[t] = false;
+            trace_mark(p, 2, k, j - u.lo, 3 + t);
+            if (j == u.t[t].hi - 1) {
+              mma_commit_elect(bar_o_full(t));  // tile t's last block of this unit
               ++o_cnt[t];
             }
           }
           if (!ok) break;
-          mma_commit(bar_empty(kslot));
-          if (have_prev_v) mma_commit(bar_empty(prev_vslot));
-          prev_vslot = vslot;
-          have_prev_v = true;
+          mma_commit_elect(bar_empty(slot_of(vidx)));
+        }
+      } else {
+        // P over S: per block j the order PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).
+        // tcgen05 MMAs execute in issue order, so S_t(j) (which overwrites the
+        // columns holding P_t) never overtakes PV_t(j-1).
+        int pend[kTilesPerUnit] = {-1, -1};  // block whose S_t waits for its P·V
+        uint32_t pend_vslot[kTilesPerUnit] = {0, 0};
+        auto flush_pv = [&](const int t) __attribute__((always_inline)) -> bool {
+          const uint32_t vidx = it0 + 2u * (pend[t] - u.lo) + 1u;
+          if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull))
+            return false;
+          if (!mbar_wait_warp(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull)) return false;
+          ++p_cnt[t];
+          if (first_pv[t] &&
+              !mbar_wait_warp(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree))
+            return false;
+          tc_fence_after();
+          issue_pv(t, slot_of(vidx), first_pv[t]);
+          first_pv[t] = false;
+          pend[t] = -1;
+          return true;
+        };
+        for (int j = u.lo; ok && j < u.hi; ++j) {
+          const uint32_t kidx = it0 + 2u * (j - u.lo);
+          const uint32_t vidx = kidx + 1u;
+          ok = mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < kTilesPerUnit; ++t) {
+            if (!ok) break;
+            const bool flushed = pend[t] >= 0;
+            if (flushed && !(ok = flush_pv(t))) break;
+            if (has_block(u.t[t], j)) {
+              issue_s(t, slot_of(kidx));
+              pend[t] = j;
+            } else if (flushed) {
+              mma_commit_elect(bar_o_full(t));  // that was tile t's last block
+              ++o_cnt[t];
+            }
+          }
+          if (!ok) break;
+          mma_commit_elect(bar_empty(slot_of(kidx)));
+          if (j > u.lo) mma_commit_elect(bar_empty(slot_of(vidx - 2u)));  // V_{j-1}
+          (void)vidx;
         }
 #pragma unroll
         for (int t = 0; t < kTilesPerUnit; ++t) {
           if (ok && pend[t] >= 0) {
-            if (!(ok = issue_pv(t))) break;
-            mma_commit(bar_o_full(t));
+            if (!(ok = flush_pv(t))) break;
+            mma_commit_elect(bar_o_full(t));
             ++o_cnt[t];
           }
         }
-        if (!ok) break;
-        if (have_prev_v) mma_commit(bar_empty(prev_vslot));
-        mma_commit(bar_q_free);
+        if (ok) mma_commit_elect(bar_empty(slot_of(it0 + 2u * (u.hi - 1 - u.lo) + 1u)));
       }
-      // Every MMA this thread issued has finished once the drain barrier flips.
-      mma_commit(bar_drain);
-      mbar_wait_drain(bar_drain, 0, wc, kSiteMmaDrain);
+      if (!ok) break;
+      it = it0 + 2u * (u.hi - u.lo);
+      mma_commit_elect(bar_q_free);
     }
+    // Every MMA this warp issued has finished once the drain barrier flips.
+    mma_commit_elect(bar_drain);
+    mbar_wait_drain(bar_drain, 0, wc, kSiteMmaDrain);
   } else {
     // -------------------------------------------------------- softmax warps
     const int t = warp >> 2;
@@ -710,6 +573,108 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exponentials, which keeps the live registers of a thread well under 168.
         auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
           constexpr bool M = decltype(masked_tag)::value;
+#if EX19_ONEPASS
+          // One TMEM read of S (128 columns). S is released right away, the row
+          // maximum and the exponentials both work from these registers.
+          uint32_t sr[128];
+          tmem_ld_x128(tS, sr);
+          if (tr) trace_mark(p, t, k, jr, 2);
+          if constexpr (kSeparateP) {  // S is in registers: the next S MMA may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar_s_free(t));
+          }
+          if constexpr (M) {  // masked keys: -inf for the max (+inf for the min), p = 0 below
+            const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c < vis_lo || c >= vis_hi) sr[c] = fill;
+          }
+          float mx;  // max over visible columns of ±s (the sign of the scale)
+          {
+            float sv[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
+            if (neg)
+              mx = -row_min128(sv);
+            else
+              mx = row_max128(sv);
+          }
+          if (tr) trace_mark(p, t, k, jr, 3);
+          const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
+          if (bm > m_ref + kRescaleThreshold) {
+            alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
+            m_ref = bm;
+            rescale = true;
+          }
+          const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+          if constexpr (kSeparateP) {
+            // P_t and O_t are read by this tile's previous P·V: wait until it is done.
+            if (s_cnt > 0) {
+              if (!mbar_wait_warp(bar_pv_done(t), (s_cnt - 1) & 1u, wc, kSiteSmxPvDone)) {
+                stop = true;
+                return;
+              }
+              tc_fence_after();
+            }
+          }
+          if (tr) trace_mark(p, t, k, jr, 4);
+#if EX19_SOFTMAX_F2
+          const float2 c2 = make_float2(Cs, Cs);
+          const float2 nmu2 = make_float2(-mu, -mu);
+          float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#else
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+#endif
+          // P in 32-column chunks of 16 packed registers, stored to TMEM (P hi at
+          // column c/2 of the P region; split P keeps each 64-key half h as
+          // [hi 32 columns | lo 32 columns] at column 64h).
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t pk[16];
+            uint32_t pk_lo[16];
+#pragma unroll
+            for (int c = c0; c < c0 + 32; c += 2) {
+#if EX19_SOFTMAX_F2
+              const float2 x = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nmu2);
+              const float x0 = x.x, x1 = x.y;
+#else
+              const float x0 = fmaf(__uint_as_float(sr[c]), Cs, -mu);
+              const float x1 = fmaf(__uint_as_float(sr[c + 1]), Cs, -mu);
+#endif
+              float p0, p1;
+              if (kPolyPairs > 0 && ((c >> 1) & 7) < kPolyPairs) {
+                exp2_poly_pair(x0, x1, p0, p1);  // on the FMA/ALU pipes
+              } else {
+                p0 = ex2_approx(x0);  // on MUFU
+                p1 = ex2_approx(x1);
+              }
+              if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
+                p0 = (c >= vis_lo && c < vis_hi) ? p0 : 0.f;
+                p1 = (c + 1 >= vis_lo && c + 1 < vis_hi) ? p1 : 0.f;
+              }
+#if EX19_SOFTMAX_F2
+              acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
+#else
+              acc[c & 3] += p0;
+              acc[(c + 1) & 3] += p1;
+#endif
+              const uint32_t hi = pack2(p0, p1, BF16);
+              pk[(c - c0) >> 1] = hi;
+              if constexpr (kSplitP)
+                pk_lo[(c - c0) >> 1] =
+                    pack2(p0 - low_as_float(hi, BF16), p1 - high_as_float(hi, BF16), BF16);
+            }
+            if constexpr (kSplitP) {
+              const int h = c0 >> 6, cl = c0 & 63;
+              tmem_st_x16(tP + 64 * h + (cl >> 1), pk);
+              tmem_st_x16(tP + 64 * h + 32 + (cl >> 1), pk_lo);
+            } else {
+              tmem_st_x16(tP + (c0 >> 1), pk);
+            }
+            if (tr && (c0 & 32)) trace_mark(p, t, k, jr, 5 + (c0 >> 6));
+          }
+#else
           float mx;  // max over visible columns of Cs·s / C (i.e. of ±s)
           {
             float m8[8];
@@ -824,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (tr) trace_mark(p, t, k, jr, 6 + 2 * h);
           }
+#endif
 #if EX19_SOFTMAX_F2
           const float rowsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
 #else

@@ -76,6 +76,9 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
 // Probe with a suspend-time hint: a thread whose phase is not complete sleeps in
 // hardware until the phase completes or `hint_ns` passes, instead of spinning and
 // taking issue slots from the warps that do the work.
+#ifndef EX19_SPIN
+#define EX19_SPIN 0  // 1: bounded waits spin on the non-blocking test instead of try_wait
+#endif
 #ifndef EX19_SUSPEND_NS
 #define EX19_SUSPEND_NS 1000000  // 1 ms: also the worst-case reaction time to an abort (0: no hint)
 #endif
@@ -121,7 +124,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
                                             uint32_t where, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
+#if EX19_SPIN
+    if (mbar_poll(bar, parity)) return true;  // pure spin: no suspension at all
+#else
     if (mbar_test_sleep(bar, parity)) return true;
+#endif
     if (honor_abort && *c.abort_flag) return false;
     if (globaltimer_ns() - t0 > c.limit_ns) {
       record_error(c, kStatusTimeout, where);
@@ -215,6 +222,38 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective forms: the whole warp calls them convergently (so operands can
+// sit in uniform registers) and one lane, picked by elect.sync, issues.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
