@@ -46,6 +46,7 @@ L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_BY_SOURCE = {
     "57cbef3a389c5a7c": 883_172_096 + 68_679_424,  # first tcgen05 version
     "73ba059d1a6a1b4f": 893_060_352 + 65_744_896,  # separate P region, two-pass softmax
+    "5aba853594b2cccb": 853_388_288 + 62_159_616,  # per-tile MMA warps, packed fp16 exps
 }
 
 

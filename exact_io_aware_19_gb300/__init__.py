@@ -67,7 +67,7 @@ def _bind(lib):
     lib.attn_debug_wait_probe.restype = i
     lib.attn_debug_wait_probe.argtypes = [p, sz, ctypes.c_uint64, p]
     lib.attn_debug_exp2.restype = i
-    lib.attn_debug_exp2.argtypes = [p, p, p, i, p]
+    lib.attn_debug_exp2.argtypes = [p, p, p, p, i, p]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i]
     lib.attn_last_error_detail.restype = ctypes.c_char_p
@@ -200,14 +200,17 @@ def set_wait_limit_ns(limit_ns: int) -> None:
     load_library().attn_set_wait_limit_ns(int(limit_ns))
 
 
-def debug_exp2(x: torch.Tensor):
-    """(2^x by the kernel's polynomial path, 2^x by MUFU ex2) for a CUDA float32 tensor."""
+def debug_exp2(x: torch.Tensor, with_f16: bool = False):
+    """2^x by the kernel's polynomial path and by MUFU ex2 (and, with ``with_f16``, by
+    the packed fp16 MUFU path) for a CUDA float32 tensor."""
     lib = load_library()
     x = x.contiguous()
     yp, ym = torch.empty_like(x), torch.empty_like(x)
-    _check(lib.attn_debug_exp2(x.data_ptr(), yp.data_ptr(), ym.data_ptr(), x.numel(),
+    yh = torch.empty_like(x) if with_f16 else None
+    _check(lib.attn_debug_exp2(x.data_ptr(), yp.data_ptr(), ym.data_ptr(),
+                               yh.data_ptr() if yh is not None else None, x.numel(),
                                _stream_handle(None)))
-    return yp, ym
+    return (yp, ym, yh) if with_f16 else (yp, ym)
 
 
 def debug_wait_probe(workspace: torch.Tensor, limit_ns: int, stream=None) -> None:

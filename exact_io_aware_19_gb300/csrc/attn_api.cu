@@ -286,7 +286,8 @@ attn_status_t attn_debug_wait_probe(void* workspace, size_t workspace_bytes, uin
   return ATTN_OK;
 }
 
-attn_status_t attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, void* stream) {
+attn_status_t attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
+                              void* stream) {
   g_detail.clear();
   if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be >= 0");
   if (n == 0) return ATTN_OK;
@@ -299,11 +300,12 @@ attn_status_t attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int 
   if (info.major != 10 || info.minor != 3)
     return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300)");
   std::string why;
-  const void* ptrs[3] = {x, y_poly, y_mufu};
-  const char* names[3] = {"x", "y_poly", "y_mufu"};
-  for (int i = 0; i < 3; ++i)
-    if (!is_device_ptr(ptrs[i], dev, &why, names[i])) return fail(ATTN_ERR_INVALID_ARG, why);
-  e = ex19::launch_exp2_probe(x, y_poly, y_mufu, n, static_cast<cudaStream_t>(stream));
+  const void* ptrs[4] = {x, y_poly, y_mufu, y_f16};
+  const char* names[4] = {"x", "y_poly", "y_mufu", "y_f16"};
+  for (int i = 0; i < 4; ++i)
+    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
+      return fail(ATTN_ERR_INVALID_ARG, why);
+  e = ex19::launch_exp2_probe(x, y_poly, y_mufu, y_f16, n, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("exp2 probe launch", e);
   return ATTN_OK;
 }

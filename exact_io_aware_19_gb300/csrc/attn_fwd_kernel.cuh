@@ -44,9 +44,9 @@ constexpr int kBM = 128;             // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;             // keys per K/V block
 constexpr int kTilesPerUnit = 2;     // query tiles per work unit
 constexpr int kUnitRows = kBM * kTilesPerUnit;
-constexpr int kThreads = 320;        // 8 softmax warps + producer warp + MMA warp
+constexpr int kThreads = 352;        // 8 softmax warps + producer warp + 2 MMA warps
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;          // warps 9 and 10: MMA issuers of tile 0 and tile 1
 constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..)
 constexpr float kRescaleThreshold = 8.0f;
 #ifndef EX19_SEPARATE_P
@@ -57,6 +57,9 @@ constexpr float kRescaleThreshold = 8.0f;
 #endif
 #ifndef EX19_TRACE
 #define EX19_TRACE 0  // 1: CTA 0 stamps clock64 at each step of its first unit (debug)
+#endif
+#ifndef EX19_EXP_F16X2
+#define EX19_EXP_F16X2 1  // fp16: exponentials two at a time on packed fp16 arguments
 #endif
 #ifndef EX19_ONEPASS
 #define EX19_ONEPASS 1  // S read from TMEM once (1) or twice, max then exponentials (0)
@@ -228,6 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Of every 8 column pairs, this many take exp2 from the FMA-pipe polynomial
   // instead of MUFU (fp16 only: the bf16 path keeps P to ~16 bits).
   constexpr int kPolyPairs = BF16 ? 0 : EX19_POLY_PAIRS;
+  // Packed fp16 exponentials (fp16 inputs): x is rounded to fp16 before 2^x, so x
+  // must stay small where P is large; the reference max is then moved whenever
+  // the row max grows by more than 2^1 instead of 2^8.
+  constexpr bool kF16Exp = !BF16 && (EX19_EXP_F16X2 != 0);
+  constexpr float kThresh = kF16Exp ? 1.0f : kRescaleThreshold;
   // TMEM columns. With P over S (d = 128, or bf16 whose split P needs 128 columns):
   // S_t = [128t, 128t+128), P_t aliased over S_t, O_t = [256+128t, ...). With a
   // separate P region (d = 64 fp16): S_t = [128t, ...), P_t = [256+64t, 256+64t+64),
@@ -264,17 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), kTilesPerUnit);  // one release per tile
     }
     mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_free, 1);
+    mbar_init(bar_q_free, kTilesPerUnit);
     for (int t = 0; t < kTilesPerUnit; ++t) {
       mbar_init(bar_s_full(t), 1);
       mbar_init(bar_p_full(t), kBM);
       mbar_init(bar_o_full(t), 1);
       mbar_init(bar_o_free(t), kBM);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, kTilesPerUnit);
     for (int t = 0; t < kTilesPerUnit; ++t) {
       mbar_init(bar_s_free(t), kBM);
       mbar_init(bar_pv_done(t), 1);
@@ -349,56 +357,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_cnt > 0) mbar_wait_drain(bar_q_full, (q_cnt - 1) & 1u, wc, kSiteDrainLoads);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------- MMA issuer
-    // The whole warp runs the issue loop with warp-uniform control flow and
-    // waits (so addresses and descriptors sit in uniform registers); one lane,
-    // picked by elect.sync, issues each tcgen05 instruction.
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------------------------------- MMA issuers, one per tile
+    // Each tile has its own issuing warp, so one tile's MMAs never queue behind
+    // the other tile's (tcgen05.mma issue blocks while the tensor core is busy).
+    // The warp runs its loop warp-uniformly; one lane, picked by elect.sync,
+    // issues each tcgen05 instruction.
+    const int t = warp - kMmaWarp;
     constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kBN, false);
     constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, kBM, D, true);
     // Descriptor bases. The start-address field holds (address >> 4) in its low
     // 14 bits; every operand address is below 256 KiB, so adding (offset >> 4)
     // to a base never carries out of that field.
-    const uint64_t dq = sdesc_sw128(sQ, 16, 1024);               // Q tiles, K-major
-    const uint64_t dk = sdesc_sw128(sKV, 16, 1024);              // K slots, K-major
-    const uint64_t dv = sdesc_sw128(sKV, G::kChunkBytes, 1024);  // V slots, MN-major
-    uint32_t it = 0, q_cnt = 0;
-    uint32_t p_cnt[kTilesPerUnit] = {0, 0};
-    uint32_t o_cnt[kTilesPerUnit] = {0, 0};
-    uint32_t ns[kTilesPerUnit] = {0, 0};  // S MMAs issued per tile
+    const uint64_t dq = sdesc_sw128(sQ + t * G::kTileBytes, 16, 1024);  // Q_t, K-major
+    const uint64_t dk = sdesc_sw128(sKV, 16, 1024);                     // K slots, K-major
+    const uint64_t dv = sdesc_sw128(sKV, G::kChunkBytes, 1024);         // V slots, MN-major
+    const uint32_t mS = tmem_base + kColS0 + kStrideS * t;
+    const uint32_t mP = tmem_base + kColP0 + kStrideP * t;
+    const uint32_t mO = tmem_base + kColO0 + kStrideO * t;
+    uint32_t it = 0, q_cnt = 0, p_cnt = 0, o_cnt = 0, ns = 0;
     bool ok = true;
     Unit u;
     auto slot_of = [&](uint32_t idx) { return idx % S; };
     auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
     // S_t = Q_t · K_jᵀ from K slot `slot` (D/16 MMAs of K = 16), then commit s_full.
-    auto issue_s = [&](const int t, uint32_t slot) __attribute__((always_inline)) {
+    auto issue_s = [&](uint32_t slot) __attribute__((always_inline)) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-        mma_ss_elect(tmem_base + kColS0 + kStrideS * t,
-                     dq + ((t * G::kTileBytes + off) >> 4),
-                     dk + ((slot * G::kTileBytes + off) >> 4), idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss_elect(mS, dq + (off >> 4), dk + ((slot * G::kTileBytes + off) >> 4), idesc_s,
+                     kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(bar_s_full(t));
-      ++ns[t];
+      ++ns;
     };
     // O_t (+)= P_t · V_j from V slot `slot`. 16 keys per MMA: 8 TMEM columns of
     // packed P, 16 rows (2 KiB) of V. Split P keeps each 64-key half as
     // [hi 32 columns | lo 32 columns].
-    auto issue_pv = [&](const int t, uint32_t slot, bool first) __attribute__((always_inline)) {
+    auto issue_pv = [&](uint32_t slot, bool first) __attribute__((always_inline)) {
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
         const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
-        mma_ts_elect(tmem_base + kColO0 + kStrideO * t, tmem_base + kColP0 + kStrideP * t + pcol,
-                     dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o,
+        mma_ts_elect(mO, mP + pcol, dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o,
                      (first && kk == 0) ? 0u : 1u);
       }
       if constexpr (kSplitP) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t pcol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
-          mma_ts_elect(tmem_base + kColO0 + kStrideO * t, tmem_base + kColP0 + kStrideP * t + pcol,
-                       dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o, 1u);
+          mma_ts_elect(mO, mP + pcol, dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o, 1u);
         }
       }
     };
@@ -409,117 +416,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t it0 = it;
-      bool first_pv[kTilesPerUnit] = {true, true};
-      if constexpr (kSeparateP) {
-        // Per block j: S_t(j+1) for both tiles as soon as each tile's softmax has
-        // read S_t(j) (s_free), then O_t += P_t(j)·V_j as each P_t(j) lands.
-        // S, P and O live in separate TMEM columns, so S(j+1) overlaps the
-        // softmax of block j.
-        auto s_for_block = [&](int j) __attribute__((always_inline)) -> bool {
-          const uint32_t kidx = it0 + 2u * (j - u.lo);
-          if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull))
-            return false;
+      const TileSpan sp = (t == 0) ? u.t[0] : u.t[1];
+      const bool live = sp.lo < sp.hi;
+      const int j_lo = live ? sp.lo : u.hi, j_hi = live ? sp.hi : u.hi;
+      auto kidx_of = [&](int j) { return it0 + 2u * (j - u.lo); };
+      // Blocks of the unit this tile does not use: release their K and V slots,
+      // but only once each load has landed — that proves the slot's previous
+      // phase (both tiles' releases of its previous load) is complete, so this
+      // release cannot be counted toward the wrong phase.
+      auto skip_block = [&](int j) __attribute__((always_inline)) -> bool {
 #pragma unroll
-          for (int t = 0; t < kTilesPerUnit; ++t) {
-            if (!has_block(u.t[t], j)) continue;
-            if (ns[t] > 0 &&
-                !mbar_wait_warp(bar_s_free(t), (ns[t] - 1) & 1u, wc, kSiteMmaSFree))
+        for (uint32_t kv = 0; kv < 2; ++kv) {
+          const uint32_t idx = kidx_of(j) + kv;
+          if (!mbar_wait_warp(bar_full(slot_of(idx)), par_of(idx), wc, kSiteMmaKFull)) return false;
+          if (lane == 0) mbar_arrive(bar_empty(slot_of(idx)));
+          __syncwarp();
+        }
+        return true;
+      };
+      bool first = true;
+      // O_t (+)= P_t(j) · V_j once P_t(j) is written; releases V_j's slot.
+      auto pv_block = [&](int j) __attribute__((always_inline)) -> bool {
+        const uint32_t vidx = kidx_of(j) + 1u;
+        if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
+        if (!mbar_wait_warp(bar_p_full(t), p_cnt & 1u, wc, kSiteMmaPFull)) return false;
+        ++p_cnt;
+        if (first && !mbar_wait_warp(bar_o_free(t), (o_cnt & 1u) ^ 1u, wc, kSiteMmaOFree))
+          return false;
+        tc_fence_after();
+        issue_pv(slot_of(vidx), first);
+        first = false;
+        if constexpr (kSeparateP) mma_commit_elect(bar_pv_done(t));
+        mma_commit_elect(bar_empty(slot_of(vidx)));
+        return true;
+      };
+      for (int j = u.lo; ok && j < j_lo; ++j) ok = skip_block(j);
+      if (ok && live) {
+        if constexpr (kSeparateP) {
+          // S_t(j+1) as soon as the softmax has read S_t(j) (s_free), then
+          // O_t += P_t(j)·V_j: S, P and O have their own TMEM columns, so
+          // S_t(j+1) overlaps the softmax of block j.
+          auto s_block = [&](int j) __attribute__((always_inline)) -> bool {
+            const uint32_t kidx = kidx_of(j);
+            if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull))
+              return false;
+            if (ns > 0 && !mbar_wait_warp(bar_s_free(t), (ns - 1) & 1u, wc, kSiteMmaSFree))
               return false;
             tc_fence_after();
-            issue_s(t, slot_of(kidx));
+            issue_s(slot_of(kidx));
+            mma_commit_elect(bar_empty(slot_of(kidx)));
+            return true;
+          };
+          ok = s_block(j_lo);
+          for (int j = j_lo; ok && j < j_hi; ++j) {
+            if (t == 0) trace_mark(p, 2, k, j - u.lo, 0);
+            if (j + 1 < j_hi && !(ok = s_block(j + 1))) break;
+            if (t == 0) trace_mark(p, 2, k, j - u.lo, 1);
+            ok = pv_block(j);
+            if (t == 0) trace_mark(p, 2, k, j - u.lo, 3);
           }
-          mma_commit_elect(bar_empty(slot_of(kidx)));
-          return true;
-        };
-        ok = s_for_block(u.lo);
-        for (int j = u.lo; ok && j < u.hi; ++j) {
-          trace_mark(p, 2, k, j - u.lo, 0);
-          if (j + 1 < u.hi && !(ok = s_for_block(j + 1))) break;
-          trace_mark(p, 2, k, j - u.lo, 1);
-          const uint32_t vidx = it0 + 2u * (j - u.lo) + 1u;
-          ok = mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull);
-          trace_mark(p, 2, k, j - u.lo, 2);
-#pragma unroll
-          for (int t = 0; t < kTilesPerUnit; ++t) {
-            if (!ok || !has_block(u.t[t], j)) continue;
-            ok = mbar_wait_warp(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull);
-            ++p_cnt[t];
-            if (ok && first_pv[t])
-              ok = mbar_wait_warp(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree);
+        } else {
+          // P over S: PV_t(j-1) is issued before S_t(j), which overwrites the
+          // columns holding P_t; tcgen05 MMAs of one thread run in issue order.
+          for (int j = j_lo; ok && j < j_hi; ++j) {
+            const uint32_t kidx = kidx_of(j);
+            ok = mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
+            if (ok && j > j_lo) ok = pv_block(j - 1);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, slot_of(vidx), first_pv[t]);
-            mma_commit_elect(bar_pv_done(t));
-            first_pv[t] = false;
-            trace_mark(p, 2, k, j - u.lo, 3 + t);
-            if (j == u.t[t].hi - 1) {
-              mma_commit_elect(bar_o_full(t));  // tile t's last block of this unit
-              ++o_cnt[t];
-            }
+            issue_s(slot_of(kidx));
+            mma_commit_elect(bar_empty(slot_of(kidx)));
           }
-          if (!ok) break;
-          mma_commit_elect(bar_empty(slot_of(vidx)));
+          if (ok) ok = pv_block(j_hi - 1);
         }
-      } else {
-        // P over S: per block j the order PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).
-        // tcgen05 MMAs execute in issue order, so S_t(j) (which overwrites the
-        // columns holding P_t) never overtakes PV_t(j-1).
-        int pend[kTilesPerUnit] = {-1, -1};  // block whose S_t waits for its P·V
-        uint32_t pend_vslot[kTilesPerUnit] = {0, 0};
-        auto flush_pv = [&](const int t) __attribute__((always_inline)) -> bool {
-          const uint32_t vidx = it0 + 2u * (pend[t] - u.lo) + 1u;
-          if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull))
-            return false;
-          if (!mbar_wait_warp(bar_p_full(t), p_cnt[t] & 1u, wc, kSiteMmaPFull)) return false;
-          ++p_cnt[t];
-          if (first_pv[t] &&
-              !mbar_wait_warp(bar_o_free(t), (o_cnt[t] & 1u) ^ 1u, wc, kSiteMmaOFree))
-            return false;
-          tc_fence_after();
-          issue_pv(t, slot_of(vidx), first_pv[t]);
-          first_pv[t] = false;
-          pend[t] = -1;
-          return true;
-        };
-        for (int j = u.lo; ok && j < u.hi; ++j) {
-          const uint32_t kidx = it0 + 2u * (j - u.lo);
-          const uint32_t vidx = kidx + 1u;
-          ok = mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < kTilesPerUnit; ++t) {
-            if (!ok) break;
-            const bool flushed = pend[t] >= 0;
-            if (flushed && !(ok = flush_pv(t))) break;
-            if (has_block(u.t[t], j)) {
-              issue_s(t, slot_of(kidx));
-              pend[t] = j;
-            } else if (flushed) {
-              mma_commit_elect(bar_o_full(t));  // that was tile t's last block
-              ++o_cnt[t];
-            }
-          }
-          if (!ok) break;
-          mma_commit_elect(bar_empty(slot_of(kidx)));
-          if (j > u.lo) mma_commit_elect(bar_empty(slot_of(vidx - 2u)));  // V_{j-1}
-          (void)vidx;
+        if (ok) {
+          mma_commit_elect(bar_o_full(t));  // the tile's last P·V of this unit
+          ++o_cnt;
         }
-#pragma unroll
-        for (int t = 0; t < kTilesPerUnit; ++t) {
-          if (ok && pend[t] >= 0) {
-            if (!(ok = flush_pv(t))) break;
-            mma_commit_elect(bar_o_full(t));
-            ++o_cnt[t];
-          }
-        }
-        if (ok) mma_commit_elect(bar_empty(slot_of(it0 + 2u * (u.hi - 1 - u.lo) + 1u)));
       }
+      for (int j = j_hi; ok && j < u.hi; ++j) ok = skip_block(j);
       if (!ok) break;
       it = it0 + 2u * (u.hi - u.lo);
       mma_commit_elect(bar_q_free);
     }
-    // Every MMA this warp issued has finished once the drain barrier flips.
+    // Every MMA this warp issued has finished once the drain barrier flips
+    // (both issuers commit to it).
     mma_commit_elect(bar_drain);
     mbar_wait_drain(bar_drain, 0, wc, kSiteMmaDrain);
   } else {
@@ -601,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (tr) trace_mark(p, t, k, jr, 3);
           const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
-          if (bm > m_ref + kRescaleThreshold) {
+          if (bm > m_ref + kThresh) {
             alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
             m_ref = bm;
             rescale = true;
@@ -632,6 +613,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t pk[16];
             uint32_t pk_lo[16];
+            if constexpr (kF16Exp) {
+              // Two exponentials per MUFU operation; the packed result is P.
+              uint32_t prev = 0;
+#pragma unroll
+              for (int c = c0; c < c0 + 32; c += 2) {
+                const float2 x = __ffma2_rn(
+                    make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                    make_float2(Cs, Cs), make_float2(-mu, -mu));
+                __half2 xh = __floats2half2_rn(x.x, x.y);
+                uint32_t pp = ex2_f16x2(*reinterpret_cast<uint32_t*>(&xh));
+                if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
+                  const uint32_t keep = ((c >= vis_lo && c < vis_hi) ? 0x0000FFFFu : 0u) |
+                                        ((c + 1 >= vis_lo && c + 1 < vis_hi) ? 0xFFFF0000u : 0u);
+                  pp &= keep;
+                }
+                pk[(c - c0) >> 1] = pp;
+                // row sum: two packed pairs added in fp16, then widened and
+                // accumulated in fp32
+                if ((c & 2) == 0) {
+                  prev = pp;
+                } else {
+                  const __half2 s2 = __hadd2(*reinterpret_cast<__half2*>(&prev),
+                                             *reinterpret_cast<__half2*>(&pp));
+#if EX19_SOFTMAX_F2
+                  acc[(c >> 2) & 1] = __fadd2_rn(acc[(c >> 2) & 1], __half22float2(s2));
+#else
+                  const float2 f = __half22float2(s2);
+                  acc[(c >> 1) & 3] += f.x;
+                  acc[((c >> 1) + 1) & 3] += f.y;
+#endif
+                }
+              }
+              tmem_st_x16(tP + (c0 >> 1), pk);
+              if (tr && (c0 & 32)) trace_mark(p, t, k, jr, 5 + (c0 >> 6));
+              continue;
+            }
 #pragma unroll
             for (int c = c0; c < c0 + 32; c += 2) {
 #if EX19_SOFTMAX_F2
@@ -702,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
           }
           const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
-          if (bm > m_ref + kRescaleThreshold) {
+          if (bm > m_ref + kThresh) {
             alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
             m_ref = bm;
             rescale = true;

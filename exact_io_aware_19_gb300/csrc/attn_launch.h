@@ -20,7 +20,7 @@ struct LaunchArgs {
 cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
-cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
+cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream);
 
 }  // namespace ex19

@@ -351,6 +351,14 @@ __device__ __forceinline__ void exp2_poly_pair(float x0, float x1, float& y0, fl
   y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
+// Two exponentials in one MUFU operation: (2^a, 2^b) for a packed pair of fp16
+// arguments, result packed as fp16 (low half = first element).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -142,13 +142,14 @@ attn_status_t attn_debug_wait_probe(void *workspace, size_t workspace_bytes,
                                     uint64_t limit_ns, void *stream);
 
 /*
- * Evaluates 2^x[i] for i < n with the two exp2 paths of the attention kernel:
- * the FMA-pipe polynomial (y_poly) and the MUFU instruction (y_mufu). Device
- * float32 arrays; used by the accuracy tests of the polynomial. The polynomial
- * (degree 3, fitted by fit_exp2_poly.py) is valid for x <= 128; inputs below -125
- * are clamped to -125.
+ * Evaluates 2^x[i] for i < n with the exp2 paths of the attention kernel: the
+ * FMA-pipe polynomial (y_poly), the fp32 MUFU instruction (y_mufu) and, when
+ * y_f16 is not NULL, the packed fp16 MUFU instruction on arguments rounded to
+ * fp16 (y_f16, widened back to float). Device float32 arrays; used by the
+ * accuracy tests. The polynomial (degree 3, fitted by fit_exp2_poly.py) is valid
+ * for x <= 128; inputs below -125 are clamped to -125.
  */
-attn_status_t attn_debug_exp2(const float *x, float *y_poly, float *y_mufu, int n,
+attn_status_t attn_debug_exp2(const float *x, float *y_poly, float *y_mufu, float *y_f16, int n,
                               void *stream);
 
 /* Static description of a status code. */

@@ -174,3 +174,18 @@ def test_exp2_polynomial_error_bound():
     # clamping: far below the range gives a tiny positive number, never inf/nan
     yp, _ = ex.debug_exp2(torch.tensor([-1000.0, -200.0, -126.0], device="cuda"))
     assert torch.isfinite(yp).all() and (yp >= 0).all() and (yp < 1e-37).all()
+
+
+def test_exp2_f16x2_accuracy():
+    """The packed fp16 MUFU path, on arguments already rounded to fp16: relative error
+    within 2^-9.9 of 2^x while the result is a normal fp16 number (x >= -14), and
+    absolute error within the fp16 subnormal spacing 2^-24 below that."""
+    import exact_io_aware_19_gb300 as ex
+    x = torch.linspace(-30.0, 1.0, 1 << 16).half().float()  # exactly representable
+    _, _, yh = ex.debug_exp2(x.cuda(), with_f16=True)
+    ref = torch.exp2(x.double())
+    got = yh.double().cpu()
+    normal = x >= -14.0
+    rel = ((got - ref) / ref).abs()[normal]
+    assert rel.max().item() <= 2.0 ** -9.9, rel.max().item()
+    assert (got - ref).abs()[~normal].max().item() <= 2.0 ** -24
