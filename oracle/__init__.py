@@ -6,6 +6,10 @@ shares no code with it.
 
 * ``attn_rows`` / ``attn_full``: the fp64 plain-definition oracle (``attn_oracle.c``,
   compiled here with the system C compiler, OpenMP over rows).
+* ``attn_rows_kv`` / ``attn_full_kv``: the same for decode-shaped problems (Lq queries
+  at the end of an Lk-long sequence), optionally over a sub-range of the keys.
+* ``merge``: the combination of partial results over disjoint key sets by their
+  log-sum-exp ("What is memory-efficient attention ...", section 4).
 * ``bruteforce.attn_materialised``: an independent numpy implementation that
   materialises S and P, used to pin the C oracle on tiny inputs.
 
@@ -53,6 +57,12 @@ def _bind(path: str):
     lib.oracle_attn_rows.restype = ctypes.c_int
     lib.oracle_attn_rows.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64,
                                      ctypes.c_int, i64, ctypes.c_double, p, i64, p, p]
+    lib.oracle_attn_rows_kv.restype = ctypes.c_int
+    lib.oracle_attn_rows_kv.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_int, i64, ctypes.c_double, i64, i64, p, i64,
+                                        p, p]
+    lib.oracle_merge.restype = None
+    lib.oracle_merge.argtypes = [i64, i64, i64, p, p, p, p]
     lib.oracle_widen.restype = None
     lib.oracle_widen.argtypes = [p, ctypes.c_int, p, i64]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -119,6 +129,53 @@ class Oracle:
             _ptr(o), _ptr(lse))
         if rc != 0:
             raise ValueError(f"oracle_attn_rows rejected its arguments (rc={rc})")
+        return o, lse
+
+    def attn_rows_kv(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale, rows,
+                     key_lo=0, key_hi=None):
+        """Decode-shaped rows: q_bits [B, Lq, Hq, d] are the last Lq positions of the
+        Lk-long sequence in k_bits / v_bits [B, Lk, Hkv, d]; keys limited to
+        [key_lo, key_hi). Rows are flat ids (b*Hq + h)*Lq + i."""
+        q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+        k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+        v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+        B, Lq, Hq, d = q_bits.shape
+        Lk, Hkv = k_bits.shape[1], k_bits.shape[2]
+        if k_bits.shape != (B, Lk, Hkv, d) or v_bits.shape != k_bits.shape:
+            raise ValueError("K/V shape mismatch")
+        key_hi = Lk if key_hi is None else key_hi
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, d), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.oracle_attn_rows_kv(
+            _ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _dtype_code(dtype), B, Lq, Lk, Hq, Hkv,
+            d, int(bool(causal)), int(window_left), float(scale), int(key_lo), int(key_hi),
+            _ptr(rows), rows.size, _ptr(o), _ptr(lse))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_rows_kv rejected its arguments (rc={rc})")
+        return o, lse
+
+    def attn_full_kv(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale,
+                     key_lo=0, key_hi=None):
+        """Full decode-shaped O [B, Lq, Hq, d] and LSE [B, Hq, Lq] in float64."""
+        B, Lq, Hq, d = q_bits.shape
+        rows = np.arange(B * Hq * Lq, dtype=np.int64)
+        o, lse = self.attn_rows_kv(q_bits, k_bits, v_bits, dtype, causal, window_left, scale,
+                                   rows, key_lo, key_hi)
+        o = o.reshape(B, Hq, Lq, d).transpose(0, 2, 1, 3).copy()
+        return o, lse.reshape(B, Hq, Lq)
+
+    def merge(self, o_parts, lse_parts):
+        """Combine partial results over disjoint key sets: o_parts [P, n, d] and
+        lse_parts [P, n] (natural log, -inf = empty part) -> O [n, d], LSE [n]."""
+        o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+        lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+        P, n, d = o_parts.shape
+        if lse_parts.shape != (P, n):
+            raise ValueError("part shapes disagree")
+        o = np.empty((n, d), dtype=np.float64)
+        lse = np.empty(n, dtype=np.float64)
+        self.lib.oracle_merge(P, n, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o), _ptr(lse))
         return o, lse
 
     def attn_full(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale):

@@ -26,6 +26,23 @@
  *   LSE[b,h,i] = m_i + ln(l_i)                                  (natural log)
  * An empty J_i (impossible for the supported masks) gives O = 0 and LSE = -inf.
  *
+ * Decode-shaped problems (oracle_attn_rows_kv): Lq query rows against Lk >= Lq
+ * keys, the queries being the LAST Lq positions of the sequence, so row i sits at
+ * position p_i = Lk - Lq + i and J_i is the set above with i replaced by p_i and
+ * L by Lk (with Lq = Lk this is the square problem). Reading: the pages say a
+ * generation step reads the whole KV cache ("What is memory-efficient attention
+ * ...", section 1, key limitations), i.e. the new query attends to every cached
+ * key before it; bottom-right alignment is that statement for Lq new queries.
+ * A key sub-range [key_lo, key_hi) restricts J_i further: the partial result of
+ * one split of the keys.
+ *
+ * Merge of partial results over disjoint key sets (oracle_merge): the softmax
+ * over a union of key sets, written from its definition. With LSE_s = m_s + ln l_s
+ * of part s, the total normaliser is sum_s exp(LSE_s), so
+ *   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) * O_s.
+ * This is how attention computed in parts is combined ("What is memory-efficient
+ * attention ...", section 4, ring attention computing attention by parts).
+ *
  * Readings of points the pages leave open (each is listed in the design notes):
  *   - layout [B, L, H, d] contiguous for Q, K, V and O; LSE is [B, Hq, L];
  *   - query head h reads K/V head h / (Hq / Hkv) (contiguous groups);
@@ -77,20 +94,27 @@ void oracle_widen(const uint16_t *in, int dtype, double *out, int64_t n)
         out[t] = widen16(in[t], dtype);
 }
 
-/* One output row (b, h, i). `s` is scratch for up to L scores. */
+/* One output row (b, h, i) of Lq query rows against Lk keys, restricted to keys
+ * [key_lo, key_hi). `s` is scratch for up to Lk scores. */
 static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
-                     int64_t L, int64_t Hq, int64_t Hkv, int64_t d, int causal,
-                     int64_t window_left, double scale, int64_t b, int64_t h, int64_t i,
-                     double *s, double *qrow, double *o, double *lse)
+                     int64_t Lq, int64_t Lk, int64_t Hq, int64_t Hkv, int64_t d, int causal,
+                     int64_t window_left, double scale, int64_t key_lo, int64_t key_hi,
+                     int64_t b, int64_t h, int64_t i, double *s, double *qrow, double *o,
+                     double *lse)
 {
     int64_t g = h / (Hq / Hkv);
+    int64_t pos = Lk - Lq + i; /* position of query row i in the sequence */
 
     /* the visible key range J_i = [j_lo, j_hi) */
-    int64_t j_lo = 0, j_hi = L;
+    int64_t j_lo = 0, j_hi = Lk;
     if (causal)
-        j_hi = i + 1;
-    if (window_left >= 0 && i - window_left > j_lo)
-        j_lo = i - window_left;
+        j_hi = pos + 1;
+    if (window_left >= 0 && pos - window_left > j_lo)
+        j_lo = pos - window_left;
+    if (key_lo > j_lo)
+        j_lo = key_lo;
+    if (key_hi < j_hi)
+        j_hi = key_hi;
 
     for (int64_t c = 0; c < d; ++c)
         o[c] = 0.0;
@@ -99,14 +123,14 @@ static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
         return;
     }
 
-    const uint16_t *qi = q + ((b * L + i) * Hq + h) * d;
+    const uint16_t *qi = q + ((b * Lq + i) * Hq + h) * d;
     for (int64_t c = 0; c < d; ++c)
         qrow[c] = widen16(qi[c], dtype);
 
     /* scores and their maximum */
     double m = -INFINITY;
     for (int64_t j = j_lo; j < j_hi; ++j) {
-        const uint16_t *kj = k + ((b * L + j) * Hkv + g) * d;
+        const uint16_t *kj = k + ((b * Lk + j) * Hkv + g) * d;
         double dot = 0.0;
         for (int64_t c = 0; c < d; ++c)
             dot += qrow[c] * widen16(kj[c], dtype);
@@ -122,7 +146,7 @@ static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
 
     /* weighted sum of values */
     for (int64_t j = j_lo; j < j_hi; ++j) {
-        const uint16_t *vj = v + ((b * L + j) * Hkv + g) * d;
+        const uint16_t *vj = v + ((b * Lk + j) * Hkv + g) * d;
         double p = exp(s[j - j_lo] - m) / l;
         for (int64_t c = 0; c < d; ++c)
             o[c] += p * widen16(vj[c], dtype);
@@ -130,28 +154,31 @@ static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     *lse = m + log(l);
 }
 
-/* Rows are flat LSE indices r = (b * Hq + h) * L + i, 0 <= r < B*Hq*L.
+/* Rows are flat LSE indices r = (b * Hq + h) * Lq + i, 0 <= r < B*Hq*Lq.
+ * q: [B, Lq, Hq, d]; k, v: [B, Lk, Hkv, d]; keys restricted to [key_lo, key_hi).
  * o_rows: nrows x d doubles; lse_rows: nrows doubles.
  * Returns 0 on success, -1 on a bad argument (nothing written). */
-int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
-                     int64_t B, int64_t L, int64_t Hq, int64_t Hkv, int64_t d, int causal,
-                     int64_t window_left, double scale, const int64_t *rows, int64_t nrows,
-                     double *o_rows, double *lse_rows)
+int oracle_attn_rows_kv(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                        int64_t B, int64_t Lq, int64_t Lk, int64_t Hq, int64_t Hkv, int64_t d,
+                        int causal, int64_t window_left, double scale, int64_t key_lo,
+                        int64_t key_hi, const int64_t *rows, int64_t nrows, double *o_rows,
+                        double *lse_rows)
 {
     if (!q || !k || !v || !rows || !o_rows || !lse_rows)
         return -1;
-    if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0 || window_left < -1)
+    if (B < 1 || Lq < 1 || Lk < Lq || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0 ||
+        window_left < -1 || key_lo < 0 || key_hi > Lk || key_lo > key_hi)
         return -1;
     if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)
         return -1;
     for (int64_t r = 0; r < nrows; ++r)
-        if (rows[r] < 0 || rows[r] >= B * Hq * L)
+        if (rows[r] < 0 || rows[r] >= B * Hq * Lq)
             return -1;
 
     int bad = 0;
 #pragma omp parallel
     {
-        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        double *s = (double *)malloc(sizeof(double) * (size_t)Lk);
         double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
         if (!s || !qrow) {
 #pragma omp atomic write
@@ -161,17 +188,56 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
         for (int64_t r = 0; r < nrows; ++r) {
             if (!s || !qrow)
                 continue;
-            int64_t i = rows[r] % L;
-            int64_t bh = rows[r] / L;
+            int64_t i = rows[r] % Lq;
+            int64_t bh = rows[r] / Lq;
             int64_t h = bh % Hq;
             int64_t b = bh / Hq;
-            attn_row(q, k, v, dtype, L, Hq, Hkv, d, causal, window_left, scale, b, h, i, s,
-                     qrow, o_rows + r * d, lse_rows + r);
+            attn_row(q, k, v, dtype, Lq, Lk, Hq, Hkv, d, causal, window_left, scale, key_lo,
+                     key_hi, b, h, i, s, qrow, o_rows + r * d, lse_rows + r);
         }
         free(s);
         free(qrow);
     }
     return bad ? -2 : 0;
+}
+
+/* The square problem (Lq = Lk = L, all keys): rows r = (b * Hq + h) * L + i. */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                     int64_t B, int64_t L, int64_t Hq, int64_t Hkv, int64_t d, int causal,
+                     int64_t window_left, double scale, const int64_t *rows, int64_t nrows,
+                     double *o_rows, double *lse_rows)
+{
+    return oracle_attn_rows_kv(q, k, v, dtype, B, L, L, Hq, Hkv, d, causal, window_left, scale,
+                               0, L, rows, nrows, o_rows, lse_rows);
+}
+
+/* Combine nparts partial results of the same nrows rows, each over a disjoint
+ * set of keys: o_parts is nparts x nrows x d, lse_parts nparts x nrows (natural
+ * log; -inf for a part that saw no key). Writes o (nrows x d) and lse (nrows). */
+void oracle_merge(int64_t nparts, int64_t nrows, int64_t d, const double *o_parts,
+                  const double *lse_parts, double *o, double *lse)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        double m = -INFINITY;
+        for (int64_t p = 0; p < nparts; ++p)
+            if (lse_parts[p * nrows + r] > m)
+                m = lse_parts[p * nrows + r];
+        for (int64_t c = 0; c < d; ++c)
+            o[r * d + c] = 0.0;
+        if (m == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double total = 0.0;
+        for (int64_t p = 0; p < nparts; ++p)
+            total += exp(lse_parts[p * nrows + r] - m);
+        lse[r] = m + log(total);
+        for (int64_t p = 0; p < nparts; ++p) {
+            double w = exp(lse_parts[p * nrows + r] - lse[r]);
+            for (int64_t c = 0; c < d; ++c)
+                o[r * d + c] += w * o_parts[(p * nrows + r) * d + c];
+        }
+    }
 }
 
 int oracle_max_threads(void)

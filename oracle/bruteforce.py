@@ -5,39 +5,46 @@ skill page, workflow 1 step 2: weights = softmax(q káµ€/âˆšd_k), out = weights Â
 written the unfused way: S = scaleÂ·Q Káµ€ is formed in full, masked with -inf, turned
 into P = exp(S - rowmax) / rowsum and multiplied by V. It is used only on tiny
 inputs to pin the C oracle, which never materialises S. The two share no code.
+Decode-shaped inputs (Lq queries, the last Lq positions of an Lk-long sequence)
+use the same visibility rule with the query positions shifted to Lk - Lq + i.
 """
 from __future__ import annotations
 
 import numpy as np
 
 
-def visibility(L: int, causal: bool, window_left: int) -> np.ndarray:
-    """Boolean L x L matrix: True where key j is visible from query row i."""
-    i = np.arange(L)[:, None]
-    j = np.arange(L)[None, :]
-    vis = np.ones((L, L), dtype=bool)
+def visibility(Lq: int, causal: bool, window_left: int, Lk: int = None) -> np.ndarray:
+    """Boolean Lq x Lk matrix: True where key j is visible from query row i.
+
+    The Lq queries are the last Lq positions of an Lk-long sequence (row i sits at
+    position Lk - Lq + i); Lk defaults to Lq, the square problem.
+    """
+    Lk = Lq if Lk is None else Lk
+    pos = (Lk - Lq + np.arange(Lq))[:, None]
+    j = np.arange(Lk)[None, :]
+    vis = np.ones((Lq, Lk), dtype=bool)
     if causal:
-        vis &= j <= i
+        vis &= j <= pos
     if window_left >= 0:
-        vis &= j >= i - window_left
+        vis &= j >= pos - window_left
     return vis
 
 
 def attn_materialised(q, k, v, causal=False, window_left=-1, scale=1.0, return_p=False):
-    """q: [B, L, Hq, d]; k, v: [B, L, Hkv, d] (float64). Returns O, LSE[, P].
+    """q: [B, Lq, Hq, d]; k, v: [B, Lk, Hkv, d] (float64), Lq <= Lk. Returns O, LSE[, P].
 
-    P has shape [B, Hq, L, L]; rows with no visible key give O = 0, LSE = -inf.
+    P has shape [B, Hq, Lq, Lk]; rows with no visible key give O = 0, LSE = -inf.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    B, L, Hq, d = q.shape
-    Hkv = k.shape[2]
+    B, Lq, Hq, d = q.shape
+    Lk, Hkv = k.shape[1], k.shape[2]
     group = Hq // Hkv
-    vis = visibility(L, causal, window_left)
-    o = np.zeros((B, L, Hq, d))
-    lse = np.full((B, Hq, L), -np.inf)
-    p_all = np.zeros((B, Hq, L, L)) if return_p else None
+    vis = visibility(Lq, causal, window_left, Lk)
+    o = np.zeros((B, Lq, Hq, d))
+    lse = np.full((B, Hq, Lq), -np.inf)
+    p_all = np.zeros((B, Hq, Lq, Lk)) if return_p else None
     for b in range(B):
         for h in range(Hq):
             g = h // group

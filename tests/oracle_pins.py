@@ -262,10 +262,83 @@ def pin_rows_api_matches_full(orc):
         assert np.array_equal(orow[n], o[b, i, h]) and lrow[n] == lse[b, h, i]
 
 
+# --- decode-shaped problems and the merge of partial results -----------------------------
+# A generation step reads the whole KV cache ("What is memory-efficient attention ...",
+# section 1): Lq new queries sit at the end of the Lk-long sequence. Attention computed
+# over parts of the keys is combined by the parts' log-sum-exp (same page, section 4).
+
+def pin_kv_matches_materialised(orc):
+    """Decode-shaped rows (Lq <= Lk, queries at positions Lk - Lq + i) equal the
+    materialised version to 1e-12."""
+    seed = 500
+    for Lq, Lk, (hq, hkv), (causal, wl) in itertools.product((1, 2, 5), (5, 17, 130), HEADS,
+                                                              MASKS):
+        seed += 1
+        q, _, _ = random_qkv(2, Lq, hq, hkv, 8, seed=seed)
+        _, k, v = random_qkv(2, Lk, hq, hkv, 8, seed=seed + 10000)
+        o, lse = orc.attn_full_kv(bits16(q), bits16(k), bits16(v), "fp16", causal, wl, 0.35)
+        qd, kd, vd = _widened(orc, q, k, v, "fp16")
+        o_ref, lse_ref = attn_materialised(qd, kd, vd, causal, wl, 0.35)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12,
+                                   err_msg=f"O Lq={Lq} Lk={Lk} h={hq}/{hkv} mask={causal, wl}")
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12,
+                                   err_msg=f"LSE Lq={Lq} Lk={Lk} h={hq}/{hkv} mask={causal, wl}")
+
+
+def pin_kv_rows_are_square_suffix(orc):
+    """A query at position p sees what row p of the square problem sees: the Lq-row
+    problem is bit for bit the last Lq rows of the Lk-row problem that ends with the
+    same queries."""
+    for (causal, wl), Lq in itertools.product(MASKS, (1, 3, 40)):
+        qf, k, v = random_qkv(1, 64, 4, 2, 16, seed=77 + Lq)
+        q = qf[:, 64 - Lq:].contiguous()
+        o, lse = orc.attn_full_kv(bits16(q), bits16(k), bits16(v), "fp16", causal, wl, 0.25)
+        of, lf = _full(orc, qf, k, v, "fp16", causal, wl, 0.25)
+        assert np.array_equal(o, of[:, 64 - Lq:]), (causal, wl, Lq)
+        assert np.array_equal(lse, lf[:, :, 64 - Lq:]), (causal, wl, Lq)
+
+
+def pin_merge_of_key_splits(orc):
+    """Attention over all keys equals the merge of attention over any partition of the
+    keys into consecutive ranges, empty ranges included."""
+    q, _, _ = random_qkv(2, 6, 4, 1, 16, seed=91)
+    _, k, v = random_qkv(2, 300, 4, 1, 16, seed=92)
+    qb, kb, vb = bits16(q), bits16(k), bits16(v)
+    rows = np.arange(2 * 4 * 6, dtype=np.int64)
+    rng = np.random.default_rng(93)
+    splits = [[0, 300], [0, 128, 300], [0, 1, 2, 299, 300], [0, 0, 150, 150, 300],
+              [0] + sorted(rng.integers(0, 301, 6).tolist()) + [300]]
+    for causal, wl in MASKS:
+        o_all, l_all = orc.attn_rows_kv(qb, kb, vb, "fp16", causal, wl, 0.3, rows)
+        for bounds in splits:
+            parts = [orc.attn_rows_kv(qb, kb, vb, "fp16", causal, wl, 0.3, rows, a, b)
+                     for a, b in zip(bounds[:-1], bounds[1:])]
+            o, lse = orc.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+            np.testing.assert_allclose(o, o_all, rtol=1e-12, atol=1e-12,
+                                       err_msg=f"mask={causal, wl} split={bounds}")
+            np.testing.assert_allclose(lse, l_all, rtol=1e-12, atol=1e-12,
+                                       err_msg=f"mask={causal, wl} split={bounds}")
+
+
+def pin_merge_hand_example(orc):
+    """Parts with normalisers 1 and 3 (LSE ln 1 and ln 3) get weights 1/4 and 3/4 and a
+    total LSE of ln 4; an empty part (-inf) gets weight 0; all parts empty give O = 0
+    and LSE = -inf."""
+    o1, o2 = np.array([1.0, -2.0]), np.array([5.0, 2.0])
+    o, lse = orc.merge(np.array([[o1], [o2], [[9.0, 9.0]]]),
+                       np.array([[0.0], [math.log(3.0)], [-math.inf]]))
+    np.testing.assert_allclose(o[0], (o1 + 3 * o2) / 4, rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(lse[0], math.log(4.0), rtol=1e-15, atol=1e-15)
+    o, lse = orc.merge(np.ones((3, 1, 2)), np.full((3, 1), -math.inf))
+    assert np.array_equal(o, np.zeros((1, 2))) and lse[0] == -math.inf
+
+
 ORACLE_PINS = [
     pin_widen_fp16_all_patterns, pin_widen_bf16_all_patterns, pin_matches_materialised,
     pin_constant_values, pin_causal_first_row, pin_window_zero_is_identity,
     pin_gqa_equals_replicated_kv, pin_scale_zero_is_mean, pin_two_keys_sigmoid,
     pin_dominant_key, pin_key_permutation_invariance, pin_negative_scale_is_negated_query,
     pin_window_row_is_causal_suffix, pin_hand_worked_example, pin_rows_api_matches_full,
+    pin_kv_matches_materialised, pin_kv_rows_are_square_suffix, pin_merge_of_key_splits,
+    pin_merge_hand_example,
 ]

@@ -17,8 +17,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 
 MUTANTS = {
     "drop_scale": ("s[j - j_lo] = scale * dot;", "s[j - j_lo] = dot;"),
-    "causal_excludes_diagonal": ("j_hi = i + 1;", "j_hi = i;"),
-    "window_one_short": ("j_lo = i - window_left;", "j_lo = i - window_left + 1;"),
+    "causal_excludes_diagonal": ("j_hi = pos + 1;", "j_hi = pos;"),
+    "window_one_short": ("j_lo = pos - window_left;", "j_lo = pos - window_left + 1;"),
     "gqa_modulo_mapping": ("int64_t g = h / (Hq / Hkv);", "int64_t g = h % Hkv;"),
     "lse_drops_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
@@ -26,12 +26,21 @@ MUTANTS = {
     "fp16_subnormal_scale": ("ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
     "no_normalisation": ("double p = exp(s[j - j_lo] - m) / l;",
                          "double p = exp(s[j - j_lo] - m);"),
-    "key_indexed_by_query_row": ("k + ((b * L + j) * Hkv + g) * d;",
-                                 "k + ((b * L + (j + i) % L) * Hkv + g) * d;"),
+    "key_indexed_by_query_row": ("k + ((b * Lk + j) * Hkv + g) * d;",
+                                 "k + ((b * Lk + (j + i) % Lk) * Hkv + g) * d;"),
     "values_read_from_keys": ("const uint16_t *vj = v + ", "const uint16_t *vj = k + "),
     "bf16_low_half": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
     "max_not_subtracted_in_weights": ("double p = exp(s[j - j_lo] - m) / l;",
                                       "double p = exp(s[j - j_lo]) / l;"),
+    "decode_queries_top_left": ("int64_t pos = Lk - Lq + i;", "int64_t pos = i;"),
+    "decode_queries_off_by_one": ("int64_t pos = Lk - Lq + i;", "int64_t pos = Lk - Lq + i - 1;"),
+    "key_range_start_ignored": ("        j_lo = key_lo;", "        j_lo = j_lo;"),
+    "key_range_end_ignored": ("        j_hi = key_hi;", "        j_hi = j_hi;"),
+    "merge_weights_unnormalised": ("double w = exp(lse_parts[p * nrows + r] - lse[r]);",
+                                   "double w = exp(lse_parts[p * nrows + r] - m);"),
+    "merge_lse_of_mean": ("lse[r] = m + log(total);", "lse[r] = m + log(total / nparts);"),
+    "merge_first_part_only": ("        for (int64_t p = 0; p < nparts; ++p) {",
+                              "        for (int64_t p = 0; p < 1; ++p) {"),
 }
 
 
