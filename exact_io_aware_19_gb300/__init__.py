@@ -8,6 +8,7 @@ library is missing or the device is not a GB300, calls raise.
 
     o, lse = attn_fwd(q, k, v, causal=True)             # q: [B, L, Hq, d] fp16/bf16
     o, lse = attn_fwd(q, k, v, causal=True, window_left=4096, out_fp32=True)
+    o, lse = attn_fwd_kv(q_new, k_cache, v_cache, causal=True)  # decode: q_new [B, Lq, Hq, d]
 
 Definition: standard attention softmax(scale · q kᵀ) v of the "Flash Attention
 optimization" skill page (workflow 1 step 2), with the causal / MQA-GQA / window
@@ -24,7 +25,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "sync_status", "AttnError",
+__all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
+           "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "debug_wait_probe", "debug_exp2",
            "STATUS"]
 
@@ -60,6 +62,13 @@ def _bind(lib):
     lib.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p, sz, p]
     lib.attn_fwd_workspace_size.restype = sz
     lib.attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.attn_fwd_kv.restype = i
+    lib.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, i, i,
+                                p, sz, p]
+    lib.attn_fwd_kv_workspace_size.restype = sz
+    lib.attn_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+    lib.attn_fwd_kv_num_splits.restype = i
+    lib.attn_fwd_kv_num_splits.argtypes = [i, i, i, i, i, i, i, i]
     lib.attn_fwd_sync_status.restype = i
     lib.attn_fwd_sync_status.argtypes = [p, p]
     lib.attn_set_wait_limit_ns.restype = None
@@ -128,11 +137,9 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
-                  workspace=None, stream=None) -> None:
-    """Write attention of (q, k, v) into preallocated ``o`` (q's dtype or float32) and
-    ``lse`` (float32 [B, Hq, L] or None). Asynchronous on ``stream``."""
-    lib = load_library()
+def _check_tensors(q, k, v, o, lse):
+    """Validate q [B, Lq, Hq, d], k/v [B, Lk, Hkv, d], o and lse; return the sizes
+    (B, Lq, Lk, Hq, Hkv, d), the dtype code and the output code."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise TypeError(f"{name} must be a CUDA tensor")
@@ -140,15 +147,15 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
             raise ValueError(f"{name} must be contiguous")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be [B, L, H, d]")
-    B, L, Hq, d = q.shape
-    Hkv = k.shape[2]
-    if tuple(k.shape) != (B, L, Hkv, d) or tuple(v.shape) != tuple(k.shape):
-        raise ValueError(f"k and v must be [B, L, Hkv, d] = {(B, L, Hkv, d)}")
+    B, Lq, Hq, d = q.shape
+    Lk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Lk, Hkv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, Lk, Hkv, d] with B = {B}, d = {d}")
     dt = _dtype_code(q)
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k and v must share one dtype")
-    if tuple(o.shape) != (B, L, Hq, d):
-        raise ValueError("o must be [B, L, Hq, d]")
+    if tuple(o.shape) != (B, Lq, Hq, d):
+        raise ValueError("o must have q's shape")
     if o.dtype == torch.float32:
         out = OUT_FP32
     elif o.dtype == q.dtype:
@@ -156,9 +163,20 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
     else:
         raise TypeError("o must have q's dtype or float32")
     if lse is not None:
-        if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, L) or \
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Lq) or \
                 not lse.is_contiguous() or not lse.is_cuda:
-            raise ValueError("lse must be a contiguous CUDA float32 tensor [B, Hq, L]")
+            raise ValueError("lse must be a contiguous CUDA float32 tensor [B, Hq, Lq]")
+    return (B, Lq, Lk, Hq, Hkv, d), dt, out
+
+
+def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
+                  workspace=None, stream=None) -> None:
+    """Write attention of (q, k, v) into preallocated ``o`` (q's dtype or float32) and
+    ``lse`` (float32 [B, Hq, L] or None). Asynchronous on ``stream``."""
+    lib = load_library()
+    (B, L, Lk, Hq, Hkv, d), dt, out = _check_tensors(q, k, v, o, lse)
+    if Lk != L:
+        raise ValueError("k and v must have q's sequence length (attn_fwd_kv takes Lq <= Lk)")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     need = workspace_size(B, L, Hq, Hkv, d, causal, window_left)
@@ -170,6 +188,50 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
     _check(code)
+
+
+def kv_num_splits(B, Lq, Lk, Hq, Hkv, d, causal=False, window_left=-1) -> int:
+    """Key-range splits attn_fwd_kv picks on the current device (num_splits = 0)."""
+    return int(load_library().attn_fwd_kv_num_splits(B, Lq, Lk, Hq, Hkv, d, int(bool(causal)),
+                                                     int(window_left)))
+
+
+def kv_workspace_size(B, Lq, Lk, Hq, Hkv, d, causal=False, window_left=-1, num_splits=0) -> int:
+    return int(load_library().attn_fwd_kv_workspace_size(B, Lq, Lk, Hq, Hkv, d,
+                                                         int(bool(causal)), int(window_left),
+                                                         int(num_splits)))
+
+
+def attn_fwd_kv_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None, num_splits=0,
+                     workspace=None, stream=None) -> None:
+    """Decode-shaped attention: q [B, Lq, Hq, d] are the last Lq positions of the
+    Lk-long sequence of k, v [B, Lk, Hkv, d]. Writes ``o`` (q's shape, q's dtype or
+    float32) and ``lse`` (float32 [B, Hq, Lq] or None). ``num_splits`` = 0 lets the
+    library choose how many key ranges run in parallel."""
+    lib = load_library()
+    (B, Lq, Lk, Hq, Hkv, d), dt, out = _check_tensors(q, k, v, o, lse)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = kv_workspace_size(B, Lq, Lk, Hq, Hkv, d, causal, window_left, num_splits)
+    if workspace is None:
+        workspace = _default_workspace(q.device, max(need, 256))
+    code = lib.attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, B, Lq, Lk, Hq, Hkv, d,
+                           int(bool(causal)), int(window_left), float(scale), dt, out,
+                           int(num_splits), workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(code)
+
+
+def attn_fwd_kv(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=False, num_splits=0,
+                return_lse=True, workspace=None, stream=None):
+    """Decode-shaped attention forward (see attn_fwd_kv_into). Returns (o, lse)."""
+    B, Lq, Hq, d = q.shape
+    o = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
+    attn_fwd_kv_into(q, k, v, o, lse, causal=causal, window_left=window_left, scale=scale,
+                     num_splits=num_splits, workspace=workspace, stream=stream)
+    return o, lse
 
 
 def attn_fwd(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=False,

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -87,9 +88,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 
 // Tensor map over a [B, L, H, d] 16-bit tensor. Dimensions are listed innermost
 // first with increasing strides (d, H, L, B); the box is 64 elements (128 bytes,
-// one swizzle span) of d, 1 head, 128 rows, 1 batch.
+// one swizzle span) of d, box_h heads, box_l rows, 1 batch.
 bool make_tensor_map(CUtensorMap* map, const void* ptr, bool bf16, int B, int L, int H, int d,
-                     std::string* why) {
+                     std::string* why, int box_h = 1, int box_l = 128) {
   cudaError_t err;
   auto encode = encode_fn(&err);
   if (encode == nullptr) {
@@ -99,7 +100,7 @@ bool make_tensor_map(CUtensorMap* map, const void* ptr, bool bf16, int B, int L,
   const cuuint64_t e = 2;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)d * e, (cuuint64_t)H * d * e, (cuuint64_t)L * H * d * e};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_h, (cuuint32_t)box_l, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                       4, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -149,6 +150,77 @@ attn_status_t check_shape(int B, int L, int Hq, int Hkv, int d, int causal, int 
   const long long rows = (long long)B * Hq * L;
   if (rows >= (1LL << 31)) return fail(ATTN_ERR_INVALID_ARG, "B * Hq * L must be < 2^31");
   return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- decode shapes
+constexpr int kKvMaxSplits = 256;
+
+attn_status_t check_kv_shape(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                             int window_left) {
+  if (B < 1 || Lq < 1 || Lk < 1 || Hq < 1 || Hkv < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, Lq, Lk, Hq and Hkv must all be >= 1");
+  if (Lq > Lk) return fail(ATTN_ERR_INVALID_ARG, "Lq must be <= Lk (queries are the last Lq positions)");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  if (Hq / Hkv > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "d must be 64 or 128");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (window_left < -1) return fail(ATTN_ERR_INVALID_ARG, "window_left must be >= -1");
+  if (window_left >= 0 && !causal)
+    return fail(ATTN_ERR_UNSUPPORTED, "a left window is only supported with causal = 1");
+  if ((long long)B * Hq * Lq >= (1LL << 31) || (long long)B * Hkv * Lk >= (1LL << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "B * Hq * Lq and B * Hkv * Lk must be < 2^31");
+  return ATTN_OK;
+}
+
+struct KvPlan {
+  int group, q_per_tile, row_tiles, items;  // items = B * Hkv * row_tiles
+  int max_blocks;                           // key blocks of the largest row tile
+};
+
+KvPlan kv_plan(int B, int Lq, int Lk, int Hq, int Hkv, int causal, int window_left) {
+  KvPlan k;
+  k.group = Hq / Hkv;
+  k.q_per_tile = std::min(Lq, 128 / k.group);
+  k.row_tiles = (Lq + k.q_per_tile - 1) / k.q_per_tile;
+  k.items = B * Hkv * k.row_tiles;
+  const int nblk = (Lk + 127) / 128;
+  k.max_blocks = 0;
+  for (int rt = 0; rt < k.row_tiles; ++rt) {
+    const int i0 = rt * k.q_per_tile, i1 = std::min(Lq, i0 + k.q_per_tile);
+    const int off = Lk - Lq;
+    const int hi = causal ? (off + i1 - 1) / 128 + 1 : nblk;
+    const int lo = window_left >= 0 ? std::max(0, off + i0 - window_left) / 128 : 0;
+    k.max_blocks = std::max(k.max_blocks, hi - lo);
+  }
+  return k;
+}
+
+// Splits that fill the SMs with one wave of CTAs, keeping at least 2 key blocks per
+// split and at most kKvMaxSplits.
+int kv_auto_splits(const KvPlan& k, int sms) {
+  int s = std::max(1, sms / std::max(1, k.items));
+  s = std::min(s, std::max(1, k.max_blocks / 2));
+  return std::min(s, kKvMaxSplits);
+}
+
+size_t kv_workspace_bytes(int B, int Lq, int Hq, int d, int splits) {
+  if (splits <= 1) return kWorkspaceBytes;
+  const size_t rows = (size_t)B * Hq * Lq;
+  const size_t lse_bytes = ((size_t)splits * rows * 4 + 255) / 256 * 256;
+  return kWorkspaceBytes + lse_bytes + (size_t)splits * rows * d * 4;
+}
+
+int current_sms(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  DeviceInfo info;
+  if (e != cudaSuccess || !device_info(dev, &info, &e)) {
+    cudaGetLastError();
+    return -1;
+  }
+  *sms = info.sms;
+  return 0;
 }
 
 }  // namespace
@@ -235,6 +307,117 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
   const bool out_f32 = out_dtype == ATTN_OUT_FP32;
   e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return ATTN_OK;
+}
+
+int attn_fwd_kv_num_splits(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                           int window_left) {
+  if (check_kv_shape(B, Lq, Lk, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
+  int sms = 0;
+  if (current_sms(&sms) != 0) {
+    fail(ATTN_ERR_CUDA, "no CUDA device");
+    return 0;
+  }
+  return kv_auto_splits(kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left), sms);
+}
+
+size_t attn_fwd_kv_workspace_size(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                                  int window_left, int num_splits) {
+  if (check_kv_shape(B, Lq, Lk, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
+  if (num_splits < 0 || num_splits > kKvMaxSplits) return 0;
+  if (num_splits == 0) {
+    num_splits = attn_fwd_kv_num_splits(B, Lq, Lk, Hq, Hkv, d, causal, window_left);
+    if (num_splits == 0) return 0;
+  }
+  return kv_workspace_bytes(B, Lq, Hq, d, num_splits);
+}
+
+attn_status_t attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                          int window_left, float scale, attn_dtype_t dtype, attn_out_t out_dtype,
+                          int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  g_detail.clear();
+  attn_status_t st = check_kv_shape(B, Lq, Lk, Hq, Hkv, d, causal, window_left);
+  if (st != ATTN_OK) return st;
+  if (num_splits < 0 || num_splits > kKvMaxSplits)
+    return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [0, 256]");
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "bad dtype");
+  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
+  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
+  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  const KvPlan plan = kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left);
+  if (num_splits > 0 && workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, num_splits))
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms);
+  if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits))
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
+  if ((long long)plan.items * splits >= (1LL << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "too many work items");
+  std::string why;
+  const void* ptrs[6] = {q, k, v, o, workspace, lse};
+  const char* names[6] = {"q", "k", "v", "o", "workspace", "lse"};
+  for (int i = 0; i < 6; ++i)
+    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
+      return fail(ATTN_ERR_INVALID_ARG, why);
+
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_tensor_map(&tm_q, q, bf16, B, Lq, Hq, d, &why, plan.group, plan.q_per_tile) ||
+      !make_tensor_map(&tm_k, k, bf16, B, Lk, Hkv, d, &why) ||
+      !make_tensor_map(&tm_v, v, bf16, B, Lk, Hkv, d, &why))
+    return fail(ATTN_ERR_CUDA, why);
+
+  ex19::KvLaunchArgs a;
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  ex19::KvParams& p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.status = static_cast<uint32_t*>(workspace);
+  const size_t rows = (size_t)B * Hq * Lq;
+  if (splits > 1) {
+    char* base = static_cast<char*>(workspace) + kWorkspaceBytes;
+    p.lse_part = reinterpret_cast<float*>(base);
+    p.o_part = reinterpret_cast<float*>(base + ((size_t)splits * rows * 4 + 255) / 256 * 256);
+  } else {
+    p.lse_part = nullptr;
+    p.o_part = nullptr;
+  }
+  p.B = B;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = plan.group;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f ? 1 : 0;
+  p.q_per_tile = plan.q_per_tile;
+  p.row_tiles = plan.row_tiles;
+  p.splits = splits;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.grid = plan.items * splits;
+  a.stream = static_cast<cudaStream_t>(stream);
+  e = ex19::launch_kv(d, bf16, out_dtype == ATTN_OUT_FP32, a);
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
 }

@@ -35,6 +35,7 @@
 #include <type_traits>
 
 #include "attn_params.h"
+#include "row_ops.cuh"
 #include "sm103_ptx.cuh"
 #include "tmem_io.cuh"
 
@@ -63,9 +64,6 @@ constexpr float kRescaleThreshold = 8.0f;
 #endif
 #ifndef EX19_ONEPASS
 #define EX19_ONEPASS 1  // S read from TMEM once (1) or twice, max then exponentials (0)
-#endif
-#ifndef EX19_MAX3
-#define EX19_MAX3 0  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
 #endif
 #ifndef EX19_POLY_PAIRS
 #define EX19_POLY_PAIRS 0  // exp2 polynomial offload: pairs out of every 8 (0 = all on MUFU)
@@ -161,62 +159,6 @@ __device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
 }
 
 __device__ __forceinline__ bool has_block(const TileSpan& s, int j) { return j >= s.lo && j < s.hi; }
-
-// Maximum of a 128-value row: 8 independent chains (16 values each), then a tree.
-__device__ __forceinline__ float row_max128(const float (&s)[128]) {
-  float m[8];
-#if EX19_MAX3
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = max3f(s[i], s[8 + i], s[16 + i]);
-#pragma unroll
-    for (int k = 24; k < 120; k += 16) a = max3f(a, s[k + i], s[k + 8 + i]);  // 24 .. 112
-    m[i] = fmaxf(a, s[120 + i]);
-  }
-  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
-#else
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = s[i];
-#pragma unroll
-    for (int k = 8; k < 128; k += 8) a = fmaxf(a, s[k + i]);
-    m[i] = a;
-  }
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-#endif
-}
-
-// Minimum of a 128-value row (used when the scale is negative).
-__device__ __forceinline__ float row_min128(const float (&s)[128]) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = s[i];
-#pragma unroll
-    for (int k = 8; k < 128; k += 8) a = fminf(a, s[k + i]);
-    m[i] = a;
-  }
-  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
-  if (bf16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float low_as_float(uint32_t packed, bool bf16) {
-  if (bf16) return __uint_as_float(packed << 16);
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(packed & 0xFFFFu)));
-}
-
-__device__ __forceinline__ float high_as_float(uint32_t packed, bool bf16) {
-  if (bf16) return __uint_as_float(packed & 0xFFFF0000u);
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(packed >> 16)));
-}
 
 template <int D, bool BF16, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)

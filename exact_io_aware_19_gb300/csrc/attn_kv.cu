@@ -1,0 +1,45 @@
+// Instantiations of the decode-shaped (split-KV) forward and its merge kernel.
+#include <atomic>
+
+#include "attn_kv_kernel.cuh"
+#include "attn_launch.h"
+
+namespace ex19 {
+namespace {
+
+template <int D, bool BF16, bool OUT_F32>
+cudaError_t launch_kv_one(const KvLaunchArgs& a) {
+  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32>;
+  constexpr int smem = kv::KvGeometry<D>::kSmemBytes;
+  static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev < 64) ? (1ull << dev) : 0ull;
+  if (bit == 0 || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  kern<<<a.grid, kv::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, a.p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.p.splits <= 1) return e;
+  const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
+  kv::attn_kv_merge_kernel<D, BF16, OUT_F32>
+      <<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(a.p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_kv_d(bool bf16, bool out_f32, const KvLaunchArgs& a) {
+  if (bf16) return out_f32 ? launch_kv_one<D, true, true>(a) : launch_kv_one<D, true, false>(a);
+  return out_f32 ? launch_kv_one<D, false, true>(a) : launch_kv_one<D, false, false>(a);
+}
+
+}  // namespace
+
+cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a) {
+  return (d == 64) ? launch_kv_d<64>(bf16, out_f32, a) : launch_kv_d<128>(bf16, out_f32, a);
+}
+
+}  // namespace ex19

@@ -1,0 +1,536 @@
+// attn_kv_kernel.cuh — decode-shaped (split-KV) exact attention forward for sm_103a.
+//
+// What it computes: the attention of the square kernel for Lq query rows that are
+// the last Lq positions of an Lk-long sequence (row i sits at position
+// Lk - Lq + i; causal and window masks are taken at that position). This is a
+// generation step reading the whole KV cache, the case "What is memory-efficient
+// attention for long context on 8x H100?" (section 1, key limitations) names as
+// bound by HBM bandwidth. The keys of a row tile may be cut into `splits`
+// consecutive ranges computed by different CTAs; each writes its partial O / l
+// and log2-sum-exp, and attn_kv_merge_kernel combines them by their log-sum-exp
+// (attention computed in parts, same page, section 4).
+//
+// GB300 mapping (one CTA per (batch, K/V head, row tile, key split)):
+//   * The `group` query heads that read one K/V head are packed into the rows of
+//     one 128-row tile: row r of the tile is query position i0 + r / group, head
+//     g * group + r % group. One TMA box {64 of d, group heads, q_per_tile rows}
+//     lands the tile in shared memory in exactly that order, so K and V stream
+//     once per group instead of once per query head.
+//   * warp 4 (producer): TMA loads of Q and of K_j, V_j into a ring of slots.
+//   * warp 5 (MMA): one elected lane issues every tcgen05.mma. Block j's
+//     S = Q K_jᵀ goes to TMEM buffer j mod 2 (128 fp32 columns); the softmax
+//     overwrites its first columns with P; O += P V_j reads P back from there.
+//     S(j + 2) is issued after P·V(j), so buffer reuse needs no barrier (MMAs of
+//     one thread run in issue order), and S(j + 1) runs under the softmax of j.
+//   * warps 0-3 (softmax): one thread per tile row (TMEM lane), as in the square
+//     kernel: running max m (base-2 units) and sum l, P = 2^(x - m), conditional
+//     O rescale, and at the end O / l and the log-sum-exp.
+//   * Every wait is bounded; a timeout sets the status word and all roles leave.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "attn_kv_params.h"
+#include "row_ops.cuh"
+#include "sm103_ptx.cuh"
+#include "tmem_io.cuh"
+
+namespace ex19 {
+namespace kv {
+
+constexpr int kBM = 128;             // rows per tile (= TMEM lanes)
+constexpr int kBN = 128;             // keys per K/V block
+constexpr int kThreads = 192;        // 4 softmax warps + producer warp + MMA warp
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256 + D)
+constexpr uint32_t kColO = 256;
+
+enum : uint32_t {
+  kSiteProdEmpty = 0x50001,
+  kSiteMmaQFull = 0x60001, kSiteMmaKFull = 0x60002, kSiteMmaVFull = 0x60003,
+  kSiteMmaPFull = 0x60004, kSiteMmaDrain = 0x60005,
+  kSiteSmxSFull = 0x70001, kSiteSmxOFull = 0x70002, kSiteSmxPvDone = 0x70003,
+  kSiteDrainLoads = 0x80001,
+};
+
+template <int D>
+struct KvGeometry {
+  static constexpr int kChunks = D / 64;          // 128-byte swizzle boxes per row
+  static constexpr int kChunkBytes = kBM * 128;   // one box column of a 128-row tile
+  static constexpr int kTileBytes = kBM * D * 2;  // a 128-row tile of Q, K or V
+  static constexpr int kSlots = (D == 64) ? 8 : 5;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kTileBytes;
+  static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
+  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full, drain
+  static constexpr int kNumBars = 2 * kSlots + 9;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemUsed = kOffMisc + 16;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
+};
+
+// The work item of this CTA and its key blocks [lo, hi).
+struct KvItem {
+  int b, g, split;
+  int i0, i1;  // query positions [i0, i1) of the tile
+  int lo, hi;  // key blocks of this split
+};
+
+__device__ __forceinline__ KvItem kv_item(const KvParams& p) {
+  KvItem it;
+  int x = blockIdx.x;
+  it.split = x % p.splits;
+  x /= p.splits;
+  const int rt = x % p.row_tiles;
+  x /= p.row_tiles;
+  it.g = x % p.Hkv;
+  it.b = x / p.Hkv;
+  it.i0 = rt * p.q_per_tile;
+  it.i1 = min(p.Lq, it.i0 + p.q_per_tile);
+  const int off = p.Lk - p.Lq;  // position of query row 0
+  const int nblk = (p.Lk + kBN - 1) / kBN;
+  const int blk_hi = p.causal ? (off + it.i1 - 1) / kBN + 1 : nblk;
+  const int blk_lo = (p.window_left >= 0) ? max(0, off + it.i0 - p.window_left) / kBN : 0;
+  const long long n = blk_hi - blk_lo;
+  it.lo = blk_lo + static_cast<int>(n * it.split / p.splits);
+  it.hi = blk_lo + static_cast<int>(n * (it.split + 1) / p.splits);
+  return it;
+}
+
+template <int D, bool BF16, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kv_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const KvParams p) {
+  using G = KvGeometry<D>;
+  constexpr int S = G::kSlots;
+  constexpr bool kSplitP = BF16;  // bf16 P as hi + lo halves (two P·V MMAs)
+  constexpr bool kF16Exp = !BF16;  // fp16: exponentials on packed fp16 pairs
+  constexpr float kThresh = kF16Exp ? 1.0f : 8.0f;  // log2 units of max growth before a rescale
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + G::kOffQ;
+  const uint32_t sKV = sbase + G::kOffKV;
+  const uint32_t bars = sbase + G::kOffBar;
+  auto bar_full = [&](uint32_t s) { return bars + 8u * s; };
+  auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
+  const uint32_t bar_q_full = bars + 8u * (2 * S);
+  auto bar_s_full = [&](uint32_t b) { return bars + 8u * (2 * S + 1 + b); };
+  auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 3 + b); };
+  auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
+  const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
+  const uint32_t bar_drain = bars + 8u * (2 * S + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const KvItem it = kv_item(p);
+  const int nblocks = max(0, it.hi - it.lo);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_s_full(b), 1);
+      mbar_init(bar_p_full(b), kBM);
+      mbar_init(bar_pv_done(b), 1);
+    }
+    mbar_init(bar_o_full, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  WaitCtl wc;
+  wc.abort_flag = abort_flag;
+  wc.status = p.status;
+  wc.limit_ns = p.wait_limit_ns;
+  wc.unit = blockIdx.x;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nblocks > 0) {
+      // The Q box is {64, group, q_per_tile, 1}; rows past Lq are zero-filled and
+      // still counted in the transaction bytes.
+      mbar_arrive_expect_tx(bar_q_full, G::kChunks * 128u * p.group * p.q_per_tile);
+      for (int c = 0; c < G::kChunks; ++c)
+        tma_load_4d(sQ + c * G::kChunkBytes, &tm_q, bar_q_full, c * 64, it.g * p.group, it.i0,
+                    it.b);
+      uint32_t n = 0;
+      bool ok = true;
+      for (int j = it.lo; ok && j < it.hi; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t slot = n % S;
+          ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
+          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+          for (int c = 0; c < G::kChunks; ++c)
+            tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
+                        c * 64, it.g, j * kBN, it.b);
+          ++n;
+        }
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA can exit.
+        for (uint32_t back = 1; back <= S && back <= n; ++back) {
+          const uint32_t m = n - back;
+          mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrainLoads);
+        }
+        mbar_wait_drain(bar_q_full, 0, wc, kSiteDrainLoads);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------- MMA issuer
+    if (nblocks > 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kBN, false);
+      constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, kBM, D, true);
+      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);               // Q tile, K-major
+      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);              // K slots, K-major
+      const uint64_t dv = sdesc_sw128(sKV, G::kChunkBytes, 1024);  // V slots, MN-major
+      const uint32_t mO = tmem_base + kColO;
+      auto slot_of = [&](uint32_t idx) { return idx % S; };
+      auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
+      // S = Q · K_jᵀ (block jj of the split) into buffer jj & 1; releases K_j.
+      auto issue_s = [&](int jj) __attribute__((always_inline)) -> bool {
+        const uint32_t kidx = 2u * jj;
+        if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull)) return false;
+        tc_fence_after();
+        const uint32_t mS = tmem_base + 128u * (jj & 1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+          mma_ss_elect(mS, dq + (off >> 4), dk + ((slot_of(kidx) * G::kTileBytes + off) >> 4),
+                       idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(bar_s_full(jj & 1));
+        mma_commit_elect(bar_empty(slot_of(kidx)));
+        return true;
+      };
+      // O (+)= P · V_j once the softmax has written P into buffer jj & 1; releases V_j.
+      auto issue_pv = [&](int jj) __attribute__((always_inline)) -> bool {
+        const uint32_t vidx = 2u * jj + 1u;
+        if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
+        if (!mbar_wait_warp(bar_p_full(jj & 1), (jj >> 1) & 1u, wc, kSiteMmaPFull)) return false;
+        tc_fence_after();
+        const uint32_t mP = tmem_base + 128u * (jj & 1);
+        const uint64_t dvs = dv + ((slot_of(vidx) * G::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
+          mma_ts_elect(mO, mP + pcol, dvs + ((kk * 2048) >> 4), idesc_o,
+                       (jj == 0 && kk == 0) ? 0u : 1u);
+        }
+        if constexpr (kSplitP) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint32_t pcol = (kk >> 2) * 64 + 32 + (kk & 3) * 8;
+            mma_ts_elect(mO, mP + pcol, dvs + ((kk * 2048) >> 4), idesc_o, 1u);
+          }
+        }
+        mma_commit_elect(bar_pv_done(jj & 1));
+        mma_commit_elect(bar_empty(slot_of(vidx)));
+        return true;
+      };
+      bool ok = mbar_wait_warp(bar_q_full, 0, wc, kSiteMmaQFull);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+        if (ok && nblocks > 1) ok = issue_s(1);
+        for (int jj = 0; ok && jj < nblocks; ++jj) {
+          ok = issue_pv(jj);
+          if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
+        }
+        if (ok) mma_commit_elect(bar_o_full);
+      }
+    }
+    // Every MMA this warp issued has finished once the drain barrier flips.
+    mma_commit_elect(bar_drain);
+    mbar_wait_drain(bar_drain, 0, wc, kSiteMmaDrain);
+  } else {
+    // -------------------------------------------------------- softmax warps
+    const int rho = warp * 32 + lane;  // row of the tile
+    const bool row_ok = rho < (it.i1 - it.i0) * p.group;
+    const int qi = it.i0 + rho / p.group;  // query position (may be >= Lq for unused rows)
+    const int h = it.g * p.group + rho % p.group;
+    const int off = p.Lk - p.Lq;
+    const int pos = off + qi;
+    const int pos_min = off + it.i0, pos_max = off + it.i1 - 1;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem_base + lane_off + kColO;
+    const float C = p.score_log2;
+    const bool neg = p.negate_scores != 0;
+    const float Cs = neg ? -C : C;  // x = Cs · s carries the sign of the scale
+    float m_ref = -INFINITY;        // reference max (base-2 units)
+    float l = 0.f;                  // running sum of P
+    bool ok = true;
+    for (int jj = 0; jj < nblocks; ++jj) {
+      const int j = it.lo + jj;
+      const uint32_t buf = jj & 1;
+      ok = mbar_wait_warp(bar_s_full(buf), (jj >> 1) & 1u, wc, kSiteSmxSFull);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tmem_base + lane_off + 128u * buf;  // S, then P, of this block
+      const int key0 = j * kBN;
+      const bool masked = (key0 + kBN > p.Lk) || (p.causal && key0 + kBN - 1 > pos_min) ||
+                          (p.window_left >= 0 && key0 < pos_max - p.window_left);
+      int vis_lo = 0, vis_hi = kBN;  // visible columns of this row: [vis_lo, vis_hi)
+      if (masked) {
+        const int hi_key = p.causal ? min(p.Lk, pos + 1) : p.Lk;
+        const int lo_key = (p.window_left >= 0) ? pos - p.window_left : 0;
+        vis_hi = max(0, min(kBN, hi_key - key0));
+        vis_lo = max(0, min(kBN, lo_key - key0));
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
+        constexpr bool M = decltype(masked_tag)::value;
+        uint32_t sr[128];
+        tmem_ld_x128(tS, sr);
+        if constexpr (M) {  // masked keys: -inf for the max (+inf for the min), p = 0 below
+          const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < vis_lo || c >= vis_hi) sr[c] = fill;
+        }
+        float mx;
+        {
+          float sv[128];
+#pragma unroll
+          for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
+          mx = neg ? -row_min128(sv) : row_max128(sv);
+        }
+        const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
+        if (bm > m_ref + kThresh) {
+          alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
+          m_ref = bm;
+          rescale = true;
+        }
+        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t pk[16];
+          uint32_t pk_lo[16];
+          uint32_t prev = 0;
+#pragma unroll
+          for (int c = c0; c < c0 + 32; c += 2) {
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                make_float2(Cs, Cs), make_float2(-mu, -mu));
+            if constexpr (kF16Exp) {
+              __half2 xh = __floats2half2_rn(x.x, x.y);
+              uint32_t pp = ex2_f16x2(*reinterpret_cast<uint32_t*>(&xh));
+              if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
+                const uint32_t keep = ((c >= vis_lo && c < vis_hi) ? 0x0000FFFFu : 0u) |
+                                      ((c + 1 >= vis_lo && c + 1 < vis_hi) ? 0xFFFF0000u : 0u);
+                pp &= keep;
+              }
+              pk[(c - c0) >> 1] = pp;
+              if ((c & 2) == 0) {
+                prev = pp;
+              } else {  // two packed pairs summed in fp16, then accumulated in fp32
+                const __half2 s2 = __hadd2(*reinterpret_cast<__half2*>(&prev),
+                                           *reinterpret_cast<__half2*>(&pp));
+                acc[(c >> 2) & 1] = __fadd2_rn(acc[(c >> 2) & 1], __half22float2(s2));
+              }
+            } else {
+              float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              if constexpr (M) {
+                p0 = (c >= vis_lo && c < vis_hi) ? p0 : 0.f;
+                p1 = (c + 1 >= vis_lo && c + 1 < vis_hi) ? p1 : 0.f;
+              }
+              acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
+              const uint32_t hi = pack2(p0, p1, BF16);
+              pk[(c - c0) >> 1] = hi;
+              if constexpr (kSplitP)
+                pk_lo[(c - c0) >> 1] =
+                    pack2(p0 - low_as_float(hi, BF16), p1 - high_as_float(hi, BF16), BF16);
+            }
+          }
+          // P over the scores this thread already holds: column c/2 (fp16), or for
+          // split P each 64-key half h as [hi 32 columns | lo 32 columns] at 64h.
+          if constexpr (kSplitP) {
+            const int hh = c0 >> 6, cl = c0 & 63;
+            tmem_st_x16(tS + 64 * hh + (cl >> 1), pk);
+            tmem_st_x16(tS + 64 * hh + 32 + (cl >> 1), pk_lo);
+          } else {
+            tmem_st_x16(tS + (c0 >> 1), pk);
+          }
+        }
+        l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
+      };
+      if (masked)
+        block_body(std::true_type{});
+      else
+        block_body(std::false_type{});
+      // O rescale once the previous P·V (which accumulates into O) is complete;
+      // the first block's P·V overwrites O.
+      if (__any_sync(0xffffffffu, rescale && jj > 0)) {
+        if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float a = (rescale && jj > 0) ? alpha : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t orow[32];
+          tmem_ld_x32(tO + c0, orow);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * a);
+          tmem_st_x32(tO + c0, orow);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p_full(buf));
+    }
+    if (ok && nblocks > 0) {
+      ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteSmxOFull);
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      // ---- epilogue: O / l and the log-sum-exp of this row over this split
+      const bool have = nblocks > 0;
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const size_t row = (static_cast<size_t>(it.b) * p.Hq + h) * p.Lq + qi;  // LSE index
+      const bool partial = p.splits > 1;
+      const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t orow[32];
+        if (have) {
+          tmem_ld_x32(tO + c0, orow);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orow[c] = 0u;
+        }
+        if (!row_ok) continue;
+        if (partial || OUT_F32) {
+          float* dst = partial ? p.o_part + (static_cast<size_t>(it.split) * nrows + row) * D + c0
+                               : static_cast<float*>(p.o) +
+                                     ((static_cast<size_t>(it.b) * p.Lq + qi) * p.Hq + h) * D + c0;
+          float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            d4[c >> 2] = make_float4(__uint_as_float(orow[c]) * inv_l,
+                                     __uint_as_float(orow[c + 1]) * inv_l,
+                                     __uint_as_float(orow[c + 2]) * inv_l,
+                                     __uint_as_float(orow[c + 3]) * inv_l);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(
+              static_cast<uint16_t*>(p.o) + ((static_cast<size_t>(it.b) * p.Lq + qi) * p.Hq + h) * D +
+              c0);
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(orow[c]) * inv_l, __uint_as_float(orow[c + 1]) * inv_l, BF16);
+            w.y = pack2(__uint_as_float(orow[c + 2]) * inv_l, __uint_as_float(orow[c + 3]) * inv_l, BF16);
+            w.z = pack2(__uint_as_float(orow[c + 4]) * inv_l, __uint_as_float(orow[c + 5]) * inv_l, BF16);
+            w.w = pack2(__uint_as_float(orow[c + 6]) * inv_l, __uint_as_float(orow[c + 7]) * inv_l, BF16);
+            dst[c >> 3] = w;
+          }
+        }
+      }
+      if (row_ok) {
+        const float lse2 = (l > 0.f) ? m_ref + lg2_approx(l) : -INFINITY;  // base 2
+        if (partial)
+          p.lse_part[static_cast<size_t>(it.split) * nrows + row] = lse2;
+        else if (p.lse != nullptr)
+          p.lse[row] = (l > 0.f) ? lse2 * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Combines the splits of each row: with L_s the partial log2-sum-exp of split s,
+// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One warp per row; each lane
+// owns D / 32 consecutive columns.
+template <int D, bool BF16, bool OUT_F32>
+__global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
+  constexpr int kCols = D / 32;
+  const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= nrows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) m = fmaxf(m, p.lse_part[s * nrows + row]);
+  float acc[kCols];
+#pragma unroll
+  for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+  float lse2 = -INFINITY;
+  if (m != -INFINITY) {
+    float total = 0.f;
+    for (int s = 0; s < p.splits; ++s) total += exp2f(p.lse_part[s * nrows + row] - m);
+    lse2 = m + log2f(total);
+    for (int s = 0; s < p.splits; ++s) {
+      const float w = exp2f(p.lse_part[s * nrows + row] - lse2);
+      if (w == 0.f) continue;  // an empty split (its partial O is zero)
+      const float* src = p.o_part + (s * nrows + row) * D + lane * kCols;
+      if constexpr (kCols == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+  }
+  const int qi = static_cast<int>(row % p.Lq);
+  const int h = static_cast<int>((row / p.Lq) % p.Hq);
+  const int b = static_cast<int>(row / (static_cast<size_t>(p.Lq) * p.Hq));
+  const size_t o_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * D + lane * kCols;
+  if constexpr (OUT_F32) {
+    float* dst = static_cast<float*>(p.o) + o_off;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) dst[c] = acc[c];
+  } else {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + o_off);
+#pragma unroll
+    for (int c = 0; c < kCols; c += 2) dst[c >> 1] = pack2(acc[c], acc[c + 1], BF16);
+  }
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[row] = (lse2 == -INFINITY) ? -INFINITY : lse2 * 0.69314718055994531f;
+}
+
+}  // namespace kv
+}  // namespace ex19

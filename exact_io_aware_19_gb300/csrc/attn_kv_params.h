@@ -1,0 +1,26 @@
+// attn_kv_params.h — parameter block of the decode-shaped (split-KV) forward, shared
+// by the host launcher and the kernels.
+#pragma once
+#include <cstdint>
+
+namespace ex19 {
+
+struct KvParams {
+  void* o;              // [B, Lq, Hq, D], input dtype or float32
+  float* lse;           // [B, Hq, Lq] or null
+  uint32_t* status;     // 4 x u32 status word in the workspace
+  float* o_part;        // [splits, B*Hq*Lq, D] float32 partial outputs (splits > 1), else null
+  float* lse_part;      // [splits, B*Hq*Lq] partial log2-sum-exp (splits > 1), else null
+  int B, Lq, Lk, Hq, Hkv;
+  int group;            // Hq / Hkv: query heads that read one K/V head
+  int causal;           // 0 / 1
+  int window_left;      // -1 or >= 0
+  float score_log2;     // |scale| * log2(e)
+  int negate_scores;    // 1 when scale < 0
+  int q_per_tile;       // query positions per 128-row tile (each with all `group` heads)
+  int row_tiles;        // ceil(Lq / q_per_tile)
+  int splits;           // key-range splits per (batch, K/V head, row tile)
+  unsigned long long wait_limit_ns;
+};
+
+}  // namespace ex19

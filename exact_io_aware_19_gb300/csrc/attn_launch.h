@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "attn_kv_params.h"
 #include "attn_params.h"
 
 namespace ex19 {
@@ -16,9 +17,20 @@ struct LaunchArgs {
   cudaStream_t stream;
 };
 
+struct KvLaunchArgs {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  KvParams p;
+  int grid;  // B * Hkv * row_tiles * splits
+  cudaStream_t stream;
+};
+
 // Each returns the CUDA error of configuring / enqueuing the kernel.
 cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
+// The decode-shaped forward (and, when p.splits > 1, its merge kernel).
+cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream);

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 typedef enum {
     ATTN_OK = 0,
@@ -116,6 +116,45 @@ attn_status_t attn_fwd_noalloc(const void *q, const void *k, const void *v, void
                                int B, int L, int Hq, int Hkv, int d, int causal,
                                int window_left, float scale, attn_dtype_t dtype,
                                attn_out_t out_dtype, void *stream);
+
+/*
+ * Decode-shaped forward: Lq query rows that are the LAST Lq positions of an
+ * Lk-long sequence whose keys and values are all given, as in a generation step
+ * that reads the whole KV cache ("What is memory-efficient attention for long
+ * context on 8x H100?", section 1, key limitations: each step reads O(n) cached
+ * data, so the step is bound by HBM bandwidth). Query row i sits at position
+ * p_i = Lk - Lq + i, and its visible keys are
+ *   J_i = { j < Lk : (causal => j <= p_i) and (window_left >= 0 => j >= p_i - window_left) },
+ * with O and LSE defined over J_i exactly as for attn_fwd (Lq = Lk gives attn_fwd's
+ * result). The keys of each row tile may be cut into `num_splits` consecutive
+ * ranges that run in parallel; their partial results are combined by their
+ * log-sum-exp (LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s; the same
+ * page, section 4, computes attention in parts this way), which gives the same O
+ * and LSE up to rounding.
+ *
+ * Layouts: q, o : [B, Lq, Hq, d]   k, v : [B, Lk, Hkv, d]   lse : [B, Hq, Lq] float32.
+ * Arguments as for attn_fwd, plus
+ *   Lq, Lk      1 <= Lq <= Lk; B*Hq*Lq < 2^31 and B*Hkv*Lk < 2^31
+ *   Hq / Hkv    at most 128 (the query heads of one K/V head share a 128-row tile)
+ *   num_splits  0 = the library's choice (attn_fwd_kv_num_splits), else 1..256
+ *   workspace   >= attn_fwd_kv_workspace_size(..., num_splits) bytes: a status word
+ *               and, when splits > 1, the float32 partial results
+ * Enqueues one kernel, plus a merge kernel when splits > 1, on `stream`.
+ *
+ * attn_fwd_kv_num_splits returns the split count attn_fwd_kv uses for num_splits
+ * = 0 on the current device (0 for rejected sizes or no device);
+ * attn_fwd_kv_workspace_size returns the workspace bytes of attn_fwd_kv for a split
+ * count (0 = the library's choice), or 0 for rejected sizes.
+ */
+int attn_fwd_kv_num_splits(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                           int window_left);
+size_t attn_fwd_kv_workspace_size(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                                  int window_left, int num_splits);
+attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
+                          int window_left, float scale, attn_dtype_t dtype,
+                          attn_out_t out_dtype, int num_splits, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /*
  * Synchronises `stream`, reads the workspace status word written by earlier

@@ -11,6 +11,11 @@ Workload shapes follow the pages:
   * "Flash Attention optimization" skill page (hermes-agent, mlops-flash-attention),
     workflow 1 steps 3-4: fp16, 2x8x{512,2048}x64, non-causal, scale 1/8; workflow 2
     step 3: fewer K/V heads (MQA/GQA) and a sliding window.
+  * Decode-shaped problems (a generation step reads the whole KV cache, "What is
+    memory-efficient attention for long context on 8x H100?", section 1): the pages
+    give no decode shapes, so the grouped-query model shape above (32 query heads,
+    8 K/V heads, d = 128, bf16) and the 4-head d = 64 fp16 shape are taken with 1
+    new query against 4k ... 128k cached keys.
 
 No seed is printed on the pages. The reading taken here: a CPU ``torch.Generator``
 seeded with ``seed``; Q, K and V are drawn in that order as float32 N(0, 1), then
@@ -77,6 +82,48 @@ class Workload:
         return q + kv + o + lse
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Lq new queries (the last Lq positions) against an Lk-long K/V sequence."""
+
+    name: str
+    B: int
+    Lq: int
+    Lk: int
+    Hq: int
+    Hkv: int
+    d: int
+    dtype: str
+    causal: bool
+    window_left: int
+    scale: float
+    seed: int
+
+    def with_lk(self, Lk: int) -> "DecodeWorkload":
+        return replace(self, Lk=Lk, name=f"{self.name.rsplit('_Lk', 1)[0]}_Lk{Lk}")
+
+    def with_lq(self, Lq: int) -> "DecodeWorkload":
+        return replace(self, Lq=Lq, name=self.name.replace(f"_Lq{self.Lq}_", f"_Lq{Lq}_"))
+
+    def visible_pairs(self) -> int:
+        """Visible (query, key) pairs per (batch, head); query i sits at Lk - Lq + i."""
+        pos = self.Lk - self.Lq + np.arange(self.Lq, dtype=np.int64)
+        hi = pos + 1 if self.causal else np.full_like(pos, self.Lk)
+        lo = np.maximum(0, pos - self.window_left) if self.window_left >= 0 else np.zeros_like(pos)
+        return int(np.sum(hi - lo))
+
+    def algorithmic_flop(self) -> float:
+        return 4.0 * self.d * self.visible_pairs() * self.B * self.Hq
+
+    def algorithmic_bytes(self, out_fp32: bool = False) -> int:
+        """Q and the K/V cache read once; O and LSE written once."""
+        e = 2
+        q = self.B * self.Lq * self.Hq * self.d * e
+        kv = 2 * self.B * self.Lk * self.Hkv * self.d * e
+        o = self.B * self.Lq * self.Hq * self.d * (4 if out_fp32 else e)
+        return q + kv + o + self.B * self.Hq * self.Lq * 4
+
+
 def _torch_dtype(name: str) -> torch.dtype:
     return {"fp16": torch.float16, "bf16": torch.bfloat16}[name]
 
@@ -100,6 +147,14 @@ WINDOW_B4_H16_D128 = Workload(
     "window4096_b4_h16_d128_bf16_L32768", B=4, L=32768, Hq=16, Hkv=16, d=128,
     dtype="bf16", causal=True, window_left=4096, scale=1.0 / math.sqrt(128), seed=1005,
     key_row_period=64, key_row_mul=8.0)
+
+DECODE_GQA_B1_H32_KV8_D128 = DecodeWorkload(
+    "decode_gqa_b1_hq32_hkv8_d128_bf16_Lq1_Lk131072", B=1, Lq=1, Lk=131072, Hq=32, Hkv=8,
+    d=128, dtype="bf16", causal=True, window_left=-1, scale=1.0 / math.sqrt(128), seed=1007)
+DECODE_B1_H4_D64 = DecodeWorkload(
+    "decode_b1_h4_d64_fp16_Lq1_Lk131072", B=1, Lq=1, Lk=131072, Hq=4, Hkv=4, d=64,
+    dtype="fp16", causal=True, window_left=-1, scale=1.0 / 8.0, seed=1008)
+DECODE_LENGTHS = (4096, 16384, 65536, 131072)
 
 WORKLOADS: Dict[str, Workload] = {
     w.name: w for w in (
@@ -131,6 +186,29 @@ def make_qkv(w: Workload, device: Optional[str] = None):
     if device is not None:
         q, k, v = q.to(device), k.to(device), v.to(device)
     return q, k, v
+
+
+def make_qkv_decode(w: DecodeWorkload, device: Optional[str] = None):
+    """Q [B, Lq, Hq, d] and K, V [B, Lk, Hkv, d] for a decode-shaped workload: the
+    make_qkv recipe (CPU generator seeded with w.seed, Q then K then V, N(0, 1),
+    round-to-nearest-even cast)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    q = torch.randn(w.B, w.Lq, w.Hq, w.d, generator=g, dtype=torch.float32)
+    k = torch.randn(w.B, w.Lk, w.Hkv, w.d, generator=g, dtype=torch.float32)
+    v = torch.randn(w.B, w.Lk, w.Hkv, w.d, generator=g, dtype=torch.float32)
+    dt = _torch_dtype(w.dtype)
+    q, k, v = q.to(dt), k.to(dt), v.to(dt)
+    if device is not None:
+        q, k, v = q.to(device), k.to(device), v.to(device)
+    return q, k, v
+
+
+def random_qkv_decode(B, Lq, Lk, Hq, Hkv, d, dtype="fp16", seed=0, device=None):
+    """Small ad-hoc seeded decode-shaped inputs (same recipe as make_qkv_decode)."""
+    w = DecodeWorkload("adhoc", B=B, Lq=Lq, Lk=Lk, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype,
+                       causal=False, window_left=-1, scale=1.0, seed=seed)
+    return make_qkv_decode(w, device=device)
 
 
 def random_qkv(B, L, Hq, Hkv, d, dtype="fp16", seed=0, mul=1.0, device=None):

@@ -85,3 +85,35 @@ def compare(q, k, v, dtype, causal, wl, scale, rows=None, label=""):
     # the in-dtype LSE is the same computation; it must match the fp32-output run
     assert torch.equal(lse, lse16), f"{label}: LSE differs between output dtypes"
     return stats
+
+
+def compare_kv(q, k, v, dtype, causal, wl, scale, num_splits=0, rows=None, label=""):
+    """Decode-shaped parity: attn_fwd_kv (float32 and in-dtype output) against the
+    oracle's decode rows, with the tolerances above. Returns error statistics."""
+    import exact_io_aware_19_gb300 as ex
+    orc = oracle.default()
+    B, Lq, Hq, d = q.shape
+    if rows is None:
+        rows = np.arange(B * Hq * Lq, dtype=np.int64)
+    o_ref, lse_ref = orc.attn_rows_kv(si.bits16(q), si.bits16(k), si.bits16(v), dtype, causal,
+                                      wl, scale, rows)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o32, lse = ex.attn_fwd_kv(qc, kc, vc, causal=causal, window_left=wl, scale=scale,
+                              out_fp32=True, num_splits=num_splits)
+    o16, lse16 = ex.attn_fwd_kv(qc, kc, vc, causal=causal, window_left=wl, scale=scale,
+                                out_fp32=False, num_splits=num_splits)
+    ex.sync_status()
+    g32, glse = gather_rows(o32, lse, rows)
+    g16, _ = gather_rows(o16, lse16, rows)
+    assert np.isfinite(g32).all() and np.isfinite(glse).all(), f"{label}: non-finite output"
+    d32 = np.abs(g32 - o_ref)
+    dl = np.abs(glse - lse_ref)
+    d16 = np.abs(g16 - o_ref)
+    assert d32.max() <= MAX_ABS_O, f"{label}: max |dO| {d32.max():.3e} > {MAX_ABS_O}"
+    assert d32.mean() <= MEAN_ABS_O, f"{label}: mean |dO| {d32.mean():.3e} > {MEAN_ABS_O}"
+    assert dl.max() <= MAX_ABS_LSE, f"{label}: max |dLSE| {dl.max():.3e} > {MAX_ABS_LSE}"
+    worst = (d16 - (MAX_ABS_O + half_ulp(o_ref, dtype))).max()
+    assert worst <= 0, f"{label}: in-dtype output exceeds 4e-3 + half ulp by {worst:.3e}"
+    assert torch.equal(lse, lse16), f"{label}: LSE differs between output dtypes"
+    return dict(label=label, rows=int(len(rows)), max_dO=float(d32.max()),
+                mean_dO=float(d32.mean()), max_dLSE=float(dl.max()))

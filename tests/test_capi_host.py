@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(ex.library_path())
     missing = [n for n in declared_functions() if not hasattr(raw, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert lib.attn_abi_version() == 1
+    assert lib.attn_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -104,3 +104,52 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 8, 1, 64, dtype=torch.float16)
     with pytest.raises(TypeError):
         ex.attn_fwd(q, q, q)
+
+
+# --- decode-shaped entry points ----------------------------------------------------------
+
+def test_kv_workspace_size(lib):
+    # one split: the status word only
+    assert lib.attn_fwd_kv_workspace_size(1, 1, 131072, 32, 8, 128, 1, -1, 1) == 256
+    # four splits of 32 rows of d = 128: status + LSE parts (512 B, 256-aligned) + O parts
+    assert lib.attn_fwd_kv_workspace_size(1, 1, 131072, 32, 8, 128, 1, -1, 4) == \
+        256 + 512 + 4 * 32 * 128 * 4
+    for bad in [(1, 0, 16, 4, 4, 64, 1, -1, 1), (1, 17, 16, 4, 4, 64, 1, -1, 1),
+                (1, 1, 16, 4, 4, 96, 1, -1, 1), (1, 1, 16, 256, 1, 64, 1, -1, 1),
+                (1, 1, 16, 4, 4, 64, 0, 3, 1), (1, 1, 16, 4, 4, 64, 1, -1, -1),
+                (1, 1, 16, 4, 4, 64, 1, -1, 257), (1, 1, 16, 6, 4, 64, 1, -1, 1)]:
+        assert lib.attn_fwd_kv_workspace_size(*bad) == 0, bad
+
+
+def call_kv(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Lq=4, Lk=4096, Hq=32, Hkv=8, d=128, causal=1, wl=-1,
+             scale=0.088, dtype=1, out=0, splits=2, ws=A, wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.attn_fwd_kv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Lq"], a["Lk"],
+                           a["Hq"], a["Hkv"], a["d"], a["causal"], a["wl"], a["scale"], a["dtype"],
+                           a["out"], a["splits"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(Lq=0), 1), (dict(Lk=0), 1), (dict(Lq=8, Lk=4), 1), (dict(Hkv=0), 1),
+    (dict(Hq=12, Hkv=8), 1), (dict(Hq=256, Hkv=1), 2), (dict(d=96), 2), (dict(causal=2), 1),
+    (dict(causal=0, wl=8), 2), (dict(wl=-3), 1), (dict(splits=-1), 1), (dict(splits=257), 1),
+    (dict(scale=float("nan")), 1), (dict(dtype=3), 1), (dict(out=2), 1), (dict(q=None), 1),
+    (dict(v=A + 8), 1), (dict(lse=A + 1), 1), (dict(ws=None), 3), (dict(ws=A + 8), 3),
+    (dict(wsb=1024), 3),
+])
+def test_kv_invalid_arguments_are_rejected_before_launch(lib, kw, code):
+    assert call_kv(lib, **kw) == code
+    assert lib.attn_last_error_detail()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_kv_without_a_gpu(lib):
+    assert call_kv(lib) == 4
+    assert lib.attn_fwd_kv_num_splits(1, 1, 4096, 32, 8, 128, 1, -1) == 0
+
+
+def test_python_kv_binding_checks_shapes():
+    q = torch.zeros(1, 8, 4, 64, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        ex.attn_fwd_kv(q, q, q)  # CPU tensors
