@@ -14,6 +14,12 @@ sum of all ranks' flop over the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference: the pages ship
 no runnable code) on a bounded row sample of the same workload.
+
+The line also carries, outside the timed region, the rest of the length sweep and a
+``decode`` object: the decode-shaped forward (one new query against 128k cached
+keys, split-KV plus merge) timed with CUDA events and reported against the measured
+HBM bandwidth, since reading the KV cache is its bound ("What is memory-efficient
+attention for long context on 8x H100?", section 1).
 """
 from __future__ import annotations
 
@@ -329,7 +335,40 @@ def ours_arm(args, world, rank, local):
         sweep[str(w.L)] = {"ms": ms, "tflops": flop / ms / 1e9}
         ex.sync_status()
 
+    # ---- decode-shaped forward (split-KV + merge): HBM-bound, one line per workload
+    decode = {}
     peaks, src = measured_peaks()
+    if not args.no_decode:
+        for wd in (si.DECODE_GQA_B1_H32_KV8_D128, si.DECODE_B1_H4_D64):
+            qd, kd, vd = si.make_qkv_decode(wd, device=dev)
+            od = torch.empty_like(qd)
+            ld = torch.empty(wd.B, wd.Hq, wd.Lq, dtype=torch.float32, device=dev)
+            splits = ex.kv_num_splits(wd.B, wd.Lq, wd.Lk, wd.Hq, wd.Hkv, wd.d, wd.causal,
+                                      wd.window_left)
+            wsd = torch.zeros(ex.kv_workspace_size(wd.B, wd.Lq, wd.Lk, wd.Hq, wd.Hkv, wd.d,
+                                                   wd.causal, wd.window_left, splits),
+                              dtype=torch.uint8, device=dev)
+            times = []
+            for r in range(13):
+                flush.fill_(float(r))
+                a = torch.cuda.Event(enable_timing=True)
+                bb = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                ex.attn_fwd_kv_into(qd, kd, vd, od, ld, causal=wd.causal, scale=wd.scale,
+                                    num_splits=splits, workspace=wsd)
+                bb.record(stream)
+                torch.cuda.synchronize(dev)
+                if r >= 3:
+                    times.append(a.elapsed_time(bb))
+            ex.sync_status(wsd)
+            t = statistics.median(times)
+            gbs = wd.algorithmic_bytes() / (t * 1e-3) / 1e9
+            decode[wd.name] = {"us": t * 1e3, "GB/s": gbs, "splits": splits,
+                               "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
+                               "algorithmic_bytes": wd.algorithmic_bytes(),
+                               "launches_per_call": 2 if splits > 1 else 1}
+            del qd, kd, vd, od, ld, wsd
+
     peak = float(peaks["bf16_tflops"])
     achieved = flop / ms / 1e9  # TFLOP/s of one launch
     traffic = TRAFFIC_BY_SOURCE.get(kernel_source_hash())
@@ -367,6 +406,7 @@ def ours_arm(args, world, rank, local):
                 t.numel() * t.element_size() for t in (q, k, v, o, lse)),
             "library_extra_bytes": peak_hbm - base_alloc,
             "sweep": sweep,
+            "decode": decode,
             "launch_ms": {"min": min(per), "max": max(per), "wall_total_s": t_wall},
         }
         if cpu is not None:
@@ -383,6 +423,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

@@ -27,7 +27,8 @@ import torch
 
 __all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
-           "library_path", "load_library", "set_wait_limit_ns", "debug_wait_probe", "debug_exp2",
+           "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
+           "PATH_SQUARE", "PATH_TILES", "debug_wait_probe", "debug_exp2",
            "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -71,6 +72,10 @@ def _bind(lib):
     lib.attn_fwd_kv_num_splits.argtypes = [i, i, i, i, i, i, i, i]
     lib.attn_fwd_sync_status.restype = i
     lib.attn_fwd_sync_status.argtypes = [p, p]
+    lib.attn_set_path_policy.restype = None
+    lib.attn_set_path_policy.argtypes = [i]
+    lib.attn_get_path_policy.restype = i
+    lib.attn_get_path_policy.argtypes = []
     lib.attn_set_wait_limit_ns.restype = None
     lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.attn_debug_wait_probe.restype = i
@@ -256,6 +261,18 @@ def sync_status(workspace: Optional[torch.Tensor] = None, device=None, stream=No
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         workspace = _default_workspace(dev, 256)
     _check(lib.attn_fwd_sync_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+PATH_AUTO, PATH_SQUARE, PATH_TILES = 0, 1, 2
+
+
+def set_path_policy(policy: int) -> int:
+    """Choose attn_fwd's kernel process-wide (PATH_AUTO, PATH_SQUARE or PATH_TILES);
+    returns the previous setting."""
+    lib = load_library()
+    old = int(lib.attn_get_path_policy())
+    lib.attn_set_path_policy(int(policy))
+    return old
 
 
 def set_wait_limit_ns(limit_ns: int) -> None:

@@ -27,6 +27,7 @@ constexpr int kUnitRows = 256;           // query rows per kernel work unit
 
 thread_local std::string g_detail;
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_path_policy{ATTN_PATH_AUTO};
 
 attn_status_t fail(attn_status_t s, const std::string& msg) {
   g_detail = msg;
@@ -223,6 +224,52 @@ int current_sms(int* sms) {
   return 0;
 }
 
+// The square problem (validated by the caller) on the one-tile kernel: Lq = Lk = L,
+// one key split, so no partial results and no merge.
+attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int L, int Hq, int Hkv, int d, int causal,
+                                  int window_left, float scale, bool bf16, bool out_f32,
+                                  void* workspace, void* stream) {
+  const KvPlan plan = kv_plan(B, L, L, Hq, Hkv, causal, window_left);
+  if (plan.group > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
+  std::string why;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why, plan.group, plan.q_per_tile) ||
+      !make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) ||
+      !make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why))
+    return fail(ATTN_ERR_CUDA, why);
+  ex19::KvLaunchArgs a;
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  ex19::KvParams& p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.status = static_cast<uint32_t*>(workspace);
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.B = B;
+  p.Lq = L;
+  p.Lk = L;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = plan.group;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f ? 1 : 0;
+  p.q_per_tile = plan.q_per_tile;
+  p.row_tiles = plan.row_tiles;
+  p.splits = 1;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.grid = plan.items;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = ex19::launch_kv(d, bf16, out_f32, a);
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return ATTN_OK;
+}
+
 }  // namespace
 
 namespace ex19 {
@@ -275,6 +322,16 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
       return fail(ATTN_ERR_INVALID_ARG, why);
 
   const bool bf16 = dtype == ATTN_BF16;
+  const bool out_f32 = out_dtype == ATTN_OUT_FP32;
+  const int num_units = B * Hq * ((L + kUnitRows - 1) / kUnitRows);
+  // Problems with at most half as many 256-row units as SMs leave most SMs idle in
+  // the persistent two-tile kernel; the one-tile kernel (the decode-shaped path with
+  // Lq = Lk and one key split) runs 128-row tiles, twice as many CTAs.
+  const int policy = g_path_policy.load();
+  if (policy == ATTN_PATH_TILES ||
+      (policy == ATTN_PATH_AUTO && 2 * num_units <= info.sms && Hq / Hkv <= 128))
+    return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, scale,
+                               bf16, out_f32, workspace, stream);
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why) ||
       !make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) ||
@@ -298,14 +355,13 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f ? 1 : 0;
   p.units_per_bh = (L + kUnitRows - 1) / kUnitRows;
-  p.num_units = B * Hq * p.units_per_bh;
+  p.num_units = num_units;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.trace = EX19_TRACE ? reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + 256)
                        : nullptr;
   a.grid = p.num_units < info.sms ? p.num_units : info.sms;
   a.stream = static_cast<cudaStream_t>(stream);
 
-  const bool out_f32 = out_dtype == ATTN_OUT_FP32;
   e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
@@ -444,6 +500,13 @@ attn_status_t attn_fwd_sync_status(void* workspace, void* stream) {
                                                       : ATTN_ERR_CUDA;
   return fail(code, buf);
 }
+
+void attn_set_path_policy(int policy) {
+  g_path_policy.store((policy == ATTN_PATH_SQUARE || policy == ATTN_PATH_TILES) ? policy
+                                                                               : ATTN_PATH_AUTO);
+}
+
+int attn_get_path_policy(void) { return g_path_policy.load(); }
 
 void attn_set_wait_limit_ns(uint64_t limit_ns) {
   g_wait_limit_ns.store(limit_ns ? (unsigned long long)limit_ns : kDefaultWaitLimitNs);

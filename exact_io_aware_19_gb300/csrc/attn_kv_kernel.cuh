@@ -479,39 +479,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Combines the splits of each row: with L_s the partial log2-sum-exp of split s,
-// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One warp per row; each lane
-// owns D / 32 consecutive columns.
+// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One warp per row: lanes take
+// the splits 32 at a time for the log-sum-exp (shuffle reductions), then every lane
+// owns D / 32 consecutive columns and accumulates the weighted partial rows, with
+// the loads of up to 8 splits in flight at once.
 template <int D, bool BF16, bool OUT_F32>
 __global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
   constexpr int kCols = D / 32;
+  constexpr int kBatch = 8;
   const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= nrows) return;
+  const int S = p.splits;
   float m = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) m = fmaxf(m, p.lse_part[s * nrows + row]);
+  for (int s = lane; s < S; s += 32) m = fmaxf(m, p.lse_part[s * nrows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float acc[kCols];
 #pragma unroll
   for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
   float lse2 = -INFINITY;
   if (m != -INFINITY) {
     float total = 0.f;
-    for (int s = 0; s < p.splits; ++s) total += exp2f(p.lse_part[s * nrows + row] - m);
+    for (int s = lane; s < S; s += 32) total += exp2f(p.lse_part[s * nrows + row] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     lse2 = m + log2f(total);
-    for (int s = 0; s < p.splits; ++s) {
-      const float w = exp2f(p.lse_part[s * nrows + row] - lse2);
-      if (w == 0.f) continue;  // an empty split (its partial O is zero)
-      const float* src = p.o_part + (s * nrows + row) * D + lane * kCols;
-      if constexpr (kCols == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      // lane t holds the weight of split s0 + t
+      const int sl = s0 + lane;
+      const float wl = (sl < S) ? exp2f(p.lse_part[sl * nrows + row] - lse2) : 0.f;
+      const int n = min(32, S - s0);
+      for (int t0 = 0; t0 < n; t0 += kBatch) {
+        float v[kBatch][kCols];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int s = s0 + t0 + u;
+          if (t0 + u < n) {
+            const float* src = p.o_part + (s * nrows + row) * D + lane * kCols;
+            if constexpr (kCols == 4) {
+              const float4 x = *reinterpret_cast<const float4*>(src);
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+              const float2 x = *reinterpret_cast<const float2*>(src);
+              v[u][0] = x.x; v[u][1] = x.y;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) v[u][c] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, (t0 + u) & 31);
+          if (t0 + u < n && w != 0.f) {  // an empty split has weight 0 (and O_s = 0)
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) acc[c] += w * v[u][c];
+          }
+        }
       }
     }
   }

@@ -164,6 +164,21 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
 attn_status_t attn_fwd_sync_status(void *workspace, void *stream);
 
 /*
+ * Which kernel attn_fwd (and attn_fwd_noalloc) uses, process-wide. Both compute the
+ * same result (up to rounding order); they differ in how the work is cut:
+ *   ATTN_PATH_AUTO    the persistent two-tile kernel (256 query rows per work unit),
+ *                     unless the problem has at most half as many such units as the
+ *                     device has SMs; then the one-tile kernel (128 rows per CTA).
+ *   ATTN_PATH_SQUARE  always the persistent two-tile kernel.
+ *   ATTN_PATH_TILES   always the one-tile kernel (attn_fwd_kv's with Lq = Lk and one
+ *                     key split).
+ * Any other value selects ATTN_PATH_AUTO. attn_get_path_policy returns the setting.
+ */
+enum { ATTN_PATH_AUTO = 0, ATTN_PATH_SQUARE = 1, ATTN_PATH_TILES = 2 };
+void attn_set_path_policy(int policy);
+int attn_get_path_policy(void);
+
+/*
  * Sets the limit, in nanoseconds, of every device-side wait in kernels launched
  * afterwards by this process (default 4e9 = 4 s; 0 restores the default). A wait
  * that runs out records ATTN_ERR_TIMEOUT in the workspace and makes every role of

@@ -153,3 +153,11 @@ def test_python_kv_binding_checks_shapes():
     q = torch.zeros(1, 8, 4, 64, dtype=torch.float16)
     with pytest.raises(TypeError):
         ex.attn_fwd_kv(q, q, q)  # CPU tensors
+
+
+def test_path_policy_round_trip(lib):
+    old = lib.attn_get_path_policy()
+    for policy, want in [(1, 1), (2, 2), (0, 0), (7, 0), (-1, 0)]:
+        lib.attn_set_path_policy(policy)
+        assert lib.attn_get_path_policy() == want
+    lib.attn_set_path_policy(old)

@@ -17,6 +17,16 @@ from parity_util import compare, gpu_run
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(params=["square", "tiles"])
+def kernel_path(request):
+    """Run the test on attn_fwd's persistent two-tile kernel and on its one-tile
+    kernel (the small-problem path), then restore the automatic choice."""
+    import exact_io_aware_19_gb300 as ex
+    old = ex.set_path_policy(ex.PATH_SQUARE if request.param == "square" else ex.PATH_TILES)
+    yield request.param
+    ex.set_path_policy(old)
+
 SMALL_L = [1, 2, 127, 128, 129, 255, 256, 257, 300, 640]
 MASKS = [(False, -1), (True, -1), (True, 0), (True, 1), (True, 100), (True, 300)]
 
@@ -24,7 +34,7 @@ MASKS = [(False, -1), (True, -1), (True, 0), (True, 1), (True, 100), (True, 300)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("L", SMALL_L)
-def test_small_shapes_all_masks(d, dtype, L):
+def test_small_shapes_all_masks(d, dtype, L, kernel_path):
     for n, ((causal, wl), (hq, hkv)) in enumerate(
             itertools.product(MASKS, [(2, 2), (4, 1)])):
         q, k, v = si.random_qkv(2, L, hq, hkv, d, dtype=dtype, seed=1000 * L + 10 * n + d)
@@ -33,13 +43,13 @@ def test_small_shapes_all_masks(d, dtype, L):
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.125, 0.5, 2.0])
-def test_scale_values(scale):
+def test_scale_values(scale, kernel_path):
     q, k, v = si.random_qkv(1, 384, 2, 1, 64, seed=77)
     for causal in (False, True):
         compare(q, k, v, "fp16", causal, -1, scale, label=f"scale={scale} causal={causal}")
 
 
-def test_gqa_group_sizes():
+def test_gqa_group_sizes(kernel_path):
     for hq, hkv in [(8, 8), (8, 4), (8, 2), (8, 1)]:
         q, k, v = si.random_qkv(1, 513, hq, hkv, 128, dtype="bf16", seed=hq * 10 + hkv)
         compare(q, k, v, "bf16", True, -1, 1 / math.sqrt(128), label=f"gqa {hq}/{hkv}")
@@ -50,11 +60,11 @@ def _workload(w, rows=None):
     return compare(q, k, v, w.dtype, w.causal, w.window_left, w.scale, rows=rows, label=w.name)
 
 
-def test_causal_b1_h4_L2048_full():
+def test_causal_b1_h4_L2048_full(kernel_path):
     _workload(si.CAUSAL_B1_H4_L2048_D64)
 
 
-def test_noncausal_b2_h8_L512_full():
+def test_noncausal_b2_h8_L512_full(kernel_path):
     _workload(si.NONCAUSAL_B2_H8_D64_L512)
 
 
@@ -91,7 +101,7 @@ def test_window4096_b4_h16_d128_L32768_sampled():
     _workload(w, rows=si.sample_rows(w, n_random=256))
 
 
-def test_repeatable_bits():
+def test_repeatable_bits(kernel_path):
     q, k, v = si.random_qkv(2, 1000, 4, 2, 64, seed=5, device="cuda")
     import exact_io_aware_19_gb300 as ex
     o1, l1 = ex.attn_fwd(q, k, v, causal=True)
@@ -99,7 +109,7 @@ def test_repeatable_bits():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_outputs_stay_inside_their_buffers():
+def test_outputs_stay_inside_their_buffers(kernel_path):
     """Guard bands around O and LSE keep their canary values (no stray writes)."""
     import exact_io_aware_19_gb300 as ex
     B, L, H, d = 1, 333, 3, 128
@@ -189,3 +199,19 @@ def test_exp2_f16x2_accuracy():
     rel = ((got - ref) / ref).abs()[normal]
     assert rel.max().item() <= 2.0 ** -9.9, rel.max().item()
     assert (got - ref).abs()[~normal].max().item() <= 2.0 ** -24
+
+
+def test_auto_path_choice():
+    """AUTO takes the one-tile kernel exactly when the problem has at most half as many
+    256-row units as SMs; both kernels agree to rounding."""
+    import exact_io_aware_19_gb300 as ex
+    assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
+    q, k, v = si.random_qkv(1, 2048, 4, 4, 64, seed=8, device="cuda")
+    o_auto, l_auto = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
+    ex.set_path_policy(ex.PATH_TILES)
+    o_t, l_t = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
+    ex.set_path_policy(ex.PATH_SQUARE)
+    o_s, l_s = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
+    ex.set_path_policy(ex.PATH_AUTO)
+    assert torch.equal(o_auto, o_t) and torch.equal(l_auto, l_t)  # 32 units: one-tile kernel
+    assert (o_t - o_s).abs().max().item() < 2e-3 and (l_t - l_s).abs().max().item() < 1e-4
