@@ -56,11 +56,12 @@ def _defines():
     EX19_TRACE (CTA 0 records a clock64 timeline of its first unit in the workspace; default 0),
     EX19_ONEPASS (the softmax reads S from TMEM once instead of twice; default 1),
     EX19_SPIN (bounded waits spin on mbarrier.test_wait instead of try_wait; default 0),
-    EX19_EXP_F16X2 (fp16: packed fp16 exponentials, two per MUFU operation; default 1)."""
+    EX19_EXP_F16X2 (fp16: packed fp16 exponentials, two per MUFU operation; default 1),
+    EX19_PV_HALVES (separate P: P handed to the P·V MMAs in two 64-key halves; default 1)."""
     out = []
     for name in ("EX19_POLY_PAIRS", "EX19_SEPARATE_P", "EX19_SOFTMAX_F2", "EX19_MAX3",
                  "EX19_SUSPEND_NS",
-                 "EX19_TRACE", "EX19_ONEPASS", "EX19_SPIN",
+                 "EX19_TRACE", "EX19_ONEPASS", "EX19_SPIN", "EX19_PV_HALVES",
                  "EX19_EXP_F16X2"):
         if os.environ.get(name):
             out.append("-D%s=%d" % (name, int(os.environ[name])))

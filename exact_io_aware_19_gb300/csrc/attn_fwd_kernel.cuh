@@ -65,6 +65,9 @@ constexpr float kRescaleThreshold = 8.0f;
 #ifndef EX19_ONEPASS
 #define EX19_ONEPASS 1  // S read from TMEM once (1) or twice, max then exponentials (0)
 #endif
+#ifndef EX19_PV_HALVES
+#define EX19_PV_HALVES 1  // separate P: hand P to the P·V MMAs in two 64-key halves (1) or whole (0)
+#endif
 #ifndef EX19_POLY_PAIRS
 #define EX19_POLY_PAIRS 0  // exp2 polynomial offload: pairs out of every 8 (0 = all on MUFU)
 #endif  // log2 units: rescale O only when m grows > 2^8
@@ -89,8 +92,8 @@ struct Geometry {
   static constexpr int kOffKV = kTilesPerUnit * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   // barriers: full[S], empty[S], q_full, q_free, s_full[2], p_full[2], o_full[2], o_free[2],
-  // drain, s_free[2], pv_done[2]
-  static constexpr int kNumBars = 2 * kSlots + 15;
+  // drain, s_free[2], pv_done[2], p_half[2]
+  static constexpr int kNumBars = 2 * kSlots + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
@@ -183,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // separate P region (d = 64 fp16): S_t = [128t, ...), P_t = [256+64t, 256+64t+64),
   // O_t = [384+64t, 384+64t+64) — all 512 columns.
   constexpr bool kSeparateP = (D == 64) && !BF16 && (EX19_SEPARATE_P != 0);
+  // Separate P: the softmax releases the first 64 keys of P (p_half) before it
+  // computes the rest, and the first four P·V MMAs run under that second half.
+  constexpr bool kHalves = kSeparateP && (EX19_PV_HALVES != 0) && (EX19_ONEPASS != 0);
   constexpr uint32_t kColS0 = 0, kStrideS = 128;
   constexpr uint32_t kColP0 = kSeparateP ? 256 : 0, kStrideP = kSeparateP ? 64 : 128;
   constexpr uint32_t kColO0 = kSeparateP ? 384 : 256, kStrideO = kSeparateP ? 64 : 128;
@@ -205,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_drain = bars + 8u * (2 * S + 10);
   auto bar_s_free = [&](int t) { return bars + 8u * (2 * S + 11 + t); };
   auto bar_pv_done = [&](int t) { return bars + 8u * (2 * S + 13 + t); };
+  auto bar_p_half = [&](int t) { return bars + 8u * (2 * S + 15 + t); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
 
@@ -228,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < kTilesPerUnit; ++t) {
       mbar_init(bar_s_free(t), kBM);
       mbar_init(bar_pv_done(t), 1);
+      mbar_init(bar_p_half(t), kBM);
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -336,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O_t (+)= P_t · V_j from V slot `slot`. 16 keys per MMA: 8 TMEM columns of
     // packed P, 16 rows (2 KiB) of V. Split P keeps each 64-key half as
     // [hi 32 columns | lo 32 columns].
-    auto issue_pv = [&](uint32_t slot, bool first) __attribute__((always_inline)) {
+    auto issue_pv = [&](uint32_t slot, bool first, int kk_lo, int kk_hi) __attribute__((always_inline)) {
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
+      for (int kk = kk_lo; kk < kk_hi; ++kk) {
         const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
         mma_ts_elect(mO, mP + pcol, dv + ((slot * G::kTileBytes + kk * 2048) >> 4), idesc_o,
                      (first && kk == 0) ? 0u : 1u);
@@ -381,12 +389,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto pv_block = [&](int j) __attribute__((always_inline)) -> bool {
         const uint32_t vidx = kidx_of(j) + 1u;
         if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
-        if (!mbar_wait_warp(bar_p_full(t), p_cnt & 1u, wc, kSiteMmaPFull)) return false;
-        ++p_cnt;
+        if constexpr (kHalves) {
+          if (!mbar_wait_warp(bar_p_half(t), p_cnt & 1u, wc, kSiteMmaPFull)) return false;
+        } else {
+          if (!mbar_wait_warp(bar_p_full(t), p_cnt & 1u, wc, kSiteMmaPFull)) return false;
+        }
         if (first && !mbar_wait_warp(bar_o_free(t), (o_cnt & 1u) ^ 1u, wc, kSiteMmaOFree))
           return false;
         tc_fence_after();
-        issue_pv(slot_of(vidx), first);
+        if constexpr (kHalves) {
+          issue_pv(slot_of(vidx), first, 0, kBN / 32);  // keys 0..63
+          if (!mbar_wait_warp(bar_p_full(t), p_cnt & 1u, wc, kSiteMmaPFull)) return false;
+          tc_fence_after();
+          issue_pv(slot_of(vidx), false, kBN / 32, kBN / 16);  // keys 64..127
+        } else {
+          issue_pv(slot_of(vidx), first, 0, kBN / 16);
+        }
+        ++p_cnt;
         first = false;
         if constexpr (kSeparateP) mma_commit_elect(bar_pv_done(t));
         mma_commit_elect(bar_empty(slot_of(vidx)));
@@ -540,6 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
           }
+          // O rescale before the first half of this block's P·V (kHalves), once half
+          // of the scores are consumed: 16 columns of O at a time.
+          auto rescale_o_early = [&]() __attribute__((always_inline)) {
+            if (__any_sync(0xffffffffu, rescale && j != span.lo)) {
+              const float a = (rescale && j != span.lo) ? alpha : 1.f;
+#pragma unroll 1
+              for (int c0 = 0; c0 < D; c0 += 16) {
+                uint32_t orow[16];
+                tmem_ld_x16(tO + c0, orow);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * a);
+                tmem_st_x16(tO + c0, orow);
+              }
+            }
+          };
           if (tr) trace_mark(p, t, k, jr, 4);
 #if EX19_SOFTMAX_F2
           const float2 c2 = make_float2(Cs, Cs);
@@ -588,6 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
               tmem_st_x16(tP + (c0 >> 1), pk);
+              if constexpr (kHalves) {
+                if (c0 == 32) {  // keys 0..63 of P are stored: release them to the P·V
+                  rescale_o_early();
+                  tmem_st_wait();
+                  tc_fence_before();
+                  mbar_arrive(bar_p_half(t));
+                }
+              }
               if (tr && (c0 & 32)) trace_mark(p, t, k, jr, 5 + (c0 >> 6));
               continue;
             }
@@ -630,6 +672,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st_x16(tP + 64 * h + 32 + (cl >> 1), pk_lo);
             } else {
               tmem_st_x16(tP + (c0 >> 1), pk);
+            }
+            if constexpr (kHalves) {
+              if (c0 == 32) {
+                rescale_o_early();
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar_p_half(t));
+              }
             }
             if (tr && (c0 & 32)) trace_mark(p, t, k, jr, 5 + (c0 >> 6));
           }
@@ -768,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O rescale. The previous P·V of this tile is complete: with P over S,
         // S_t(j) was issued after it and s_full tracks all earlier MMAs; with a
         // separate P region, pv_done was waited just above.
-        if (__any_sync(0xffffffffu, rescale && j != span.lo)) {
+        if (!kHalves && __any_sync(0xffffffffu, rescale && j != span.lo)) {
           const float a = (rescale && j != span.lo) ? alpha : 1.f;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
