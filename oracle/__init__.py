@@ -165,6 +165,34 @@ class Oracle:
         o = o.reshape(B, Hq, Lq, d).transpose(0, 2, 1, 3).copy()
         return o, lse.reshape(B, Hq, Lq)
 
+    def attn_paged(self, q_bits, kc_bits, vc_bits, block_table, seq_lens, dtype, causal,
+                   window_left, scale):
+        """Decode-shaped attention over a paged K/V cache ("What is memory-efficient
+        attention ...", section 3: the cache is cut into fixed-size blocks of tokens,
+        stored anywhere, and a page table maps each sequence's logical blocks to
+        physical pages).
+
+        q_bits [B, Lq, Hq, d]; kc_bits / vc_bits [num_pages, page_size, Hkv, d];
+        block_table [B, max_pages] (int); seq_lens [B]: sequence b's keys are logical
+        positions 0 .. seq_lens[b]-1, position t sitting at row t % page_size of page
+        block_table[b, t // page_size]. Each sequence is gathered into its dense
+        [1, seq_lens[b], Hkv, d] form and evaluated by attn_full_kv.
+        Returns O [B, Lq, Hq, d] and LSE [B, Hq, Lq] (float64).
+        """
+        B, Lq, Hq, d = q_bits.shape
+        ps = kc_bits.shape[1]
+        o = np.empty((B, Lq, Hq, d))
+        lse = np.empty((B, Hq, Lq))
+        for b in range(B):
+            Lk = int(seq_lens[b])
+            t = np.arange(Lk)
+            pages = np.asarray(block_table[b])[t // ps]
+            kb = np.asarray(kc_bits)[pages, t % ps][None]
+            vb = np.asarray(vc_bits)[pages, t % ps][None]
+            o[b:b + 1], lse[b:b + 1] = self.attn_full_kv(q_bits[b:b + 1], kb, vb, dtype, causal,
+                                                         window_left, scale)
+        return o, lse
+
     def merge(self, o_parts, lse_parts):
         """Combine partial results over disjoint key sets: o_parts [P, n, d] and
         lse_parts [P, n] (natural log, -inf = empty part) -> O [n, d], LSE [n]."""

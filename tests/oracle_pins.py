@@ -333,6 +333,39 @@ def pin_merge_hand_example(orc):
     assert np.array_equal(o, np.zeros((1, 2))) and lse[0] == -math.inf
 
 
+def pin_paged_equals_dense(orc):
+    """A sequence stored in scattered pages (any page order, any unused pages, a
+    partial last page) gives exactly the dense result of the same sequence."""
+    rng = np.random.default_rng(7)
+    for ps, lens in [(16, [2, 16, 17, 100]), (32, [33, 64]), (128, [129, 5])]:
+        B = len(lens)
+        q, _, _ = random_qkv(B, 2, 4, 2, 8, seed=ps)
+        dense = [random_qkv(1, L, 4, 2, 8, seed=ps * 100 + L)[1:] for L in lens]
+        npg = [-(-L // ps) for L in lens]
+        num_pages = sum(npg) + 5  # some pages belong to nobody
+        perm = rng.permutation(num_pages)
+        kc = np.zeros((num_pages, ps, 2, 8), dtype=np.uint16)
+        vc = np.full((num_pages, ps, 2, 8), 0x7E00, dtype=np.uint16)  # unused slots: fp16 NaN
+        table = np.full((B, max(npg) + 2), -1, dtype=np.int64)
+        nxt = 0
+        for b, L in enumerate(lens):
+            kb, vb = bits16(dense[b][0])[0], bits16(dense[b][1])[0]
+            for lp in range(npg[b]):
+                phys = perm[nxt]
+                nxt += 1
+                table[b, lp] = phys
+                rows = slice(lp * ps, min(L, (lp + 1) * ps))
+                n = rows.stop - rows.start
+                kc[phys, :n], vc[phys, :n] = kb[rows], vb[rows]
+        for causal, wl in [(False, -1), (True, -1), (True, 3)]:
+            o, lse = orc.attn_paged(bits16(q), kc, vc, table, lens, "fp16", causal, wl, 0.3)
+            for b, L in enumerate(lens):
+                od, ld = orc.attn_full_kv(bits16(q)[b:b + 1], bits16(dense[b][0]),
+                                          bits16(dense[b][1]), "fp16", causal, wl, 0.3)
+                assert np.array_equal(o[b:b + 1], od) and np.array_equal(lse[b:b + 1], ld), \
+                    (ps, L, causal, wl)
+
+
 ORACLE_PINS = [
     pin_widen_fp16_all_patterns, pin_widen_bf16_all_patterns, pin_matches_materialised,
     pin_constant_values, pin_causal_first_row, pin_window_zero_is_identity,
@@ -340,5 +373,5 @@ ORACLE_PINS = [
     pin_dominant_key, pin_key_permutation_invariance, pin_negative_scale_is_negated_query,
     pin_window_row_is_causal_suffix, pin_hand_worked_example, pin_rows_api_matches_full,
     pin_kv_matches_materialised, pin_kv_rows_are_square_suffix, pin_merge_of_key_splits,
-    pin_merge_hand_example,
+    pin_merge_hand_example, pin_paged_equals_dense,
 ]
