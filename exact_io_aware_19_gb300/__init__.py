@@ -26,6 +26,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
+           "attn_fwd_kv_paged",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
            "PATH_SQUARE", "PATH_TILES", "debug_wait_probe", "debug_exp2",
@@ -66,6 +67,9 @@ def _bind(lib):
     lib.attn_fwd_kv.restype = i
     lib.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, i, i,
                                 p, sz, p]
+    lib.attn_fwd_kv_paged.restype = i
+    lib.attn_fwd_kv_paged.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, i, i, i,
+                                      ctypes.c_float, i, i, i, p, sz, p]
     lib.attn_fwd_kv_workspace_size.restype = sz
     lib.attn_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
     lib.attn_fwd_kv_num_splits.restype = i
@@ -251,6 +255,52 @@ def attn_fwd(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=False,
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if return_lse else None
     attn_fwd_into(q, k, v, o, lse, causal=causal, window_left=window_left, scale=scale,
                   workspace=workspace, stream=stream)
+    return o, lse
+
+
+def attn_fwd_kv_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, causal=False,
+                      window_left=-1, scale=None, out_fp32=False, num_splits=0, return_lse=True,
+                      workspace=None, stream=None):
+    """Decode-shaped attention over a paged K/V cache.
+
+    q [B, Lq, Hq, d]; k_cache, v_cache [num_pages, page_size, Hkv, d] (q's dtype);
+    block_table int32 [B, max_pages_per_seq] and seq_lens int32 [B] on the device;
+    ``max_seq_len`` (a host int) bounds seq_lens. Sequence b's key t is row
+    t % page_size of page block_table[b, t // page_size]; its queries are its last Lq
+    positions. Returns (o, lse) like attn_fwd_kv.
+    """
+    lib = load_library()
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_table", block_table), ("seq_lens", seq_lens)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    B, Lq, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_cache.shape
+    if dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must be [num_pages, page_size, Hkv, d]")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q and the caches must share one dtype")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages_per_seq] and seq_lens [B]")
+    dt = _dtype_code(q)
+    o = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = kv_workspace_size(B, Lq, max_seq_len, Hq, Hkv, d, causal, window_left, num_splits)
+    if workspace is None:
+        workspace = _default_workspace(q.device, max(need, 256))
+    code = lib.attn_fwd_kv_paged(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+        seq_lens.data_ptr(), o.data_ptr(), lse.data_ptr() if lse is not None else None, B, Lq, Hq,
+        Hkv, d, page_size, num_pages, block_table.shape[1], int(max_seq_len), int(bool(causal)),
+        int(window_left), float(scale), dt, OUT_FP32 if out_fp32 else OUT_SAME, int(num_splits),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(code)
     return o, lse
 
 

@@ -224,6 +224,131 @@ int current_sms(int* sms) {
   return 0;
 }
 
+// Paged K/V cache description (attn_fwd_kv_paged); null for the dense entry point.
+struct PagedArgs {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int page_size, num_pages, max_pages;
+};
+
+// attn_fwd_kv and attn_fwd_kv_paged: validation, plan, tensor maps and launch. For
+// the paged call k and v are the caches and Lk is the maximum sequence length.
+attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Lq, int Lk, int Hq, int Hkv, int d, int causal, int window_left,
+                     float scale, attn_dtype_t dtype, attn_out_t out_dtype, int num_splits,
+                     void* workspace, size_t workspace_bytes, void* stream,
+                     const PagedArgs* paged) {
+  g_detail.clear();
+  attn_status_t st = check_kv_shape(B, Lq, Lk, Hq, Hkv, d, causal, window_left);
+  if (st != ATTN_OK) return st;
+  if (num_splits < 0 || num_splits > kKvMaxSplits)
+    return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [0, 256]");
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "bad dtype");
+  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
+  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (paged) {
+    const int ps = paged->page_size;
+    if (ps != 8 && ps != 16 && ps != 32 && ps != 64 && ps != 128)
+      return fail(ATTN_ERR_UNSUPPORTED, "page_size must be 8, 16, 32, 64 or 128");
+    if (paged->num_pages < 1 || (long long)paged->num_pages * ps >= (1LL << 31))
+      return fail(ATTN_ERR_INVALID_ARG, "num_pages must be >= 1 and num_pages * page_size < 2^31");
+    if (paged->max_pages < (Lk + ps - 1) / ps)
+      return fail(ATTN_ERR_INVALID_ARG, "max_pages_per_seq must cover max_seq_len");
+    if (!paged->block_table || !paged->seq_lens)
+      return fail(ATTN_ERR_INVALID_ARG, "block_table and seq_lens must be non-null");
+    if (!aligned(paged->block_table, 4) || !aligned(paged->seq_lens, 4))
+      return fail(ATTN_ERR_INVALID_ARG, "block_table and seq_lens must be 4-byte aligned");
+  }
+  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
+  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  const KvPlan plan = kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left);
+  if (num_splits > 0 && workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, num_splits))
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms);
+  if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits))
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
+  if ((long long)plan.items * splits >= (1LL << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "too many work items");
+  std::string why;
+  const void* ptrs[8] = {q, k, v, o, workspace, lse, paged ? paged->block_table : nullptr,
+                         paged ? paged->seq_lens : nullptr};
+  const char* names[8] = {"q", "k", "v", "o", "workspace", "lse", "block_table", "seq_lens"};
+  for (int i = 0; i < 8; ++i)
+    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
+      return fail(ATTN_ERR_INVALID_ARG, why);
+
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap tm_q, tm_k, tm_v;
+  bool maps_ok = make_tensor_map(&tm_q, q, bf16, B, Lq, Hq, d, &why, plan.group, plan.q_per_tile);
+  if (maps_ok && paged) {
+    // the caches as one sequence of num_pages * page_size rows; one box = one page
+    const int rows = paged->num_pages * paged->page_size;
+    maps_ok = make_tensor_map(&tm_k, k, bf16, 1, rows, Hkv, d, &why, 1, paged->page_size) &&
+              make_tensor_map(&tm_v, v, bf16, 1, rows, Hkv, d, &why, 1, paged->page_size);
+  } else if (maps_ok) {
+    maps_ok = make_tensor_map(&tm_k, k, bf16, B, Lk, Hkv, d, &why) &&
+              make_tensor_map(&tm_v, v, bf16, B, Lk, Hkv, d, &why);
+  }
+  if (!maps_ok) return fail(ATTN_ERR_CUDA, why);
+
+  ex19::KvLaunchArgs a = {};
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  ex19::KvParams& p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.status = static_cast<uint32_t*>(workspace);
+  const size_t rows = (size_t)B * Hq * Lq;
+  if (splits > 1) {
+    char* base = static_cast<char*>(workspace) + kWorkspaceBytes;
+    p.lse_part = reinterpret_cast<float*>(base);
+    p.o_part = reinterpret_cast<float*>(base + ((size_t)splits * rows * 4 + 255) / 256 * 256);
+  }
+  p.B = B;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = plan.group;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f ? 1 : 0;
+  p.q_per_tile = plan.q_per_tile;
+  p.row_tiles = plan.row_tiles;
+  p.splits = splits;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  if (paged) {
+    p.block_table = paged->block_table;
+    p.seq_lens = paged->seq_lens;
+    p.page_size = paged->page_size;
+    p.max_pages = paged->max_pages;
+    p.num_pages = paged->num_pages;
+  }
+  a.grid = plan.items * splits;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const bool out_f32 = out_dtype == ATTN_OUT_FP32;
+  e = paged ? ex19::launch_kv_paged(d, bf16, out_f32, a) : ex19::launch_kv(d, bf16, out_f32, a);
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return ATTN_OK;
+}
+
 // The square problem (validated by the caller) on the one-tile kernel: Lq = Lk = L,
 // one key split, so no partial results and no merge.
 attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, void* o,
@@ -239,7 +364,7 @@ attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, v
       !make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) ||
       !make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why))
     return fail(ATTN_ERR_CUDA, why);
-  ex19::KvLaunchArgs a;
+  ex19::KvLaunchArgs a = {};
   a.tm_q = &tm_q;
   a.tm_k = &tm_k;
   a.tm_v = &tm_v;
@@ -393,89 +518,20 @@ attn_status_t attn_fwd_kv(const void* q, const void* k, const void* v, void* o, 
                           int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,
                           int window_left, float scale, attn_dtype_t dtype, attn_out_t out_dtype,
                           int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
-  g_detail.clear();
-  attn_status_t st = check_kv_shape(B, Lq, Lk, Hq, Hkv, d, causal, window_left);
-  if (st != ATTN_OK) return st;
-  if (num_splits < 0 || num_splits > kKvMaxSplits)
-    return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [0, 256]");
-  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
-  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "bad dtype");
-  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
-    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
-  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
-    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
-  if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
-  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
-  const KvPlan plan = kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left);
-  if (num_splits > 0 && workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, num_splits))
-    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
+  return kv_run(q, k, v, o, lse, B, Lq, Lk, Hq, Hkv, d, causal, window_left, scale, dtype,
+                out_dtype, num_splits, workspace, workspace_bytes, stream, nullptr);
+}
 
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
-  DeviceInfo info;
-  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
-  if (info.major != 10 || info.minor != 3)
-    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
-                                          std::to_string(info.major) + "." +
-                                          std::to_string(info.minor));
-  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms);
-  if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits))
-    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
-  if ((long long)plan.items * splits >= (1LL << 31))
-    return fail(ATTN_ERR_INVALID_ARG, "too many work items");
-  std::string why;
-  const void* ptrs[6] = {q, k, v, o, workspace, lse};
-  const char* names[6] = {"q", "k", "v", "o", "workspace", "lse"};
-  for (int i = 0; i < 6; ++i)
-    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
-      return fail(ATTN_ERR_INVALID_ARG, why);
-
-  const bool bf16 = dtype == ATTN_BF16;
-  CUtensorMap tm_q, tm_k, tm_v;
-  if (!make_tensor_map(&tm_q, q, bf16, B, Lq, Hq, d, &why, plan.group, plan.q_per_tile) ||
-      !make_tensor_map(&tm_k, k, bf16, B, Lk, Hkv, d, &why) ||
-      !make_tensor_map(&tm_v, v, bf16, B, Lk, Hkv, d, &why))
-    return fail(ATTN_ERR_CUDA, why);
-
-  ex19::KvLaunchArgs a;
-  a.tm_q = &tm_q;
-  a.tm_k = &tm_k;
-  a.tm_v = &tm_v;
-  ex19::KvParams& p = a.p;
-  p.o = o;
-  p.lse = lse;
-  p.status = static_cast<uint32_t*>(workspace);
-  const size_t rows = (size_t)B * Hq * Lq;
-  if (splits > 1) {
-    char* base = static_cast<char*>(workspace) + kWorkspaceBytes;
-    p.lse_part = reinterpret_cast<float*>(base);
-    p.o_part = reinterpret_cast<float*>(base + ((size_t)splits * rows * 4 + 255) / 256 * 256);
-  } else {
-    p.lse_part = nullptr;
-    p.o_part = nullptr;
-  }
-  p.B = B;
-  p.Lq = Lq;
-  p.Lk = Lk;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.group = plan.group;
-  p.causal = causal;
-  p.window_left = window_left;
-  p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
-  p.negate_scores = scale < 0.f ? 1 : 0;
-  p.q_per_tile = plan.q_per_tile;
-  p.row_tiles = plan.row_tiles;
-  p.splits = splits;
-  p.wait_limit_ns = g_wait_limit_ns.load();
-  a.grid = plan.items * splits;
-  a.stream = static_cast<cudaStream_t>(stream);
-  e = ex19::launch_kv(d, bf16, out_dtype == ATTN_OUT_FP32, a);
-  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
-  return ATTN_OK;
+attn_status_t attn_fwd_kv_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, void* o,
+                                float* lse, int B, int Lq, int Hq, int Hkv, int d, int page_size,
+                                int num_pages, int max_pages_per_seq, int max_seq_len, int causal,
+                                int window_left, float scale, attn_dtype_t dtype,
+                                attn_out_t out_dtype, int num_splits, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  const PagedArgs pg = {block_table, seq_lens, page_size, num_pages, max_pages_per_seq};
+  return kv_run(q, k_cache, v_cache, o, lse, B, Lq, max_seq_len, Hq, Hkv, d, causal, window_left,
+                scale, dtype, out_dtype, num_splits, workspace, workspace_bytes, stream, &pg);
 }
 
 attn_status_t attn_fwd_sync_status(void* workspace, void* stream) {

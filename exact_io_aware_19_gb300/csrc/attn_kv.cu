@@ -7,9 +7,9 @@
 namespace ex19 {
 namespace {
 
-template <int D, bool BF16, bool OUT_F32>
+template <int D, bool BF16, bool OUT_F32, bool PAGED>
 cudaError_t launch_kv_one(const KvLaunchArgs& a) {
-  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32>;
+  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32, PAGED>;
   constexpr int smem = kv::KvGeometry<D>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
   int dev = 0;
@@ -30,16 +30,21 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_kv_d(bool bf16, bool out_f32, const KvLaunchArgs& a) {
-  if (bf16) return out_f32 ? launch_kv_one<D, true, true>(a) : launch_kv_one<D, true, false>(a);
-  return out_f32 ? launch_kv_one<D, false, true>(a) : launch_kv_one<D, false, false>(a);
+  if (bf16)
+    return out_f32 ? launch_kv_one<D, true, true, PAGED>(a) : launch_kv_one<D, true, false, PAGED>(a);
+  return out_f32 ? launch_kv_one<D, false, true, PAGED>(a) : launch_kv_one<D, false, false, PAGED>(a);
 }
 
 }  // namespace
 
 cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a) {
-  return (d == 64) ? launch_kv_d<64>(bf16, out_f32, a) : launch_kv_d<128>(bf16, out_f32, a);
+  return (d == 64) ? launch_kv_d<64, false>(bf16, out_f32, a) : launch_kv_d<128, false>(bf16, out_f32, a);
+}
+
+cudaError_t launch_kv_paged(int d, bool bf16, bool out_f32, const KvLaunchArgs& a) {
+  return (d == 64) ? launch_kv_d<64, true>(bf16, out_f32, a) : launch_kv_d<128, true>(bf16, out_f32, a);
 }
 
 }  // namespace ex19

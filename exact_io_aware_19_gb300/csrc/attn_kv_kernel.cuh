@@ -25,6 +25,17 @@
 //   * warps 0-3 (softmax): one thread per tile row (TMEM lane), as in the square
 //     kernel: running max m (base-2 units) and sum l, P = 2^(x - m), conditional
 //     O rescale, and at the end O / l and the log-sum-exp.
+//   * Paged K/V cache ("What is memory-efficient attention ...", section 3: the
+//     cache is cut into fixed-size blocks of tokens stored anywhere, and a page
+//     table maps each sequence's logical blocks to physical pages): a 128-key block
+//     is fetched as 128 / page_size TMA boxes of page_size rows, one per page, each
+//     landing at its row offset of the slot (the 128-byte swizzle depends only on
+//     the shared-memory address, so the pieces form the same tile as one box).
+//     Each sequence has its own length. Pages past its end, and table entries
+//     outside [0, num_pages), are fetched at an out-of-range row, which TMA fills
+//     with zeros. The unused rows of a partial last page hold whatever the cache
+//     holds, so the MMA warp zeroes those V rows in shared memory before that
+//     block's P·V (P is 0 there, but 0 · NaN would not be).
 //   * Every wait is bounded; a timeout sets the status word and all roles leave.
 #pragma once
 #include <cuda.h>
@@ -56,6 +67,7 @@ enum : uint32_t {
   kSiteMmaPFull = 0x60004, kSiteMmaDrain = 0x60005,
   kSiteSmxSFull = 0x70001, kSiteSmxOFull = 0x70002, kSiteSmxPvDone = 0x70003,
   kSiteDrainLoads = 0x80001,
+  kSiteBadSeqLen = 0x90001,  // a paged sequence length outside [Lq, max_seq_len]
 };
 
 template <int D>
@@ -79,8 +91,11 @@ struct KvItem {
   int b, g, split;
   int i0, i1;  // query positions [i0, i1) of the tile
   int lo, hi;  // key blocks of this split
+  int Lk;      // keys of this batch entry's sequence
+  bool bad;    // paged: the sequence length is out of range (nothing is computed)
 };
 
+template <bool PAGED>
 __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   KvItem it;
   int x = blockIdx.x;
@@ -92,17 +107,27 @@ __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   it.b = x / p.Hkv;
   it.i0 = rt * p.q_per_tile;
   it.i1 = min(p.Lq, it.i0 + p.q_per_tile);
-  const int off = p.Lk - p.Lq;  // position of query row 0
-  const int nblk = (p.Lk + kBN - 1) / kBN;
+  it.Lk = p.Lk;
+  it.bad = false;
+  if constexpr (PAGED) {
+    it.Lk = p.seq_lens[it.b];
+    if (it.Lk < p.Lq || it.Lk > p.Lk) {
+      it.bad = true;
+      it.Lk = p.Lq;
+    }
+  }
+  const int off = it.Lk - p.Lq;  // position of query row 0
+  const int nblk = (it.Lk + kBN - 1) / kBN;
   const int blk_hi = p.causal ? (off + it.i1 - 1) / kBN + 1 : nblk;
   const int blk_lo = (p.window_left >= 0) ? max(0, off + it.i0 - p.window_left) / kBN : 0;
   const long long n = blk_hi - blk_lo;
   it.lo = blk_lo + static_cast<int>(n * it.split / p.splits);
   it.hi = blk_lo + static_cast<int>(n * (it.split + 1) / p.splits);
+  if (it.bad) it.hi = it.lo;
   return it;
 }
 
-template <int D, bool BF16, bool OUT_F32>
+template <int D, bool BF16, bool OUT_F32, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kv_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -133,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const KvItem it = kv_item(p);
+  const KvItem it = kv_item<PAGED>(p);
   const int nblocks = max(0, it.hi - it.lo);
 
   if (threadIdx.x == 0) {
@@ -171,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   wc.status = p.status;
   wc.limit_ns = p.wait_limit_ns;
   wc.unit = blockIdx.x;
+  if (it.bad) {
+    // Nothing of this batch entry is computed or written; report it once per CTA.
+    if (threadIdx.x == 0) record_error(wc, kStatusInvalidArg, kSiteBadSeqLen);
+  }
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -190,9 +219,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
           const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-          for (int c = 0; c < G::kChunks; ++c)
-            tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
-                        c * 64, it.g, j * kBN, it.b);
+          if constexpr (PAGED) {
+            // one box of page_size rows per page of this block
+            const int per_block = kBN / p.page_size;
+            const int oob_row = p.num_pages * p.page_size;  // past the cache: zero-filled
+            for (int pp = 0; pp < per_block; ++pp) {
+              const int lp = j * per_block + pp;  // logical page of the sequence
+              int row = oob_row;
+              if (lp * p.page_size < it.Lk) {
+                const int phys = p.block_table[static_cast<size_t>(it.b) * p.max_pages + lp];
+                if (phys >= 0 && phys < p.num_pages) row = phys * p.page_size;
+              }
+              for (int c = 0; c < G::kChunks; ++c)
+                tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + pp * p.page_size * 128,
+                            tm, bar_full(slot), c * 64, it.g, row, 0);
+            }
+          } else {
+            for (int c = 0; c < G::kChunks; ++c)
+              tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
+                          c * 64, it.g, j * kBN, it.b);
+          }
           ++n;
         }
       }
@@ -236,6 +282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int jj) __attribute__((always_inline)) -> bool {
         const uint32_t vidx = 2u * jj + 1u;
         if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
+        if constexpr (PAGED) {
+          // Rows past the sequence in its last block: the part of a partial page
+          // the TMA did load holds arbitrary cache contents; make every such V row 0.
+          const int r0 = it.Lk - (it.lo + jj) * kBN;
+          if (r0 < kBN) {
+            const uint32_t base = sKV + slot_of(vidx) * G::kTileBytes;
+            for (int idx = lane; idx < (kBN - r0) * 8 * G::kChunks; idx += 32) {
+              const int c = idx / ((kBN - r0) * 8), rem = idx % ((kBN - r0) * 8);
+              st_shared_zero16(base + c * G::kChunkBytes + (r0 + rem / 8) * 128 + (rem % 8) * 16);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+          }
+        }
         if (!mbar_wait_warp(bar_p_full(jj & 1), (jj >> 1) & 1u, wc, kSiteMmaPFull)) return false;
         tc_fence_after();
         const uint32_t mP = tmem_base + 128u * (jj & 1);
@@ -275,10 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- softmax warps
     const int rho = warp * 32 + lane;  // row of the tile
-    const bool row_ok = rho < (it.i1 - it.i0) * p.group;
+    const bool row_ok = !it.bad && rho < (it.i1 - it.i0) * p.group;
     const int qi = it.i0 + rho / p.group;  // query position (may be >= Lq for unused rows)
     const int h = it.g * p.group + rho % p.group;
-    const int off = p.Lk - p.Lq;
+    const int Lk = it.Lk;
+    const int off = Lk - p.Lq;
     const int pos = off + qi;
     const int pos_min = off + it.i0, pos_max = off + it.i1 - 1;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -297,11 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tS = tmem_base + lane_off + 128u * buf;  // S, then P, of this block
       const int key0 = j * kBN;
-      const bool masked = (key0 + kBN > p.Lk) || (p.causal && key0 + kBN - 1 > pos_min) ||
+      const bool masked = (key0 + kBN > Lk) || (p.causal && key0 + kBN - 1 > pos_min) ||
                           (p.window_left >= 0 && key0 < pos_max - p.window_left);
       int vis_lo = 0, vis_hi = kBN;  // visible columns of this row: [vis_lo, vis_hi)
       if (masked) {
-        const int hi_key = p.causal ? min(p.Lk, pos + 1) : p.Lk;
+        const int hi_key = p.causal ? min(Lk, pos + 1) : Lk;
         const int lo_key = (p.window_left >= 0) ? pos - p.window_left : 0;
         vis_hi = max(0, min(kBN, hi_key - key0));
         vis_lo = max(0, min(kBN, lo_key - key0));

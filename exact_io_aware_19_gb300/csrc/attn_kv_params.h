@@ -21,6 +21,14 @@ struct KvParams {
   int row_tiles;        // ceil(Lq / q_per_tile)
   int splits;           // key-range splits per (batch, K/V head, row tile)
   unsigned long long wait_limit_ns;
+  // Paged K/V cache (paged kernels only): k, v are [num_pages, page_size, Hkv, D];
+  // sequence b's key t sits at row t % page_size of page block_table[b * max_pages +
+  // t / page_size]; its length is seq_lens[b] (Lq <= seq_lens[b] <= Lk, the maximum).
+  const int* block_table;
+  const int* seq_lens;
+  int page_size;        // divides 128
+  int max_pages;        // row stride of block_table
+  int num_pages;
 };
 
 }  // namespace ex19

@@ -31,6 +31,8 @@ cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
 // The decode-shaped forward (and, when p.splits > 1, its merge kernel).
 cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
+// The same over a paged K/V cache (a.p.block_table, seq_lens, page_size, ... set).
+cudaError_t launch_kv_paged(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream);

@@ -16,7 +16,7 @@ namespace ex19 {
 // ---------------------------------------------------------------- status words
 // The device status word (in the caller's workspace): [0] = attn_status_t code of
 // the first error, [1] = where it happened (role << 16 | site), [2] = CTA, [3] = unit.
-enum : uint32_t { kStatusTimeout = 5 };
+enum : uint32_t { kStatusInvalidArg = 1, kStatusTimeout = 5 };  // attn_status_t codes
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -192,6 +192,17 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+// 16 zero bytes to shared memory (generic proxy).
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tcgen05.mma operand reads) that is ordered after it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {

@@ -164,6 +164,36 @@ attn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, 
 attn_status_t attn_fwd_sync_status(void *workspace, void *stream);
 
 /*
+ * attn_fwd_kv over a paged K/V cache ("What is memory-efficient attention for long
+ * context on 8x H100?", section 3: the cache is cut into fixed-size blocks of
+ * tokens stored anywhere in memory, and a page table maps each sequence's logical
+ * blocks to physical pages). Sequence b has seq_lens[b] keys; its key t is row
+ * t % page_size of page block_table[b * max_pages_per_seq + t / page_size] of the
+ * caches, and its Lq queries are its last Lq positions (as in attn_fwd_kv, with
+ * Lk = seq_lens[b]).
+ *   k_cache, v_cache  device, [num_pages, page_size, Hkv, d] of `dtype`, 16-byte aligned
+ *   block_table       device int32 [B, max_pages_per_seq]; entries past a sequence's
+ *                     last page are never read, entries outside [0, num_pages) read
+ *                     as pages of zeros
+ *   seq_lens          device int32 [B], each in [Lq, max_seq_len]; a length outside
+ *                     that range records ATTN_ERR_INVALID_ARG in the workspace status
+ *                     word and leaves that sequence's outputs unspecified
+ *   page_size         8, 16, 32, 64 or 128; num_pages * page_size < 2^31
+ *   max_pages_per_seq >= ceil(max_seq_len / page_size)
+ *   max_seq_len       host-side bound of seq_lens; sizes the grid and the workspace:
+ *                     use attn_fwd_kv_workspace_size / attn_fwd_kv_num_splits with
+ *                     Lk = max_seq_len
+ * Other arguments and the result as for attn_fwd_kv.
+ */
+attn_status_t attn_fwd_kv_paged(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_table, const int32_t *seq_lens, void *o,
+                                float *lse, int B, int Lq, int Hq, int Hkv, int d, int page_size,
+                                int num_pages, int max_pages_per_seq, int max_seq_len,
+                                int causal, int window_left, float scale, attn_dtype_t dtype,
+                                attn_out_t out_dtype, int num_splits, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
  * Which kernel attn_fwd (and attn_fwd_noalloc) uses, process-wide. Both compute the
  * same result (up to rounding order); they differ in how the work is cut:
  *   ATTN_PATH_AUTO    the persistent two-tile kernel (256 query rows per work unit),

@@ -161,3 +161,25 @@ def test_path_policy_round_trip(lib):
         lib.attn_set_path_policy(policy)
         assert lib.attn_get_path_policy() == want
     lib.attn_set_path_policy(old)
+
+
+def call_paged(lib, **kw):
+    a = dict(q=A, kc=A, vc=A, table=A, lens=A, o=A, lse=A, B=2, Lq=1, Hq=32, Hkv=8, d=128, ps=16,
+             npages=1024, maxp=64, maxlen=1024, causal=1, wl=-1, scale=0.088, dtype=1, out=0,
+             splits=2, ws=A, wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.attn_fwd_kv_paged(a["q"], a["kc"], a["vc"], a["table"], a["lens"], a["o"], a["lse"],
+                                 a["B"], a["Lq"], a["Hq"], a["Hkv"], a["d"], a["ps"], a["npages"],
+                                 a["maxp"], a["maxlen"], a["causal"], a["wl"], a["scale"],
+                                 a["dtype"], a["out"], a["splits"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ps=12), 2), (dict(ps=256), 2), (dict(ps=4), 2), (dict(npages=0), 1),
+    (dict(npages=1 << 28), 1), (dict(maxp=63), 1), (dict(table=None), 1), (dict(lens=None), 1),
+    (dict(table=A + 2), 1), (dict(lens=A + 1), 1), (dict(maxlen=0), 1), (dict(Lq=2, maxlen=1), 1),
+    (dict(kc=A + 8), 1), (dict(splits=300), 1), (dict(wsb=256), 3),
+])
+def test_paged_invalid_arguments_are_rejected_before_launch(lib, kw, code):
+    assert call_paged(lib, **kw) == code
+    assert lib.attn_last_error_detail()
