@@ -212,7 +212,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     it.b);
       uint32_t n = 0;
       bool ok = true;
+      // Paged: the physical rows of block j's pages, read one block ahead so the
+      // page-table loads are in flight while the producer waits for a free slot.
+      constexpr int kMaxPagesPerBlock = kBN / 8;
+      int rows_cur[kMaxPagesPerBlock], rows_next[kMaxPagesPerBlock];
+      auto page_rows = [&](int j, int (&rows)[kMaxPagesPerBlock]) __attribute__((always_inline)) {
+        const int per_block = kBN / p.page_size;
+        const int oob_row = p.num_pages * p.page_size;  // past the cache: zero-filled
+#pragma unroll
+        for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) {
+          const int lp = j * per_block + pp;  // logical page of the sequence
+          int phys = -1;
+          if (pp < per_block && lp * p.page_size < it.Lk)
+            phys = p.block_table[static_cast<size_t>(it.b) * p.max_pages + lp];
+          rows[pp] = (phys >= 0 && phys < p.num_pages) ? phys * p.page_size : oob_row;
+        }
+      };
+      if constexpr (PAGED) page_rows(it.lo, rows_cur);
       for (int j = it.lo; ok && j < it.hi; ++j) {
+        if constexpr (PAGED) {
+          if (j + 1 < it.hi) page_rows(j + 1, rows_next);
+        }
         for (int kv = 0; kv < 2; ++kv) {
           const uint32_t slot = n % S;
           ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
@@ -222,17 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (PAGED) {
             // one box of page_size rows per page of this block
             const int per_block = kBN / p.page_size;
-            const int oob_row = p.num_pages * p.page_size;  // past the cache: zero-filled
-            for (int pp = 0; pp < per_block; ++pp) {
-              const int lp = j * per_block + pp;  // logical page of the sequence
-              int row = oob_row;
-              if (lp * p.page_size < it.Lk) {
-                const int phys = p.block_table[static_cast<size_t>(it.b) * p.max_pages + lp];
-                if (phys >= 0 && phys < p.num_pages) row = phys * p.page_size;
-              }
+#pragma unroll
+            for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) {
+              if (pp >= per_block) break;
               for (int c = 0; c < G::kChunks; ++c)
                 tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + pp * p.page_size * 128,
-                            tm, bar_full(slot), c * 64, it.g, row, 0);
+                            tm, bar_full(slot), c * 64, it.g, rows_cur[pp], 0);
             }
           } else {
             for (int c = 0; c < G::kChunks; ++c)
@@ -240,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           c * 64, it.g, j * kBN, it.b);
           }
           ++n;
+        }
+        if constexpr (PAGED) {
+#pragma unroll
+          for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) rows_cur[pp] = rows_next[pp];
         }
       }
       if (!ok) {

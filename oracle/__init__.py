@@ -59,8 +59,8 @@ def _bind(path: str):
                                      ctypes.c_int, i64, ctypes.c_double, p, i64, p, p]
     lib.oracle_attn_rows_kv.restype = ctypes.c_int
     lib.oracle_attn_rows_kv.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64, i64,
-                                        ctypes.c_int, i64, ctypes.c_double, i64, i64, p, i64,
-                                        p, p]
+                                        ctypes.c_int, i64, i64, ctypes.c_double, i64, i64, p,
+                                        i64, p, p]
     lib.oracle_merge.restype = None
     lib.oracle_merge.argtypes = [i64, i64, i64, p, p, p, p]
     lib.oracle_widen.restype = None
@@ -132,10 +132,11 @@ class Oracle:
         return o, lse
 
     def attn_rows_kv(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale, rows,
-                     key_lo=0, key_hi=None):
+                     key_lo=0, key_hi=None, window_right=-1):
         """Decode-shaped rows: q_bits [B, Lq, Hq, d] are the last Lq positions of the
         Lk-long sequence in k_bits / v_bits [B, Lk, Hkv, d]; keys limited to
-        [key_lo, key_hi). Rows are flat ids (b*Hq + h)*Lq + i."""
+        [key_lo, key_hi) and, with window_right = r >= 0, to j <= position + r.
+        Rows are flat ids (b*Hq + h)*Lq + i."""
         q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
         k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
         v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
@@ -149,19 +150,19 @@ class Oracle:
         lse = np.empty(rows.size, dtype=np.float64)
         rc = self.lib.oracle_attn_rows_kv(
             _ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _dtype_code(dtype), B, Lq, Lk, Hq, Hkv,
-            d, int(bool(causal)), int(window_left), float(scale), int(key_lo), int(key_hi),
-            _ptr(rows), rows.size, _ptr(o), _ptr(lse))
+            d, int(bool(causal)), int(window_left), int(window_right), float(scale), int(key_lo),
+            int(key_hi), _ptr(rows), rows.size, _ptr(o), _ptr(lse))
         if rc != 0:
             raise ValueError(f"oracle_attn_rows_kv rejected its arguments (rc={rc})")
         return o, lse
 
     def attn_full_kv(self, q_bits, k_bits, v_bits, dtype, causal, window_left, scale,
-                     key_lo=0, key_hi=None):
+                     key_lo=0, key_hi=None, window_right=-1):
         """Full decode-shaped O [B, Lq, Hq, d] and LSE [B, Hq, Lq] in float64."""
         B, Lq, Hq, d = q_bits.shape
         rows = np.arange(B * Hq * Lq, dtype=np.int64)
         o, lse = self.attn_rows_kv(q_bits, k_bits, v_bits, dtype, causal, window_left, scale,
-                                   rows, key_lo, key_hi)
+                                   rows, key_lo, key_hi, window_right)
         o = o.reshape(B, Hq, Lq, d).transpose(0, 2, 1, 3).copy()
         return o, lse.reshape(B, Hq, Lq)
 

@@ -18,7 +18,8 @@
  *     i.e. it returns this same softmax(Q Kᵀ) V; it only changes where S lives.
  *
  * For every batch b, query head h < Hq and row i < L, with g = h / (Hq / Hkv):
- *   J_i      = { j : 0 <= j < L, (causal => j <= i), (window_left >= 0 => j >= i - window_left) }
+ *   J_i      = { j : 0 <= j < L, (causal => j <= i), (window_left >= 0 => j >= i - window_left),
+ *                   (window_right >= 0 => j <= i + window_right) }
  *   s_ij     = scale * sum_k q[b,i,h,k] * k[b,j,g,k]            (double)
  *   m_i      = max_{j in J_i} s_ij
  *   l_i      = sum_{j in J_i} exp(s_ij - m_i)
@@ -34,7 +35,10 @@
  * ...", section 1, key limitations), i.e. the new query attends to every cached
  * key before it; bottom-right alignment is that statement for Lq new queries.
  * A key sub-range [key_lo, key_hi) restricts J_i further: the partial result of
- * one split of the keys.
+ * one split of the keys. A right window window_right = r >= 0 restricts it to
+ * j <= p_i + r ("Flash Attention optimization" skill page, workflow 2 step 3:
+ * window_size = (left, right), -1 = unbounded; (256, 256) is its symmetric
+ * example); causal is the right window 0.
  *
  * Merge of partial results over disjoint key sets (oracle_merge): the softmax
  * over a union of key sets, written from its definition. With LSE_s = m_s + ln l_s
@@ -98,7 +102,8 @@ void oracle_widen(const uint16_t *in, int dtype, double *out, int64_t n)
  * [key_lo, key_hi). `s` is scratch for up to Lk scores. */
 static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                      int64_t Lq, int64_t Lk, int64_t Hq, int64_t Hkv, int64_t d, int causal,
-                     int64_t window_left, double scale, int64_t key_lo, int64_t key_hi,
+                     int64_t window_left, int64_t window_right, double scale, int64_t key_lo,
+                     int64_t key_hi,
                      int64_t b, int64_t h, int64_t i, double *s, double *qrow, double *o,
                      double *lse)
 {
@@ -109,6 +114,8 @@ static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     int64_t j_lo = 0, j_hi = Lk;
     if (causal)
         j_hi = pos + 1;
+    if (window_right >= 0 && pos + window_right + 1 < j_hi)
+        j_hi = pos + window_right + 1;
     if (window_left >= 0 && pos - window_left > j_lo)
         j_lo = pos - window_left;
     if (key_lo > j_lo)
@@ -160,14 +167,14 @@ static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
  * Returns 0 on success, -1 on a bad argument (nothing written). */
 int oracle_attn_rows_kv(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                         int64_t B, int64_t Lq, int64_t Lk, int64_t Hq, int64_t Hkv, int64_t d,
-                        int causal, int64_t window_left, double scale, int64_t key_lo,
-                        int64_t key_hi, const int64_t *rows, int64_t nrows, double *o_rows,
-                        double *lse_rows)
+                        int causal, int64_t window_left, int64_t window_right, double scale,
+                        int64_t key_lo, int64_t key_hi, const int64_t *rows, int64_t nrows,
+                        double *o_rows, double *lse_rows)
 {
     if (!q || !k || !v || !rows || !o_rows || !lse_rows)
         return -1;
     if (B < 1 || Lq < 1 || Lk < Lq || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0 ||
-        window_left < -1 || key_lo < 0 || key_hi > Lk || key_lo > key_hi)
+        window_left < -1 || window_right < -1 || key_lo < 0 || key_hi > Lk || key_lo > key_hi)
         return -1;
     if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)
         return -1;
@@ -192,8 +199,8 @@ int oracle_attn_rows_kv(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             int64_t bh = rows[r] / Lq;
             int64_t h = bh % Hq;
             int64_t b = bh / Hq;
-            attn_row(q, k, v, dtype, Lq, Lk, Hq, Hkv, d, causal, window_left, scale, key_lo,
-                     key_hi, b, h, i, s, qrow, o_rows + r * d, lse_rows + r);
+            attn_row(q, k, v, dtype, Lq, Lk, Hq, Hkv, d, causal, window_left, window_right, scale,
+                     key_lo, key_hi, b, h, i, s, qrow, o_rows + r * d, lse_rows + r);
         }
         free(s);
         free(qrow);
@@ -207,8 +214,8 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
                      int64_t window_left, double scale, const int64_t *rows, int64_t nrows,
                      double *o_rows, double *lse_rows)
 {
-    return oracle_attn_rows_kv(q, k, v, dtype, B, L, L, Hq, Hkv, d, causal, window_left, scale,
-                               0, L, rows, nrows, o_rows, lse_rows);
+    return oracle_attn_rows_kv(q, k, v, dtype, B, L, L, Hq, Hkv, d, causal, window_left, -1,
+                               scale, 0, L, rows, nrows, o_rows, lse_rows);
 }
 
 /* Combine nparts partial results of the same nrows rows, each over a disjoint

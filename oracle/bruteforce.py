@@ -13,7 +13,8 @@ from __future__ import annotations
 import numpy as np
 
 
-def visibility(Lq: int, causal: bool, window_left: int, Lk: int = None) -> np.ndarray:
+def visibility(Lq: int, causal: bool, window_left: int, Lk: int = None,
+               window_right: int = -1) -> np.ndarray:
     """Boolean Lq x Lk matrix: True where key j is visible from query row i.
 
     The Lq queries are the last Lq positions of an Lk-long sequence (row i sits at
@@ -27,10 +28,13 @@ def visibility(Lq: int, causal: bool, window_left: int, Lk: int = None) -> np.nd
         vis &= j <= pos
     if window_left >= 0:
         vis &= j >= pos - window_left
+    if window_right >= 0:
+        vis &= j <= pos + window_right
     return vis
 
 
-def attn_materialised(q, k, v, causal=False, window_left=-1, scale=1.0, return_p=False):
+def attn_materialised(q, k, v, causal=False, window_left=-1, scale=1.0, return_p=False,
+                      window_right=-1):
     """q: [B, Lq, Hq, d]; k, v: [B, Lk, Hkv, d] (float64), Lq <= Lk. Returns O, LSE[, P].
 
     P has shape [B, Hq, Lq, Lk]; rows with no visible key give O = 0, LSE = -inf.
@@ -41,7 +45,7 @@ def attn_materialised(q, k, v, causal=False, window_left=-1, scale=1.0, return_p
     B, Lq, Hq, d = q.shape
     Lk, Hkv = k.shape[1], k.shape[2]
     group = Hq // Hkv
-    vis = visibility(Lq, causal, window_left, Lk)
+    vis = visibility(Lq, causal, window_left, Lk, window_right)
     o = np.zeros((B, Lq, Hq, d))
     lse = np.full((B, Hq, Lq), -np.inf)
     p_all = np.zeros((B, Hq, Lq, Lk)) if return_p else None

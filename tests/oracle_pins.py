@@ -366,6 +366,55 @@ def pin_paged_equals_dense(orc):
                     (ps, L, causal, wl)
 
 
+# --- right and symmetric windows ---------------------------------------------------------
+# window_size = (left, right) with -1 unbounded ("Flash Attention optimization" skill page,
+# workflow 2 step 3, whose symmetric example is (256, 256)).
+
+def pin_right_window_matches_materialised(orc):
+    """Rows with a right window (and a left one) equal the materialised version."""
+    seed = 900
+    for L, (wl, wr), (hq, hkv) in itertools.product((1, 7, 70), [(2, 3), (-1, 0), (0, -1), (5, 0),
+                                                               (0, 0), (-1, 4), (30, 30)], HEADS):
+        seed += 1
+        q, k, v = random_qkv(2, L, hq, hkv, 8, seed=seed)
+        rows = np.arange(2 * hq * L, dtype=np.int64)
+        o, lse = orc.attn_rows_kv(bits16(q), bits16(k), bits16(v), "fp16", False, wl, 0.4, rows,
+                                  window_right=wr)
+        qd, kd, vd = _widened(orc, q, k, v, "fp16")
+        o_ref, lse_ref = attn_materialised(qd, kd, vd, False, wl, 0.4, window_right=wr)
+        o_ref = o_ref.transpose(0, 2, 1, 3).reshape(-1, 8)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12, err_msg=f"L={L} w={wl, wr}")
+        np.testing.assert_allclose(lse, lse_ref.reshape(-1), rtol=1e-12, atol=1e-12)
+
+
+def pin_right_window_zero_is_causal(orc):
+    """Right window 0 admits exactly the causal keys: bit-identical to causal = True."""
+    q, k, v = random_qkv(1, 90, 4, 2, 16, seed=31)
+    rows = np.arange(4 * 90, dtype=np.int64)
+    for wl in (-1, 0, 7):
+        a = orc.attn_rows_kv(bits16(q), bits16(k), bits16(v), "fp16", False, wl, 0.2, rows,
+                             window_right=0)
+        b = orc.attn_rows_kv(bits16(q), bits16(k), bits16(v), "fp16", True, wl, 0.2, rows)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def pin_symmetric_window_mirror(orc):
+    """Reversing the sequence swaps the left and right windows: row i of (l, r) equals
+    row L-1-i of (r, l) on the reversed K and V."""
+    q, k, v = random_qkv(1, 50, 2, 2, 8, seed=33)
+    qr, kr, vr = q.flip(1).contiguous(), k.flip(1).contiguous(), v.flip(1).contiguous()
+    rows = np.arange(2 * 50, dtype=np.int64)
+    for wl, wr in [(3, 9), (0, 5), (-1, 2), (256, 256)]:
+        o, lse = orc.attn_rows_kv(bits16(q), bits16(k), bits16(v), "fp16", False, wl, 0.3, rows,
+                                  window_right=wr)
+        o2, lse2 = orc.attn_rows_kv(bits16(qr), bits16(kr), bits16(vr), "fp16", False, wr, 0.3,
+                                    rows, window_right=wl)
+        o2 = o2.reshape(2, 50, 8)[:, ::-1].reshape(-1, 8)
+        lse2 = lse2.reshape(2, 50)[:, ::-1].reshape(-1)
+        np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-13)
+
+
 ORACLE_PINS = [
     pin_widen_fp16_all_patterns, pin_widen_bf16_all_patterns, pin_matches_materialised,
     pin_constant_values, pin_causal_first_row, pin_window_zero_is_identity,
@@ -373,5 +422,6 @@ ORACLE_PINS = [
     pin_dominant_key, pin_key_permutation_invariance, pin_negative_scale_is_negated_query,
     pin_window_row_is_causal_suffix, pin_hand_worked_example, pin_rows_api_matches_full,
     pin_kv_matches_materialised, pin_kv_rows_are_square_suffix, pin_merge_of_key_splits,
-    pin_merge_hand_example, pin_paged_equals_dense,
+    pin_merge_hand_example, pin_paged_equals_dense, pin_right_window_matches_materialised,
+    pin_right_window_zero_is_causal, pin_symmetric_window_mirror,
 ]

@@ -41,6 +41,9 @@ MUTANTS = {
     "merge_lse_of_mean": ("lse[r] = m + log(total);", "lse[r] = m + log(total / nparts);"),
     "merge_first_part_only": ("        for (int64_t p = 0; p < nparts; ++p) {",
                               "        for (int64_t p = 0; p < 1; ++p) {"),
+    "right_window_one_short": ("j_hi = pos + window_right + 1;", "j_hi = pos + window_right;"),
+    "right_window_ignored": ("if (window_right >= 0 && pos + window_right + 1 < j_hi)",
+                             "if (0 && pos + window_right + 1 < j_hi)"),
 }
 
 
