@@ -26,7 +26,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
-           "attn_fwd_kv_paged",
+           "attn_fwd_kv_paged", "attn_fwd_window",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
            "PATH_SQUARE", "PATH_TILES", "debug_wait_probe", "debug_exp2",
@@ -67,6 +67,9 @@ def _bind(lib):
     lib.attn_fwd_kv.restype = i
     lib.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, i, i,
                                 p, sz, p]
+    lib.attn_fwd_window.restype = i
+    lib.attn_fwd_window.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p,
+                                    sz, p]
     lib.attn_fwd_kv_paged.restype = i
     lib.attn_fwd_kv_paged.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, i, i, i,
                                       ctypes.c_float, i, i, i, p, sz, p]
@@ -197,6 +200,29 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
     _check(code)
+
+
+def attn_fwd_window(q, k, v, window_left=-1, window_right=-1, scale=None, out_fp32=False,
+                    return_lse=True, workspace=None, stream=None):
+    """Attention with a window on both sides: row i sees keys i - window_left ..
+    i + window_right (-1 = unbounded on that side; (-1, 0) is causal). Returns (o, lse)."""
+    lib = load_library()
+    B, L, Hq, d = q.shape
+    o = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if return_lse else None
+    (B, L, Lk, Hq, Hkv, d), dt, out = _check_tensors(q, k, v, o, lse)
+    if Lk != L:
+        raise ValueError("k and v must have q's sequence length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = _default_workspace(q.device, 256)
+    _check(lib.attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
+                               int(window_left), int(window_right), float(scale), dt, out,
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream)))
+    return o, lse
 
 
 def kv_num_splits(B, Lq, Lk, Hq, Hkv, d, causal=False, window_left=-1) -> int:

@@ -328,6 +328,7 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
   p.group = plan.group;
   p.causal = causal;
   p.window_left = window_left;
+  p.window_right = -1;
   p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f ? 1 : 0;
   p.q_per_tile = plan.q_per_tile;
@@ -353,8 +354,8 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
 // one key split, so no partial results and no merge.
 attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int L, int Hq, int Hkv, int d, int causal,
-                                  int window_left, float scale, bool bf16, bool out_f32,
-                                  void* workspace, void* stream) {
+                                  int window_left, int window_right, float scale, bool bf16,
+                                  bool out_f32, void* workspace, void* stream) {
   const KvPlan plan = kv_plan(B, L, L, Hq, Hkv, causal, window_left);
   if (plan.group > 128)
     return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
@@ -382,6 +383,7 @@ attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, v
   p.group = plan.group;
   p.causal = causal;
   p.window_left = window_left;
+  p.window_right = window_right;
   p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f ? 1 : 0;
   p.q_per_tile = plan.q_per_tile;
@@ -455,7 +457,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   const int policy = g_path_policy.load();
   if (policy == ATTN_PATH_TILES ||
       (policy == ATTN_PATH_AUTO && 2 * num_units <= info.sms && Hq / Hkv <= 128))
-    return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, scale,
+    return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, -1, scale,
                                bf16, out_f32, workspace, stream);
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why) ||
@@ -490,6 +492,51 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
+}
+
+attn_status_t attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int L, int Hq, int Hkv, int d, int window_left,
+                              int window_right, float scale, attn_dtype_t dtype,
+                              attn_out_t out_dtype, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  g_detail.clear();
+  if (window_left < -1 || window_right < -1)
+    return fail(ATTN_ERR_INVALID_ARG, "window_left and window_right must be >= -1");
+  // the shape rules of attn_fwd, checked as a non-causal problem without a left window
+  attn_status_t st = check_shape(B, L, Hq, Hkv, d, 0, -1);
+  if (st != ATTN_OK) return st;
+  if (Hq / Hkv > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "bad dtype");
+  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
+  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
+  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  if (workspace_bytes < kWorkspaceBytes)
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_workspace_size()");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  std::string why;
+  const void* ptrs[6] = {q, k, v, o, workspace, lse};
+  const char* names[6] = {"q", "k", "v", "o", "workspace", "lse"};
+  for (int i = 0; i < 6; ++i)
+    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
+      return fail(ATTN_ERR_INVALID_ARG, why);
+  return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, 0, window_left, window_right,
+                             scale, dtype == ATTN_BF16, out_dtype == ATTN_OUT_FP32, workspace,
+                             stream);
 }
 
 int attn_fwd_kv_num_splits(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,

@@ -2,7 +2,10 @@
 //
 // What it computes: the attention of the square kernel for Lq query rows that are
 // the last Lq positions of an Lk-long sequence (row i sits at position
-// Lk - Lq + i; causal and window masks are taken at that position). This is a
+// Lk - Lq + i; causal and window masks are taken at that position). Row p sees
+// keys [p - window_left, p + window_right] (each bound -1 = none; causal is the
+// right bound 0), the window_size = (left, right) option of the "Flash Attention
+// optimization" skill page (workflow 2 step 3). This is a
 // generation step reading the whole KV cache, the case "What is memory-efficient
 // attention for long context on 8x H100?" (section 1, key limitations) names as
 // bound by HBM bandwidth. The keys of a row tile may be cut into `splits`
@@ -95,6 +98,9 @@ struct KvItem {
   bool bad;    // paged: the sequence length is out of range (nothing is computed)
 };
 
+// Right bound of a row's visible keys relative to its position (-1: none).
+__device__ __forceinline__ int right_bound(const KvParams& p) { return p.causal ? 0 : p.window_right; }
+
 template <bool PAGED>
 __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   KvItem it;
@@ -118,7 +124,8 @@ __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   }
   const int off = it.Lk - p.Lq;  // position of query row 0
   const int nblk = (it.Lk + kBN - 1) / kBN;
-  const int blk_hi = p.causal ? (off + it.i1 - 1) / kBN + 1 : nblk;
+  const int wr = right_bound(p);
+  const int blk_hi = (wr >= 0) ? min(nblk, (off + it.i1 - 1 + wr) / kBN + 1) : nblk;
   const int blk_lo = (p.window_left >= 0) ? max(0, off + it.i0 - p.window_left) / kBN : 0;
   const long long n = blk_hi - blk_lo;
   it.lo = blk_lo + static_cast<int>(n * it.split / p.splits);
@@ -243,11 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // one box of page_size rows per page of this block
             const int per_block = kBN / p.page_size;
 #pragma unroll
-            for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) {
-              if (pp >= per_block) break;
-              for (int c = 0; c < G::kChunks; ++c)
-                tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + pp * p.page_size * 128,
-                            tm, bar_full(slot), c * 64, it.g, rows_cur[pp], 0);
+            for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) {  // predicated: rows stay in registers
+              if (pp < per_block) {
+#pragma unroll
+                for (int c = 0; c < G::kChunks; ++c)
+                  tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + pp * p.page_size * 128,
+                              tm, bar_full(slot), c * 64, it.g, rows_cur[pp], 0);
+              }
             }
           } else {
             for (int c = 0; c < G::kChunks; ++c)
@@ -361,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int off = Lk - p.Lq;
     const int pos = off + qi;
     const int pos_min = off + it.i0, pos_max = off + it.i1 - 1;
+    const int wr = right_bound(p);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tO = tmem_base + lane_off + kColO;
     const float C = p.score_log2;
@@ -377,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tS = tmem_base + lane_off + 128u * buf;  // S, then P, of this block
       const int key0 = j * kBN;
-      const bool masked = (key0 + kBN > Lk) || (p.causal && key0 + kBN - 1 > pos_min) ||
+      const bool masked = (key0 + kBN > Lk) || (wr >= 0 && key0 + kBN - 1 > pos_min + wr) ||
                           (p.window_left >= 0 && key0 < pos_max - p.window_left);
       int vis_lo = 0, vis_hi = kBN;  // visible columns of this row: [vis_lo, vis_hi)
       if (masked) {
-        const int hi_key = p.causal ? min(Lk, pos + 1) : Lk;
+        const int hi_key = (wr >= 0) ? min(Lk, pos + wr + 1) : Lk;
         const int lo_key = (p.window_left >= 0) ? pos - p.window_left : 0;
         vis_hi = max(0, min(kBN, hi_key - key0));
         vis_lo = max(0, min(kBN, lo_key - key0));

@@ -15,6 +15,7 @@ struct KvParams {
   int group;            // Hq / Hkv: query heads that read one K/V head
   int causal;           // 0 / 1
   int window_left;      // -1 or >= 0
+  int window_right;     // -1 or >= 0: keys j <= position + window_right (causal acts as 0)
   float score_log2;     // |scale| * log2(e)
   int negate_scores;    // 1 when scale < 0
   int q_per_tile;       // query positions per 128-row tile (each with all `group` heads)

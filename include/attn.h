@@ -93,6 +93,24 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * attn_fwd with a window on both sides, the window_size = (left, right) option of
+ * the "Flash Attention optimization" skill page (workflow 2 step 3; its symmetric
+ * example is (256, 256)). Row i sees keys
+ *   J_i = { j < L : (window_left >= 0 => j >= i - window_left) and
+ *                   (window_right >= 0 => j <= i + window_right) },
+ * each bound -1 for none: (-1, 0) is causal attention, (-1, -1) full attention.
+ * Other arguments, layouts, workspace (attn_fwd_workspace_size) and errors as for
+ * attn_fwd; at most 128 query heads per K/V head. It runs on the one-tile kernel
+ * (ATTN_PATH_TILES below): a band of a few hundred keys per row is little work per
+ * query tile, which that kernel spreads over one CTA per 128-row tile.
+ */
+attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int L, int Hq, int Hkv, int d, int window_left,
+                              int window_right, float scale, attn_dtype_t dtype,
+                              attn_out_t out_dtype, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
  * attn_fwd without a caller-provided workspace, for callers that cannot allocate
  * device memory: code running where cudaMalloc is forbidden or unsafe (inside an
  * allocator or memory-pool callback, under another framework's allocator that owns

@@ -183,3 +183,22 @@ def call_paged(lib, **kw):
 def test_paged_invalid_arguments_are_rejected_before_launch(lib, kw, code):
     assert call_paged(lib, **kw) == code
     assert lib.attn_last_error_detail()
+
+
+def call_window(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, L=256, Hq=4, Hkv=4, d=64, wl=256, wr=256,
+             scale=0.125, dtype=0, out=0, ws=A, wsb=256, stream=None)
+    a.update(kw)
+    return lib.attn_fwd_window(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"],
+                               a["Hkv"], a["d"], a["wl"], a["wr"], a["scale"], a["dtype"],
+                               a["out"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(wl=-2), 1), (dict(wr=-5), 1), (dict(B=0), 1), (dict(Hq=6, Hkv=4), 1), (dict(d=96), 2),
+    (dict(Hq=256, Hkv=1), 2), (dict(scale=float("inf")), 1), (dict(dtype=7), 1), (dict(q=None), 1),
+    (dict(o=A + 4), 1), (dict(ws=None), 3), (dict(wsb=8), 3),
+])
+def test_window_invalid_arguments_are_rejected_before_launch(lib, kw, code):
+    assert call_window(lib, **kw) == code
+    assert lib.attn_last_error_detail()
