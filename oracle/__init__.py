@@ -34,7 +34,7 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FP16, BF16 = 0, 1
+FP16, BF16, FP8_E4M3 = 0, 1, 2
 
 
 def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
@@ -86,6 +86,8 @@ def _dtype_code(dtype) -> int:
         return FP16
     if dtype in ("bf16", BF16):
         return BF16
+    if dtype in ("fp8e4m3", FP8_E4M3):
+        return FP8_E4M3
     raise ValueError(f"unsupported dtype {dtype!r}")
 
 

@@ -65,14 +65,32 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_FP16 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_FP16 = 0, ORACLE_BF16 = 1, ORACLE_FP8_E4M3 = 2 };
 
-/* Exact widening of one 16-bit storage value to double.
+/* Exact widening of one storage value to double.
  * bfloat16: the upper half of an IEEE-754 binary32 value.
  * binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits;
- *           exponent 0 is the subnormal range f * 2^-24, exponent 31 is inf/NaN. */
+ *           exponent 0 is the subnormal range f * 2^-24, exponent 31 is inf/NaN.
+ * float8 e4m3 (in the low byte; the FP8 inputs of the "Flash Attention
+ *           optimization" skill page, workflow 3 step 3, torch.float8_e4m3fn):
+ *           1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; exponent 0 is
+ *           the subnormal range f * 2^-9; exponent 15 with fraction 7 is NaN (there
+ *           is no infinity), so the largest value is 448. */
 static double widen16(uint16_t bits, int dtype)
 {
+    if (dtype == ORACLE_FP8_E4M3) {
+        int sign8 = (bits >> 7) & 1;
+        int e8 = (bits >> 3) & 0xf;
+        int f8 = bits & 7;
+        double m8;
+        if (e8 == 15 && f8 == 7)
+            m8 = NAN;
+        else if (e8 == 0)
+            m8 = ldexp((double)f8, -9);
+        else
+            m8 = ldexp((double)(f8 + 8), e8 - 10);
+        return sign8 ? -m8 : m8;
+    }
     if (dtype == ORACLE_BF16) {
         uint32_t u = (uint32_t)bits << 16;
         float f;
@@ -176,7 +194,7 @@ int oracle_attn_rows_kv(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (B < 1 || Lq < 1 || Lk < Lq || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0 ||
         window_left < -1 || window_right < -1 || key_lo < 0 || key_hi > Lk || key_lo > key_hi)
         return -1;
-    if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)
+    if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16 && dtype != ORACLE_FP8_E4M3)
         return -1;
     for (int64_t r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= B * Hq * Lq)

@@ -219,7 +219,10 @@ def random_qkv(B, L, Hq, Hkv, d, dtype="fp16", seed=0, mul=1.0, device=None):
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
-    """The raw 16-bit patterns of a CPU fp16/bf16 tensor, as a uint16 numpy array."""
+    """The raw storage patterns of a CPU fp16/bf16 tensor (16 bits) or float8 e4m3 tensor
+    (8 bits, in the low byte), as a uint16 numpy array."""
+    if t.dtype == torch.float8_e4m3fn:
+        return t.contiguous().view(torch.uint8).numpy().astype(np.uint16)
     assert t.dtype in (torch.float16, torch.bfloat16)
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 

@@ -64,7 +64,31 @@ def pin_widen_bf16_all_patterns(orc):
     assert np.array_equal(got[~nan], ref[~nan])
 
 
+def pin_widen_fp8_e4m3_all_patterns(orc):
+    """All 256 float8 e4m3 patterns widen exactly as torch's float8_e4m3fn does."""
+    bits = np.arange(256, dtype=np.uint16)
+    got = orc.widen(bits, "fp8e4m3")
+    ref = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
 # --- the independent materialised implementation --------------------------------------
+
+def pin_fp8_attention_matches_materialised(orc):
+    """float8 e4m3 inputs (the skill page's workflow 3 casts N(0, 1) tensors straight to
+    float8_e4m3fn): the fp64 loop equals the materialised version on the widened values."""
+    for L, (causal, wl) in itertools.product((1, 9, 70), [(False, -1), (True, -1), (True, 4)]):
+        g = torch.Generator().manual_seed(L)
+        q, k, v = (torch.randn(2, L, h, 16, generator=g).to(torch.float8_e4m3fn)
+                   for h in (4, 2, 2))
+        o, lse = _full(orc, q, k, v, "fp8e4m3", causal, wl, 0.25)
+        qd, kd, vd = (orc.widen(bits16(t), "fp8e4m3") for t in (q, k, v))
+        o_ref, lse_ref = attn_materialised(qd, kd, vd, causal, wl, 0.25)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
 
 MASKS = [(False, -1), (True, -1), (True, 0), (True, 1), (True, 5), (False, 3)]
 HEADS = [(1, 1), (4, 2), (4, 1)]
@@ -416,7 +440,8 @@ def pin_symmetric_window_mirror(orc):
 
 
 ORACLE_PINS = [
-    pin_widen_fp16_all_patterns, pin_widen_bf16_all_patterns, pin_matches_materialised,
+    pin_widen_fp16_all_patterns, pin_widen_bf16_all_patterns, pin_widen_fp8_e4m3_all_patterns,
+    pin_fp8_attention_matches_materialised, pin_matches_materialised,
     pin_constant_values, pin_causal_first_row, pin_window_zero_is_identity,
     pin_gqa_equals_replicated_kv, pin_scale_zero_is_mean, pin_two_keys_sigmoid,
     pin_dominant_key, pin_key_permutation_invariance, pin_negative_scale_is_negated_query,

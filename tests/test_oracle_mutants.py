@@ -42,6 +42,9 @@ MUTANTS = {
     "merge_first_part_only": ("        for (int64_t p = 0; p < nparts; ++p) {",
                               "        for (int64_t p = 0; p < 1; ++p) {"),
     "right_window_one_short": ("j_hi = pos + window_right + 1;", "j_hi = pos + window_right;"),
+    "fp8_exponent_bias": ("m8 = ldexp((double)(f8 + 8), e8 - 10);",
+                          "m8 = ldexp((double)(f8 + 8), e8 - 11);"),
+    "fp8_subnormal_scale": ("m8 = ldexp((double)f8, -9);", "m8 = ldexp((double)f8, -10);"),
     "right_window_ignored": ("if (window_right >= 0 && pos + window_right + 1 < j_hi)",
                              "if (0 && pos + window_right + 1 < j_hi)"),
 }
