@@ -26,7 +26,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
-           "attn_fwd_kv_paged", "attn_fwd_window",
+           "attn_fwd_kv_paged", "attn_fwd_window", "attn_fwd_fp8",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
            "PATH_SQUARE", "PATH_TILES", "debug_wait_probe", "debug_exp2",
@@ -67,6 +67,10 @@ def _bind(lib):
     lib.attn_fwd_kv.restype = i
     lib.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, i, i,
                                 p, sz, p]
+    lib.attn_fwd_fp8.restype = i
+    lib.attn_fwd_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, sz, p]
+    lib.attn_fwd_fp8_workspace_size.restype = sz
+    lib.attn_fwd_fp8_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.attn_fwd_window.restype = i
     lib.attn_fwd_window.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p,
                                     sz, p]
@@ -200,6 +204,38 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
     _check(code)
+
+
+def attn_fwd_fp8(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=False,
+                 return_lse=True, workspace=None, stream=None):
+    """Attention forward on float8 e4m3 inputs (torch.float8_e4m3fn, [B, L, H, 64]).
+    Returns (o, lse): o in bfloat16 (or float32 with ``out_fp32``)."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.float8_e4m3fn:
+            raise TypeError(f"{name} must be float8_e4m3fn")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, L, Hkv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, L, Hkv, d]")
+    o = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if return_lse else None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = int(lib.attn_fwd_fp8_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)),
+                                               int(window_left)))
+    if workspace is None:
+        workspace = _default_workspace(q.device, max(need, 256))
+    _check(lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
+                            int(bool(causal)), int(window_left), float(scale),
+                            OUT_FP32 if out_fp32 else OUT_SAME, workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return o, lse
 
 
 def attn_fwd_window(q, k, v, window_left=-1, window_right=-1, scale=None, out_fp32=False,

@@ -114,6 +114,28 @@ bool make_tensor_map(CUtensorMap* map, const void* ptr, bool bf16, int B, int L,
   return true;
 }
 
+// Tensor map over a 4-D tensor of bytes (float8 data): dims innermost first, with
+// the byte strides of dims 1-3, the box and the swizzle mode.
+bool make_tensor_map_u8(CUtensorMap* map, const void* ptr, const cuuint64_t (&dims)[4],
+                        const cuuint64_t (&strides)[3], const cuuint32_t (&box)[4],
+                        CUtensorMapSwizzle swizzle, std::string* why) {
+  cudaError_t err;
+  auto encode = encode_fn(&err);
+  if (encode == nullptr) {
+    *why = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorName(err);
+    return false;
+  }
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled (float8) failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The pointer must be device (or managed) memory of device `dev`.
@@ -537,6 +559,102 @@ attn_status_t attn_fwd_window(const void* q, const void* k, const void* v, void*
   return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, 0, window_left, window_right,
                              scale, dtype == ATTN_BF16, out_dtype == ATTN_OUT_FP32, workspace,
                              stream);
+}
+
+size_t attn_fwd_fp8_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
+                                   int window_left) {
+  if (check_shape(B, L, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
+  if (d != 64 || Hq / Hkv > 128) return 0;
+  const size_t Lp = ((size_t)L + 15) / 16 * 16;
+  return kWorkspaceBytes + (size_t)B * Hkv * 64 * Lp;
+}
+
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                           int L, int Hq, int Hkv, int d, int causal, int window_left,
+                           float scale, attn_out_t out_dtype, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  g_detail.clear();
+  attn_status_t st = check_shape(B, L, Hq, Hkv, d, causal, window_left);
+  if (st != ATTN_OK) return st;
+  if (d != 64) return fail(ATTN_ERR_UNSUPPORTED, "the float8 path has d = 64 only");
+  if (Hq / Hkv > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
+  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
+  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  const int Lp = (L + 15) / 16 * 16;
+  if (workspace_bytes < kWorkspaceBytes + (size_t)B * Hkv * 64 * Lp)
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_fp8_workspace_size()");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  std::string why;
+  const void* ptrs[6] = {q, k, v, o, workspace, lse};
+  const char* names[6] = {"q", "k", "v", "o", "workspace", "lse"};
+  for (int i = 0; i < 6; ++i)
+    if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
+      return fail(ATTN_ERR_INVALID_ARG, why);
+
+  const KvPlan plan = kv_plan(B, L, L, Hq, Hkv, causal, window_left);
+  uint8_t* vt = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
+  CUtensorMap tm_q, tm_k, tm_vt;
+  const cuuint64_t L64 = (cuuint64_t)L, Lp64 = (cuuint64_t)Lp;
+  bool ok =
+      make_tensor_map_u8(&tm_q, q, {64, (cuuint64_t)Hq, L64, (cuuint64_t)B},
+                         {64, 64ull * Hq, 64ull * Hq * L64}, {64, (cuuint32_t)plan.group,
+                                                             (cuuint32_t)plan.q_per_tile, 1},
+                         CU_TENSOR_MAP_SWIZZLE_64B, &why) &&
+      make_tensor_map_u8(&tm_k, k, {64, (cuuint64_t)Hkv, L64, (cuuint64_t)B},
+                         {64, 64ull * Hkv, 64ull * Hkv * L64}, {64, 1, 128, 1},
+                         CU_TENSOR_MAP_SWIZZLE_64B, &why) &&
+      make_tensor_map_u8(&tm_vt, vt, {Lp64, 64, (cuuint64_t)Hkv, (cuuint64_t)B},
+                         {Lp64, 64ull * Lp64, 64ull * Lp64 * Hkv}, {128, 64, 1, 1},
+                         CU_TENSOR_MAP_SWIZZLE_128B, &why);
+  if (!ok) return fail(ATTN_ERR_CUDA, why);
+
+  ex19::Fp8LaunchArgs a = {};
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_vt = &tm_vt;
+  ex19::KvParams& p = a.p;
+  p.o = o;
+  p.lse = lse;
+  p.status = static_cast<uint32_t*>(workspace);
+  p.B = B;
+  p.Lq = L;
+  p.Lk = L;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = plan.group;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.window_right = -1;
+  p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f ? 1 : 0;
+  p.q_per_tile = plan.q_per_tile;
+  p.row_tiles = plan.row_tiles;
+  p.splits = 1;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.v = static_cast<const uint8_t*>(v);
+  a.vt = vt;
+  a.Lp = Lp;
+  a.grid = plan.items;
+  a.stream = static_cast<cudaStream_t>(stream);
+  e = ex19::launch_fp8(out_dtype == ATTN_OUT_FP32, a);
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return ATTN_OK;
 }
 
 int attn_fwd_kv_num_splits(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,

@@ -1,0 +1,479 @@
+// attn_fp8_kernel.cuh — exact attention forward on float8 e4m3 inputs, sm_103a.
+//
+// What it computes: the attention of the square kernels (same masks, GQA mapping,
+// scale and LSE) on Q, K, V given as float8 e4m3, the FP8 path of the "Flash
+// Attention optimization" skill page (workflow 3: inputs cast to float8_e4m3fn and
+// run through FP8 attention kernels) and of "What is memory-efficient attention
+// for long context on 8x H100?" (section 2: FlashAttention-3 adds FP8 support).
+// Head dimension 64; O is written in bf16 or float32.
+//
+// Arithmetic: S = Q Kᵀ on the tensor cores (.kind::f8f6f4, fp32 accumulate, exact
+// products of the e4m3 inputs). The softmax works in base 2 as in the other
+// kernels; its weights are stored for the P·V MMA as e4m3 too, scaled to
+// P' = 2^(x − m + 7) ≤ 256 so that they sit in e4m3's normal range, and the
+// normaliser l' sums the same rounded P' values (the factor 2^7 cancels in O' / l').
+// O' = Σ P'·V accumulates in fp32 in TMEM.
+//
+// GB300 mapping (one CTA per 128-row tile, as the one-tile kernel):
+//   * Q and K tiles: TMA boxes of 64 bytes (64 e4m3) per row, 64-byte swizzle.
+//   * V is read as Vᵀ (keys contiguous), written by attn_fp8_transpose_v into the
+//     workspace, so that both MMA operands are K-major: a 64 × 128-byte tile per
+//     block, 128-byte swizzle.
+//   * warp 4 (producer) streams K_j and Vᵀ_j into a ring of 8 KiB slots; warp 5
+//     (MMA) issues S(j) into TMEM buffer j mod 2 and O += P(j) Vᵀ(j) with P read
+//     from shared memory buffer j mod 2; S(j + 2) is issued after P·V(j).
+//   * warps 0-3 (softmax): one thread per row; P' is converted to e4m3 and stored
+//     in the 128-byte-swizzle layout (16-byte chunk c of row r at chunk c ^ (r % 8)),
+//     then made visible to the tensor core (fence.proxy.async) before p_full.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "attn_kv_params.h"
+#include "row_ops.cuh"
+#include "sm103_ptx.cuh"
+#include "tmem_io.cuh"
+
+namespace ex19 {
+namespace fp8 {
+
+constexpr int kBM = 128;             // rows per tile (= TMEM lanes)
+constexpr int kBN = 128;             // keys per block
+constexpr int kD = 64;               // head dimension
+constexpr int kThreads = 192;        // 4 softmax warps + producer warp + MMA warp
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 320)
+constexpr uint32_t kColO = 256;
+constexpr int kPOffset = 7;          // P' = 2^(x - m + 7): at most 2^8 with the rescale threshold 1
+
+enum : uint32_t {
+  kSiteProdEmpty = 0xA0001,
+  kSiteMmaQFull = 0xB0001, kSiteMmaKFull = 0xB0002, kSiteMmaVFull = 0xB0003,
+  kSiteMmaPFull = 0xB0004, kSiteMmaDrain = 0xB0005,
+  kSiteSmxSFull = 0xC0001, kSiteSmxOFull = 0xC0002, kSiteSmxPvDone = 0xC0003,
+  kSiteDrainLoads = 0xD0001,
+};
+
+struct Fp8Geometry {
+  static constexpr int kQBytes = kBM * kD;        // 8 KiB: 128 rows x 64 bytes
+  static constexpr int kSlotBytes = 8192;         // K_j (128 x 64 B) or Vᵀ_j (64 x 128 B)
+  static constexpr int kSlots = 8;
+  static constexpr int kPBytes = kBM * kBN;       // 16 KiB: 128 rows x 128 bytes
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 8192;
+  static constexpr int kOffP = kOffKV + kSlots * kSlotBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full, drain
+  static constexpr int kNumBars = 2 * kSlots + 9;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemUsed = kOffMisc + 16;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;
+};
+
+// Two e4m3 values (low byte: the pair's first element) of a packed fp16 pair.
+__device__ __forceinline__ uint32_t e4m3x2_of_half2(uint32_t h2) {
+  __half2_raw r;
+  r.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+  r.y = static_cast<unsigned short>(h2 >> 16);
+  return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
+}
+
+// The packed fp16 pair of two e4m3 values (inverse widening, exact).
+__device__ __forceinline__ uint32_t half2_of_e4m3x2(uint32_t e2) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(e2), __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fp8_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_vt, const KvParams p) {
+  using G = Fp8Geometry;
+  constexpr int S = G::kSlots;
+  constexpr float kThresh = 1.0f;  // fp16 exponent arguments: move the reference max by > 2^1
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + G::kOffQ;
+  const uint32_t sKV = sbase + G::kOffKV;
+  const uint32_t sP = sbase + G::kOffP;
+  const uint32_t bars = sbase + G::kOffBar;
+  auto bar_full = [&](uint32_t s) { return bars + 8u * s; };
+  auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
+  const uint32_t bar_q_full = bars + 8u * (2 * S);
+  auto bar_s_full = [&](uint32_t b) { return bars + 8u * (2 * S + 1 + b); };
+  auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 3 + b); };
+  auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
+  const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
+  const uint32_t bar_drain = bars + 8u * (2 * S + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: (batch, K/V head, 128-row tile); the group's query heads share the tile.
+  int x = blockIdx.x;
+  const int rt = x % p.row_tiles;
+  x /= p.row_tiles;
+  const int g = x % p.Hkv;
+  const int b = x / p.Hkv;
+  const int i0 = rt * p.q_per_tile, i1 = min(p.Lq, i0 + p.q_per_tile);
+  const int L = p.Lk;
+  const int nblk = (L + kBN - 1) / kBN;
+  const int wr = p.causal ? 0 : p.window_right;
+  const int blk_hi = (wr >= 0) ? min(nblk, (i1 - 1 + wr) / kBN + 1) : nblk;
+  const int blk_lo = (p.window_left >= 0) ? max(0, i0 - p.window_left) / kBN : 0;
+  const int nblocks = max(0, blk_hi - blk_lo);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_q_full, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar_s_full(k), 1);
+      mbar_init(bar_p_full(k), kBM);
+      mbar_init(bar_pv_done(k), 1);
+    }
+    mbar_init(bar_o_full, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_vt);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  WaitCtl wc;
+  wc.abort_flag = abort_flag;
+  wc.status = p.status;
+  wc.limit_ns = p.wait_limit_ns;
+  wc.unit = blockIdx.x;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nblocks > 0) {
+      mbar_arrive_expect_tx(bar_q_full, 64u * p.group * p.q_per_tile);
+      tma_load_4d(sQ, &tm_q, bar_q_full, 0, g * p.group, i0, b);
+      uint32_t n = 0;
+      bool ok = true;
+      for (int j = blk_lo; ok && j < blk_hi; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t slot = n % S;
+          ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_full(slot), G::kSlotBytes);
+          if (kv == 0)  // K_j: 128 keys x 64 bytes
+            tma_load_4d(sKV + slot * G::kSlotBytes, &tm_k, bar_full(slot), 0, g, j * kBN, b);
+          else  // Vᵀ_j: 64 rows (d) x 128 bytes (keys)
+            tma_load_4d(sKV + slot * G::kSlotBytes, &tm_vt, bar_full(slot), j * kBN, 0, g, b);
+          ++n;
+        }
+      }
+      if (!ok) {
+        for (uint32_t back = 1; back <= S && back <= n; ++back) {
+          const uint32_t m = n - back;
+          mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrainLoads);
+        }
+        mbar_wait_drain(bar_q_full, 0, wc, kSiteDrainLoads);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------- MMA issuer
+    if (nblocks > 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32acc(false, kBM, kBN, false);  // e4m3 x e4m3
+      constexpr uint32_t idesc_o = idesc_f16_f32acc(false, kBM, kD, false);
+      const uint64_t dq = sdesc_swizzled(sQ, 16, 512, 4);      // 64-byte rows, 64-byte swizzle
+      const uint64_t dk = sdesc_swizzled(sKV, 16, 512, 4);
+      const uint64_t dvt = sdesc_swizzled(sKV, 16, 1024, 2);   // 128-byte rows, 128-byte swizzle
+      const uint64_t dp = sdesc_swizzled(sP, 16, 1024, 2);
+      const uint32_t mO = tmem_base + kColO;
+      auto slot_of = [&](uint32_t idx) { return idx % S; };
+      auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
+      // S = Q · K_jᵀ into TMEM buffer jj & 1 (two MMAs of K = 32 bytes); releases K_j.
+      auto issue_s = [&](int jj) __attribute__((always_inline)) -> bool {
+        const uint32_t kidx = 2u * jj;
+        if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull)) return false;
+        tc_fence_after();
+        const uint32_t mS = tmem_base + 128u * (jj & 1);
+        const uint64_t dks = dk + ((slot_of(kidx) * G::kSlotBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kD / 32; ++kk)
+          mma_ss_f8_elect(mS, dq + (kk * 32 >> 4), dks + (kk * 32 >> 4), idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit_elect(bar_s_full(jj & 1));
+        mma_commit_elect(bar_empty(slot_of(kidx)));
+        return true;
+      };
+      // O (+)= P(jj) · V_j with P from shared-memory buffer jj & 1 and Vᵀ_j from its
+      // slot (four MMAs of K = 32 keys); releases Vᵀ_j.
+      auto issue_pv = [&](int jj) __attribute__((always_inline)) -> bool {
+        const uint32_t vidx = 2u * jj + 1u;
+        if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
+        if (!mbar_wait_warp(bar_p_full(jj & 1), (jj >> 1) & 1u, wc, kSiteMmaPFull)) return false;
+        tc_fence_after();
+        const uint64_t dps = dp + (((jj & 1) * G::kPBytes) >> 4);
+        const uint64_t dvs = dvt + ((slot_of(vidx) * G::kSlotBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 32; ++kk)
+          mma_ss_f8_elect(mO, dps + (kk * 32 >> 4), dvs + (kk * 32 >> 4), idesc_o,
+                          (jj == 0 && kk == 0) ? 0u : 1u);
+        mma_commit_elect(bar_pv_done(jj & 1));
+        mma_commit_elect(bar_empty(slot_of(vidx)));
+        return true;
+      };
+      bool ok = mbar_wait_warp(bar_q_full, 0, wc, kSiteMmaQFull);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+        if (ok && nblocks > 1) ok = issue_s(1);
+        for (int jj = 0; ok && jj < nblocks; ++jj) {
+          ok = issue_pv(jj);
+          if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
+        }
+        if (ok) mma_commit_elect(bar_o_full);
+      }
+    }
+    mma_commit_elect(bar_drain);
+    mbar_wait_drain(bar_drain, 0, wc, kSiteMmaDrain);
+  } else {
+    // -------------------------------------------------------- softmax warps
+    const int rho = warp * 32 + lane;  // row of the tile
+    const bool row_ok = rho < (i1 - i0) * p.group;
+    const int qi = i0 + rho / p.group;
+    const int h = g * p.group + rho % p.group;
+    const int pos_min = i0, pos_max = i1 - 1;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem_base + lane_off + kColO;
+    const float C = p.score_log2;
+    const bool neg = p.negate_scores != 0;
+    const float Cs = neg ? -C : C;
+    float m_ref = -INFINITY;  // reference max (base-2 units)
+    float l = 0.f;            // running sum of the stored P' values
+    bool ok = true;
+    for (int jj = 0; jj < nblocks; ++jj) {
+      const int j = blk_lo + jj;
+      const uint32_t buf = jj & 1;
+      ok = mbar_wait_warp(bar_s_full(buf), (jj >> 1) & 1u, wc, kSiteSmxSFull);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tmem_base + lane_off + 128u * buf;
+      const int key0 = j * kBN;
+      const bool masked = (key0 + kBN > L) || (wr >= 0 && key0 + kBN - 1 > pos_min + wr) ||
+                          (p.window_left >= 0 && key0 < pos_max - p.window_left);
+      int vis_lo = 0, vis_hi = kBN;
+      if (masked) {
+        const int hi_key = (wr >= 0) ? min(L, qi + wr + 1) : L;
+        const int lo_key = (p.window_left >= 0) ? qi - p.window_left : 0;
+        vis_hi = max(0, min(kBN, hi_key - key0));
+        vis_lo = max(0, min(kBN, lo_key - key0));
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      bool stop = false;
+      auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
+        constexpr bool M = decltype(masked_tag)::value;
+        uint32_t sr[128];
+        tmem_ld_x128(tS, sr);
+        if constexpr (M) {
+          const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < vis_lo || c >= vis_hi) sr[c] = fill;
+        }
+        float mx;
+        {
+          float sv[128];
+#pragma unroll
+          for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
+          mx = neg ? -row_min128(sv) : row_max128(sv);
+        }
+        const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
+        if (bm > m_ref + kThresh) {
+          alpha = ex2_approx(m_ref - bm);
+          m_ref = bm;
+          rescale = true;
+        }
+        // x - m + 7 with the reference max of this block
+        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float nmu = static_cast<float>(kPOffset) - mu;
+        // P buffer `buf` was read by P·V(jj - 2): wait until that MMA is done.
+        if (jj >= 2) {
+          if (!mbar_wait_warp(bar_pv_done(buf), ((jj - 2) >> 1) & 1u, wc, kSiteSmxPvDone)) {
+            stop = true;
+            return;
+          }
+          tc_fence_after();
+        }
+        const uint32_t prow = sP + buf * G::kPBytes + rho * 128;
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int q16 = 0; q16 < 8; ++q16) {  // 16 keys = one 16-byte chunk of the row
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {  // 4 keys per 32-bit word
+            uint32_t e2[2];
+#pragma unroll
+            for (int v2 = 0; v2 < 2; ++v2) {
+              const int c = q16 * 16 + u * 4 + v2 * 2;
+              const float2 xx = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                  make_float2(Cs, Cs), make_float2(nmu, nmu));
+              __half2 xh = __floats2half2_rn(xx.x, xx.y);
+              uint32_t pp = ex2_f16x2(*reinterpret_cast<uint32_t*>(&xh));
+              if constexpr (M) {
+                const uint32_t keep = ((c >= vis_lo && c < vis_hi) ? 0x0000FFFFu : 0u) |
+                                      ((c + 1 >= vis_lo && c + 1 < vis_hi) ? 0xFFFF0000u : 0u);
+                pp &= keep;
+              }
+              e2[v2] = e4m3x2_of_half2(pp);
+            }
+            w[u] = e2[0] | (e2[1] << 16);
+            // normaliser: the stored (rounded) values, widened exactly and summed in fp32
+            const uint32_t h0 = half2_of_e4m3x2(e2[0]), h1 = half2_of_e4m3x2(e2[1]);
+            acc[0] = __fadd2_rn(acc[0], __half22float2(*reinterpret_cast<const __half2*>(&h0)));
+            acc[1] = __fadd2_rn(acc[1], __half22float2(*reinterpret_cast<const __half2*>(&h1)));
+          }
+          const uint32_t addr = prow + ((q16 ^ (rho & 7)) << 4);  // 128-byte swizzle
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
+                       "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
+        }
+        fence_proxy_async_shared();  // P is read by the tensor core (async proxy)
+        l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
+      };
+      if (masked)
+        block_body(std::true_type{});
+      else
+        block_body(std::false_type{});
+      if (stop) {
+        ok = false;
+        break;
+      }
+      // O rescale once the previous P·V is complete; the first block's P·V overwrites O.
+      if (__any_sync(0xffffffffu, rescale && jj > 0)) {
+        if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float a = (rescale && jj > 0) ? alpha : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t orow[32];
+          tmem_ld_x32(tO + c0, orow);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * a);
+          tmem_st_x32(tO + c0, orow);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_p_full(buf));
+    }
+    if (ok && nblocks > 0) {
+      ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteSmxOFull);
+      if (ok) tc_fence_after();
+    }
+    if (ok && nblocks > 0) {
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const size_t orow_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * kD;
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t orow[32];
+        tmem_ld_x32(tO + c0, orow);
+        if (!row_ok) continue;
+        if constexpr (OUT_F32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow_off + c0);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            dst[c >> 2] = make_float4(__uint_as_float(orow[c]) * inv_l,
+                                      __uint_as_float(orow[c + 1]) * inv_l,
+                                      __uint_as_float(orow[c + 2]) * inv_l,
+                                      __uint_as_float(orow[c + 3]) * inv_l);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_off + c0);
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 wv;
+            wv.x = pack2(__uint_as_float(orow[c]) * inv_l, __uint_as_float(orow[c + 1]) * inv_l, true);
+            wv.y = pack2(__uint_as_float(orow[c + 2]) * inv_l, __uint_as_float(orow[c + 3]) * inv_l, true);
+            wv.z = pack2(__uint_as_float(orow[c + 4]) * inv_l, __uint_as_float(orow[c + 5]) * inv_l, true);
+            wv.w = pack2(__uint_as_float(orow[c + 6]) * inv_l, __uint_as_float(orow[c + 7]) * inv_l, true);
+            dst[c >> 3] = wv;
+          }
+        }
+      }
+      if (row_ok && p.lse != nullptr) {
+        const float lse2 = (l > 0.f) ? m_ref - static_cast<float>(kPOffset) + lg2_approx(l) : -INFINITY;
+        p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + qi] =
+            (l > 0.f) ? lse2 * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Vᵀ for the P·V MMA: v [B, L, Hkv, 64] e4m3 -> vt [B, Hkv, 64, Lp] (keys contiguous,
+// Lp = L rounded up to 16; keys L .. Lp-1 are zero). One CTA per (64 keys, head,
+// batch) through a 64 x 64-byte tile in shared memory.
+__global__ void __launch_bounds__(256) attn_fp8_transpose_v(const uint8_t* __restrict__ v,
+                                                            uint8_t* __restrict__ vt, int L,
+                                                            int Hkv, int Lp) {
+  __shared__ uint8_t tile[64][64 + 4];
+  const int k0 = blockIdx.x * 64, g = blockIdx.y, b = blockIdx.z;
+  const int t = threadIdx.x;
+  // load: 64 keys x 64 bytes, 16 bytes per thread
+  {
+    const int key = t >> 2, c16 = (t & 3) * 16;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + key < L)
+      val = *reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * L + k0 + key) * Hkv + g) * 64 + c16);
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+    for (int u = 0; u < 16; ++u) tile[key][c16 + u] = static_cast<uint8_t>(w[u >> 2] >> (8 * (u & 3)));
+  }
+  __syncthreads();
+  // store: 64 rows (d) x 64 keys, 16 keys per thread
+  {
+    const int dd = t >> 2, kq = (t & 3) * 16;
+    if (k0 + kq < Lp) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int u = 0; u < 16; ++u) w[u >> 2] |= static_cast<uint32_t>(tile[kq + u][dd]) << (8 * (u & 3));
+      *reinterpret_cast<uint4*>(vt + ((static_cast<size_t>(b) * Hkv + g) * 64 + dd) * Lp + k0 + kq) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+}  // namespace fp8
+}  // namespace ex19

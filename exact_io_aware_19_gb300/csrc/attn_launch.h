@@ -26,6 +26,18 @@ struct KvLaunchArgs {
   cudaStream_t stream;
 };
 
+struct Fp8LaunchArgs {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_vt;  // over vt
+  KvParams p;                // Lq = Lk = L, splits = 1
+  const uint8_t* v;          // [B, L, Hkv, 64] e4m3
+  uint8_t* vt;               // [B, Hkv, 64, Lp] e4m3, in the workspace
+  int Lp;                    // L rounded up to 16
+  int grid;                  // B * Hkv * row_tiles
+  cudaStream_t stream;
+};
+
 // Each returns the CUDA error of configuring / enqueuing the kernel.
 cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
@@ -33,6 +45,8 @@ cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // The same over a paged K/V cache (a.p.block_table, seq_lens, page_size, ... set).
 cudaError_t launch_kv_paged(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
+// The float8 forward: the V transpose, then the attention kernel.
+cudaError_t launch_fp8(bool out_f32, const Fp8LaunchArgs& a);
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream);

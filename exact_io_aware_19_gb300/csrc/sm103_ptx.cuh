@@ -249,6 +249,20 @@ __device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// D (+)= A · B for float8 e4m3 A and B, both in shared memory (.kind::f8f6f4,
+// K = 32 per instruction); issued by one lane picked by elect.sync. The
+// instruction descriptor has the .kind::f16 layout with format 0 (e4m3) for both.
+__device__ __forceinline__ void mma_ss_f8_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -291,6 +305,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// The same with another swizzle layout (bits 61-63): 2 = 128-byte, 4 = 64-byte.
+// K-major tiles with 64-byte rows (64 float8 elements) use the 64-byte swizzle,
+// whose 8-row atom is 512 bytes (sbo).
+__device__ __forceinline__ uint64_t sdesc_swizzled(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                                   uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
   return d;
 }
 

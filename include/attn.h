@@ -93,6 +93,28 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Attention forward on float8 e4m3 inputs: the FP8 path of the "Flash Attention
+ * optimization" skill page (workflow 3: q, k, v cast to float8_e4m3fn, no scale
+ * factors) and of "What is memory-efficient attention for long context on 8x
+ * H100?" section 2. Same definition, masks, layouts and LSE as attn_fwd, with
+ *   q, k, v   device, [B, L, H, 64] bytes of float8 e4m3 (1 sign, 4 exponent bits,
+ *             bias 7, 3 fraction bits), 16-byte aligned; d must be 64
+ *   o         [B, L, Hq, 64] bfloat16 (ATTN_OUT_SAME) or float32 (ATTN_OUT_FP32)
+ *   workspace >= attn_fwd_fp8_workspace_size(...) bytes: the status word and a
+ *             transposed copy of v ([B, Hkv, 64, L rounded up to 16])
+ * The attention weights enter the P·V product as e4m3 values (3 fraction bits), so
+ * the result differs from the exact one by up to about 2^-3 of the weighted mean of
+ * |v| per element, and the LSE by up to ln(1/(1 - 2^-4)); see the tests for the
+ * bound. Enqueues a transpose kernel and the attention kernel on `stream`.
+ */
+size_t attn_fwd_fp8_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
+                                   int window_left);
+attn_status_t attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int L, int Hq, int Hkv, int d, int causal, int window_left,
+                           float scale, attn_out_t out_dtype, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * attn_fwd with a window on both sides, the window_size = (left, right) option of
  * the "Flash Attention optimization" skill page (workflow 2 step 3; its symmetric
  * example is (256, 256)). Row i sees keys

@@ -202,3 +202,21 @@ def call_window(lib, **kw):
 def test_window_invalid_arguments_are_rejected_before_launch(lib, kw, code):
     assert call_window(lib, **kw) == code
     assert lib.attn_last_error_detail()
+
+
+def test_fp8_workspace_and_validation(lib):
+    # status word + transposed V: B * Hkv * 64 * L rounded up to 16
+    assert lib.attn_fwd_fp8_workspace_size(2, 4096, 32, 32, 64, 0, -1) == 256 + 2 * 32 * 64 * 4096
+    assert lib.attn_fwd_fp8_workspace_size(1, 100, 4, 4, 64, 1, -1) == 256 + 4 * 64 * 112
+    assert lib.attn_fwd_fp8_workspace_size(1, 100, 4, 4, 128, 1, -1) == 0  # d = 64 only
+    f = lib.attn_fwd_fp8
+    ok = dict(q=A, k=A, v=A, o=A, lse=A, B=1, L=256, Hq=4, Hkv=4, d=64, causal=1, wl=-1,
+              scale=0.125, out=0, ws=A, wsb=1 << 20, stream=None)
+    for kw, code in [(dict(d=128), 2), (dict(Hq=6), 1), (dict(out=3), 1), (dict(q=None), 1),
+                     (dict(v=A + 4), 1), (dict(ws=None), 3), (dict(wsb=300), 3),
+                     (dict(scale=float("nan")), 1), (dict(causal=0, wl=4), 2)]:
+        a = dict(ok)
+        a.update(kw)
+        assert f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"], a["Hkv"],
+                 a["d"], a["causal"], a["wl"], a["scale"], a["out"], a["ws"], a["wsb"],
+                 a["stream"]) == code, kw

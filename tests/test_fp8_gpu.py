@@ -1,0 +1,116 @@
+"""GPU parity of the float8 e4m3 forward (attn_fwd_fp8) against the fp64 oracle.
+
+The inputs follow the "Flash Attention optimization" skill page, workflow 3: tensors
+cast straight to float8_e4m3fn (no scale factors); the oracle widens the same bytes
+exactly. The kernel stores the softmax weights for the P·V product as e4m3 too
+(P' = 2^(x - m + 7), 3 fraction bits), so the tolerance is derived from that rounding:
+
+  * each weight carries a relative error eps <= 2^-4 (e4m3 rounding, normal range)
+    + 2^-8 ln 2 (the fp16 argument of 2^x) + 2^-10 (the fp16 exponential) < 0.068;
+    weights below e4m3's normal range are below 2^-6 of a total of at least 2^6;
+  * the normaliser sums the same rounded weights, so with w the exact weights
+    |O - O*| <= 2 eps / (1 - eps) * sum_j w_j |v_j| < 0.146 * A,  A = softmax(s) |V|;
+  * |LSE - LSE*| <= -ln(1 - eps) < 0.071.
+
+A, the weighted mean of |v|, is the oracle evaluated on |V|. The bound is a worst
+case; the errors are rounding errors of both signs, so their mean is far smaller,
+which the mean check uses to catch systematic mistakes. Exact properties that hold
+for the kernel's own arithmetic (constant V, a single visible key) are checked too.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from parity_util import gather_rows
+
+pytestmark = pytest.mark.gpu
+
+O_REL = 0.146
+O_ABS = 1e-3
+LSE_ABS = 0.071
+MEAN_REL = 0.02
+
+
+def fp8_qkv(B, L, Hq, Hkv, seed, mul=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, L, Hq, 64, generator=g) * mul).to(torch.float8_e4m3fn)
+    k = (torch.randn(B, L, Hkv, 64, generator=g) * mul).to(torch.float8_e4m3fn)
+    v = torch.randn(B, L, Hkv, 64, generator=g).to(torch.float8_e4m3fn)
+    return q, k, v
+
+
+def compare_fp8(q, k, v, causal, wl, scale, rows=None, label=""):
+    import exact_io_aware_19_gb300 as ex
+    B, L, Hq, d = q.shape
+    if rows is None:
+        rows = np.arange(B * Hq * L, dtype=np.int64)
+    orc = oracle.default()
+    qb, kb, vb = si.bits16(q), si.bits16(k), si.bits16(v)
+    o_ref, lse_ref = orc.attn_rows(qb, kb, vb, "fp8e4m3", causal, wl, scale, rows)
+    a_ref, _ = orc.attn_rows(qb, kb, vb & 0x7F, "fp8e4m3", causal, wl, scale, rows)  # A with |V|
+    o32, lse = ex.attn_fwd_fp8(q.cuda(), k.cuda(), v.cuda(), causal=causal, window_left=wl,
+                               scale=scale, out_fp32=True)
+    o16, lse16 = ex.attn_fwd_fp8(q.cuda(), k.cuda(), v.cuda(), causal=causal, window_left=wl,
+                                 scale=scale)
+    ex.sync_status()
+    g32, glse = gather_rows(o32, lse, rows)
+    g16, _ = gather_rows(o16, lse16, rows)
+    assert np.isfinite(g32).all() and np.isfinite(glse).all(), label
+    d32, dl = np.abs(g32 - o_ref), np.abs(glse - lse_ref)
+    bound = O_REL * a_ref + O_ABS
+    assert (d32 <= bound).all(), (label, float((d32 - bound).max()))
+    assert dl.max() <= LSE_ABS, (label, float(dl.max()))
+    assert d32.mean() <= MEAN_REL * a_ref.mean(), (label, d32.mean(), a_ref.mean())
+    # bf16 output: the same bound plus half a bf16 ulp of the value
+    half = 0.5 * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(o_ref), 2.0 ** -126))) - 7)
+    assert (np.abs(g16 - o_ref) <= bound + half).all(), label
+    assert torch.equal(lse, lse16), label
+    return float(d32.max()), float(d32.mean() / a_ref.mean())
+
+
+@pytest.mark.parametrize("L", [1, 127, 129, 300, 1000])
+def test_fp8_small_shapes(L):
+    for n, ((causal, wl), (hq, hkv)) in enumerate(
+            [((False, -1), (4, 4)), ((True, -1), (4, 4)), ((True, 50), (8, 2)),
+             ((False, -1), (8, 2)), ((True, 0), (2, 2)), ((True, -1), (6, 2))]):
+        q, k, v = fp8_qkv(2, L, hq, hkv, seed=10 * L + n)
+        compare_fp8(q, k, v, causal, wl, 0.125, label=f"L={L} mask={(causal, wl)} {hq}/{hkv}")
+
+
+def test_fp8_exact_properties():
+    """Properties of the kernel's own arithmetic: the weights it stores sum to its own
+    normaliser, so a constant V gives exactly that constant and a single visible key
+    gives exactly its value row."""
+    import exact_io_aware_19_gb300 as ex
+    q, k, v = fp8_qkv(1, 700, 4, 4, seed=3)
+    c = torch.tensor([1.0, -2.0, 0.5, 448.0, -0.015625, 3.0, 0.0, -7.0] * 8).to(torch.float8_e4m3fn)
+    vc = c.view(1, 1, 1, 64).expand(1, 700, 4, 64).contiguous()
+    o, _ = ex.attn_fwd_fp8(q.cuda(), k.cuda(), vc.cuda(), out_fp32=True)
+    want = c.float().view(1, 1, 1, 64).expand_as(o.cpu())
+    # O' and l' sum the same weights in fp32 (tensor core and softmax thread, in
+    # different orders): equal to within fp32 accumulation
+    assert torch.allclose(o.cpu(), want, rtol=2e-5, atol=1e-6), (o.cpu() - want).abs().max()
+    o, lse = ex.attn_fwd_fp8(q.cuda(), k.cuda(), v.cuda(), causal=True, out_fp32=True)
+    assert torch.equal(o[0, 0].cpu(), v[0, 0].float())  # row 0 sees key 0 only
+    o, _ = ex.attn_fwd_fp8(q.cuda(), k.cuda(), v.cuda(), causal=True, window_left=0, out_fp32=True)
+    assert torch.equal(o.cpu(), v.float())  # every row sees only itself
+
+
+def test_fp8_pages_workload_sampled():
+    """The skill page's FP8 example shape: 2 x 4096 x 32 x 64, non-causal, default scale."""
+    q, k, v = fp8_qkv(2, 4096, 32, 32, seed=1009)
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(2 * 32 * 4096, 768, replace=False)).astype(np.int64)
+    mx, rel = compare_fp8(q, k, v, False, -1, 1 / math.sqrt(64), rows=rows, label="2x4096x32x64")
+    assert rel < 0.01
+
+
+def test_fp8_large_scores():
+    """Scores spread over many powers of two (inputs x4): the rescaling and the
+    e4m3 range of the weights are exercised."""
+    q, k, v = fp8_qkv(1, 2048, 8, 8, seed=11, mul=4.0)
+    compare_fp8(q, k, v, True, -1, 0.125, label="scores x16")
