@@ -61,6 +61,9 @@ def _bind(path: str):
     lib.oracle_attn_rows_kv.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64, i64,
                                         ctypes.c_int, i64, i64, ctypes.c_double, i64, i64, p,
                                         i64, p, p]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
+    lib.oracle_attn_bwd.argtypes = [p, p, p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                    ctypes.c_int, i64, ctypes.c_double, p, p, p]
     lib.oracle_merge.restype = None
     lib.oracle_merge.argtypes = [i64, i64, i64, p, p, p, p]
     lib.oracle_widen.restype = None
@@ -195,6 +198,27 @@ class Oracle:
             o[b:b + 1], lse[b:b + 1] = self.attn_full_kv(q_bits[b:b + 1], kb, vb, dtype, causal,
                                                          window_left, scale)
         return o, lse
+
+    def attn_bwd(self, q_bits, k_bits, v_bits, do_bits, dtype, causal, window_left, scale):
+        """Gradients (dQ [B, L, Hq, d], dK, dV [B, L, Hkv, d], float64) of the square
+        problem for the upstream gradient dO [B, L, Hq, d] (same storage dtype)."""
+        q_bits, k_bits, v_bits, do_bits = (np.ascontiguousarray(a, dtype=np.uint16)
+                                           for a in (q_bits, k_bits, v_bits, do_bits))
+        B, L, Hq, d = q_bits.shape
+        Hkv = k_bits.shape[2]
+        if k_bits.shape != (B, L, Hkv, d) or v_bits.shape != k_bits.shape or \
+                do_bits.shape != q_bits.shape:
+            raise ValueError("shape mismatch")
+        dq = np.empty(q_bits.shape)
+        dk = np.empty(k_bits.shape)
+        dv = np.empty(k_bits.shape)
+        rc = self.lib.oracle_attn_bwd(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _ptr(do_bits),
+                                      _dtype_code(dtype), B, L, Hq, Hkv, d, int(bool(causal)),
+                                      int(window_left), float(scale), _ptr(dq), _ptr(dk),
+                                      _ptr(dv))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd rejected its arguments (rc={rc})")
+        return dq, dk, dv
 
     def merge(self, o_parts, lse_parts):
         """Combine partial results over disjoint key sets: o_parts [P, n, d] and

@@ -236,6 +236,115 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
                                scale, 0, L, rows, nrows, o_rows, lse_rows);
 }
 
+/* Gradients of the square problem (Lq = Lk = L) for an upstream gradient dO of O:
+ * the chain rule applied to the definition above. With P_ij = exp(s_ij - LSE_i) on
+ * J_i (0 elsewhere) and O_i = sum_j P_ij v_j:
+ *   D_i   = sum_c dO_ic O_ic
+ *   dV_j  = sum_{i : j in J_i} P_ij dO_i
+ *   dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_{i : j in J_i} dS_ij q_i
+ * with dK and dV summed over the query heads that share a K/V head. O and LSE are
+ * recomputed here in double from the definition. The spec page ("compare Hyena vs
+ * FlashAttention at 128k", stage 5) lists the backward pass as not measured; this
+ * is its plain definition. dq: [B, L, Hq, d]; dk, dv: [B, L, Hkv, d] (doubles).
+ * Returns 0, -1 on a bad argument, -2 when scratch cannot be allocated. */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                    int dtype, int64_t B, int64_t L, int64_t Hq, int64_t Hkv, int64_t d,
+                    int causal, int64_t window_left, double scale, double *dq, double *dk,
+                    double *dv)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv)
+        return -1;
+    if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0 || window_left < -1)
+        return -1;
+    if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16 && dtype != ORACLE_FP8_E4M3)
+        return -1;
+    int64_t G = Hq / Hkv;
+    int bad = 0;
+    memset(dq, 0, sizeof(double) * (size_t)(B * L * Hq * d));
+    memset(dk, 0, sizeof(double) * (size_t)(B * L * Hkv * d));
+    memset(dv, 0, sizeof(double) * (size_t)(B * L * Hkv * d));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bg = 0; bg < B * Hkv; ++bg) {
+        int64_t b = bg / Hkv, g = bg % Hkv;
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        double *qi = (double *)malloc(sizeof(double) * (size_t)d);
+        double *doi = (double *)malloc(sizeof(double) * (size_t)d);
+        double *oi = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!s || !qi || !doi || !oi) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                for (int64_t i = 0; i < L; ++i) {
+                    int64_t j_lo = 0, j_hi = L;
+                    if (causal)
+                        j_hi = i + 1;
+                    if (window_left >= 0 && i - window_left > j_lo)
+                        j_lo = i - window_left;
+                    if (j_hi <= j_lo)
+                        continue;
+                    const uint16_t *qrow = q + ((b * L + i) * Hq + h) * d;
+                    const uint16_t *drow = dout + ((b * L + i) * Hq + h) * d;
+                    for (int64_t c = 0; c < d; ++c) {
+                        qi[c] = widen16(qrow[c], dtype);
+                        doi[c] = widen16(drow[c], dtype);
+                        oi[c] = 0.0;
+                    }
+                    /* scores, their maximum, the normaliser and LSE */
+                    double m = -INFINITY;
+                    for (int64_t j = j_lo; j < j_hi; ++j) {
+                        const uint16_t *krow = k + ((b * L + j) * Hkv + g) * d;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c)
+                            dot += qi[c] * widen16(krow[c], dtype);
+                        s[j - j_lo] = dot * scale;
+                        if (s[j - j_lo] > m)
+                            m = s[j - j_lo];
+                    }
+                    double l = 0.0;
+                    for (int64_t j = j_lo; j < j_hi; ++j)
+                        l += exp(s[j - j_lo] - m);
+                    double lse = m + log(l);
+                    /* O_i and D_i */
+                    for (int64_t j = j_lo; j < j_hi; ++j) {
+                        const uint16_t *vrow = v + ((b * L + j) * Hkv + g) * d;
+                        double p = exp(s[j - j_lo] - lse);
+                        for (int64_t c = 0; c < d; ++c)
+                            oi[c] += p * widen16(vrow[c], dtype);
+                    }
+                    double D = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        D += doi[c] * oi[c];
+                    /* gradients */
+                    double *dqi = dq + ((b * L + i) * Hq + h) * d;
+                    for (int64_t j = j_lo; j < j_hi; ++j) {
+                        const uint16_t *krow = k + ((b * L + j) * Hkv + g) * d;
+                        const uint16_t *vrow = v + ((b * L + j) * Hkv + g) * d;
+                        double *dkj = dk + ((b * L + j) * Hkv + g) * d;
+                        double *dvj = dv + ((b * L + j) * Hkv + g) * d;
+                        double p = exp(s[j - j_lo] - lse);
+                        double dp = 0.0;
+                        for (int64_t c = 0; c < d; ++c)
+                            dp += doi[c] * widen16(vrow[c], dtype);
+                        double ds = p * (dp - D);
+                        for (int64_t c = 0; c < d; ++c) {
+                            dqi[c] += scale * ds * widen16(krow[c], dtype);
+                            dkj[c] += scale * ds * qi[c];
+                            dvj[c] += p * doi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(s);
+        free(qi);
+        free(doi);
+        free(oi);
+    }
+    return bad ? -2 : 0;
+}
+
 /* Combine nparts partial results of the same nrows rows, each over a disjoint
  * set of keys: o_parts is nparts x nrows x d, lse_parts nparts x nrows (natural
  * log; -inf for a part that saw no key). Writes o (nrows x d) and lse (nrows). */

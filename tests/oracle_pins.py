@@ -439,6 +439,86 @@ def pin_symmetric_window_mirror(orc):
         np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-13)
 
 
+# --- gradients (backward pass) -------------------------------------------------------------
+# The spec page ("compare Hyena vs FlashAttention at 128k", stage 5) lists the backward
+# pass as not measured; its definition is the gradient of the forward definition.
+
+def _torch_attention(q, k, v, causal, wl, scale):
+    """Materialised attention in torch float64 (an autograd-able statement of the
+    forward, separate from the oracle and from bruteforce.py)."""
+    B, L, Hq, d = q.shape
+    G = Hq // k.shape[2]
+    kk = k.repeat_interleave(G, dim=2)
+    vv = v.repeat_interleave(G, dim=2)
+    s = torch.einsum("bihc,bjhc->bhij", q, kk) * scale
+    i = torch.arange(L)[:, None]
+    j = torch.arange(L)[None, :]
+    vis = torch.ones(L, L, dtype=torch.bool)
+    if causal:
+        vis &= j <= i
+    if wl >= 0:
+        vis &= j >= i - wl
+    s = s.masked_fill(~vis, float("-inf"))
+    return torch.einsum("bhij,bjhc->bihc", torch.softmax(s, dim=-1), vv)
+
+
+def pin_backward_matches_autograd(orc):
+    """dQ, dK, dV equal float64 autograd of a materialised forward (1e-11)."""
+    for L, (hq, hkv), (causal, wl), dtype in [(1, (2, 2), (False, -1), "fp16"),
+                                              (17, (4, 2), (True, -1), "fp16"),
+                                              (40, (4, 1), (True, 5), "bf16"),
+                                              (33, (2, 2), (False, -1), "bf16")]:
+        q, k, v = random_qkv(2, L, hq, hkv, 8, dtype=dtype, seed=L)
+        do, _, _ = random_qkv(2, L, hq, hkv, 8, dtype=dtype, seed=L + 500)
+        dq, dk, dv = orc.attn_bwd(bits16(q), bits16(k), bits16(v), bits16(do), dtype, causal,
+                                  wl, 0.3)
+        qt, kt, vt = (t.double().requires_grad_() for t in (q, k, v))
+        o = _torch_attention(qt, kt, vt, causal, wl, 0.3)
+        (o * do.double()).sum().backward()
+        for got, ref in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+            np.testing.assert_allclose(got, ref.numpy(), rtol=1e-11, atol=1e-11,
+                                       err_msg=f"L={L} mask={causal, wl}")
+
+
+def pin_backward_finite_differences(orc):
+    """Central differences of the materialised forward agree with the oracle's
+    gradients on sampled input elements."""
+    q, k, v = random_qkv(1, 12, 2, 1, 4, seed=44)
+    do, _, _ = random_qkv(1, 12, 2, 1, 4, seed=45)
+    qd, kd, vd, dod = (orc.widen(bits16(t), "fp16") for t in (q, k, v, do))
+    dq, dk, dv = orc.attn_bwd(bits16(q), bits16(k), bits16(v), bits16(do), "fp16", True, 3, 0.5)
+
+    def loss(qq, kk, vv):
+        o, _ = attn_materialised(qq, kk, vv, True, 3, 0.5)
+        return float((o * dod).sum())
+
+    h = 1e-6
+    for name, arr, grad in (("q", qd, dq), ("k", kd, dk), ("v", vd, dv)):
+        for idx in [(0, 0, 0, 0), (0, 5, 0, 3), (0, 11, 0, 1)] + (
+                [(0, 7, 1, 2)] if name == "q" else []):
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += h
+            minus[idx] -= h
+            args_p = {"q": (plus, kd, vd), "k": (qd, plus, vd), "v": (qd, kd, plus)}[name]
+            args_m = {"q": (minus, kd, vd), "k": (qd, minus, vd), "v": (qd, kd, minus)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def pin_backward_sum_identities(orc):
+    """Each softmax row sums to 1, so per head group sum_j dK_j = 0 and
+    sum_j dV_j = sum_i dO_i (over the group's query heads)."""
+    for causal, wl in [(False, -1), (True, -1), (True, 7)]:
+        q, k, v = random_qkv(2, 50, 6, 2, 8, seed=61)
+        do, _, _ = random_qkv(2, 50, 6, 2, 8, seed=62)
+        dq, dk, dv = orc.attn_bwd(bits16(q), bits16(k), bits16(v), bits16(do), "fp16", causal,
+                                  wl, 0.25)
+        dod = orc.widen(bits16(do), "fp16")
+        np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+        grouped = dod.reshape(2, 50, 2, 3, 8).sum(axis=(1, 3))
+        np.testing.assert_allclose(dv.sum(axis=1), grouped, rtol=1e-12, atol=1e-12)
+
+
 ORACLE_PINS = [
     pin_widen_fp16_all_patterns, pin_widen_bf16_all_patterns, pin_widen_fp8_e4m3_all_patterns,
     pin_fp8_attention_matches_materialised, pin_matches_materialised,
@@ -448,5 +528,6 @@ ORACLE_PINS = [
     pin_window_row_is_causal_suffix, pin_hand_worked_example, pin_rows_api_matches_full,
     pin_kv_matches_materialised, pin_kv_rows_are_square_suffix, pin_merge_of_key_splits,
     pin_merge_hand_example, pin_paged_equals_dense, pin_right_window_matches_materialised,
-    pin_right_window_zero_is_causal, pin_symmetric_window_mirror,
+    pin_right_window_zero_is_causal, pin_symmetric_window_mirror, pin_backward_matches_autograd,
+    pin_backward_finite_differences, pin_backward_sum_identities,
 ]

@@ -45,6 +45,11 @@ MUTANTS = {
     "fp8_exponent_bias": ("m8 = ldexp((double)(f8 + 8), e8 - 10);",
                           "m8 = ldexp((double)(f8 + 8), e8 - 11);"),
     "fp8_subnormal_scale": ("m8 = ldexp((double)f8, -9);", "m8 = ldexp((double)f8, -10);"),
+    "bwd_drops_D": ("double ds = p * (dp - D);", "double ds = p * dp;"),
+    "bwd_dk_unscaled": ("dkj[c] += scale * ds * qi[c];", "dkj[c] += ds * qi[c];"),
+    "bwd_dv_uses_dp": ("dvj[c] += p * doi[c];", "dvj[c] += dp * doi[c];"),
+    "bwd_dq_uses_query": ("dqi[c] += scale * ds * widen16(krow[c], dtype);",
+                          "dqi[c] += scale * ds * qi[c];"),
     "right_window_ignored": ("if (window_right >= 0 && pos + window_right + 1 < j_hi)",
                              "if (0 && pos + window_right + 1 < j_hi)"),
 }
