@@ -26,7 +26,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
-           "attn_fwd_kv_paged", "attn_fwd_window", "attn_fwd_fp8",
+           "attn_fwd_kv_paged", "attn_fwd_window", "attn_fwd_fp8", "attn_bwd",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
            "PATH_SQUARE", "PATH_TILES", "debug_wait_probe", "debug_exp2",
@@ -67,6 +67,11 @@ def _bind(lib):
     lib.attn_fwd_kv.restype = i
     lib.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, i, i,
                                 p, sz, p]
+    lib.attn_bwd.restype = i
+    lib.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i,
+                             p, sz, p]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.attn_fwd_fp8.restype = i
     lib.attn_fwd_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, p, sz, p]
     lib.attn_fwd_fp8_workspace_size.restype = sz
@@ -204,6 +209,34 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
     _check(code)
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal=False, window_left=-1, scale=None, out_fp32=False,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attention for the upstream gradient ``dout`` of O.
+    ``o`` and ``lse`` are attn_fwd's outputs for (q, k, v) (o in q's dtype)."""
+    lib = load_library()
+    (B, L, Lk, Hq, Hkv, d), dt, out = _check_tensors(q, k, v, o, lse)
+    if Lk != L or out != OUT_SAME:
+        raise ValueError("k, v must have q's length and o q's dtype")
+    if not isinstance(dout, torch.Tensor) or tuple(dout.shape) != tuple(q.shape) or \
+            dout.dtype != q.dtype or not dout.is_cuda or not dout.is_contiguous():
+        raise ValueError("dout must be a contiguous CUDA tensor like q")
+    odt = torch.float32 if out_fp32 else q.dtype
+    dq = torch.empty(q.shape, dtype=odt, device=q.device)
+    dk = torch.empty(k.shape, dtype=odt, device=q.device)
+    dv = torch.empty(k.shape, dtype=odt, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = int(lib.attn_bwd_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)), int(window_left)))
+    if workspace is None:
+        workspace = _default_workspace(q.device, max(need, 256))
+    _check(lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, L, Hq,
+                        Hkv, d, int(bool(causal)), int(window_left), float(scale), dt,
+                        OUT_FP32 if out_fp32 else OUT_SAME, workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_fwd_fp8(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=False,

@@ -136,6 +136,31 @@ bool make_tensor_map_u8(CUtensorMap* map, const void* ptr, const cuuint64_t (&di
   return true;
 }
 
+// 2-D tensor map over float32 rows [rows, cols] (cols contiguous), boxes of
+// box_cols x 1, no swizzle.
+bool make_tensor_map_f32_rows(CUtensorMap* map, const void* ptr, int rows, int cols, int box_cols,
+                              std::string* why) {
+  cudaError_t err;
+  auto encode = encode_fn(&err);
+  if (encode == nullptr) {
+    *why = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorName(err);
+    return false;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled (float32 rows) failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The pointer must be device (or managed) memory of device `dev`.
@@ -653,6 +678,117 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   a.grid = plan.items;
   a.stream = static_cast<cudaStream_t>(stream);
   e = ex19::launch_fp8(out_dtype == ATTN_OUT_FP32, a);
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
+                               int window_left) {
+  if (check_shape(B, L, Hq, Hkv, d, causal, window_left) != ATTN_OK || Hq / Hkv > 128) return 0;
+  const size_t Lpad = ((size_t)L + 127) / 128 * 128;
+  return kWorkspaceBytes + 2 * (size_t)B * Hq * Lpad * 4;
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                       int L, int Hq, int Hkv, int d, int causal, int window_left, float scale,
+                       attn_dtype_t dtype, attn_out_t out_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  g_detail.clear();
+  attn_status_t st = check_shape(B, L, Hq, Hkv, d, causal, window_left);
+  if (st != ATTN_OK) return st;
+  if (Hq / Hkv > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "bad dtype");
+  if (out_dtype != ATTN_OUT_SAME && out_dtype != ATTN_OUT_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "bad out_dtype");
+  const void* in[6] = {q, k, v, o, dout, lse};
+  void* out[3] = {dq, dk, dv};
+  for (const void* x : in)
+    if (!x) return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, lse and dout must be non-null");
+  for (void* x : out)
+    if (!x) return fail(ATTN_ERR_INVALID_ARG, "dq, dk and dv must be non-null");
+  for (int i = 0; i < 5; ++i)
+    if (!aligned(in[i], 16))
+      return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o and dout must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  for (void* x : out)
+    if (!aligned(x, 16)) return fail(ATTN_ERR_INVALID_ARG, "dq, dk and dv must be 16-byte aligned");
+  if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
+  if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  const int Lpad = (L + 127) / 128 * 128;
+  if (workspace_bytes < kWorkspaceBytes + 2 * (size_t)B * Hq * Lpad * 4)
+    return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_bwd_workspace_size()");
+  if ((long long)B * Hq * Lpad >= (1LL << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "B * Hq * L rounded up to 128 must be < 2^31");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  std::string why;
+  const void* ptrs[10] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  const char* names[10] = {"q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "workspace"};
+  for (int i = 0; i < 10; ++i)
+    if (!is_device_ptr(ptrs[i], dev, &why, names[i])) return fail(ATTN_ERR_INVALID_ARG, why);
+
+  const bool bf16 = dtype == ATTN_BF16;
+  const KvPlan plan = kv_plan(B, L, L, Hq, Hkv, causal, window_left);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceBytes);
+  float* dsum = lse2 + (size_t)B * Hq * Lpad;
+  CUtensorMap tm_qp, tm_dop, tm_q, tm_do, tm_k, tm_v, tm_lse2, tm_dsum;
+  const bool maps_ok =
+      make_tensor_map(&tm_qp, q, bf16, B, L, Hq, d, &why, plan.group, plan.q_per_tile) &&
+      make_tensor_map(&tm_dop, dout, bf16, B, L, Hq, d, &why, plan.group, plan.q_per_tile) &&
+      make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why) &&
+      make_tensor_map(&tm_do, dout, bf16, B, L, Hq, d, &why) &&
+      make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) &&
+      make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why) &&
+      make_tensor_map_f32_rows(&tm_lse2, lse2, B * Hq, Lpad, 128, &why) &&
+      make_tensor_map_f32_rows(&tm_dsum, dsum, B * Hq, Lpad, 128, &why);
+  if (!maps_ok) return fail(ATTN_ERR_CUDA, why);
+
+  ex19::BwdLaunchArgs a = {};
+  a.tm_qp = &tm_qp;
+  a.tm_dop = &tm_dop;
+  a.tm_q = &tm_q;
+  a.tm_do = &tm_do;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  a.tm_lse2 = &tm_lse2;
+  a.tm_dsum = &tm_dsum;
+  ex19::bwd::BwdParams& p = a.p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.lse2 = lse2;
+  p.dsum = dsum;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = static_cast<uint32_t*>(workspace);
+  p.B = B;
+  p.L = L;
+  p.Lpad = Lpad;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = plan.group;
+  p.causal = causal;
+  p.window_left = window_left;
+  p.c2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.q_per_tile = plan.q_per_tile;
+  p.row_tiles = plan.row_tiles;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.grid_dq = plan.items;
+  a.grid_dkdv = B * Hkv * ((L + 127) / 128);
+  a.stream = static_cast<cudaStream_t>(stream);
+  e = ex19::launch_bwd(d, bf16, out_dtype == ATTN_OUT_FP32, a);
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
 }

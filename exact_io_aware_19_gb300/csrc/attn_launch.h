@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "attn_bwd_params.h"
 #include "attn_kv_params.h"
 #include "attn_params.h"
 
@@ -38,6 +39,20 @@ struct Fp8LaunchArgs {
   cudaStream_t stream;
 };
 
+struct BwdLaunchArgs {
+  const CUtensorMap* tm_qp;   // Q, packed 128-row tiles (dQ kernel)
+  const CUtensorMap* tm_dop;  // dO, packed likewise
+  const CUtensorMap* tm_q;    // Q, one head per 128-row tile (dK / dV kernel)
+  const CUtensorMap* tm_do;   // dO, likewise
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_lse2;  // [B * Hq, Lpad] float32, boxes of 128
+  const CUtensorMap* tm_dsum;
+  bwd::BwdParams p;
+  int grid_dq, grid_dkdv;
+  cudaStream_t stream;
+};
+
 // Each returns the CUDA error of configuring / enqueuing the kernel.
 cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
@@ -47,6 +62,8 @@ cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 cudaError_t launch_kv_paged(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // The float8 forward: the V transpose, then the attention kernel.
 cudaError_t launch_fp8(bool out_f32, const Fp8LaunchArgs& a);
+// The backward pass: the D / LSE2 pass, the dQ kernel and the dK / dV kernel.
+cudaError_t launch_bwd(int d, bool bf16, bool out_f32, const BwdLaunchArgs& a);
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream);

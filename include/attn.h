@@ -115,6 +115,29 @@ attn_status_t attn_fwd_fp8(const void *q, const void *k, const void *v, void *o,
                            size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass: the gradients dq, dk, dv of the square problem (attn_fwd's
+ * definition, causal and left-window masks, GQA) for an upstream gradient dout of O:
+ *   P = softmax rows of scale·q kᵀ on the visible keys, D_i = Σ_c dout_ic o_ic,
+ *   dV = Pᵀ dout, dS = P ∘ (dout vᵀ − D), dQ = scale · dS k, dK = scale · dSᵀ q,
+ * with dk and dv summed over the query heads that share a K/V head. The spec page
+ * ("compare Hyena vs FlashAttention at 128k", stage 5) lists the backward pass as
+ * not measured. Inputs: q, k, v, dtype and sizes as for attn_fwd; o [B, L, Hq, d]
+ * and lse [B, Hq, L] are attn_fwd's outputs for these inputs (o in the input dtype);
+ * dout [B, L, Hq, d] in the input dtype. Outputs dq [B, L, Hq, d], dk, dv [B, L,
+ * Hkv, d] in the input dtype (ATTN_OUT_SAME) or float32. workspace >=
+ * attn_bwd_workspace_size(...) bytes (the status word and per-row D and LSE). At
+ * most 128 query heads per K/V head. Enqueues three kernels on `stream`; nothing of
+ * size L x L is stored.
+ */
+size_t attn_bwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
+                               int window_left);
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                       int L, int Hq, int Hkv, int d, int causal, int window_left, float scale,
+                       attn_dtype_t dtype, attn_out_t out_dtype, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * attn_fwd with a window on both sides, the window_size = (left, right) option of
  * the "Flash Attention optimization" skill page (workflow 2 step 3; its symmetric
  * example is (256, 256)). Row i sees keys

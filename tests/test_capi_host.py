@@ -220,3 +220,21 @@ def test_fp8_workspace_and_validation(lib):
         assert f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["Hq"], a["Hkv"],
                  a["d"], a["causal"], a["wl"], a["scale"], a["out"], a["ws"], a["wsb"],
                  a["stream"]) == code, kw
+
+
+def test_bwd_workspace_and_validation(lib):
+    # status word + D and LSE2 rows of Lpad = L rounded up to 128 (float32 each)
+    assert lib.attn_bwd_workspace_size(1, 300, 8, 2, 64, 1, -1) == 256 + 2 * 8 * 384 * 4
+    assert lib.attn_bwd_workspace_size(1, 300, 256, 1, 64, 1, -1) == 0  # group > 128
+    f = lib.attn_bwd
+    ok = dict(q=A, k=A, v=A, o=A, lse=A, do=A, dq=A, dk=A, dv=A, B=1, L=256, Hq=4, Hkv=4, d=64,
+              causal=1, wl=-1, scale=0.125, dtype=0, out=0, ws=A, wsb=1 << 20, stream=None)
+    for kw, code in [(dict(d=96), 2), (dict(Hq=6), 1), (dict(out=3), 1), (dict(do=None), 1),
+                     (dict(dk=A + 8), 1), (dict(lse=A + 2), 1), (dict(ws=None), 3),
+                     (dict(wsb=300), 3), (dict(scale=float("inf")), 1), (dict(dtype=2), 1),
+                     (dict(causal=0, wl=3), 2)]:
+        a = dict(ok)
+        a.update(kw)
+        assert f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                 a["B"], a["L"], a["Hq"], a["Hkv"], a["d"], a["causal"], a["wl"], a["scale"],
+                 a["dtype"], a["out"], a["ws"], a["wsb"], a["stream"]) == code, kw
