@@ -399,6 +399,35 @@ def ours_arm(args, world, rank, local):
                "launches_per_call": 2}
         del q8, k8, v8, ws8
 
+    # ---- backward pass on the sweep's shape at L = 16384 (gradients of the forward)
+    backward = {}
+    if not args.no_decode:
+        wb = w.with_length(16384)
+        qb, kb, vb = (t.to(dev) for t in si.make_qkv(wb))
+        gb = torch.Generator().manual_seed(1010)
+        dob = torch.randn(qb.shape, generator=gb).to(qb.dtype).to(dev)
+        ob, lb = ex.attn_fwd(qb, kb, vb, causal=True, scale=wb.scale)
+        times = []
+        for r in range(8):
+            flush.fill_(float(r))
+            a = torch.cuda.Event(enable_timing=True)
+            bb = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex.attn_bwd(qb, kb, vb, ob, lb, dob, causal=True, scale=wb.scale)
+            bb.record(stream)
+            torch.cuda.synchronize(dev)
+            if r >= 2:
+                times.append(a.elapsed_time(bb))
+        ex.sync_status()
+        t = statistics.median(times)
+        fb = 2.5 * wb.algorithmic_flop()
+        backward = {"workload": wb.name, "ms": t, "tflops": fb / t / 1e9,
+                    "flop_convention": "2.5 x the forward's algorithmic flop (five products of "
+                                       "2 d flop per visible pair)",
+                    "frac_of_tensor_peak": fb / t / 1e9 / float(peaks["bf16_tflops"]),
+                    "launches_per_call": 3}
+        del qb, kb, vb, dob, ob, lb
+
     peak = float(peaks["bf16_tflops"])
     achieved = flop / ms / 1e9  # TFLOP/s of one launch
     traffic = TRAFFIC_BY_SOURCE.get(kernel_source_hash())
@@ -438,6 +467,7 @@ def ours_arm(args, world, rank, local):
             "sweep": sweep,
             "decode": decode,
             "fp8": fp8,
+            "backward": backward,
             "launch_ms": {"min": min(per), "max": max(per), "wall_total_s": t_wall},
         }
         if cpu is not None:
