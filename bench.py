@@ -56,8 +56,8 @@ TRAFFIC_BY_SOURCE = {
 }
 
 
-KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "sm103_ptx.cuh", "tmem_io.cuh", "attn_params.h",
-                  "exp2_poly.h", "attn_fwd_d64.cu", "attn_fwd_d128.cu")
+KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "row_ops.cuh", "sm103_ptx.cuh", "tmem_io.cuh",
+                  "attn_params.h", "exp2_poly.h", "attn_fwd_d64.cu", "attn_fwd_d128.cu")
 
 
 def kernel_source_hash() -> str:
