@@ -12,16 +12,22 @@
 // kernels; its weights are stored for the P·V MMA as e4m3 too, scaled to
 // P' = 2^(x − m + 7) ≤ 256 so that they sit in e4m3's normal range, and the
 // normaliser l' sums the same rounded P' values (the factor 2^7 cancels in O' / l').
-// O' = Σ P'·V accumulates in fp32 in TMEM.
+// O' = Σ P'·V accumulates in fp32 in TMEM, and so does l': the B operand of the
+// P·V MMA carries 16 rows of ones after the 64 rows of Vᵀ (N = 80), so O column 64
+// is Σ P' summed by the tensor core from the very bytes it multiplies V with, and
+// the O rescale scales it together with O.
 //
-// GB300 mapping (one CTA per 128-row tile, as the one-tile kernel):
+// GB300 mapping (one CTA per 128-row tile, two CTAs per SM so that one CTA's
+// softmax fills the other's waits; 256 TMEM columns and ~101 KiB of shared memory
+// each):
 //   * Q and K tiles: TMA boxes of 64 bytes (64 e4m3) per row, 64-byte swizzle.
 //   * V is read as Vᵀ (keys contiguous), written by attn_fp8_transpose_v into the
 //     workspace, so that both MMA operands are K-major: a 64 × 128-byte tile per
-//     block, 128-byte swizzle.
-//   * warp 4 (producer) streams K_j and Vᵀ_j into a ring of 8 KiB slots; warp 5
-//     (MMA) issues S(j) into TMEM buffer j mod 2 and O += P(j) Vᵀ(j) with P read
-//     from shared memory buffer j mod 2; S(j + 2) is issued after P·V(j).
+//     block, 128-byte swizzle, followed in its slot by the constant rows of ones.
+//   * warp 4 (producer) streams K_j and Vᵀ_j into a ring of 10 KiB slots; warp 5
+//     (MMA) issues S(j) into the TMEM S buffer, S(j + 1) as soon as the softmax
+//     has read S(j) into registers (s_free), then O += P(j) Vᵀ(j) with P read
+//     from shared memory buffer j mod 2.
 //   * warps 0-3 (softmax): one thread per row; P' is converted to e4m3 and stored
 //     in the 128-byte-swizzle layout (16-byte chunk c of row r at chunk c ^ (r % 8)),
 //     then made visible to the tensor core (fence.proxy.async) before p_full.
@@ -48,28 +54,33 @@ constexpr int kD = 64;               // head dimension
 constexpr int kThreads = 192;        // 4 softmax warps + producer warp + MMA warp
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 320)
-constexpr uint32_t kColO = 256;
+constexpr int kON = 80;              // P·V columns: O (64) and the normaliser (16 copies)
+constexpr uint32_t kTmemCols = 256;  // S [0,128), O and l' [128, 208)
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;
 constexpr int kPOffset = 7;          // P' = 2^(x - m + 7): at most 2^8 with the rescale threshold 1
 
 enum : uint32_t {
   kSiteProdEmpty = 0xA0001,
   kSiteMmaQFull = 0xB0001, kSiteMmaKFull = 0xB0002, kSiteMmaVFull = 0xB0003,
   kSiteMmaPFull = 0xB0004, kSiteMmaDrain = 0xB0005,
+  kSiteMmaSFree = 0xB0006,
   kSiteSmxSFull = 0xC0001, kSiteSmxOFull = 0xC0002, kSiteSmxPvDone = 0xC0003,
   kSiteDrainLoads = 0xD0001,
 };
 
 struct Fp8Geometry {
   static constexpr int kQBytes = kBM * kD;        // 8 KiB: 128 rows x 64 bytes
-  static constexpr int kSlotBytes = 8192;         // K_j (128 x 64 B) or Vᵀ_j (64 x 128 B)
-  static constexpr int kSlots = 8;
+  static constexpr int kTileBytes = 8192;         // K_j (128 x 64 B) or Vᵀ_j (64 x 128 B)
+  static constexpr int kOnesBytes = (kON - kD) * 128;  // rows of ones after Vᵀ_j
+  static constexpr int kSlotBytes = kTileBytes + kOnesBytes;  // 10 KiB, 1 KiB aligned
+  static constexpr int kSlots = 6;                // even: K_j in even slots, Vᵀ_j in odd
   static constexpr int kPBytes = kBM * kBN;       // 16 KiB: 128 rows x 128 bytes
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 8192;
   static constexpr int kOffP = kOffKV + kSlots * kSlotBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full, drain
+  // barriers: full[S], empty[S], q_full, s_full, s_free, p_full[2], pv_done[2], o_full, drain
   static constexpr int kNumBars = 2 * kSlots + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
@@ -84,14 +95,8 @@ __device__ __forceinline__ uint32_t e4m3x2_of_half2(uint32_t h2) {
   return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
 }
 
-// The packed fp16 pair of two e4m3 values (inverse widening, exact).
-__device__ __forceinline__ uint32_t half2_of_e4m3x2(uint32_t e2) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(e2), __NV_E4M3);
-  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
-}
-
 template <bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     attn_fp8_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_vt, const KvParams p) {
@@ -110,7 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_full = [&](uint32_t s) { return bars + 8u * s; };
   auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
   const uint32_t bar_q_full = bars + 8u * (2 * S);
-  auto bar_s_full = [&](uint32_t b) { return bars + 8u * (2 * S + 1 + b); };
+  const uint32_t bar_s_full = bars + 8u * (2 * S + 1);
+  const uint32_t bar_s_free = bars + 8u * (2 * S + 2);
   auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 3 + b); };
   auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
   const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
@@ -141,8 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_q_full, 1);
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_s_free, kBM);
     for (int k = 0; k < 2; ++k) {
-      mbar_init(bar_s_full(k), 1);
       mbar_init(bar_p_full(k), kBM);
       mbar_init(bar_pv_done(k), 1);
     }
@@ -160,6 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // the rows of ones (e4m3 1.0 = 0x38) behind every slot's tile; the TMA loads never
+  // write them
+  for (int t = threadIdx.x; t < S * (G::kOnesBytes / 16); t += kThreads) {
+    const int slot = t / (G::kOnesBytes / 16), c = t % (G::kOnesBytes / 16);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
+                     sKV + slot * G::kSlotBytes + G::kTileBytes + c * 16),
+                 "r"(0x38383838u)
+                 : "memory");
+  }
+  fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -183,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t slot = n % S;
           ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar_full(slot), G::kSlotBytes);
+          mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
           if (kv == 0)  // K_j: 128 keys x 64 bytes
             tma_load_4d(sKV + slot * G::kSlotBytes, &tm_k, bar_full(slot), 0, g, j * kBN, b);
           else  // Vᵀ_j: 64 rows (d) x 128 bytes (keys)
@@ -203,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- MMA issuer
     if (nblocks > 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32acc(false, kBM, kBN, false);  // e4m3 x e4m3
-      constexpr uint32_t idesc_o = idesc_f16_f32acc(false, kBM, kD, false);
+      constexpr uint32_t idesc_o = idesc_f16_f32acc(false, kBM, kON, false);
       const uint64_t dq = sdesc_swizzled(sQ, 16, 512, 4);      // 64-byte rows, 64-byte swizzle
       const uint64_t dk = sdesc_swizzled(sKV, 16, 512, 4);
       const uint64_t dvt = sdesc_swizzled(sKV, 16, 1024, 2);   // 128-byte rows, 128-byte swizzle
@@ -211,22 +228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t mO = tmem_base + kColO;
       auto slot_of = [&](uint32_t idx) { return idx % S; };
       auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
-      // S = Q · K_jᵀ into TMEM buffer jj & 1 (two MMAs of K = 32 bytes); releases K_j.
+      // S = Q · K_jᵀ into the TMEM S buffer (two MMAs of K = 32 bytes); releases K_j.
       auto issue_s = [&](int jj) __attribute__((always_inline)) -> bool {
         const uint32_t kidx = 2u * jj;
         if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull)) return false;
         tc_fence_after();
-        const uint32_t mS = tmem_base + 128u * (jj & 1);
+        const uint32_t mS = tmem_base + kColS;
         const uint64_t dks = dk + ((slot_of(kidx) * G::kSlotBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 32; ++kk)
           mma_ss_f8_elect(mS, dq + (kk * 32 >> 4), dks + (kk * 32 >> 4), idesc_s, kk > 0 ? 1u : 0u);
-        mma_commit_elect(bar_s_full(jj & 1));
+        mma_commit_elect(bar_s_full);
         mma_commit_elect(bar_empty(slot_of(kidx)));
         return true;
       };
-      // O (+)= P(jj) · V_j with P from shared-memory buffer jj & 1 and Vᵀ_j from its
-      // slot (four MMAs of K = 32 keys); releases Vᵀ_j.
+      // [O | l'] (+)= P(jj) · [V_j | 1] with P from shared-memory buffer jj & 1 and
+      // Vᵀ_j and the ones from its slot (four MMAs of K = 32 keys); releases Vᵀ_j.
       auto issue_pv = [&](int jj) __attribute__((always_inline)) -> bool {
         const uint32_t vidx = 2u * jj + 1u;
         if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
@@ -246,10 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         ok = issue_s(0);
-        if (ok && nblocks > 1) ok = issue_s(1);
         for (int jj = 0; ok && jj < nblocks; ++jj) {
-          ok = issue_pv(jj);
-          if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
+          if (jj + 1 < nblocks) {  // S(jj + 1) once the softmax holds S(jj) in registers
+            ok = mbar_wait_warp(bar_s_free, jj & 1u, wc, kSiteMmaSFree);
+            if (ok) {
+              tc_fence_after();
+              ok = issue_s(jj + 1);
+            }
+          }
+          if (ok) ok = issue_pv(jj);
         }
         if (ok) mma_commit_elect(bar_o_full);
       }
@@ -269,15 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool neg = p.negate_scores != 0;
     const float Cs = neg ? -C : C;
     float m_ref = -INFINITY;  // reference max (base-2 units)
-    float l = 0.f;            // running sum of the stored P' values
     bool ok = true;
     for (int jj = 0; jj < nblocks; ++jj) {
       const int j = blk_lo + jj;
       const uint32_t buf = jj & 1;
-      ok = mbar_wait_warp(bar_s_full(buf), (jj >> 1) & 1u, wc, kSiteSmxSFull);
+      ok = mbar_wait_warp(bar_s_full, jj & 1u, wc, kSiteSmxSFull);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem_base + lane_off + 128u * buf;
+      const uint32_t tS = tmem_base + lane_off + kColS;
       const int key0 = j * kBN;
       const bool masked = (key0 + kBN > L) || (wr >= 0 && key0 + kBN - 1 > pos_min + wr) ||
                           (p.window_left >= 0 && key0 < pos_max - p.window_left);
@@ -295,6 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr bool M = decltype(masked_tag)::value;
         uint32_t sr[128];
         tmem_ld_x128(tS, sr);
+        tc_fence_before();
+        mbar_arrive(bar_s_free);  // the S buffer may take S(jj + 1)
         if constexpr (M) {
           const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
 #pragma unroll
@@ -326,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
         const uint32_t prow = sP + buf * G::kPBytes + rho * 128;
-        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int q16 = 0; q16 < 8; ++q16) {  // 16 keys = one 16-byte chunk of the row
           uint32_t w[4];
@@ -349,10 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               e2[v2] = e4m3x2_of_half2(pp);
             }
             w[u] = e2[0] | (e2[1] << 16);
-            // normaliser: the stored (rounded) values, widened exactly and summed in fp32
-            const uint32_t h0 = half2_of_e4m3x2(e2[0]), h1 = half2_of_e4m3x2(e2[1]);
-            acc[0] = __fadd2_rn(acc[0], __half22float2(*reinterpret_cast<const __half2*>(&h0)));
-            acc[1] = __fadd2_rn(acc[1], __half22float2(*reinterpret_cast<const __half2*>(&h1)));
           }
           const uint32_t addr = prow + ((q16 ^ (rho & 7)) << 4);  // 128-byte swizzle
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
@@ -360,7 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : "memory");
         }
         fence_proxy_async_shared();  // P is read by the tensor core (async proxy)
-        l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
       };
       if (masked)
         block_body(std::true_type{});
@@ -386,6 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * a);
           tmem_st_x32(tO + c0, orow);
         }
+        {  // l' (column 64; its 15 copies are never read)
+          uint32_t lrow[16];
+          tmem_ld_x16(tO + kD, lrow);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) lrow[c] = __float_as_uint(__uint_as_float(lrow[c]) * a);
+          tmem_st_x16(tO + kD, lrow);
+        }
         tmem_st_wait();
       }
       tc_fence_before();
@@ -396,6 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok && nblocks > 0) {
+      float l;
+      {
+        uint32_t lrow[16];
+        tmem_ld_x16(tO + kD, lrow);
+        l = __uint_as_float(lrow[0]);
+      }
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const size_t orow_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * kD;
 #pragma unroll

@@ -91,8 +91,8 @@ def test_fp8_exact_properties():
     vc = c.view(1, 1, 1, 64).expand(1, 700, 4, 64).contiguous()
     o, _ = ex.attn_fwd_fp8(q.cuda(), k.cuda(), vc.cuda(), out_fp32=True)
     want = c.float().view(1, 1, 1, 64).expand_as(o.cpu())
-    # O' and l' sum the same weights in fp32 (tensor core and softmax thread, in
-    # different orders): equal to within fp32 accumulation
+    # O' and l' are columns of one P·V product (l' multiplies the weights by a column
+    # of ones), both accumulated in fp32: equal to within fp32 accumulation
     assert torch.allclose(o.cpu(), want, rtol=2e-5, atol=1e-6), (o.cpu() - want).abs().max()
     o, lse = ex.attn_fwd_fp8(q.cuda(), k.cuda(), v.cuda(), causal=True, out_fp32=True)
     assert torch.equal(o[0, 0].cpu(), v[0, 0].float())  # row 0 sees key 0 only
