@@ -221,24 +221,29 @@ template <int N, bool BF16, bool kW, bool kMasked, typename Vec4Fn>
 __device__ __forceinline__ void elementwise_cols(const uint32_t (&xs)[N], const uint32_t (&dxs)[N],
                                                  int x0, float c2, int vis_lo, int vis_hi, Vec4Fn vec4,
                                                  uint32_t* wpk, uint32_t* dspk) {
+  // paired fp32 arithmetic (one FFMA2 / FADD2 / FMUL2 per two columns; each lane
+  // rounds as the scalar operation would)
+  const float2 c22 = make_float2(c2, c2);
 #pragma unroll
   for (int c = 0; c < N; c += 4) {
     float l[4], d[4];
     vec4(x0 + c, l, d);
-    float w[4], s[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int cc = x0 + c + u;
-      w[u] = ex2_approx(__uint_as_float(xs[c + u]) * c2 - l[u]);
-      if constexpr (kMasked) w[u] = (cc >= vis_lo && cc < vis_hi) ? w[u] : 0.f;
-      s[u] = w[u] * (__uint_as_float(dxs[c + u]) - d[u]);
+    for (int u = 0; u < 4; u += 2) {
+      const float2 a = __ffma2_rn(make_float2(__uint_as_float(xs[c + u]), __uint_as_float(xs[c + u + 1])),
+                                  c22, make_float2(-l[u], -l[u + 1]));
+      float w0 = ex2_approx(a.x), w1 = ex2_approx(a.y);
+      if constexpr (kMasked) {
+        const int cc = x0 + c + u;
+        w0 = (cc >= vis_lo && cc < vis_hi) ? w0 : 0.f;
+        w1 = (cc + 1 >= vis_lo && cc + 1 < vis_hi) ? w1 : 0.f;
+      }
+      const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dxs[c + u]), __uint_as_float(dxs[c + u + 1])),
+                                   make_float2(-d[u], -d[u + 1]));
+      const float2 sv = __fmul2_rn(make_float2(w0, w1), dd);
+      if constexpr (kW) wpk[(c + u) >> 1] = pack_in(w0, w1, BF16);
+      dspk[(c + u) >> 1] = pack_in(sv.x, sv.y, BF16);
     }
-    if constexpr (kW) {
-      wpk[c >> 1] = pack_in(w[0], w[1], BF16);
-      wpk[(c >> 1) + 1] = pack_in(w[2], w[3], BF16);
-    }
-    dspk[c >> 1] = pack_in(s[0], s[1], BF16);
-    dspk[(c >> 1) + 1] = pack_in(s[2], s[3], BF16);
   }
 }
 
