@@ -24,10 +24,13 @@
 // Overlap: a group releases its half of the S / dP columns as soon as it has loaded
 // them into registers, and the MMA warp issues the next block's S and dP half into
 // them at once, so the tensor core computes block j + 1 while the elementwise warps
-// work on block j. The 16-bit results go to separate TMEM buffers (dQ kernel: two,
-// dK/dV kernel at d = 64: one); at d = 128 the dK/dV kernel has no TMEM left for
-// them (Sᵀ, dPᵀ, dV, dK fill 512 columns), writes Pᵀ and dSᵀ over the columns it
-// has read, and issues the next block after the accumulating MMAs.
+// work on block j. The accumulating MMAs are split the same way (K = the group's 64
+// keys or queries), so the issue order per block is: half 0 of block j + 1, group 0's
+// share of block j, half 1 of block j + 1, group 1's share of block j; each waits
+// only for its own group. The 16-bit results go to separate TMEM buffers (dQ kernel:
+// two per group, dK/dV kernel at d = 64: one); at d = 128 the dK/dV kernel has no
+// TMEM left for them (Sᵀ, dPᵀ, dV, dK fill 512 columns), writes Pᵀ and dSᵀ over the
+// columns it has read, and issues a half of the next step after that group's share.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -103,8 +106,9 @@ struct BwdGeometry {
   static constexpr int kOffVec = kOffRing + kSlots * kTileBytes;  // dK/dV kernel: LSE2, D rows
   static constexpr int kVecBytes = 2 * kBN * 4;                   // per stage
   static constexpr int kOffBar = kOffVec + (kSlots / 2) * kVecBytes;
-  // barriers: full[S], empty[S], res_full, s_full[2], ld_free[2], p_full[2], acc_done[2], drain
-  static constexpr int kNumBars = 2 * kSlots + 10;
+  // barriers: full[S], empty[S], res_full, s_full[2], ld_free[2], p_full[2][2],
+  // acc_done[2][2], drain
+  static constexpr int kNumBars = 2 * kSlots + 14;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -148,8 +152,9 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
 // Common preamble of both kernels: barriers, TMEM, wait control.
 //   s_full[h]   MMA -> group h: the block's S and dP columns of half h are written
 //   ld_free[h]  group h -> MMA: half h of S and dP is in registers (128 arrivals)
-//   p_full[b]   groups -> MMA: 16-bit results in buffer b are written (256 arrivals)
-//   acc_done[b] MMA -> groups: the accumulating MMAs that read buffer b are complete
+//   p_full[h][b]   group h -> MMA: its 16-bit results in buffer b are written (128 arrivals)
+//   acc_done[h][b] MMA -> group h: the accumulating MMAs that read them are complete
+//   drain          MMA -> all: every MMA of the CTA is complete (epilogues wait here)
 #define EX19_BWD_PREAMBLE()                                                                    \
   using G = BwdGeometry<D>;                                                                    \
   constexpr int S = G::kSlots;                                                                 \
@@ -166,9 +171,9 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
   const uint32_t bar_res = bars + 8u * (2 * S);                                                \
   auto bar_s_full = [&](uint32_t h) { return bars + 8u * (2 * S + 1 + h); };                   \
   auto bar_ld_free = [&](uint32_t h) { return bars + 8u * (2 * S + 3 + h); };                  \
-  auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };                   \
-  auto bar_acc_done = [&](uint32_t b) { return bars + 8u * (2 * S + 7 + b); };                 \
-  const uint32_t bar_drain = bars + 8u * (2 * S + 9);                                          \
+  auto bar_p_full = [&](uint32_t h, uint32_t b) { return bars + 8u * (2 * S + 5 + 2 * h + b); }; \
+  auto bar_acc_done = [&](uint32_t h, uint32_t b) { return bars + 8u * (2 * S + 9 + 2 * h + b); }; \
+  const uint32_t bar_drain = bars + 8u * (2 * S + 13);                                         \
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);                       \
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4); \
   const int warp = threadIdx.x >> 5;                                                           \
@@ -182,8 +187,10 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
     for (int k = 0; k < 2; ++k) {                                                              \
       mbar_init(bar_s_full(k), 1);                                                             \
       mbar_init(bar_ld_free(k), 4 * 32);                                                       \
-      mbar_init(bar_p_full(k), kEwWarps * 32);                                                 \
-      mbar_init(bar_acc_done(k), 1);                                                           \
+      for (int b2 = 0; b2 < 2; ++b2) {                                                         \
+        mbar_init(bar_p_full(k, b2), 4 * 32);                                                  \
+        mbar_init(bar_acc_done(k, b2), 1);                                                     \
+      }                                                                                        \
     }                                                                                          \
     mbar_init(bar_drain, 1);                                                                   \
     *abort_flag = 0u;                                                                          \
@@ -365,25 +372,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = issue_half(0, 0) && issue_half(0, 1);
       }
       for (int jj = 0; ok && jj < nblocks; ++jj) {
-        if (jj + 1 < nblocks) {  // block jj + 1 into each half as soon as its group has read it
-          for (int hh = 0; ok && hh < 2; ++hh) {
-            ok = mbar_wait_warp(bar_ld_free(hh), jj & 1u, wc, kSiteMma) && issue_half(jj + 1, hh);
-          }
-          if (!ok) break;
-        }
         const uint32_t buf = jj & 1;
-        ok = mbar_wait_warp(bar_p_full(buf), (jj >> 1) & 1u, wc, kSiteMma);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ += dS · K_j: dS as 16-bit pairs in dS buffer `buf` (keys 0..127 in columns 0..63)
         const uint32_t kidx = 2u * jj;
         const uint64_t kslot = ((kidx % S) * G::kTileBytes) >> 4;
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          // half hh of block jj + 1 as soon as group hh has read its half of block jj
+          if (jj + 1 < nblocks) {
+            ok = mbar_wait_warp(bar_ld_free(hh), jj & 1u, wc, kSiteMma) && issue_half(jj + 1, hh);
+            if (!ok) break;
+          }
+          // dQ += dS[:, keys of half hh] · K_j[keys of half hh]: group hh's dS pairs sit in
+          // columns 32 hh .. 32 hh + 31 of dS buffer `buf`
+          ok = mbar_wait_warp(bar_p_full(hh, buf), (jj >> 1) & 1u, wc, kSiteMma);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_elect(tmem_base + kColDQ, tmem_base + col_ds(buf) + kk * 8,
-                       dkmn + kslot + ((kk * 2048) >> 4), idesc_q, (jj > 0 || kk > 0) ? 1u : 0u);
+          for (int k4 = 0; k4 < kHalfN / 16; ++k4) {
+            const int kk = 4 * hh + k4;
+            mma_ts_elect(tmem_base + kColDQ, tmem_base + col_ds(buf) + kk * 8,
+                         dkmn + kslot + ((kk * 2048) >> 4), idesc_q, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_elect(bar_acc_done(hh, buf));
+        }
+        if (!ok) break;
         mma_commit_elect(bar_empty(kidx % S));
-        mma_commit_elect(bar_acc_done(buf));
       }
     }
     mma_commit_elect(bar_drain);
@@ -435,21 +447,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           elementwise_cols<64, BF16, false, false>(xs, dxs, x0, p.c2, vis_lo, vis_hi, vec4, nullptr, dspk);
       }
-      // dS buffer `buf` was read by the dQ MMA of block jj - 2
+      // this group's part of dS buffer `buf` was read by its dQ MMAs of block jj - 2
       if (jj >= 2) {
-        ok = mbar_wait_warp(bar_acc_done(buf), ((jj - 2) >> 1) & 1u, wc, kSiteEw);
+        ok = mbar_wait_warp(bar_acc_done(hh, buf), ((jj - 2) >> 1) & 1u, wc, kSiteEw);
         if (!ok) break;
         tc_fence_after();
       }
       tmem_st_x32(tmem_base + lane_off + col_ds(buf) + 32 * hh, dspk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p_full(buf));
+      mbar_arrive(bar_p_full(hh, buf));
     }
-    // epilogue: dQ · scale, group h writes columns [h D/2, (h + 1) D/2)
+    // epilogue: dQ · scale once every MMA is complete (both groups' shares);
+    // group h writes columns [h D/2, (h + 1) D/2)
     if (ok && nblocks > 0) {
-      const uint32_t last = nblocks - 1;
-      ok = mbar_wait_warp(bar_acc_done(last & 1), (last >> 1) & 1u, wc, kSiteEw);
+      ok = mbar_wait_warp(bar_drain, 0, wc, kSiteEw);
       if (ok) tc_fence_after();
     }
     if (ok && nblocks > 0) {
@@ -566,31 +578,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = issue_half(0, 0) && issue_half(0, 1);
       }
       for (int st = 0; ok && st < nsteps; ++st) {
-        if (kSeparate && st + 1 < nsteps) {
-          for (int hh = 0; ok && hh < 2; ++hh)
-            ok = mbar_wait_warp(bar_ld_free(hh), st & 1u, wc, kSiteMma) && issue_half(st + 1, hh);
-          if (!ok) break;
-        }
-        ok = mbar_wait_warp(bar_p_full(0), st & 1u, wc, kSiteMma);
-        if (!ok) break;
-        tc_fence_after();
         const uint32_t qidx = 2u * st, didx = qidx + 1u;
         const uint64_t qs = ((qidx % S) * G::kTileBytes) >> 4;
         const uint64_t ds = ((didx % S) * G::kTileBytes) >> 4;
-        // dV += Pᵀ · dO_i and dK += dSᵀ · Q_i
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          // separate buffers: half hh of step st + 1 as soon as group hh has read step st
+          if (kSeparate && st + 1 < nsteps) {
+            ok = mbar_wait_warp(bar_ld_free(hh), st & 1u, wc, kSiteMma) && issue_half(st + 1, hh);
+            if (!ok) break;
+          }
+          ok = mbar_wait_warp(bar_p_full(hh, 0), st & 1u, wc, kSiteMma);
+          if (!ok) break;
+          tc_fence_after();
+          // dV += Pᵀ · dO_i and dK += dSᵀ · Q_i over the queries of half hh (group hh's pairs)
 #pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk) {
-          const uint32_t acc = (st > 0 || kk > 0) ? 1u : 0u;
-          mma_ts_elect(tmem_base + kColDV, tmem_base + op_col(kColPT, kk),
-                       drmn + ds + ((kk * 2048) >> 4), idesc_a, acc);
-          mma_ts_elect(tmem_base + kColDK, tmem_base + op_col(kColDST, kk),
-                       drmn + qs + ((kk * 2048) >> 4), idesc_a, acc);
+          for (int k4 = 0; k4 < kHalfN / 16; ++k4) {
+            const int kk = 4 * hh + k4;
+            const uint32_t acc = (st > 0 || kk > 0) ? 1u : 0u;
+            mma_ts_elect(tmem_base + kColDV, tmem_base + op_col(kColPT, kk),
+                         drmn + ds + ((kk * 2048) >> 4), idesc_a, acc);
+            mma_ts_elect(tmem_base + kColDK, tmem_base + op_col(kColDST, kk),
+                         drmn + qs + ((kk * 2048) >> 4), idesc_a, acc);
+          }
+          mma_commit_elect(bar_acc_done(hh, 0));
+          // in place: half hh of the next step follows these MMAs (issue order), which
+          // read the columns it overwrites
+          if (!kSeparate && st + 1 < nsteps) {
+            ok = issue_half(st + 1, hh);
+            if (!ok) break;
+          }
         }
+        if (!ok) break;
         mma_commit_elect(bar_empty(qidx % S));
         mma_commit_elect(bar_empty(didx % S));
-        mma_commit_elect(bar_acc_done(0));
-        // in place: the next step's Sᵀ / dPᵀ follow these MMAs (issue order)
-        if (!kSeparate && st + 1 < nsteps) ok = issue_half(st + 1, 0) && issue_half(st + 1, 1);
       }
     }
     mma_commit_elect(bar_drain);
@@ -654,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the single Pᵀ / dSᵀ buffer was read by step st - 1 (in place that is implied by
       // s_full; the wait keeps this thread at most one acc_done phase behind)
       if (st >= 1) {
-        ok = mbar_wait_warp(bar_acc_done(0), (st - 1) & 1u, wc, kSiteEw);
+        ok = mbar_wait_warp(bar_acc_done(hh, 0), (st - 1) & 1u, wc, kSiteEw);
         if (!ok) break;
         tc_fence_after();
       }
@@ -662,10 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_x32(tmem_base + lane_off + kColDST + (kSeparate ? 32 * hh : kHalfN * hh), dspk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p_full(0));
+      mbar_arrive(bar_p_full(hh, 0));
     }
-    if (ok && nsteps > 0) {
-      ok = mbar_wait_warp(bar_acc_done(0), (nsteps - 1) & 1u, wc, kSiteEw);
+    if (ok && nsteps > 0) {  // every MMA (both groups' shares) is complete
+      ok = mbar_wait_warp(bar_drain, 0, wc, kSiteEw);
       if (ok) tc_fence_after();
     }
     const bool row_ok = key < p.L;
