@@ -12,7 +12,9 @@
 //
 // GB300 mapping: three kernels, each with 8 elementwise warps in two groups of 4
 // (group h owns columns [64h, 64h + 64) of every 128 x 128 block, the warp's lane
-// quarter owns 32 rows), one TMA producer warp and one MMA warp; every wait bounded:
+// quarter owns 32 rows), one TMA producer warp and two MMA warps, one issuing the
+// S / dP products and one the accumulating products, so that neither stream of
+// MMAs waits behind the other's barrier; every wait bounded:
 //   * attn_bwd_prep: D and LSE2 per row into the workspace.
 //   * attn_bwd_dq_kernel (query-stationary, one CTA per 128-row tile packed as in
 //     the one-tile forward): per key block, S = Q Kᵀ and dP = dO Vᵀ (SS MMAs into
@@ -50,9 +52,10 @@ namespace bwd {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kEwWarps = 8;
-constexpr int kThreads = 32 * (kEwWarps + 2);  // elementwise warps + producer warp + MMA warp
+constexpr int kThreads = 32 * (kEwWarps + 3);  // elementwise warps + producer + two MMA warps
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;   // S / dP MMAs (and the TMEM allocation)
+constexpr int kAccWarp = 10;  // accumulating MMAs (dQ, or dV and dK)
 constexpr int kHalfN = 64;      // columns per elementwise group (and per S / dP MMA half)
 constexpr uint32_t kTmemCols = 512;
 
@@ -154,8 +157,11 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
 //   ld_free[h]  group h -> MMA: half h of S and dP is in registers (128 arrivals)
 //   p_full[h][b]   group h -> MMA: its 16-bit results in buffer b are written (128 arrivals)
 //   acc_done[h][b] MMA -> group h: the accumulating MMAs that read them are complete
-//   drain          MMA -> all: every MMA of the CTA is complete (epilogues wait here)
-#define EX19_BWD_PREAMBLE()                                                                    \
+//   drain          MMA -> all: every MMA of the CTA is complete (both MMA warps commit;
+//                  the epilogues wait here)
+// A slot read by both MMA warps is released by two commits: EMPTY_EVEN / EMPTY_ODD
+// arrivals for the even (K or Q) and odd (V or dO) slots.
+#define EX19_BWD_PREAMBLE(EMPTY_EVEN, EMPTY_ODD)                                               \
   using G = BwdGeometry<D>;                                                                    \
   constexpr int S = G::kSlots;                                                                 \
   extern __shared__ uint8_t smem_raw[];                                                        \
@@ -181,7 +187,7 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
   if (threadIdx.x == 0) {                                                                      \
     for (int s = 0; s < S; ++s) {                                                              \
       mbar_init(bar_full(s), 1);                                                               \
-      mbar_init(bar_empty(s), 1);                                                              \
+      mbar_init(bar_empty(s), (s & 1) ? (EMPTY_ODD) : (EMPTY_EVEN));                           \
     }                                                                                          \
     mbar_init(bar_res, 1);                                                                     \
     for (int k = 0; k < 2; ++k) {                                                              \
@@ -192,7 +198,7 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
         mbar_init(bar_acc_done(k, b2), 1);                                                     \
       }                                                                                        \
     }                                                                                          \
-    mbar_init(bar_drain, 1);                                                                   \
+    mbar_init(bar_drain, 2);                                                                   \
     *abort_flag = 0u;                                                                          \
     fence_mbar_init();                                                                         \
   }                                                                                            \
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const BwdParams p) {
-  EX19_BWD_PREAMBLE()
+  EX19_BWD_PREAMBLE(2, 1)  // K_j: S (MMA warp) and dQ (accumulating warp); V_j: dP only
   // item: (batch, K/V head, packed row tile), the last row tiles (most key blocks
   // when causal) first so that the short ones fill the end of the grid
   const int nbg = p.B * p.Hkv;
@@ -340,11 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (nblocks > 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kHalfN, false);
-      constexpr uint32_t idesc_q = idesc_f16_f32acc(BF16, kBM, D, true);
       const uint64_t dq_ = sdesc_sw128(sRes, 16, 1024);                   // Q, K-major
       const uint64_t ddo = sdesc_sw128(sRes + G::kTileBytes, 16, 1024);   // dO, K-major
       const uint64_t dkv = sdesc_sw128(sRing, 16, 1024);                  // K / V, K-major
-      const uint64_t dkmn = sdesc_sw128(sRing, G::kChunkBytes, 1024);     // K, MN-major
       // S and dP of block jj, keys [64h, 64h + 64): N = 64 MMAs into columns 64h..
       auto issue_half = [&](int jj, int hh) __attribute__((always_inline)) -> bool {
         const uint32_t kidx = 2u * jj, vidx = kidx + 1u;
@@ -363,7 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_elect(tmem_base + kColDP + kHalfN * hh, ddo + off, dkv + vslot + off, idesc_s, kk > 0);
         }
         mma_commit_elect(bar_s_full(hh));
-        if (hh == 1) mma_commit_elect(bar_empty(vidx % S));  // V_j is only read by dP
+        if (hh == 1) {
+          mma_commit_elect(bar_empty(vidx % S));  // V_j is only read by dP
+          mma_commit_elect(bar_empty(kidx % S));  // this warp's share of K_j
+        }
         return true;
       };
       bool ok = mbar_wait_warp(bar_res, 0, wc, kSiteMma);
@@ -371,19 +378,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         ok = issue_half(0, 0) && issue_half(0, 1);
       }
+      // half hh of block jj + 1 as soon as group hh has read its half of block jj
+      for (int jj = 0; ok && jj + 1 < nblocks; ++jj)
+        for (int hh = 0; ok && hh < 2; ++hh)
+          ok = mbar_wait_warp(bar_ld_free(hh), jj & 1u, wc, kSiteMma) && issue_half(jj + 1, hh);
+    }
+    mma_commit_elect(bar_drain);
+    mbar_wait_drain(bar_drain, 0, wc, kSiteDrain);
+  } else if (warp == kAccWarp) {
+    if (nblocks > 0) {
+      constexpr uint32_t idesc_q = idesc_f16_f32acc(BF16, kBM, D, true);
+      const uint64_t dkmn = sdesc_sw128(sRing, G::kChunkBytes, 1024);     // K, MN-major
+      bool ok = true;
       for (int jj = 0; ok && jj < nblocks; ++jj) {
         const uint32_t buf = jj & 1;
         const uint32_t kidx = 2u * jj;
         const uint64_t kslot = ((kidx % S) * G::kTileBytes) >> 4;
         for (int hh = 0; ok && hh < 2; ++hh) {
-          // half hh of block jj + 1 as soon as group hh has read its half of block jj
-          if (jj + 1 < nblocks) {
-            ok = mbar_wait_warp(bar_ld_free(hh), jj & 1u, wc, kSiteMma) && issue_half(jj + 1, hh);
-            if (!ok) break;
-          }
           // dQ += dS[:, keys of half hh] · K_j[keys of half hh]: group hh's dS pairs sit in
           // columns 32 hh .. 32 hh + 31 of dS buffer `buf`
           ok = mbar_wait_warp(bar_p_full(hh, buf), (jj >> 1) & 1u, wc, kSiteMma);
+          // K_j's load (complete long before: S_j was computed from it); this warp holds
+          // the slot until its commit below, so the phase cannot move on
+          if (ok && hh == 0) ok = mbar_wait_warp(bar_full(kidx % S), (kidx / S) & 1u, wc, kSiteMma);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -480,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_lse2,
                          const __grid_constant__ CUtensorMap tm_dsum, const BwdParams p) {
-  EX19_BWD_PREAMBLE()
+  EX19_BWD_PREAMBLE(2, 2)  // Q_i and dO_i are read by both MMA warps
   // Pᵀ and dSᵀ in their own TMEM columns (block st + 1 overlaps block st), or over
   // the columns of Sᵀ and dPᵀ that hold them (no room at d = 128)
   constexpr bool kSeparate = (D == 64);
@@ -547,11 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (nsteps > 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kHalfN, false);
-      constexpr uint32_t idesc_a = idesc_f16_f32acc(BF16, kBM, D, true);
       const uint64_t dk_ = sdesc_sw128(sRes, 16, 1024);                  // K_j, K-major
       const uint64_t dv_ = sdesc_sw128(sRes + G::kTileBytes, 16, 1024);  // V_j, K-major
       const uint64_t dr = sdesc_sw128(sRing, 16, 1024);                  // Q_i / dO_i, K-major
-      const uint64_t drmn = sdesc_sw128(sRing, G::kChunkBytes, 1024);    // Q_i / dO_i, MN-major
       // Sᵀ and dPᵀ of step st, queries [64h, 64h + 64): N = 64 MMAs into columns 64h..
       auto issue_half = [&](int st, int hh) __attribute__((always_inline)) -> bool {
         const uint32_t qidx = 2u * st, didx = qidx + 1u;
@@ -570,6 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_elect(tmem_base + kColDP + kHalfN * hh, dv_ + off, dr + ds + off, idesc_s, kk > 0);
         }
         mma_commit_elect(bar_s_full(hh));
+        if (hh == 1) {  // this warp's share of Q_i and dO_i
+          mma_commit_elect(bar_empty(qidx % S));
+          mma_commit_elect(bar_empty(didx % S));
+        }
         return true;
       };
       bool ok = mbar_wait_warp(bar_res, 0, wc, kSiteMma);
@@ -577,17 +596,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         ok = issue_half(0, 0) && issue_half(0, 1);
       }
+      // half hh of step st + 1 once group hh has read step st (separate buffers), or
+      // once the accumulating MMAs that read group hh's pairs in place are complete
+      for (int st = 0; ok && st + 1 < nsteps; ++st)
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          ok = kSeparate ? mbar_wait_warp(bar_ld_free(hh), st & 1u, wc, kSiteMma)
+                         : mbar_wait_warp(bar_acc_done(hh, 0), st & 1u, wc, kSiteMma);
+          ok = ok && issue_half(st + 1, hh);
+        }
+    }
+    mma_commit_elect(bar_drain);
+    mbar_wait_drain(bar_drain, 0, wc, kSiteDrain);
+  } else if (warp == kAccWarp) {
+    if (nsteps > 0) {
+      constexpr uint32_t idesc_a = idesc_f16_f32acc(BF16, kBM, D, true);
+      const uint64_t drmn = sdesc_sw128(sRing, G::kChunkBytes, 1024);    // Q_i / dO_i, MN-major
+      bool ok = true;
       for (int st = 0; ok && st < nsteps; ++st) {
         const uint32_t qidx = 2u * st, didx = qidx + 1u;
         const uint64_t qs = ((qidx % S) * G::kTileBytes) >> 4;
         const uint64_t ds = ((didx % S) * G::kTileBytes) >> 4;
         for (int hh = 0; ok && hh < 2; ++hh) {
-          // separate buffers: half hh of step st + 1 as soon as group hh has read step st
-          if (kSeparate && st + 1 < nsteps) {
-            ok = mbar_wait_warp(bar_ld_free(hh), st & 1u, wc, kSiteMma) && issue_half(st + 1, hh);
-            if (!ok) break;
-          }
           ok = mbar_wait_warp(bar_p_full(hh, 0), st & 1u, wc, kSiteMma);
+          // Q_i and dO_i loads (complete long before: Sᵀ and dPᵀ were computed from
+          // them); this warp holds both slots until its commits below
+          if (ok && hh == 0)
+            ok = mbar_wait_warp(bar_full(qidx % S), (qidx / S) & 1u, wc, kSiteMma) &&
+                 mbar_wait_warp(bar_full(didx % S), (didx / S) & 1u, wc, kSiteMma);
           if (!ok) break;
           tc_fence_after();
           // dV += Pᵀ · dO_i and dK += dSᵀ · Q_i over the queries of half hh (group hh's pairs)
@@ -601,12 +636,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                          drmn + qs + ((kk * 2048) >> 4), idesc_a, acc);
           }
           mma_commit_elect(bar_acc_done(hh, 0));
-          // in place: half hh of the next step follows these MMAs (issue order), which
-          // read the columns it overwrites
-          if (!kSeparate && st + 1 < nsteps) {
-            ok = issue_half(st + 1, hh);
-            if (!ok) break;
-          }
         }
         if (!ok) break;
         mma_commit_elect(bar_empty(qidx % S));
