@@ -110,8 +110,8 @@ struct BwdGeometry {
   static constexpr int kVecBytes = 2 * kBN * 4;                   // per stage
   static constexpr int kOffBar = kOffVec + (kSlots / 2) * kVecBytes;
   // barriers: full[S], empty[S], res_full, s_full[2], ld_free[2], p_full[2][2],
-  // acc_done[2][2], drain
-  static constexpr int kNumBars = 2 * kSlots + 14;
+  // acc_done[2][2], drain, a_ready
+  static constexpr int kNumBars = 2 * kSlots + 15;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -159,6 +159,7 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
 //   acc_done[h][b] MMA -> group h: the accumulating MMAs that read them are complete
 //   drain          MMA -> all: every MMA of the CTA is complete (both MMA warps commit;
 //                  the epilogues wait here)
+//   a_ready        elementwise -> MMA: resident tiles copied into TMEM (d = 64)
 // A slot read by both MMA warps is released by two commits: EMPTY_EVEN / EMPTY_ODD
 // arrivals for the even (K or Q) and odd (V or dO) slots.
 #define EX19_BWD_PREAMBLE(EMPTY_EVEN, EMPTY_ODD)                                               \
@@ -180,6 +181,7 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
   auto bar_p_full = [&](uint32_t h, uint32_t b) { return bars + 8u * (2 * S + 5 + 2 * h + b); }; \
   auto bar_acc_done = [&](uint32_t h, uint32_t b) { return bars + 8u * (2 * S + 9 + 2 * h + b); }; \
   const uint32_t bar_drain = bars + 8u * (2 * S + 13);                                         \
+  const uint32_t bar_a_ready = bars + 8u * (2 * S + 14);                                       \
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);                       \
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4); \
   const int warp = threadIdx.x >> 5;                                                           \
@@ -199,6 +201,7 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
       }                                                                                        \
     }                                                                                          \
     mbar_init(bar_drain, 2);                                                                   \
+    mbar_init(bar_a_ready, kEwWarps * 32);                                                     \
     *abort_flag = 0u;                                                                          \
     fence_mbar_init();                                                                         \
   }                                                                                            \
@@ -260,6 +263,21 @@ __device__ __forceinline__ void elementwise_cols(const uint32_t (&xs)[N], const 
   }
 }
 
+// Copies row r of a 128 x 64 16-bit tile in the 128-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ (r mod 8)) into the thread's TMEM lane as 32 columns of pairs:
+// the layout of a TMEM A operand (K-step kk at columns 8 kk .. 8 kk + 7).
+__device__ __forceinline__ void tile_row_to_tmem64(uint32_t s_tile, int r, uint32_t taddr) {
+  uint32_t v[32];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t a = s_tile + r * 128 + ((c ^ (r & 7)) << 4);
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                 : "r"(a));
+  }
+  tmem_st_x32(taddr, v);
+}
+
 // Writes columns [c_lo, c_lo + D/2) of the thread's row of a TMEM fp32 accumulator,
 // times f, to out (input dtype or float32).
 template <int D, bool BF16, bool OUT_F32>
@@ -308,8 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int blk_hi = p.causal ? (i1 - 1) / kBN + 1 : nblk;
   const int blk_lo = (p.window_left >= 0) ? max(0, i0 - p.window_left) / kBN : 0;
   const int nblocks = max(0, blk_hi - blk_lo);
-  // TMEM: S [0,128), dP [128,256), dQ [256, 256 + D), dS buffers of 64 columns after dQ
+  // TMEM: S [0,128), dP [128,256), dQ [256, 256 + D), dS buffers of 64 columns after dQ;
+  // d = 64: Q [448, 480) and dO [480, 512) as A operands, so that S and dP are TS
+  // MMAs reading only K and V from shared memory
+  constexpr bool kATmem = (D == 64);
   const uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  constexpr uint32_t kColQ = 448, kColDO = 480;
   auto col_ds = [](uint32_t buf) { return 256u + D + 64u * buf; };
 
   if (warp == kProducerWarp) {
@@ -363,8 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * G::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_elect(tmem_base + kColS + kHalfN * hh, dq_ + off, dkv + kslot + off, idesc_s, kk > 0);
-          mma_ss_elect(tmem_base + kColDP + kHalfN * hh, ddo + off, dkv + vslot + off, idesc_s, kk > 0);
+          if constexpr (kATmem) {
+            mma_ts_elect(tmem_base + kColS + kHalfN * hh, tmem_base + kColQ + kk * 8, dkv + kslot + off,
+                         idesc_s, kk > 0);
+            mma_ts_elect(tmem_base + kColDP + kHalfN * hh, tmem_base + kColDO + kk * 8, dkv + vslot + off,
+                         idesc_s, kk > 0);
+          } else {
+            mma_ss_elect(tmem_base + kColS + kHalfN * hh, dq_ + off, dkv + kslot + off, idesc_s, kk > 0);
+            mma_ss_elect(tmem_base + kColDP + kHalfN * hh, ddo + off, dkv + vslot + off, idesc_s, kk > 0);
+          }
         }
         mma_commit_elect(bar_s_full(hh));
         if (hh == 1) {
@@ -373,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      bool ok = mbar_wait_warp(bar_res, 0, wc, kSiteMma);
+      bool ok = kATmem ? mbar_wait_warp(bar_a_ready, 0, wc, kSiteMma) : mbar_wait_warp(bar_res, 0, wc, kSiteMma);
       if (ok) {
         tc_fence_after();
         ok = issue_half(0, 0) && issue_half(0, 1);
@@ -430,6 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos_min = i0, pos_max = i1 - 1;
     const int x0 = kHalfN * hh;
     bool ok = true;
+    if constexpr (kATmem) {  // group 0 copies Q, group 1 dO, into their TMEM columns
+      if (nblocks > 0) {
+        ok = mbar_wait_warp(bar_res, 0, wc, kSiteEw);
+        if (ok) {
+          tile_row_to_tmem64(sRes + hh * G::kTileBytes, rho, tmem_base + lane_off + (hh ? kColDO : kColQ));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar_a_ready);
+        }
+      }
+    }
     for (int jj = 0; ok && jj < nblocks; ++jj) {
       const int key0 = (blk_lo + jj) * kBN;
       const uint32_t buf = jj & 1;
