@@ -200,9 +200,8 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
         raise ValueError("k and v must have q's sequence length (attn_fwd_kv takes Lq <= Lk)")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = workspace_size(B, L, Hq, Hkv, d, causal, window_left)
-    if workspace is None:
-        workspace = _default_workspace(q.device, need)
+    if workspace is None:  # a given workspace's size is checked by the library
+        workspace = _default_workspace(q.device, workspace_size(B, L, Hq, Hkv, d, causal, window_left))
     code = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                         lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
                         int(bool(causal)), int(window_left), float(scale), dt, out,
@@ -228,8 +227,8 @@ def attn_bwd(q, k, v, o, lse, dout, causal=False, window_left=-1, scale=None, ou
     dv = torch.empty(k.shape, dtype=odt, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = int(lib.attn_bwd_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)), int(window_left)))
     if workspace is None:
+        need = int(lib.attn_bwd_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)), int(window_left)))
         workspace = _default_workspace(q.device, max(need, 256))
     _check(lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                         dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, L, Hq,
@@ -259,9 +258,9 @@ def attn_fwd_fp8(q, k, v, causal=False, window_left=-1, scale=None, out_fp32=Fal
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if return_lse else None
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = int(lib.attn_fwd_fp8_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)),
-                                               int(window_left)))
     if workspace is None:
+        need = int(lib.attn_fwd_fp8_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)),
+                                                   int(window_left)))
         workspace = _default_workspace(q.device, max(need, 256))
     _check(lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                             lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
@@ -316,8 +315,8 @@ def attn_fwd_kv_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None, 
     (B, Lq, Lk, Hq, Hkv, d), dt, out = _check_tensors(q, k, v, o, lse)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = kv_workspace_size(B, Lq, Lk, Hq, Hkv, d, causal, window_left, num_splits)
-    if workspace is None:
+    if workspace is None:  # a given workspace's size is checked by the library
+        need = kv_workspace_size(B, Lq, Lk, Hq, Hkv, d, causal, window_left, num_splits)
         workspace = _default_workspace(q.device, max(need, 256))
     code = lib.attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                            lse.data_ptr() if lse is not None else None, B, Lq, Lk, Hq, Hkv, d,
@@ -386,8 +385,8 @@ def attn_fwd_kv_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, c
     lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device) if return_lse else None
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = kv_workspace_size(B, Lq, max_seq_len, Hq, Hkv, d, causal, window_left, num_splits)
     if workspace is None:
+        need = kv_workspace_size(B, Lq, max_seq_len, Hq, Hkv, d, causal, window_left, num_splits)
         workspace = _default_workspace(q.device, max(need, 256))
     code = lib.attn_fwd_kv_paged(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
