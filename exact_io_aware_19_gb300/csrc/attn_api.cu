@@ -500,10 +500,15 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   const int num_units = B * Hq * ((L + kUnitRows - 1) / kUnitRows);
   // Problems with at most half as many 256-row units as SMs leave most SMs idle in
   // the persistent two-tile kernel; the one-tile kernel (the decode-shaped path with
-  // Lq = Lk and one key split) runs 128-row tiles, twice as many CTAs.
+  // Lq = Lk and one key split) runs 128-row tiles, twice as many CTAs. Under a causal
+  // mask the work per tile grows with its position, and the persistent kernel's time
+  // is then set by its longest unit (the last two tiles, all key blocks, one after
+  // another); the one-tile kernel starts the longest tiles first and spreads the
+  // rest, which wins up to one unit per SM (measured at L = 8192, 4 heads: 72 against
+  // 97 µs; at twice that the persistent kernel's throughput wins).
   const int policy = g_path_policy.load();
-  if (policy == ATTN_PATH_TILES ||
-      (policy == ATTN_PATH_AUTO && 2 * num_units <= info.sms && Hq / Hkv <= 128))
+  const bool few_units = causal ? num_units <= info.sms : 2 * num_units <= info.sms;
+  if (policy == ATTN_PATH_TILES || (policy == ATTN_PATH_AUTO && few_units && Hq / Hkv <= 128))
     return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, -1, scale,
                                bf16, out_f32, workspace, stream);
   CUtensorMap tm_q, tm_k, tm_v;

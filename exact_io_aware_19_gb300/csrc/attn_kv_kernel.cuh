@@ -104,11 +104,15 @@ __device__ __forceinline__ int right_bound(const KvParams& p) { return p.causal 
 template <bool PAGED>
 __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   KvItem it;
+  // CTA order: row tile outermost and descending (under a causal mask the last row
+  // tiles see the most keys), then (batch, K/V head), then split, so that the CTAs
+  // with the most work start first and the short ones fill the end of the grid
   int x = blockIdx.x;
   it.split = x % p.splits;
   x /= p.splits;
-  const int rt = x % p.row_tiles;
-  x /= p.row_tiles;
+  const int nbg = p.B * p.Hkv;
+  const int rt = p.row_tiles - 1 - x / nbg;
+  x %= nbg;
   it.g = x % p.Hkv;
   it.b = x / p.Hkv;
   it.i0 = rt * p.q_per_tile;

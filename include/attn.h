@@ -261,7 +261,8 @@ attn_status_t attn_fwd_kv_paged(const void *q, const void *k_cache, const void *
  * same result (up to rounding order); they differ in how the work is cut:
  *   ATTN_PATH_AUTO    the persistent two-tile kernel (256 query rows per work unit),
  *                     unless the problem has at most half as many such units as the
- *                     device has SMs; then the one-tile kernel (128 rows per CTA).
+ *                     device has SMs (causal: at most as many); then the one-tile
+ *                     kernel (128 rows per CTA, the longest tiles first).
  *   ATTN_PATH_SQUARE  always the persistent two-tile kernel.
  *   ATTN_PATH_TILES   always the one-tile kernel (attn_fwd_kv's with Lq = Lk and one
  *                     key split).

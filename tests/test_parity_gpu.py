@@ -201,9 +201,26 @@ def test_exp2_f16x2_accuracy():
     assert (got - ref).abs()[~normal].max().item() <= 2.0 ** -24
 
 
+def test_auto_path_choice_causal_one_unit_per_sm():
+    """Causal problems with at most one 256-row unit per SM take the one-tile kernel
+    (128 units at L = 8192, 4 heads); a non-causal problem of the same size takes the
+    persistent kernel. AUTO gives exactly the chosen kernel's bits."""
+    import exact_io_aware_19_gb300 as ex
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 128 <= sms
+    for causal, B, L, H, pick in ((True, 1, 8192, 4, ex.PATH_TILES), (False, 2, 2048, 8, ex.PATH_SQUARE)):
+        q, k, v = si.random_qkv(B, L, H, H, 64, seed=L, device="cuda")
+        assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
+        o_auto, l_auto = ex.attn_fwd(q, k, v, causal=causal, out_fp32=True)
+        ex.set_path_policy(pick)
+        o_p, l_p = ex.attn_fwd(q, k, v, causal=causal, out_fp32=True)
+        ex.set_path_policy(ex.PATH_AUTO)
+        assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (causal, L)
+
+
 def test_auto_path_choice():
     """AUTO takes the one-tile kernel exactly when the problem has at most half as many
-    256-row units as SMs; both kernels agree to rounding."""
+    256-row units as SMs (causal: at most as many); both kernels agree to rounding."""
     import exact_io_aware_19_gb300 as ex
     assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
     q, k, v = si.random_qkv(1, 2048, 4, 4, 64, seed=8, device="cuda")
