@@ -576,11 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One warp per row: lanes take
 // the splits 32 at a time for the log-sum-exp (shuffle reductions), then every lane
 // owns D / 32 consecutive columns and accumulates the weighted partial rows, with
-// the loads of up to 8 splits in flight at once.
+// the loads of up to 32 (d = 64) or 16 (d = 128) splits in flight at once.
 template <int D, bool BF16, bool OUT_F32>
 __global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
   constexpr int kCols = D / 32;
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 64 / kCols;  // splits whose loads are in flight at once (64 registers)
   const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
