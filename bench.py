@@ -416,6 +416,53 @@ def ours_arm(args, world, rank, local):
                                          "per-call mean (median of 6)",
                                "us_single_call": statistics.median(single) * 1e3}
             del qd, kd, vd, od, ld, wsd
+        # the GQA decode over a paged cache: 16-token pages in shuffled order
+        wd = si.DECODE_GQA_B1_H32_KV8_D128
+        qd, kd, vd = si.make_qkv_decode(wd, device=dev)
+        ps = 16
+        npg = wd.Lk // ps
+        perm = torch.randperm(npg, generator=torch.Generator().manual_seed(1011)).to(dev)
+        kc = torch.empty(npg, ps, wd.Hkv, wd.d, dtype=kd.dtype, device=dev)
+        vc = torch.empty_like(kc)
+        kc[perm] = kd[0].view(npg, ps, wd.Hkv, wd.d)
+        vc[perm] = vd[0].view(npg, ps, wd.Hkv, wd.d)
+        del kd, vd
+        table = perm.view(1, npg).to(torch.int32)
+        lens = torch.tensor([wd.Lk], dtype=torch.int32, device=dev)
+        splits = ex.kv_num_splits(wd.B, wd.Lq, wd.Lk, wd.Hq, wd.Hkv, wd.d, wd.causal,
+                                  wd.window_left)
+        wsd = torch.zeros(ex.kv_workspace_size(wd.B, wd.Lq, wd.Lk, wd.Hq, wd.Hkv, wd.d,
+                                               wd.causal, wd.window_left, splits),
+                          dtype=torch.uint8, device=dev)
+
+        def paged_call():
+            ex.attn_fwd_kv_paged(qd, kc, vc, table, lens, wd.Lk, causal=wd.causal,
+                                 scale=wd.scale, num_splits=splits, workspace=wsd)
+
+        times = []
+        for r in range(8):
+            flush.fill_(float(r))
+            a = torch.cuda.Event(enable_timing=True)
+            bb = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(per_rep):
+                paged_call()
+            bb.record(stream)
+            torch.cuda.synchronize(dev)
+            if r >= 2:
+                times.append(a.elapsed_time(bb) / per_rep)
+        ex.sync_status(wsd)
+        t = statistics.median(times)
+        pbytes = wd.algorithmic_bytes() + table.numel() * 4
+        gbs = pbytes / (t * 1e-3) / 1e9
+        decode[wd.name + "_paged16"] = {
+            "us": t * 1e3, "GB/s": gbs, "splits": splits,
+            "frac_of_hbm": gbs / float(peaks["hbm_gbs"]), "algorithmic_bytes": pbytes,
+            "launches_per_call": 2 if splits > 1 else 1,
+            "timing": f"{per_rep} calls back to back between CUDA events, per-call mean "
+                      "(median of 6)",
+            "layout": "K/V cache in 16-token pages, pages in shuffled order"}
+        del qd, kc, vc, table, lens, wsd
 
     # ---- float8 e4m3 forward on the skill page's FP8 example shape (2 x 4096 x 32 x 64)
     fp8 = {}

@@ -39,6 +39,10 @@
 //     with zeros. The unused rows of a partial last page hold whatever the cache
 //     holds, so the MMA warp zeroes those V rows in shared memory before that
 //     block's P·V (P is 0 there, but 0 · NaN would not be).
+//     The paged producer is the whole warp: its lanes hold the page rows of the next
+//     32 / (128 / page_size) blocks, loaded a window ahead, and lane pp issues page
+//     pp's copies, so neither page-table latency nor a serial issue of small boxes
+//     paces the stream.
 //   * Every wait is bounded; a timeout sets the status word and all roles leave.
 #pragma once
 #include <cuda.h>
@@ -214,67 +218,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nblocks > 0) {
-      // The Q box is {64, group, q_per_tile, 1}; rows past Lq are zero-filled and
-      // still counted in the transaction bytes.
-      mbar_arrive_expect_tx(bar_q_full, G::kChunks * 128u * p.group * p.q_per_tile);
-      for (int c = 0; c < G::kChunks; ++c)
-        tma_load_4d(sQ + c * G::kChunkBytes, &tm_q, bar_q_full, c * 64, it.g * p.group, it.i0,
-                    it.b);
+    if (nblocks > 0) {
+      if (lane == 0) {
+        // The Q box is {64, group, q_per_tile, 1}; rows past Lq are zero-filled and
+        // still counted in the transaction bytes.
+        mbar_arrive_expect_tx(bar_q_full, G::kChunks * 128u * p.group * p.q_per_tile);
+        for (int c = 0; c < G::kChunks; ++c)
+          tma_load_4d(sQ + c * G::kChunkBytes, &tm_q, bar_q_full, c * 64, it.g * p.group, it.i0,
+                      it.b);
+      }
       uint32_t n = 0;
       bool ok = true;
-      // Paged: the physical rows of block j's pages, read one block ahead so the
-      // page-table loads are in flight while the producer waits for a free slot.
-      constexpr int kMaxPagesPerBlock = kBN / 8;
-      int rows_cur[kMaxPagesPerBlock], rows_next[kMaxPagesPerBlock];
-      auto page_rows = [&](int j, int (&rows)[kMaxPagesPerBlock]) __attribute__((always_inline)) {
-        const int per_block = kBN / p.page_size;
+      if constexpr (PAGED) {
+        // The whole warp runs the loop: its 32 lanes hold the physical rows of the
+        // pages of a window of W = 32 / P blocks (P = 128 / page_size pages per block),
+        // and the next window's page-table loads are issued when the current window
+        // starts, so they land long before they are needed (a table read per block,
+        // right before its TMA, put an L2 round trip under load on every block).
+        // Lane 0 takes each page's row by shuffle and issues the copies.
+        const int P = kBN / p.page_size;
+        const int W = 32 / P;
         const int oob_row = p.num_pages * p.page_size;  // past the cache: zero-filled
-#pragma unroll
-        for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) {
-          const int lp = j * per_block + pp;  // logical page of the sequence
+        auto fetch = [&](int j0) -> int {  // this lane's page of the window starting at j0
+          const int jb = j0 + lane / P, lp = jb * P + lane % P;  // block, logical page
           int phys = -1;
-          if (pp < per_block && lp * p.page_size < it.Lk)
+          if (jb < it.hi && lp * p.page_size < it.Lk)
             phys = p.block_table[static_cast<size_t>(it.b) * p.max_pages + lp];
-          rows[pp] = (phys >= 0 && phys < p.num_pages) ? phys * p.page_size : oob_row;
-        }
-      };
-      if constexpr (PAGED) page_rows(it.lo, rows_cur);
-      for (int j = it.lo; ok && j < it.hi; ++j) {
-        if constexpr (PAGED) {
-          if (j + 1 < it.hi) page_rows(j + 1, rows_next);
-        }
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t slot = n % S;
-          ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
-          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-          if constexpr (PAGED) {
-            // one box of page_size rows per page of this block
-            const int per_block = kBN / p.page_size;
+          return (phys >= 0 && phys < p.num_pages) ? phys * p.page_size : oob_row;
+        };
+        int cur = fetch(it.lo), nxt = oob_row;
+        for (int j = it.lo; ok && j < it.hi; ++j) {
+          const int jw = (j - it.lo) % W;
+          if (jw == 0) nxt = fetch(j + W);
+          for (int kv = 0; ok && kv < 2; ++kv) {
+            const uint32_t slot = n % S;
+            ok = mbar_wait_warp(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
+            __syncwarp();  // the transaction count is set before any copy can complete
+            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+            // lane pp < P copies page pp of this block: one box of page_size rows
+            const int row = __shfl_sync(0xffffffffu, cur, jw * P + (lane % P));
+            if (lane < P) {
 #pragma unroll
-            for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) {  // predicated: rows stay in registers
-              if (pp < per_block) {
-#pragma unroll
-                for (int c = 0; c < G::kChunks; ++c)
-                  tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + pp * p.page_size * 128,
-                              tm, bar_full(slot), c * 64, it.g, rows_cur[pp], 0);
-              }
+              for (int c = 0; c < G::kChunks; ++c)
+                tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + lane * p.page_size * 128,
+                            tm, bar_full(slot), c * 64, it.g, row, 0);
             }
-          } else {
+            ++n;
+          }
+          if (jw == W - 1) cur = nxt;
+        }
+      } else if (lane == 0) {
+        for (int j = it.lo; ok && j < it.hi; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t slot = n % S;
+            ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
+            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
             for (int c = 0; c < G::kChunks; ++c)
               tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
                           c * 64, it.g, j * kBN, it.b);
+            ++n;
           }
-          ++n;
-        }
-        if constexpr (PAGED) {
-#pragma unroll
-          for (int pp = 0; pp < kMaxPagesPerBlock; ++pp) rows_cur[pp] = rows_next[pp];
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // Let the copies already in flight land before the CTA can exit.
         for (uint32_t back = 1; back <= S && back <= n; ++back) {
           const uint32_t m = n - back;
