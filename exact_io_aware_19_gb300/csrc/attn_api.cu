@@ -244,10 +244,12 @@ KvPlan kv_plan(int B, int Lq, int Lk, int Hq, int Hkv, int causal, int window_le
   return k;
 }
 
-// Splits that fill the SMs with one wave of CTAs, keeping at least 2 key blocks per
-// split and at most kKvMaxSplits.
-int kv_auto_splits(const KvPlan& k, int sms) {
-  int s = std::max(1, sms / std::max(1, k.items));
+// Splits that fill the SMs with one wave of CTAs (two per SM for the one-tile
+// kernel's decode mode: d = 64 with at most 32 rows per tile), keeping at least 2 key
+// blocks per split and at most kKvMaxSplits.
+int kv_auto_splits(const KvPlan& k, int sms, int d) {
+  const int ctas = ex19::kv_decode_shape(d, k.q_per_tile, k.group) ? 2 * sms : sms;
+  int s = std::max(1, ctas / std::max(1, k.items));
   s = std::min(s, std::max(1, k.max_blocks / 2));
   return std::min(s, kKvMaxSplits);
 }
@@ -326,7 +328,7 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
     return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
                                           std::to_string(info.major) + "." +
                                           std::to_string(info.minor));
-  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms);
+  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms, d);
   if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits))
     return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
   if ((long long)plan.items * splits >= (1LL << 31))
@@ -806,7 +808,7 @@ int attn_fwd_kv_num_splits(int B, int Lq, int Lk, int Hq, int Hkv, int d, int ca
     fail(ATTN_ERR_CUDA, "no CUDA device");
     return 0;
   }
-  return kv_auto_splits(kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left), sms);
+  return kv_auto_splits(kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left), sms, d);
 }
 
 size_t attn_fwd_kv_workspace_size(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,

@@ -7,10 +7,10 @@
 namespace ex19 {
 namespace {
 
-template <int D, bool BF16, bool OUT_F32, bool PAGED>
+template <int D, bool BF16, bool OUT_F32, bool PAGED, bool DEC>
 cudaError_t launch_kv_one(const KvLaunchArgs& a) {
-  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32, PAGED>;
-  constexpr int smem = kv::KvGeometry<D>::kSmemBytes;
+  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32, PAGED, DEC>;
+  constexpr int smem = kv::KvGeometry<D, DEC>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -21,20 +21,26 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<a.grid, kv::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, a.p);
+  kern<<<a.grid, kv::KvRoles<DEC>::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, a.p);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.p.splits <= 1) return e;
   const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
-  kv::attn_kv_merge_kernel<D, BF16, OUT_F32>
-      <<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(a.p);
+  kv::attn_kv_merge_kernel<D, BF16, OUT_F32><<<static_cast<unsigned>(rows), 256, 0, a.stream>>>(a.p);
   return cudaGetLastError();
 }
 
 template <int D, bool PAGED>
 cudaError_t launch_kv_d(bool bf16, bool out_f32, const KvLaunchArgs& a) {
   if (bf16)
-    return out_f32 ? launch_kv_one<D, true, true, PAGED>(a) : launch_kv_one<D, true, false, PAGED>(a);
-  return out_f32 ? launch_kv_one<D, false, true, PAGED>(a) : launch_kv_one<D, false, false, PAGED>(a);
+    return out_f32 ? launch_kv_one<D, true, true, PAGED, false>(a)
+                   : launch_kv_one<D, true, false, PAGED, false>(a);
+  if constexpr (D == 64) {
+    if (kv_decode_mode(D, bf16, a.p.q_per_tile, a.p.group))
+      return out_f32 ? launch_kv_one<D, false, true, PAGED, true>(a)
+                     : launch_kv_one<D, false, false, PAGED, true>(a);
+  }
+  return out_f32 ? launch_kv_one<D, false, true, PAGED, false>(a)
+                 : launch_kv_one<D, false, false, PAGED, false>(a);
 }
 
 }  // namespace

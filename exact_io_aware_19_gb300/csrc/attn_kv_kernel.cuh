@@ -43,6 +43,13 @@
 //     32 / (128 / page_size) blocks, loaded a window ahead, and lane pp issues page
 //     pp's copies, so neither page-table latency nor a serial issue of small boxes
 //     paces the stream.
+//   * Decode mode (DEC; fp16, d = 64, at most 32 valid rows per tile, as in one new
+//     token per sequence): the tile's rows fit one softmax warp, so the CTA has 3
+//     warps (softmax, producer, MMA), one S buffer with P in its own 64 columns and
+//     O (256 TMEM columns) and 5 ring slots (96 KiB), and two CTAs share an SM: two
+//     softmax chains per SM instead of one, for a shape whose time per key block is
+//     one row's softmax latency. S(j + 1) is issued once the softmax has read S(j)
+//     into registers (s_free); the softmax writes P(j) after P·V(j − 1) is done.
 //   * Every wait is bounded; a timeout sets the status word and all roles leave.
 #pragma once
 #include <cuda.h>
@@ -62,11 +69,20 @@ namespace kv {
 
 constexpr int kBM = 128;             // rows per tile (= TMEM lanes)
 constexpr int kBN = 128;             // keys per K/V block
-constexpr int kThreads = 192;        // 4 softmax warps + producer warp + MMA warp
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256 + D)
-constexpr uint32_t kColO = 256;
+
+// Warp roles and TMEM columns of the two modes.
+template <bool DEC>
+struct KvRoles {
+  static constexpr int kSmxWarps = DEC ? 1 : 4;               // softmax warps (32 rows each)
+  static constexpr int kThreads = 32 * (kSmxWarps + 2);        // + producer warp + MMA warp
+  static constexpr int kProducerWarp = kSmxWarps;
+  static constexpr int kMmaWarp = kSmxWarps + 1;
+  static constexpr uint32_t kTmemCols = DEC ? 256 : 512;
+  // DEC: S [0,128), P [128,192), O [192,256); else S0 [0,128), S1 [128,256) with P
+  // over them, O [256, 256 + D)
+  static constexpr uint32_t kColP = 128;
+  static constexpr uint32_t kColO = DEC ? 192 : 256;
+};
 
 enum : uint32_t {
   kSiteProdEmpty = 0x50001,
@@ -77,16 +93,17 @@ enum : uint32_t {
   kSiteBadSeqLen = 0x90001,  // a paged sequence length outside [Lq, max_seq_len]
 };
 
-template <int D>
+template <int D, bool DEC = false>
 struct KvGeometry {
   static constexpr int kChunks = D / 64;          // 128-byte swizzle boxes per row
   static constexpr int kChunkBytes = kBM * 128;   // one box column of a 128-row tile
   static constexpr int kTileBytes = kBM * D * 2;  // a 128-row tile of Q, K or V
-  static constexpr int kSlots = (D == 64) ? 8 : 5;
+  static constexpr int kSlots = DEC ? 5 : (D == 64) ? 8 : 5;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full, drain
+  // barriers: full[S], empty[S], q_full, s_full[2] (DEC: s_full, s_free), p_full[2],
+  // pv_done[2], o_full, drain
   static constexpr int kNumBars = 2 * kSlots + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffMisc + 16;
@@ -142,12 +159,18 @@ __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   return it;
 }
 
-template <int D, bool BF16, bool OUT_F32, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool BF16, bool OUT_F32, bool PAGED, bool DEC>
+__global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     attn_kv_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const KvParams p) {
-  using G = KvGeometry<D>;
+  static_assert(!DEC || (D == 64 && !BF16), "decode mode: fp16, d = 64 (P in 64 TMEM columns)");
+  using G = KvGeometry<D, DEC>;
+  using R = KvRoles<DEC>;
+  constexpr int kProducerWarp = R::kProducerWarp;
+  constexpr int kMmaWarp = R::kMmaWarp;
+  constexpr uint32_t kTmemCols = R::kTmemCols;
+  constexpr uint32_t kColO = R::kColO;
   constexpr int S = G::kSlots;
   constexpr bool kSplitP = BF16;  // bf16 P as hi + lo halves (two P·V MMAs)
   constexpr bool kF16Exp = !BF16;  // fp16: exponentials on packed fp16 pairs
@@ -164,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
   const uint32_t bar_q_full = bars + 8u * (2 * S);
   auto bar_s_full = [&](uint32_t b) { return bars + 8u * (2 * S + 1 + b); };
+  const uint32_t bar_s_free = bar_s_full(1);  // DEC: the softmax has read S
   auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 3 + b); };
   auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
   const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
@@ -183,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_q_full, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s_full(b), 1);
-      mbar_init(bar_p_full(b), kBM);
+      mbar_init(bar_s_full(b), (DEC && b == 1) ? R::kSmxWarps * 32 : 1);  // DEC: s_free
+      mbar_init(bar_p_full(b), R::kSmxWarps * 32);
       mbar_init(bar_pv_done(b), 1);
     }
     mbar_init(bar_o_full, 1);
@@ -309,14 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kidx = 2u * jj;
         if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull)) return false;
         tc_fence_after();
-        const uint32_t mS = tmem_base + 128u * (jj & 1);
+        const uint32_t mS = tmem_base + (DEC ? 0u : 128u * (jj & 1));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
           mma_ss_elect(mS, dq + (off >> 4), dk + ((slot_of(kidx) * G::kTileBytes + off) >> 4),
                        idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit_elect(bar_s_full(jj & 1));
+        mma_commit_elect(bar_s_full(DEC ? 0 : (jj & 1)));
         mma_commit_elect(bar_empty(slot_of(kidx)));
         return true;
       };
@@ -338,9 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
         }
-        if (!mbar_wait_warp(bar_p_full(jj & 1), (jj >> 1) & 1u, wc, kSiteMmaPFull)) return false;
+        if (!mbar_wait_warp(bar_p_full(DEC ? 0 : (jj & 1)), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc,
+                            kSiteMmaPFull))
+          return false;
         tc_fence_after();
-        const uint32_t mP = tmem_base + 128u * (jj & 1);
+        const uint32_t mP = tmem_base + (DEC ? R::kColP : 128u * (jj & 1));
         const uint64_t dvs = dv + ((slot_of(vidx) * G::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -355,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts_elect(mO, mP + pcol, dvs + ((kk * 2048) >> 4), idesc_o, 1u);
           }
         }
-        mma_commit_elect(bar_pv_done(jj & 1));
+        mma_commit_elect(bar_pv_done(DEC ? 0 : (jj & 1)));
         mma_commit_elect(bar_empty(slot_of(vidx)));
         return true;
       };
@@ -363,10 +389,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         ok = issue_s(0);
-        if (ok && nblocks > 1) ok = issue_s(1);
-        for (int jj = 0; ok && jj < nblocks; ++jj) {
-          ok = issue_pv(jj);
-          if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
+        if constexpr (DEC) {
+          // one S buffer: S(jj + 1) once the softmax holds S(jj) in registers
+          for (int jj = 0; ok && jj < nblocks; ++jj) {
+            if (jj + 1 < nblocks) {
+              ok = mbar_wait_warp(bar_s_free, jj & 1u, wc, kSiteMmaPFull);
+              if (ok) {
+                tc_fence_after();
+                ok = issue_s(jj + 1);
+              }
+            }
+            if (ok) ok = issue_pv(jj);
+          }
+        } else {
+          if (ok && nblocks > 1) ok = issue_s(1);
+          for (int jj = 0; ok && jj < nblocks; ++jj) {
+            ok = issue_pv(jj);
+            if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
+          }
         }
         if (ok) mma_commit_elect(bar_o_full);
       }
@@ -395,11 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int jj = 0; jj < nblocks; ++jj) {
       const int j = it.lo + jj;
-      const uint32_t buf = jj & 1;
-      ok = mbar_wait_warp(bar_s_full(buf), (jj >> 1) & 1u, wc, kSiteSmxSFull);
+      const uint32_t buf = DEC ? 0u : (jj & 1);
+      ok = mbar_wait_warp(bar_s_full(buf), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc, kSiteSmxSFull);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem_base + lane_off + 128u * buf;  // S, then P, of this block
+      // S of this block, then P over it (DEC: P in its own columns)
+      const uint32_t tS = tmem_base + lane_off + (DEC ? 0u : 128u * buf);
+      const uint32_t tP = DEC ? tmem_base + lane_off + R::kColP : tS;
       const int key0 = j * kBN;
       const bool masked = (key0 + kBN > Lk) || (wr >= 0 && key0 + kBN - 1 > pos_min + wr) ||
                           (p.window_left >= 0 && key0 < pos_max - p.window_left);
@@ -412,10 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float alpha = 1.f;
       bool rescale = false;
+      bool stop = false;
       auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
         constexpr bool M = decltype(masked_tag)::value;
         uint32_t sr[128];
         tmem_ld_x128(tS, sr);
+        if constexpr (DEC) {
+          tc_fence_before();
+          mbar_arrive(bar_s_free);  // the S buffer may take S(jj + 1)
+        }
         if constexpr (M) {  // masked keys: -inf for the max (+inf for the min), p = 0 below
           const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
 #pragma unroll
@@ -436,6 +483,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        if constexpr (DEC) {  // the P columns were read by P·V(jj - 1)
+          if (jj >= 1) {
+            if (!mbar_wait_warp(bar_pv_done(0), (jj - 1) & 1u, wc, kSiteSmxPvDone)) {
+              stop = true;
+              return;
+            }
+            tc_fence_after();
+          }
+        }
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -481,10 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // split P each 64-key half h as [hi 32 columns | lo 32 columns] at 64h.
           if constexpr (kSplitP) {
             const int hh = c0 >> 6, cl = c0 & 63;
-            tmem_st_x16(tS + 64 * hh + (cl >> 1), pk);
-            tmem_st_x16(tS + 64 * hh + 32 + (cl >> 1), pk_lo);
+            tmem_st_x16(tP + 64 * hh + (cl >> 1), pk);
+            tmem_st_x16(tP + 64 * hh + 32 + (cl >> 1), pk_lo);
           } else {
-            tmem_st_x16(tS + (c0 >> 1), pk);
+            tmem_st_x16(tP + (c0 >> 1), pk);
           }
         }
         l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
@@ -493,10 +549,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         block_body(std::true_type{});
       else
         block_body(std::false_type{});
+      if (stop) {
+        ok = false;
+        break;
+      }
       // O rescale once the previous P·V (which accumulates into O) is complete;
       // the first block's P·V overwrites O.
       if (__any_sync(0xffffffffu, rescale && jj > 0)) {
-        if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone)) {
+        if (!mbar_wait_warp(bar_pv_done(DEC ? 0 : ((jj - 1) & 1)),
+                            DEC ? ((jj - 1) & 1u) : (((jj - 1) >> 1) & 1u), wc, kSiteSmxPvDone)) {
           ok = false;
           break;
         }
@@ -583,82 +644,100 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Combines the splits of each row: with L_s the partial log2-sum-exp of split s,
-// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One warp per row: lanes take
-// the splits 32 at a time for the log-sum-exp (shuffle reductions), then every lane
-// owns D / 32 consecutive columns and accumulates the weighted partial rows, with
-// the loads of up to 32 (d = 64) or 16 (d = 128) splits in flight at once.
+// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One CTA (8 warps) per row, so
+// that a decode row's many splits cost one round trip of loads: the CTA reduces the
+// log-sum-exp over the splits, warp w accumulates the weighted partial rows of splits
+// w, w + 8, ... (lane = D / 32 consecutive columns; up to 16 splits' loads in flight
+// per warp), and the 8 partial sums meet in shared memory.
 template <int D, bool BF16, bool OUT_F32>
 __global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
   constexpr int kCols = D / 32;
-  constexpr int kBatch = 64 / kCols;  // splits whose loads are in flight at once (64 registers)
+  constexpr int kWarps = 8;
+  constexpr int kBatch = 16;  // splits per warp whose loads are in flight at once
+  __shared__ float red[kWarps];
+  __shared__ float part[kWarps][D];
   const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
-  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= nrows) return;
+  const size_t row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.splits;
-  float m = -INFINITY;
-  for (int s = lane; s < S; s += 32) m = fmaxf(m, p.lse_part[s * nrows + row]);
+  auto block_reduce = [&](float v, bool is_max) -> float {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = 16; o > 0; o >>= 1) {
+      const float x = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, x) : v + x;
+    }
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    __syncthreads();
+    return r;
+  };
+  float m = -INFINITY;
+  for (int s = threadIdx.x; s < S; s += kWarps * 32) m = fmaxf(m, p.lse_part[s * nrows + row]);
+  m = block_reduce(m, true);
+  float lse2 = -INFINITY;
+  if (m != -INFINITY) {  // CTA-uniform
+    float t = 0.f;
+    for (int s = threadIdx.x; s < S; s += kWarps * 32) t += exp2f(p.lse_part[s * nrows + row] - m);
+    lse2 = m + log2f(block_reduce(t, false));
+  }
   float acc[kCols];
 #pragma unroll
   for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
-  float lse2 = -INFINITY;
-  if (m != -INFINITY) {
-    float total = 0.f;
-    for (int s = lane; s < S; s += 32) total += exp2f(p.lse_part[s * nrows + row] - m);
+  if (lse2 != -INFINITY) {
+    for (int s0 = warp; s0 < S; s0 += kWarps * kBatch) {
+      float wt[kBatch], v[kBatch][kCols];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-    lse2 = m + log2f(total);
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      // lane t holds the weight of split s0 + t
-      const int sl = s0 + lane;
-      const float wl = (sl < S) ? exp2f(p.lse_part[sl * nrows + row] - lse2) : 0.f;
-      const int n = min(32, S - s0);
-      for (int t0 = 0; t0 < n; t0 += kBatch) {
-        float v[kBatch][kCols];
+      for (int u = 0; u < kBatch; ++u) {
+        const int s = s0 + kWarps * u;
+        wt[u] = 0.f;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int s = s0 + t0 + u;
-          if (t0 + u < n) {
-            const float* src = p.o_part + (s * nrows + row) * D + lane * kCols;
-            if constexpr (kCols == 4) {
-              const float4 x = *reinterpret_cast<const float4*>(src);
-              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-            } else {
-              const float2 x = *reinterpret_cast<const float2*>(src);
-              v[u][0] = x.x; v[u][1] = x.y;
-            }
+        for (int c = 0; c < kCols; ++c) v[u][c] = 0.f;
+        if (s < S) {
+          wt[u] = exp2f(p.lse_part[s * nrows + row] - lse2);  // 0 for an empty split
+          const float* src = p.o_part + (s * nrows + row) * D + lane * kCols;
+          if constexpr (kCols == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
           } else {
-#pragma unroll
-            for (int c = 0; c < kCols; ++c) v[u][c] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const float w = __shfl_sync(0xffffffffu, wl, (t0 + u) & 31);
-          if (t0 + u < n && w != 0.f) {  // an empty split has weight 0 (and O_s = 0)
-#pragma unroll
-            for (int c = 0; c < kCols; ++c) acc[c] += w * v[u][c];
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            v[u][0] = x.x; v[u][1] = x.y;
           }
         }
       }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (wt[u] != 0.f) {  // an empty split has weight 0 (and O_s = 0)
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) acc[c] += wt[u] * v[u][c];
+        }
     }
   }
+#pragma unroll
+  for (int c = 0; c < kCols; ++c) part[warp][lane * kCols + c] = acc[c];
+  __syncthreads();
   const int qi = static_cast<int>(row % p.Lq);
   const int h = static_cast<int>((row / p.Lq) % p.Hq);
   const int b = static_cast<int>(row / (static_cast<size_t>(p.Lq) * p.Hq));
-  const size_t o_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * D + lane * kCols;
-  if constexpr (OUT_F32) {
-    float* dst = static_cast<float*>(p.o) + o_off;
+  const size_t o_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * D;
+  for (int c = 2 * threadIdx.x; c < D; c += 2 * kWarps * 32) {  // two columns per thread
+    float o0 = 0.f, o1 = 0.f;
 #pragma unroll
-    for (int c = 0; c < kCols; ++c) dst[c] = acc[c];
-  } else {
-    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + o_off);
-#pragma unroll
-    for (int c = 0; c < kCols; c += 2) dst[c >> 1] = pack2(acc[c], acc[c + 1], BF16);
+    for (int w = 0; w < kWarps; ++w) {
+      o0 += part[w][c];
+      o1 += part[w][c + 1];
+    }
+    if constexpr (OUT_F32) {
+      float* dst = static_cast<float*>(p.o) + o_off + c;
+      dst[0] = o0;
+      dst[1] = o1;
+    } else {
+      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + o_off + c) = pack2(o0, o1, BF16);
+    }
   }
-  if (lane == 0 && p.lse != nullptr)
+  if (threadIdx.x == 0 && p.lse != nullptr)
     p.lse[row] = (lse2 == -INFINITY) ? -INFINITY : lse2 * 0.69314718055994531f;
 }
 

@@ -58,6 +58,16 @@ cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
 // The decode-shaped forward (and, when p.splits > 1, its merge kernel).
 cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
+// The one-tile kernel's decode mode (one softmax warp, two CTAs per SM): fp16 at
+// d = 64 with at most 32 rows per tile (q_per_tile * group). Its split count targets
+// two CTAs per SM (kv_decode_shape: the same rule without the dtype, which the split
+// count of attn_fwd_kv_num_splits cannot see).
+inline bool kv_decode_shape(int d, int q_per_tile, int group) {
+  return d == 64 && q_per_tile * group <= 32;
+}
+inline bool kv_decode_mode(int d, bool bf16, int q_per_tile, int group) {
+  return !bf16 && kv_decode_shape(d, q_per_tile, group);
+}
 // The same over a paged K/V cache (a.p.block_table, seq_lens, page_size, ... set).
 cudaError_t launch_kv_paged(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // The float8 forward: the V transpose, then the attention kernel.
