@@ -496,8 +496,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t pk[16];
-          uint32_t pk_lo[16];
-          uint32_t prev = 0;
+          [[maybe_unused]] uint32_t pk_lo[16];  // bf16: the low halves of split P
+          [[maybe_unused]] uint32_t prev = 0;   // fp16: the pair summed with the next
 #pragma unroll
           for (int c = c0; c < c0 + 32; c += 2) {
             const float2 x = __ffma2_rn(
