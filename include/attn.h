@@ -29,6 +29,12 @@
  * wait that ran out) are recorded in the workspace status word and reported by
  * attn_fwd_sync_status.
  *
+ * Graphs. Every entry point may be captured into a CUDA graph (stream capture): the
+ * capture records the kernels with the call's pointers and sizes, so a replay
+ * recomputes the result from whatever the same buffers hold, without the host-side
+ * preparation of a call (checks, tensor-map encoding). Make one call of the entry
+ * point on the device before the capture starts (one-time function setup).
+ *
  * Threading. Calls are thread-safe; concurrent calls must use distinct workspaces.
  */
 #ifndef EXACT_ATTN_H
