@@ -51,7 +51,7 @@ def _defines():
     softmax columns whose exp2 runs on the FMA-pipe polynomial; default 0),
     EX19_SEPARATE_P (d = 64 fp16 keeps P in its own TMEM columns; default 1),
     EX19_SOFTMAX_F2 (paired fp32 FMA / adds in the softmax; default 1),
-    EX19_MAX3 (3-input max instruction in the row max; default 0),
+    EX19_MAX3 (3-input max instruction in the row max; default 1),
     EX19_SUSPEND_NS (sleep hint of the mbarrier polls in ns; default 1e6, 0 = none),
     EX19_TRACE (CTA 0 records a clock64 timeline of its first unit in the workspace; default 0),
     EX19_ONEPASS (the softmax reads S from TMEM once instead of twice; default 1),

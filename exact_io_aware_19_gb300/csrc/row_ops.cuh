@@ -10,7 +10,7 @@
 #include "sm103_ptx.cuh"
 
 #ifndef EX19_MAX3
-#define EX19_MAX3 0  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
+#define EX19_MAX3 1  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
 #endif
 
 namespace ex19 {
