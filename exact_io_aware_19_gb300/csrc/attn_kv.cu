@@ -25,7 +25,13 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
   e = cudaGetLastError();
   if (e != cudaSuccess || a.p.splits <= 1) return e;
   const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
-  kv::attn_kv_merge_kernel<D, BF16, OUT_F32><<<static_cast<unsigned>(rows), 256, 0, a.stream>>>(a.p);
+  int sms = 148;  // `dev` is the current device (above)
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (rows <= sms)  // few rows (decode): one CTA per row
+    kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 8><<<static_cast<unsigned>(rows), 256, 0, a.stream>>>(a.p);
+  else  // many rows: one warp per row
+    kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 1>
+        <<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(a.p);
   return cudaGetLastError();
 }
 

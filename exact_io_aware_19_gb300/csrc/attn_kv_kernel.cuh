@@ -644,54 +644,64 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
 }
 
 // Combines the splits of each row: with L_s the partial log2-sum-exp of split s,
-// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. One CTA (8 warps) per row, so
-// that a decode row's many splits cost one round trip of loads: the CTA reduces the
-// log-sum-exp over the splits, warp w accumulates the weighted partial rows of splits
-// w, w + 8, ... (lane = D / 32 consecutive columns; up to 16 splits' loads in flight
-// per warp), and the 8 partial sums meet in shared memory.
-template <int D, bool BF16, bool OUT_F32>
+// L = log2 Σ_s 2^(L_s) and O = Σ_s 2^(L_s − L) · O_s. WPR warps per row, 8 warps per
+// CTA: a decode call has a few rows and many splits, and one CTA per row (WPR = 8)
+// makes that one round trip of loads; a square problem cut into splits has many rows
+// and few splits, and one warp per row (WPR = 1) keeps the grid small. The warps of a
+// row reduce the log-sum-exp over the splits, warp w of the row accumulates the
+// weighted partial rows of splits w, w + WPR, ... (lane = D / 32 consecutive columns;
+// up to 16 splits' loads in flight), and the partial sums meet in shared memory.
+template <int D, bool BF16, bool OUT_F32, int WPR>
 __global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
+  static_assert(WPR == 1 || WPR == 8, "one warp or one CTA per row");
   constexpr int kCols = D / 32;
   constexpr int kWarps = 8;
-  constexpr int kBatch = 16;  // splits per warp whose loads are in flight at once
+  constexpr int kBatch = (WPR == 1) ? 8 : 16;  // splits per warp whose loads are in flight at once
   __shared__ float red[kWarps];
   __shared__ float part[kWarps][D];
   const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
-  const size_t row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = static_cast<size_t>(blockIdx.x) * (kWarps / WPR) + warp / WPR;
+  const int sw = warp % WPR;  // this warp's index among the row's warps
+  if constexpr (WPR == 1) {
+    if (row >= nrows) return;  // no CTA-wide barrier in this mode
+  }
   const int S = p.splits;
-  auto block_reduce = [&](float v, bool is_max) -> float {
+  // Reduction over the row's warps (a warp shuffle, then shared memory when WPR = 8).
+  auto row_reduce = [&](float v, bool is_max) -> float {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float x = __shfl_xor_sync(0xffffffffu, v, o);
       v = is_max ? fmaxf(v, x) : v + x;
     }
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float r = red[0];
+    if constexpr (WPR > 1) {
+      if (lane == 0) red[warp] = v;
+      __syncthreads();
+      v = red[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-    __syncthreads();
-    return r;
+      for (int w = 1; w < WPR; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+      __syncthreads();
+    }
+    return v;
   };
   float m = -INFINITY;
-  for (int s = threadIdx.x; s < S; s += kWarps * 32) m = fmaxf(m, p.lse_part[s * nrows + row]);
-  m = block_reduce(m, true);
+  for (int s = sw * 32 + lane; s < S; s += WPR * 32) m = fmaxf(m, p.lse_part[s * nrows + row]);
+  m = row_reduce(m, true);
   float lse2 = -INFINITY;
-  if (m != -INFINITY) {  // CTA-uniform
+  if (m != -INFINITY) {  // uniform over the row's warps
     float t = 0.f;
-    for (int s = threadIdx.x; s < S; s += kWarps * 32) t += exp2f(p.lse_part[s * nrows + row] - m);
-    lse2 = m + log2f(block_reduce(t, false));
+    for (int s = sw * 32 + lane; s < S; s += WPR * 32) t += exp2f(p.lse_part[s * nrows + row] - m);
+    lse2 = m + log2f(row_reduce(t, false));
   }
   float acc[kCols];
 #pragma unroll
   for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
   if (lse2 != -INFINITY) {
-    for (int s0 = warp; s0 < S; s0 += kWarps * kBatch) {
+    for (int s0 = sw; s0 < S; s0 += WPR * kBatch) {
       float wt[kBatch], v[kBatch][kCols];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int s = s0 + kWarps * u;
+        const int s = s0 + WPR * u;
         wt[u] = 0.f;
 #pragma unroll
         for (int c = 0; c < kCols; ++c) v[u][c] = 0.f;
@@ -715,29 +725,34 @@ __global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
         }
     }
   }
+  if constexpr (WPR > 1) {
 #pragma unroll
-  for (int c = 0; c < kCols; ++c) part[warp][lane * kCols + c] = acc[c];
-  __syncthreads();
+    for (int c = 0; c < kCols; ++c) part[warp][lane * kCols + c] = acc[c];
+    __syncthreads();
+    if (warp != 0) return;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < WPR; ++w) t += part[w][lane * kCols + c];
+      acc[c] = t;
+    }
+  }
+  // the row's first warp writes O (lane = kCols consecutive columns) and the LSE
   const int qi = static_cast<int>(row % p.Lq);
   const int h = static_cast<int>((row / p.Lq) % p.Hq);
   const int b = static_cast<int>(row / (static_cast<size_t>(p.Lq) * p.Hq));
-  const size_t o_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * D;
-  for (int c = 2 * threadIdx.x; c < D; c += 2 * kWarps * 32) {  // two columns per thread
-    float o0 = 0.f, o1 = 0.f;
+  const size_t o_off = ((static_cast<size_t>(b) * p.Lq + qi) * p.Hq + h) * D + lane * kCols;
+  if constexpr (OUT_F32) {
+    float* dst = static_cast<float*>(p.o) + o_off;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      o0 += part[w][c];
-      o1 += part[w][c + 1];
-    }
-    if constexpr (OUT_F32) {
-      float* dst = static_cast<float*>(p.o) + o_off + c;
-      dst[0] = o0;
-      dst[1] = o1;
-    } else {
-      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + o_off + c) = pack2(o0, o1, BF16);
-    }
+    for (int c = 0; c < kCols; ++c) dst[c] = acc[c];
+  } else {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + o_off);
+#pragma unroll
+    for (int c = 0; c < kCols; c += 2) dst[c >> 1] = pack2(acc[c], acc[c + 1], BF16);
   }
-  if (threadIdx.x == 0 && p.lse != nullptr)
+  if (lane == 0 && p.lse != nullptr)
     p.lse[row] = (lse2 == -INFINITY) ? -INFINITY : lse2 * 0.69314718055994531f;
 }
 
