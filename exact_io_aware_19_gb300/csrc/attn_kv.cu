@@ -27,12 +27,23 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
   const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
   int sms = 148;  // `dev` is the current device (above)
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (rows <= sms)  // few rows (decode): one CTA per row
-    kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 8><<<static_cast<unsigned>(rows), 256, 0, a.stream>>>(a.p);
-  else  // many rows: one warp per row
-    kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 1>
-        <<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(a.p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the merge's launch overlaps the end of the split
+  // kernel (the merge waits for it with griddepcontrol.wait before reading).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (rows <= sms) {  // few rows (decode): one CTA per row
+    cfg.gridDim = dim3(static_cast<unsigned>(rows));
+    return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 8>, a.p);
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));  // many rows: one warp per row
+  return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 1>, a.p);
 }
 
 template <int D, bool PAGED>

@@ -654,6 +654,9 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
 template <int D, bool BF16, bool OUT_F32, int WPR>
 __global__ void __launch_bounds__(256) attn_kv_merge_kernel(const KvParams p) {
   static_assert(WPR == 1 || WPR == 8, "one warp or one CTA per row");
+  // Launched as a programmatic dependent of the split kernel: its CTAs may start
+  // while that kernel finishes; the partial results are read only after it is done.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kCols = D / 32;
   constexpr int kWarps = 8;
   constexpr int kBatch = (WPR == 1) ? 8 : 16;  // splits per warp whose loads are in flight at once
