@@ -19,15 +19,21 @@
 //     g * group + r % group. One TMA box {64 of d, group heads, q_per_tile rows}
 //     lands the tile in shared memory in exactly that order, so K and V stream
 //     once per group instead of once per query head.
-//   * warp 4 (producer): TMA loads of Q and of K_j, V_j into a ring of slots.
-//   * warp 5 (MMA): one elected lane issues every tcgen05.mma. Block j's
+//   * warp 8 (producer): TMA loads of Q and of K_j, V_j into a ring of slots.
+//   * warp 9 (MMA): one elected lane issues every tcgen05.mma. Block j's
 //     S = Q K_jᵀ goes to TMEM buffer j mod 2 (128 fp32 columns); the softmax
-//     overwrites its first columns with P; O += P V_j reads P back from there.
+//     writes P over the scores it has read (keys 64h .. 64h + 63 of half h from
+//     column 64h); O += P V_j reads P back from there.
 //     S(j + 2) is issued after P·V(j), so buffer reuse needs no barrier (MMAs of
 //     one thread run in issue order), and S(j + 1) runs under the softmax of j.
-//   * warps 0-3 (softmax): one thread per tile row (TMEM lane), as in the square
-//     kernel: running max m (base-2 units) and sum l, P = 2^(x - m), conditional
-//     O rescale, and at the end O / l and the log-sum-exp.
+//   * warps 0-7 (softmax): two threads per tile row. Warp w reads TMEM lanes
+//     32 (w mod 4) .. + 31 and the key half w / 4 (64 of the block's 128 scores),
+//     so each SM sub-partition runs two softmax warps with half a row's work each.
+//     The two halves of a row trade their partial maxima through shared memory
+//     (an mbarrier per warp pair and buffer, bounded waits) and both take the same
+//     reference max; each keeps its own running sum l, P = 2^(x - m) for its keys
+//     and the O rescale of its half of the columns; the halves' sums meet once in
+//     the epilogue, which writes O / l and the log-sum-exp.
 //   * Paged K/V cache ("What is memory-efficient attention ...", section 3: the
 //     cache is cut into fixed-size blocks of tokens stored anywhere, and a page
 //     table maps each sequence's logical blocks to physical pages): a 128-key block
@@ -73,7 +79,8 @@ constexpr int kBN = 128;             // keys per K/V block
 // Warp roles and TMEM columns of the two modes.
 template <bool DEC>
 struct KvRoles {
-  static constexpr int kSmxWarps = DEC ? 1 : 4;               // softmax warps (32 rows each)
+  static constexpr int kSmxWarps = DEC ? 1 : 8;               // softmax warps (32 rows each)
+  static constexpr int kHalves = DEC ? 1 : 2;                  // softmax threads per row
   static constexpr int kThreads = 32 * (kSmxWarps + 2);        // + producer warp + MMA warp
   static constexpr int kProducerWarp = kSmxWarps;
   static constexpr int kMmaWarp = kSmxWarps + 1;
@@ -89,6 +96,7 @@ enum : uint32_t {
   kSiteMmaQFull = 0x60001, kSiteMmaKFull = 0x60002, kSiteMmaVFull = 0x60003,
   kSiteMmaPFull = 0x60004, kSiteMmaDrain = 0x60005,
   kSiteSmxSFull = 0x70001, kSiteSmxOFull = 0x70002, kSiteSmxPvDone = 0x70003,
+  kSiteSmxExchange = 0x70004,
   kSiteDrainLoads = 0x80001,
   kSiteBadSeqLen = 0x90001,  // a paged sequence length outside [Lq, max_seq_len]
 };
@@ -103,10 +111,13 @@ struct KvGeometry {
   static constexpr int kOffKV = kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   // barriers: full[S], empty[S], q_full, s_full[2] (DEC: s_full, s_free), p_full[2],
-  // pv_done[2], o_full, drain
-  static constexpr int kNumBars = 2 * kSlots + 9;
+  // pv_done[2], o_full, drain, exchange[4 warp pairs][2 buffers]
+  static constexpr int kNumBars = 2 * kSlots + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemUsed = kOffMisc + 16;
+  // the two halves of a row trade one float per round: [2 buffers][2 halves][128 rows]
+  static constexpr int kOffX = kOffMisc + 16;
+  static constexpr int kXBytes = DEC ? 0 : 2 * 2 * kBM * 4;
+  static constexpr int kSmemUsed = kOffX + kXBytes;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
 };
 
@@ -192,6 +203,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
   auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
   const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
   const uint32_t bar_drain = bars + 8u * (2 * S + 8);
+  // exchange between the two softmax warps of lane quarter q, buffer b
+  auto bar_x = [&](int q, uint32_t b) { return bars + 8u * (2 * S + 9 + 2 * q + b); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
 
@@ -213,6 +226,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     }
     mbar_init(bar_o_full, 1);
     mbar_init(bar_drain, 1);
+    for (int q = 0; q < 4; ++q)
+      for (uint32_t b = 0; b < 2; ++b) mbar_init(bar_x(q, b), 64);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -370,7 +385,9 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         const uint64_t dvs = dv + ((slot_of(vidx) * G::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t pcol = kSplitP ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
+          // keys 16 kk .. 16 kk + 15: DEC P is packed from column 0; otherwise each
+          // 64-key half h sits at column 64 h (bf16: hi there, lo 32 columns on)
+          const uint32_t pcol = DEC ? kk * 8 : (kk >> 2) * 64 + (kk & 3) * 8;
           mma_ts_elect(mO, mP + pcol, dvs + ((kk * 2048) >> 4), idesc_o,
                        (jj == 0 && kk == 0) ? 0u : 1u);
         }
@@ -416,7 +433,13 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     mbar_wait_drain(bar_drain, 0, wc, kSiteMmaDrain);
   } else {
     // -------------------------------------------------------- softmax warps
-    const int rho = warp * 32 + lane;  // row of the tile
+    constexpr int kHalves = R::kHalves;
+    constexpr int kCols = kBN / kHalves;  // scores of a block per softmax thread
+    constexpr int kOCols = D / kHalves;   // O columns this thread rescales and writes
+    const int quarter = warp & 3;         // TMEM lane quarter of this warp
+    const int ch = warp >> 2;             // key half of this warp (0 in DEC)
+    const int col0 = ch * kCols;          // first score column of this thread
+    const int rho = quarter * 32 + lane;  // row of the tile
     const bool row_ok = !it.bad && rho < (it.i1 - it.i0) * p.group;
     const int qi = it.i0 + rho / p.group;  // query position (may be >= Lq for unused rows)
     const int h = it.g * p.group + rho % p.group;
@@ -425,21 +448,35 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     const int pos = off + qi;
     const int pos_min = off + it.i0, pos_max = off + it.i1 - 1;
     const int wr = right_bound(p);
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tO = tmem_base + lane_off + kColO;
     const float C = p.score_log2;
     const bool neg = p.negate_scores != 0;
     const float Cs = neg ? -C : C;  // x = Cs · s carries the sign of the scale
-    float m_ref = -INFINITY;        // reference max (base-2 units)
-    float l = 0.f;                  // running sum of P
+    float m_ref = -INFINITY;        // reference max (base-2 units), the same in both halves
+    float l = 0.f;                  // running sum of this thread's P
     bool ok = true;
+    // Round n of the two halves of a row: each stores its value, arrives on the
+    // pair's barrier of buffer n mod 2 and, once both have, reads the other's. A
+    // buffer is written again two rounds later, after the round in between has
+    // completed, which needs the other half's arrival, made after its read.
+    float* xbuf = reinterpret_cast<float*>(smem + G::kOffX);
+    auto exchange = [&](uint32_t n, float v, float& other) -> bool {
+      const uint32_t b = n & 1u;
+      xbuf[(b * 2 + ch) * kBM + rho] = v;
+      mbar_arrive(bar_x(quarter, b));
+      if (!mbar_wait_warp(bar_x(quarter, b), (n >> 1) & 1u, wc, kSiteSmxExchange)) return false;
+      other = xbuf[(b * 2 + (ch ^ 1)) * kBM + rho];
+      return true;
+    };
     for (int jj = 0; jj < nblocks; ++jj) {
       const int j = it.lo + jj;
       const uint32_t buf = DEC ? 0u : (jj & 1);
       ok = mbar_wait_warp(bar_s_full(buf), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc, kSiteSmxSFull);
       if (!ok) break;
       tc_fence_after();
-      // S of this block, then P over it (DEC: P in its own columns)
+      // S of this block, then P over the scores this thread has read (DEC: P in its
+      // own columns)
       const uint32_t tS = tmem_base + lane_off + (DEC ? 0u : 128u * buf);
       const uint32_t tP = DEC ? tmem_base + lane_off + R::kColP : tS;
       const int key0 = j * kBN;
@@ -457,8 +494,11 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       bool stop = false;
       auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
         constexpr bool M = decltype(masked_tag)::value;
-        uint32_t sr[128];
-        tmem_ld_x128(tS, sr);
+        uint32_t sr[kCols];
+        if constexpr (kCols == 128)
+          tmem_ld_x128(tS, sr);
+        else
+          tmem_ld_x64(tS + col0, sr);
         if constexpr (DEC) {
           tc_fence_before();
           mbar_arrive(bar_s_free);  // the S buffer may take S(jj + 1)
@@ -466,15 +506,27 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         if constexpr (M) {  // masked keys: -inf for the max (+inf for the min), p = 0 below
           const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < vis_lo || c >= vis_hi) sr[c] = fill;
+          for (int c = 0; c < kCols; ++c)
+            if (col0 + c < vis_lo || col0 + c >= vis_hi) sr[c] = fill;
         }
         float mx;
         {
-          float sv[128];
+          float sv[kCols];
 #pragma unroll
-          for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
-          mx = neg ? -row_min128(sv) : row_max128(sv);
+          for (int c = 0; c < kCols; ++c) sv[c] = __uint_as_float(sr[c]);
+          if constexpr (kCols == 128)
+            mx = neg ? -row_min128(sv) : row_max128(sv);
+          else
+            mx = neg ? -row_min64(sv) : row_max64(sv);
+        }
+        if constexpr (kHalves == 2) {
+          // the row max over both halves, combined in the same order by both
+          float other;
+          if (!exchange(static_cast<uint32_t>(jj), mx, other)) {
+            stop = true;
+            return;
+          }
+          mx = (ch == 0) ? fmaxf(mx, other) : fmaxf(other, mx);
         }
         const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
         if (bm > m_ref + kThresh) {
@@ -494,12 +546,13 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         }
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < kCols; c0 += 32) {
           uint32_t pk[16];
           [[maybe_unused]] uint32_t pk_lo[16];  // bf16: the low halves of split P
           [[maybe_unused]] uint32_t prev = 0;   // fp16: the pair summed with the next
 #pragma unroll
           for (int c = c0; c < c0 + 32; c += 2) {
+            const int cg = col0 + c;  // column within the block
             const float2 x = __ffma2_rn(
                 make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
                 make_float2(Cs, Cs), make_float2(-mu, -mu));
@@ -507,8 +560,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
               __half2 xh = __floats2half2_rn(x.x, x.y);
               uint32_t pp = ex2_f16x2(*reinterpret_cast<uint32_t*>(&xh));
               if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
-                const uint32_t keep = ((c >= vis_lo && c < vis_hi) ? 0x0000FFFFu : 0u) |
-                                      ((c + 1 >= vis_lo && c + 1 < vis_hi) ? 0xFFFF0000u : 0u);
+                const uint32_t keep = ((cg >= vis_lo && cg < vis_hi) ? 0x0000FFFFu : 0u) |
+                                      ((cg + 1 >= vis_lo && cg + 1 < vis_hi) ? 0xFFFF0000u : 0u);
                 pp &= keep;
               }
               pk[(c - c0) >> 1] = pp;
@@ -522,8 +575,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
             } else {
               float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
               if constexpr (M) {
-                p0 = (c >= vis_lo && c < vis_hi) ? p0 : 0.f;
-                p1 = (c + 1 >= vis_lo && c + 1 < vis_hi) ? p1 : 0.f;
+                p0 = (cg >= vis_lo && cg < vis_hi) ? p0 : 0.f;
+                p1 = (cg + 1 >= vis_lo && cg + 1 < vis_hi) ? p1 : 0.f;
               }
               acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
               const uint32_t hi = pack2(p0, p1, BF16);
@@ -533,14 +586,18 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
                     pack2(p0 - low_as_float(hi, BF16), p1 - high_as_float(hi, BF16), BF16);
             }
           }
-          // P over the scores this thread already holds: column c/2 (fp16), or for
-          // split P each 64-key half h as [hi 32 columns | lo 32 columns] at 64h.
+          // P of keys [64 hh, 64 hh + 64) at column 64 hh, over scores this thread has
+          // already read (DEC: packed from column 0 of its own region); split P keeps
+          // [hi 32 columns | lo 32 columns] there.
+          const int cb = col0 + c0;  // first key of this chunk
           if constexpr (kSplitP) {
-            const int hh = c0 >> 6, cl = c0 & 63;
+            const int hh = cb >> 6, cl = cb & 63;
             tmem_st_x16(tP + 64 * hh + (cl >> 1), pk);
             tmem_st_x16(tP + 64 * hh + 32 + (cl >> 1), pk_lo);
+          } else if constexpr (DEC) {
+            tmem_st_x16(tP + (cb >> 1), pk);
           } else {
-            tmem_st_x16(tP + (c0 >> 1), pk);
+            tmem_st_x16(tP + 64 * (cb >> 6) + ((cb & 63) >> 1), pk);
           }
         }
         l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
@@ -553,8 +610,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         ok = false;
         break;
       }
-      // O rescale once the previous P·V (which accumulates into O) is complete;
-      // the first block's P·V overwrites O.
+      // O rescale (this thread's columns) once the previous P·V, which accumulates
+      // into O, is complete; the first block's P·V overwrites O.
       if (__any_sync(0xffffffffu, rescale && jj > 0)) {
         if (!mbar_wait_warp(bar_pv_done(DEC ? 0 : ((jj - 1) & 1)),
                             DEC ? ((jj - 1) & 1u) : (((jj - 1) >> 1) & 1u), wc, kSiteSmxPvDone)) {
@@ -564,7 +621,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         tc_fence_after();
         const float a = (rescale && jj > 0) ? alpha : 1.f;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = ch * kOCols; c0 < (ch + 1) * kOCols; c0 += 32) {
           uint32_t orow[32];
           tmem_ld_x32(tO + c0, orow);
 #pragma unroll
@@ -580,15 +637,24 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteSmxOFull);
       if (ok) tc_fence_after();
     }
+    if constexpr (kHalves == 2) {
+      if (ok) {
+        // the row sum over both halves (one more exchange round), same order in both
+        float other = 0.f;
+        ok = exchange(static_cast<uint32_t>(nblocks), l, other);
+        l = (ch == 0) ? l + other : other + l;
+      }
+    }
     if (ok) {
-      // ---- epilogue: O / l and the log-sum-exp of this row over this split
+      // ---- epilogue: O / l and the log-sum-exp of this row over this split; each
+      // half of the row writes its half of the O columns
       const bool have = nblocks > 0;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const size_t row = (static_cast<size_t>(it.b) * p.Hq + h) * p.Lq + qi;  // LSE index
       const bool partial = p.splits > 1;
       const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = ch * kOCols; c0 < (ch + 1) * kOCols; c0 += 32) {
         uint32_t orow[32];
         if (have) {
           tmem_ld_x32(tO + c0, orow);
@@ -623,7 +689,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
           }
         }
       }
-      if (row_ok) {
+      if (row_ok && ch == 0) {
         const float lse2 = (l > 0.f) ? m_ref + lg2_approx(l) : -INFINITY;  // base 2
         if (partial)
           p.lse_part[static_cast<size_t>(it.split) * nrows + row] = lse2;
