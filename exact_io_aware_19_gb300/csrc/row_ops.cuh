@@ -39,39 +39,6 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
 #endif
 }
 
-// Maximum of a 64-value half row: 8 independent chains (8 values each), then a tree.
-__device__ __forceinline__ float row_max64(const float (&s)[64]) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-#if EX19_MAX3
-    float a = max3f(s[i], s[8 + i], s[16 + i]);
-    a = max3f(a, s[24 + i], s[32 + i]);
-    a = max3f(a, s[40 + i], s[48 + i]);
-    m[i] = fmaxf(a, s[56 + i]);
-#else
-    float a = s[i];
-#pragma unroll
-    for (int k = 8; k < 64; k += 8) a = fmaxf(a, s[k + i]);
-    m[i] = a;
-#endif
-  }
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
-
-// Minimum of a 64-value half row (used when the scale is negative).
-__device__ __forceinline__ float row_min64(const float (&s)[64]) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = s[i];
-#pragma unroll
-    for (int k = 8; k < 64; k += 8) a = fminf(a, s[k + i]);
-    m[i] = a;
-  }
-  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
-}
-
 // Minimum of a 128-value row (used when the scale is negative).
 __device__ __forceinline__ float row_min128(const float (&s)[128]) {
   float m[8];
