@@ -21,23 +21,28 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<a.grid, kv::KvRoles<DEC>::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, a.p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.p.splits <= 1) return e;
-  const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
-  int sms = 148;  // `dev` is the current device (above)
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // Programmatic dependent launch: the merge's launch overlaps the end of the split
-  // kernel (the merge waits for it with griddepcontrol.wait before reading).
+  // Both kernels are programmatic dependent launches: each may start while the
+  // previous kernel on the stream finishes, and waits for it (griddepcontrol.wait)
+  // before touching global memory. The split kernel's prologue (barriers, TMEM
+  // allocation, tensor-map prefetch) and the merge's launch overlap the kernel
+  // before them.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = a.grid;
+  cfg.blockDim = dim3(kv::KvRoles<DEC>::kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_v, a.p);
+  if (e != cudaSuccess || a.p.splits <= 1) return e;
+  const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
+  int sms = 148;  // `dev` is the current device (above)
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
   if (rows <= sms) {  // few rows (decode): one CTA per row
     cfg.gridDim = dim3(static_cast<unsigned>(rows));
     return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 8>, a.p);
