@@ -28,8 +28,8 @@ cudaError_t launch_fp8_one(const Fp8LaunchArgs& a) {
 }  // namespace
 
 cudaError_t launch_fp8(bool out_f32, const Fp8LaunchArgs& a) {
-  const dim3 tgrid((a.Lp + 63) / 64, a.p.Hkv, a.p.B);
-  fp8::attn_fp8_transpose_v<<<tgrid, 256, 0, a.stream>>>(a.v, a.vt, a.p.Lk, a.p.Hkv, a.Lp);
+  const dim3 tgrid((a.Lp + 127) / 128, a.p.Hkv, a.p.B);
+  fp8::attn_fp8_transpose_v<<<tgrid, 128, 0, a.stream>>>(a.v, a.vt, a.p.Lk, a.p.Hkv, a.Lp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return out_f32 ? launch_fp8_one<true>(a) : launch_fp8_one<false>(a);

@@ -473,35 +473,42 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // Vᵀ for the P·V MMA: v [B, L, Hkv, 64] e4m3 -> vt [B, Hkv, 64, Lp] (keys contiguous,
-// Lp = L rounded up to 16; keys L .. Lp-1 are zero). One CTA per (64 keys, head,
-// batch) through a 64 x 64-byte tile in shared memory.
-__global__ void __launch_bounds__(256) attn_fp8_transpose_v(const uint8_t* __restrict__ v,
+// Lp = L rounded up to 16; keys L .. Lp-1 are zero). One CTA of 4 warps per (128 keys,
+// head, batch): warp w moves bytes 16w .. 16w + 15 of d, lane l keys 4l .. 4l + 3.
+// A lane loads its 4 keys' 16-byte pieces, transposes each 4 x 4 byte block in
+// registers (byte permutes) and stores 16 words, one per d row: the warp's 32 lanes
+// write 128 consecutive bytes of that row.
+__global__ void __launch_bounds__(128) attn_fp8_transpose_v(const uint8_t* __restrict__ v,
                                                             uint8_t* __restrict__ vt, int L,
                                                             int Hkv, int Lp) {
-  __shared__ uint8_t tile[64][64 + 4];
-  const int k0 = blockIdx.x * 64, g = blockIdx.y, b = blockIdx.z;
-  const int t = threadIdx.x;
-  // load: 64 keys x 64 bytes, 16 bytes per thread
-  {
-    const int key = t >> 2, c16 = (t & 3) * 16;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = blockIdx.x * 128 + 4 * lane;  // first key of this lane (Lp is a multiple of 4)
+  if (k >= Lp) return;
+  uint32_t a[4][4];  // a[i][q]: bytes 16w + 4q .. + 3 of key k + i
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (k0 + key < L)
-      val = *reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * L + k0 + key) * Hkv + g) * 64 + c16);
-    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
-#pragma unroll
-    for (int u = 0; u < 16; ++u) tile[key][c16 + u] = static_cast<uint8_t>(w[u >> 2] >> (8 * (u & 3)));
+    if (k + i < L)
+      val = *reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * L + k + i) * Hkv + g) * 64 + 16 * w);
+    a[i][0] = val.x;
+    a[i][1] = val.y;
+    a[i][2] = val.z;
+    a[i][3] = val.w;
   }
-  __syncthreads();
-  // store: 64 rows (d) x 64 keys, 16 keys per thread
-  {
-    const int dd = t >> 2, kq = (t & 3) * 16;
-    if (k0 + kq < Lp) {
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
+  uint8_t* dst = vt + ((static_cast<size_t>(b) * Hkv + g) * 64 + 16 * w) * Lp + k;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) w[u >> 2] |= static_cast<uint32_t>(tile[kq + u][dd]) << (8 * (u & 3));
-      *reinterpret_cast<uint4*>(vt + ((static_cast<size_t>(b) * Hkv + g) * 64 + dd) * Lp + k0 + kq) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-    }
+  for (int q = 0; q < 4; ++q) {
+    // 4 x 4 byte transpose: t0 .. t3 pair up the keys' bytes, col[e] = byte e of keys 0 .. 3
+    const uint32_t t0 = __byte_perm(a[0][q], a[1][q], 0x5140);  // k0.b0 k1.b0 k0.b1 k1.b1
+    const uint32_t t1 = __byte_perm(a[2][q], a[3][q], 0x5140);  // k2.b0 k3.b0 k2.b1 k3.b1
+    const uint32_t t2 = __byte_perm(a[0][q], a[1][q], 0x7362);  // k0.b2 k1.b2 k0.b3 k1.b3
+    const uint32_t t3 = __byte_perm(a[2][q], a[3][q], 0x7362);  // k2.b2 k3.b2 k2.b3 k3.b3
+    const uint32_t col[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632),
+                             __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(4 * q + e) * Lp) = col[e];
   }
 }
 
