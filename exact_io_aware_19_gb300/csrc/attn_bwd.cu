@@ -35,11 +35,24 @@ cudaError_t launch_bwd_one(const BwdLaunchArgs& a) {
   auto kdkdv = bwd::attn_bwd_dkdv_kernel<D, BF16, OUT_F32>;
   if ((e = set_smem_once(kdq, smem, conf_dq)) != cudaSuccess) return e;
   if ((e = set_smem_once(kdkdv, smem, conf_dkdv)) != cudaSuccess) return e;
-  kdq<<<a.grid_dq, bwd::kThreads, smem, a.stream>>>(*a.tm_qp, *a.tm_dop, *a.tm_k, *a.tm_v, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kdkdv<<<a.grid_dkdv, bwd::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_do, *a.tm_k, *a.tm_v,
-                                                        *a.tm_lse2, *a.tm_dsum, p);
-  return cudaGetLastError();
+  // The dQ and dK / dV kernels are programmatic dependent launches: each may start
+  // (barriers, TMEM allocation) as the kernel before it finishes, and waits for it
+  // with griddepcontrol.wait before reading global memory.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(bwd::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = a.grid_dq;
+  if ((e = cudaLaunchKernelEx(&cfg, kdq, *a.tm_qp, *a.tm_dop, *a.tm_k, *a.tm_v, p)) != cudaSuccess)
+    return e;
+  cfg.gridDim = a.grid_dkdv;
+  return cudaLaunchKernelEx(&cfg, kdkdv, *a.tm_q, *a.tm_do, *a.tm_k, *a.tm_v, *a.tm_lse2, *a.tm_dsum,
+                            p);
 }
 
 template <int D>

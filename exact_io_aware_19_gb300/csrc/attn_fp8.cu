@@ -21,8 +21,19 @@ cudaError_t launch_fp8_one(const Fp8LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<a.grid, fp8::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_vt, a.p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the prologue (barriers, TMEM allocation) overlaps
+  // the end of the V transpose; the kernel waits for it before any global access.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = a.grid;
+  cfg.blockDim = dim3(fp8::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_vt, a.p);
 }
 
 }  // namespace

@@ -181,6 +181,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent of the V transpose: Vᵀ (and everything
+  // before it on the stream) is complete and visible past this point.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   WaitCtl wc;
   wc.abort_flag = abort_flag;
