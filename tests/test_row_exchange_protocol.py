@@ -1,18 +1,19 @@
-"""Host-side model of the one-tile kernel's row-half exchange (no GPU).
+"""Host-side model of the one-tile kernel's row-part exchange (no GPU).
 
 In attn_kv_sm103_kernel two softmax warps share each row of a tile: per key block
-(and once more in the epilogue) each half stores one float in shared memory
-(buffer n mod 2, its own half), arrives on the pair's mbarrier of that buffer and,
-once the phase completes, reads the other half's value. This test runs that
-protocol for two agents under random interleavings with mbarrier semantics
-(count 2, phases completed by arrivals, parity waits) and checks:
+(and once more in the epilogue) each part stores one float in shared memory
+(buffer n mod 2, its own slot), arrives on the lane quarter's mbarrier of that
+buffer and, once the phase completes, reads the other part's value. This test runs
+that protocol for R agents (R = 2, and 4 for a row split four ways) under random
+interleavings with mbarrier semantics (count R, phases completed by arrivals,
+parity waits) and checks:
 
   * every round ends (no deadlock) and every wait sees exactly the phase it means
     (no parity aliasing: a waiter never falls two phases behind);
-  * every read returns the partner's value of the same round (a buffer is never
-    rewritten before the partner has read it);
-  * when one half gives up (a timed-out wait elsewhere sets the abort flag), the
-    other's bounded wait returns instead of blocking.
+  * every read returns the other parts' values of the same round (a buffer is
+    never rewritten before every part has read it);
+  * when one part gives up (a timed-out wait elsewhere sets the abort flag), the
+    others' bounded waits return instead of blocking.
 
 A mutant with a single buffer must fail the race check, so the model can tell a
 broken protocol from a sound one.
@@ -46,32 +47,30 @@ def value(n, ch):
     return 1000 * n + ch
 
 
-def run(rounds, seed, buffers=2, abort_at=None):
-    """Run both halves to completion under a seeded random schedule.
+def run(rounds, seed, buffers=2, abort_at=None, parts=2):
+    """Run every part to completion under a seeded random schedule.
 
-    Returns (finished, reads): finished[ch] is True when the half completed all
-    rounds, reads[ch] the list of (round, value read).
+    Returns (finished, reads): finished[ch] is True when part ch completed all
+    rounds, reads[ch] the list of (round, tuple of the other parts' values read).
     """
     rng = random.Random(seed)
-    bars = [MBarrier(2) for _ in range(buffers)]
+    bars = [MBarrier(parts) for _ in range(buffers)]
     xbuf = {}
     abort = [False]
     # per agent: round n and step (0 store, 1 arrive, 2 wait, 3 read)
-    state = [[0, 0], [0, 0]]
-    done = [False, False]
-    finished = [False, False]
-    reads = [[], []]
+    state = [[0, 0] for _ in range(parts)]
+    done = [False] * parts
+    finished = [False] * parts
+    reads = [[] for _ in range(parts)]
     stalled = 0
     while not all(done):
-        ch = rng.randrange(2)
-        if done[ch]:
-            ch ^= 1
+        ch = rng.choice([c for c in range(parts) if not done[c]])
         n, step = state[ch]
         if n == rounds:
             done[ch] = finished[ch] = True
             continue
         if abort_at is not None and ch == abort_at[0] and n == abort_at[1] and step == 0:
-            abort[0] = True  # this half's wait elsewhere timed out: it leaves its loop
+            abort[0] = True  # this part's wait elsewhere timed out: it leaves its loop
             done[ch] = True
             continue
         b = n % buffers
@@ -85,14 +84,14 @@ def run(rounds, seed, buffers=2, abort_at=None):
             if bars[b].test_wait(want):
                 # the completed phase must be this round's, not one two phases on
                 assert bars[b].phase == n // buffers + 1, (
-                    f"half {ch} round {n}: barrier {b} at phase {bars[b].phase}")
+                    f"part {ch} round {n}: barrier {b} at phase {bars[b].phase}")
             elif abort[0]:
                 done[ch] = True  # the bounded wait returns on the abort flag
                 continue
             else:
                 progressed = False
         else:
-            reads[ch].append((n, xbuf[(b, ch ^ 1)]))
+            reads[ch].append((n, tuple(xbuf[(b, o)] for o in range(parts) if o != ch)))
         if progressed:
             stalled = 0
             step += 1
@@ -105,41 +104,48 @@ def run(rounds, seed, buffers=2, abort_at=None):
     return finished, reads
 
 
+def expected(rounds, ch, parts):
+    return [(n, tuple(value(n, o) for o in range(parts) if o != ch)) for n in range(rounds)]
+
+
+@pytest.mark.parametrize("parts", [2, 4])
 @pytest.mark.parametrize("rounds", [1, 2, 3, 8, 33])
-def test_exchange_completes_and_reads_partner_value(rounds):
+def test_exchange_completes_and_reads_partner_values(rounds, parts):
     for seed in range(300):
-        finished, reads = run(rounds, seed)
-        assert finished == [True, True]
-        for ch in (0, 1):
-            assert reads[ch] == [(n, value(n, ch ^ 1)) for n in range(rounds)], (seed, ch)
+        finished, reads = run(rounds, seed, parts=parts)
+        assert finished == [True] * parts
+        for ch in range(parts):
+            assert reads[ch] == expected(rounds, ch, parts), (seed, ch)
 
 
-def test_abort_releases_the_other_half():
+@pytest.mark.parametrize("parts", [2, 4])
+def test_abort_releases_the_other_parts(parts):
     for seed in range(300):
         r = random.Random(seed)
         rounds = r.randrange(2, 12)
-        who, when = r.randrange(2), r.randrange(rounds)
-        finished, reads = run(rounds, seed, abort_at=(who, when))
+        who, when = r.randrange(parts), r.randrange(rounds)
+        finished, reads = run(rounds, seed, abort_at=(who, when), parts=parts)
         assert not finished[who]
-        # the other half either finished (it was ahead) or returned at a wait
-        for n, v in reads[who ^ 1]:
-            if n < when:
-                assert v == value(n, who)
+        # the others either finished (they were ahead) or returned at a wait
+        for ch in range(parts):
+            if ch != who:
+                for n, vals in reads[ch]:
+                    if n < when:
+                        assert vals == expected(rounds, ch, parts)[n][1]
 
 
-def test_single_buffer_mutant_is_caught():
-    """With one buffer a fast half can overwrite its value before the slow half has
+@pytest.mark.parametrize("parts", [2, 4])
+def test_single_buffer_mutant_is_caught(parts):
+    """With one buffer a fast part can overwrite its value before a slow part has
     read it (or the waits alias); some schedule must expose that."""
     caught = False
     for seed in range(500):
         try:
-            finished, reads = run(8, seed, buffers=1)
+            finished, reads = run(8, seed, buffers=1, parts=parts)
         except AssertionError:
             caught = True
             break
-        for ch in (0, 1):
-            if reads[ch] != [(n, value(n, ch ^ 1)) for n in range(8)]:
-                caught = True
-        if caught:
+        if any(reads[ch] != expected(8, ch, parts) for ch in range(parts)):
+            caught = True
             break
     assert caught
