@@ -1,0 +1,277 @@
+"""Host-side model of the one-tile kernel's whole barrier protocol (no GPU).
+
+attn_kv_sm103_kernel coordinates a TMA producer, an MMA-issuing warp and the
+softmax warps through mbarriers. This test replays that protocol, role by role,
+under random interleavings:
+
+  * the producer waits for a ring slot's release (`empty`), then issues its copy;
+    copies land in any order and complete the slot's `full` barrier;
+  * the MMA warp waits for K, V and P as the kernel does and issues S = Q Kᵀ and
+    O += P V; the tensor core runs the MMAs of that one thread in issue order, and
+    each commit arrives once every MMA issued before it has finished;
+  * the softmax parts (two per row, or one in decode mode) wait for S, trade their
+    row maxima (exchange rounds), write P, rescale O when the row max moved (after
+    the previous P·V is done), release P and finally read O.
+
+Every wait is checked for parity aliasing (a waiter is never two phases away from
+the phase it means), the run must not deadlock, and each consumer must see the
+data generation it expects: the K or V block of its index in a slot, S(j) or P(j)
+in a TMEM buffer, O holding exactly the P·V products issued so far. Mutants with a
+missing wait must be caught, which shows the checks can fail.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    """mbarrier: `count` arrivals complete a phase; `done` counts completed phases."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.done = name, count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, self.name
+        if self.pending == 0:
+            self.done += 1
+            self.pending = self.count
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+def check(cond, msg):
+    if not cond:
+        raise ProtocolError(msg)
+
+
+def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
+    """One CTA's run over `nb` key blocks. Raises ProtocolError on a violation."""
+    rng = random.Random(seed)
+    parts = 1 if dec else 2
+    full = [Bar(f"full{s}", 1) for s in range(slots)]
+    empty = [Bar(f"empty{s}", 1) for s in range(slots)]
+    q_full = Bar("q_full", 1)
+    nbuf = 1 if dec else 2
+    s_full = [Bar(f"s_full{b}", 1) for b in range(nbuf)]
+    s_free = Bar("s_free", parts)  # decode mode only
+    p_full = [Bar(f"p_full{b}", parts) for b in range(nbuf)]
+    pv_done = [Bar(f"pv_done{b}", 1) for b in range(nbuf)]
+    o_full = Bar("o_full", 1)
+    xbar = [Bar(f"x{b}", parts) for b in range(2)]
+
+    slot_gen = [None] * slots          # which load a ring slot holds
+    consumed = set()                   # loads the MMAs have read
+    # TMEM contents: S buffers (tags per part: the key range each part owns), P region (decode)
+    sbuf = [[None] * parts for _ in range(nbuf)]
+    preg = [None]
+    s_read = set()                     # (jj, part): the part has S(jj) in registers
+    o_count = [0]                      # P·V products accumulated in O
+    o_pending = [0]                    # P·V issued but not finished
+    xdata = {}
+
+    mma_queue = []                     # the tensor core's in-order queue: ops and commits
+    tma_inflight = []                  # copies issued, landing in any order
+
+    def wait(bar, target):
+        """Parity wait for `target` completed phases (the phase target - 1)."""
+        return ("wait", bar, target)
+
+    # ------------------------------------------------------------------ roles
+    def producer():
+        if nb == 0:
+            return
+        tma_inflight.append(("q",))
+        n = 0
+        for _ in range(nb):
+            for _kv in range(2):
+                s = n % slots
+                if mutant != "producer_skips_empty":
+                    yield wait(empty[s], n // slots)
+                tma_inflight.append(("kv", s, n))
+                n += 1
+
+    def mma_warp():
+        if nb == 0:
+            return
+        yield wait(q_full, 1)
+
+        def issue_s(jj):
+            kidx = 2 * jj
+            s = kidx % slots
+            yield wait(full[s], kidx // slots + 1)
+            b = 0 if dec else jj & 1
+            mma_queue.append(("S", jj, s, b))
+            mma_queue.append(("commit", s_full[b]))
+            mma_queue.append(("commit", empty[s]))
+
+        def issue_pv(jj):
+            vidx = 2 * jj + 1
+            s = vidx % slots
+            yield wait(full[s], vidx // slots + 1)
+            b = 0 if dec else jj & 1
+            if mutant != "mma_skips_p_full":
+                yield wait(p_full[b], (jj + 1) if dec else (jj >> 1) + 1)
+            mma_queue.append(("PV", jj, s, b))
+            o_pending[0] += 1
+            mma_queue.append(("commit", pv_done[b]))
+            mma_queue.append(("commit", empty[s]))
+
+        yield from issue_s(0)
+        if dec:
+            for jj in range(nb):
+                if jj + 1 < nb:
+                    if mutant != "mma_skips_s_free":
+                        yield wait(s_free, jj + 1)
+                    yield from issue_s(jj + 1)
+                yield from issue_pv(jj)
+        else:
+            if nb > 1:
+                yield from issue_s(1)
+            for jj in range(nb):
+                yield from issue_pv(jj)
+                if jj + 2 < nb:
+                    yield from issue_s(jj + 2)
+        mma_queue.append(("commit", o_full))
+
+    def softmax(part):
+        def exchange(n):
+            xdata[(n & 1, part)] = (n, part)
+            xbar[n & 1].arrive()
+            yield wait(xbar[n & 1], (n >> 1) + 1)
+            for o in range(parts):
+                check(xdata[(n & 1, o)] == (n, o), f"part {part} round {n} read {xdata[(n & 1, o)]}")
+
+        for jj in range(nb):
+            b = 0 if dec else jj & 1
+            yield wait(s_full[b], (jj + 1) if dec else (jj >> 1) + 1)
+            check(sbuf[b][part] == ("S", jj), f"part {part} reads {sbuf[b][part]} for S({jj})")
+            s_read.add((jj, part))
+            if dec:
+                s_free.arrive()
+            if parts > 1:
+                yield from exchange(jj)
+            if dec and jj >= 1 and mutant != "softmax_skips_pv_done":
+                yield wait(pv_done[0], jj)  # P·V(jj - 1) has read the P region
+            if dec:
+                check(o_pending[0] == 0 or preg[0] is None or o_count[0] >= jj,
+                      f"P({jj}) written while P·V({jj - 1}) may still read it")
+                preg[0] = ("P", jj)
+            else:
+                sbuf[b][part] = ("P", jj)  # over this part's own scores
+            if jj > 0 and rng.random() < rescale_p:
+                bp = 0 if dec else (jj - 1) & 1
+                yield wait(pv_done[bp], jj if dec else ((jj - 1) >> 1) + 1)
+                check(o_pending[0] == 0 and o_count[0] == jj,
+                      f"O rescaled at block {jj} with {o_pending[0]} P·V in flight, {o_count[0]} done")
+            p_full[b].arrive()
+        if nb > 0:
+            yield wait(o_full, 1)
+        if parts > 1:
+            yield from exchange(nb)
+        check(o_count[0] == nb and o_pending[0] == 0, f"epilogue reads O after {o_count[0]} of {nb} P·V")
+
+    # ------------------------------------------------------------- engines
+    def run_mma_op():
+        op = mma_queue.pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, jj, s, b = op
+        if kind == "S":
+            check(slot_gen[s] == 2 * jj, f"S({jj}) reads slot {s} holding load {slot_gen[s]}")
+            consumed.add(2 * jj)
+            for pt in range(parts):
+                prev = sbuf[b][pt]
+                if dec:
+                    check(jj == 0 or (jj - 1, pt) in s_read, f"S({jj}) overwrites S({jj - 1}) before it is read")
+                else:
+                    check(prev is None or prev == ("P", jj - 2), f"S({jj}) overwrites {prev}")
+                sbuf[b][pt] = ("S", jj)
+        else:
+            check(slot_gen[s] == 2 * jj + 1, f"P·V({jj}) reads slot {s} holding load {slot_gen[s]}")
+            consumed.add(2 * jj + 1)
+            if dec:
+                check(preg[0] == ("P", jj), f"P·V({jj}) reads {preg[0]}")
+            else:
+                for pt in range(parts):
+                    check(sbuf[b][pt] == ("P", jj), f"P·V({jj}) reads {sbuf[b][pt]} (part {pt})")
+            check(o_count[0] == jj, f"P·V({jj}) onto O holding {o_count[0]} products")
+            o_count[0] += 1
+            o_pending[0] -= 1
+
+    def land_copy():
+        cp = tma_inflight.pop(rng.randrange(len(tma_inflight)))
+        if cp[0] == "q":
+            q_full.arrive()
+            return
+        _, s, n = cp
+        if n >= slots:
+            check(n - slots in consumed, f"load {n} overwrites load {n - slots} before its MMA read it")
+        slot_gen[s] = n
+        full[s].arrive()
+
+    # ---------------------------------------------------------- scheduler
+    agents = {"producer": producer(), "mma": mma_warp()}
+    for pt in range(parts):
+        agents[f"softmax{pt}"] = softmax(pt)
+    pending = {name: None for name in agents}
+    finished = set()
+
+    def ready(name):
+        req = pending[name]
+        if req is None:
+            return True
+        _, bar, target = req
+        check(target - 1 <= bar.done <= target,
+              f"{name} waits for {target} phases of {bar.name}, which has {bar.done}: parity alias")
+        return bar.done == target
+
+    steps = 0
+    while True:
+        steps += 1
+        check(steps < 200_000, "runaway")
+        choices = [("agent", n) for n in agents if n not in finished and ready(n)]
+        if mma_queue:
+            choices.append(("mma", None))
+        if tma_inflight:
+            choices.append(("tma", None))
+        if not choices:
+            check(len(finished) == len(agents), f"deadlock: waiting {pending}")
+            break
+        kind, name = rng.choice(choices)
+        if kind == "mma":
+            run_mma_op()
+        elif kind == "tma":
+            land_copy()
+        else:
+            try:
+                pending[name] = next(agents[name])
+            except StopIteration:
+                pending[name] = None
+                finished.add(name)
+    return True
+
+
+CASES = [(nb, slots, dec) for dec in (False, True) for slots in (5, 8) for nb in (0, 1, 2, 3, 5, 11)]
+
+
+@pytest.mark.parametrize("nb,slots,dec", CASES)
+def test_protocol_holds_under_random_schedules(nb, slots, dec):
+    for seed in range(150):
+        simulate(nb, slots, dec, seed)
+
+
+@pytest.mark.parametrize("mutant,dec", [("producer_skips_empty", False), ("mma_skips_p_full", False),
+                                        ("mma_skips_s_free", True), ("softmax_skips_pv_done", True)])
+def test_mutants_are_caught(mutant, dec):
+    caught = False
+    for seed in range(400):
+        try:
+            simulate(6, 5, dec, seed, mutant=mutant)
+        except ProtocolError:
+            caught = True
+            break
+    assert caught, mutant
