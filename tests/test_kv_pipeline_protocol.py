@@ -151,6 +151,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             s_read.add((jj, part))
             if dec:
                 s_free.arrive()
+            yield ("step",)
             if parts > 1:
                 yield from exchange(jj)
             if dec and jj >= 1 and mutant != "softmax_skips_pv_done":
@@ -161,12 +162,14 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
                 preg[0] = ("P", jj)
             else:
                 sbuf[b][part] = ("P", jj)  # over this part's own scores
+            yield ("step",)
             if jj > 0 and rng.random() < rescale_p:
                 bp = 0 if dec else (jj - 1) & 1
                 yield wait(pv_done[bp], jj if dec else ((jj - 1) >> 1) + 1)
                 check(o_pending[0] == 0 and o_count[0] == jj,
                       f"O rescaled at block {jj} with {o_pending[0]} P·V in flight, {o_count[0]} done")
             p_full[b].arrive()
+            yield ("step",)
         if nb > 0:
             yield wait(o_full, 1)
         if parts > 1:
@@ -222,7 +225,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
 
     def ready(name):
         req = pending[name]
-        if req is None:
+        if req is None or req[0] == "step":
             return True
         _, bar, target = req
         check(target - 1 <= bar.done <= target,

@@ -1,0 +1,331 @@
+"""Host-side model of the persistent two-tile kernel's barrier protocol (no GPU).
+
+attn_fwd_sm103_kernel (d = 64 fp16 layout: separate P, P handed over in two
+halves) runs a list of work units per CTA. Each unit is two 128-row query tiles
+that share one stream of K/V blocks. A producer fills a ring of slots that both
+tiles release, one MMA warp per tile issues S = Q Kᵀ and O += P V, and the softmax
+warps of each tile read S, write P (first half, then second half) and write O / l
+at the end of the unit. This test replays that protocol under random
+interleavings, with the unit spans computed the kernel's way from random lengths
+and masks (causal, left window, ragged tails, a second tile past the end):
+
+  * waits never alias (a waiter is never two phases away from the phase it means)
+    and the run never deadlocks;
+  * the MMAs read the K or V block of their own index from a slot and the Q tiles
+    of their own unit; a slot is reloaded only after both tiles are done with it;
+  * S, each half of P, and O in TMEM are the generation each reader expects: the
+    next S waits for the softmax's read, P waits for the previous P·V, the first
+    P·V of a unit waits for the previous unit's epilogue, an O rescale happens
+    with no P·V in flight.
+
+Mutants with one wait removed must be caught. (Removing the MMA warp's o_free
+wait is not among them: the model shows it is implied, since the first P·V of a
+unit also waits for that unit's first P, which the softmax writes only after its
+epilogue of the previous unit.)
+"""
+import random
+
+import pytest
+
+KBM = KBN = 128
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.done = name, count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, self.name
+        if self.pending == 0:
+            self.done += 1
+            self.pending = self.count
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+def check(cond, msg):
+    if not cond:
+        raise ProtocolError(msg)
+
+
+def tile_span(L, causal, wl, row0):
+    """Key blocks [lo, hi) of a 128-row tile starting at row0 (empty past the end)."""
+    if row0 >= L:
+        return (0, 0)
+    last = min(row0 + KBM - 1, L - 1)
+    nblk = (L + KBN - 1) // KBN
+    hi = last // KBN + 1 if causal else nblk
+    lo = max(0, row0 - wl) // KBN if wl >= 0 else 0
+    return (lo, hi)
+
+
+def make_units(rng):
+    L = rng.randrange(1, 1700)
+    causal = rng.random() < 0.7
+    wl = rng.choice([-1, -1, 0, 100, 300]) if causal else -1
+    n_units = (L + 2 * KBM - 1) // (2 * KBM)
+    units = []
+    for mb in range(n_units):
+        t = [tile_span(L, causal, wl, mb * 2 * KBM + i * KBM) for i in range(2)]
+        live = [s for s in t if s[0] < s[1]]
+        assert live, "the first tile of a unit is always inside the sequence"
+        units.append((t, min(s[0] for s in live), max(s[1] for s in live)))
+    # one CTA's share: a random subsequence, heaviest first as the scheduler deals them
+    mine = [u for u in reversed(units) if rng.random() < 0.6] or [units[-1]]
+    return mine
+
+
+def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
+    rng = random.Random(seed)
+    full = [Bar(f"full{s}", 1) for s in range(slots)]
+    empty = [Bar(f"empty{s}", 2) for s in range(slots)]  # one release per tile
+    q_full, q_free = Bar("q_full", 1), Bar("q_free", 2)
+    s_full = [Bar(f"s_full{t}", 1) for t in range(2)]
+    s_free = [Bar(f"s_free{t}", 1) for t in range(2)]
+    p_half = [Bar(f"p_half{t}", 1) for t in range(2)]
+    p_full = [Bar(f"p_full{t}", 1) for t in range(2)]
+    pv_done = [Bar(f"pv_done{t}", 1) for t in range(2)]
+    o_full = [Bar(f"o_full{t}", 1) for t in range(2)]
+    o_free = [Bar(f"o_free{t}", 1) for t in range(2)]
+    drain = Bar("drain", 2)
+
+    slot_gen = [None] * slots
+    released = {}                       # load index -> tiles that read or skipped it
+    q_gen = [None]                      # unit whose Q tiles are in shared memory
+    s_reads_pending = [0]               # S MMAs of the current Q generation not yet run
+    sbuf = [None, None]                 # ("S", k, j) per tile
+    s_read = set()                      # (t, k, j) read by the softmax
+    preg = [[None, None], [None, None]] # P halves per tile: ("P", k, j)
+    o_state = [[None, 0, 0], [None, 0, 0]]  # per tile: unit, P·V halves done, P·V halves in flight
+    o_read = set()                      # (t, k): epilogue done
+    pv_blocks = [0, 0]                  # blocks whose P·V (both halves) has run, per tile
+    mma_queue = [[], []]                # per MMA warp, in issue order (one tensor core, two queues)
+    tma = []
+
+    def wait(bar, target):
+        return ("wait", bar, target)
+
+    def producer():
+        it = 0
+        for k, (spans, lo, hi) in enumerate(units):
+            if mutant != "producer_skips_q_free":
+                yield wait(q_free, k)
+            tma.append(("q", k))
+            for j in range(lo, hi):
+                for kv in range(2):
+                    s = it % slots
+                    yield wait(empty[s], it // slots)
+                    tma.append(("kv", s, it))
+                    it += 1
+
+    def mma_warp(t):
+        it = 0
+        ns = p_cnt = o_cnt = 0
+        q = mma_queue[t]
+        for k, (spans, lo, hi) in enumerate(units):
+            yield wait(q_full, k + 1)
+            it0 = it
+            slo, shi = spans[t]
+            live = slo < shi
+            j_lo, j_hi = (slo, shi) if live else (hi, hi)
+            kidx = lambda j: it0 + 2 * (j - lo)
+
+            def skip(j):
+                for kv in range(2):
+                    idx = kidx(j) + kv
+                    yield wait(full[idx % slots], idx // slots + 1)
+                    released.setdefault(idx, set()).add(t)
+                    empty[idx % slots].arrive()
+
+            for j in range(lo, j_lo):
+                yield from skip(j)
+            if live:
+                def s_block(j):
+                    nonlocal ns
+                    idx = kidx(j)
+                    yield wait(full[idx % slots], idx // slots + 1)
+                    if ns > 0 and mutant != "mma_skips_s_free":
+                        yield wait(s_free[t], ns)
+                    q.append(("S", t, k, j, idx))
+                    q.append(("commit", s_full[t]))
+                    ns += 1
+                    q.append(("commit", empty[idx % slots]))
+
+                def pv_block(j, first):
+                    nonlocal p_cnt
+                    idx = kidx(j) + 1
+                    yield wait(full[idx % slots], idx // slots + 1)
+                    if mutant != "mma_skips_p_half":
+                        yield wait(p_half[t], p_cnt + 1)
+                    if first:
+                        yield wait(o_free[t], o_cnt)
+                    q.append(("PV", t, k, j, idx, 0, first))
+                    o_state[t][2] += 1
+                    if mutant != "mma_skips_p_full":
+                        yield wait(p_full[t], p_cnt + 1)
+                    q.append(("PV", t, k, j, idx, 1, False))
+                    o_state[t][2] += 1
+                    p_cnt += 1
+                    q.append(("commit", pv_done[t]))
+                    q.append(("commit", empty[idx % slots]))
+
+                yield from s_block(j_lo)
+                for j in range(j_lo, j_hi):
+                    if j + 1 < j_hi:
+                        yield from s_block(j + 1)
+                    yield from pv_block(j, j == j_lo)
+                q.append(("commit", o_full[t]))
+                o_cnt += 1
+            for j in range(j_hi, hi):
+                yield from skip(j)
+            it = it0 + 2 * (hi - lo)
+            q.append(("commit", q_free))
+        q.append(("commit", drain))
+        yield wait(drain, 1)
+
+    def softmax(t):
+        s_cnt = o_cnt = 0
+        for k, (spans, lo, hi) in enumerate(units):
+            slo, shi = spans[t]
+            if slo >= shi:
+                continue
+            for j in range(slo, shi):
+                yield wait(s_full[t], s_cnt + 1)
+                check(sbuf[t] == ("S", k, j), f"tile {t} reads {sbuf[t]} for S({k}, {j})")
+                s_read.add((t, k, j))
+                s_free[t].arrive()
+                yield ("step",)
+                rescale = j != slo and rng.random() < rescale_p
+                if s_cnt > 0 and mutant != "softmax_skips_pv_done":
+                    yield wait(pv_done[t], s_cnt)
+                # the previous block's P·V has read both halves of P
+                check(pv_blocks[t] == s_cnt, f"tile {t} writes P({k}, {j}) before P·V of block {pv_blocks[t]} ran")
+                preg[t][0] = ("P", k, j)
+                if rescale:
+                    check(o_state[t][2] == 0, f"tile {t} rescales O with a P·V in flight")
+                    check(o_state[t][0] == k and o_state[t][1] == 2 * (j - slo),
+                          f"tile {t} rescales O holding {o_state[t]} at block {j}")
+                p_half[t].arrive()
+                yield ("step",)
+                preg[t][1] = ("P", k, j)
+                p_full[t].arrive()
+                yield ("step",)
+                s_cnt += 1
+            yield wait(o_full[t], o_cnt + 1)
+            check(o_state[t][0] == k and o_state[t][1] == 2 * (shi - slo) and o_state[t][2] == 0,
+                  f"tile {t} epilogue reads O {o_state[t]} for unit {k}")
+            o_read.add((t, k))
+            o_free[t].arrive()
+            o_cnt += 1
+
+    def run_mma(t):
+        op = mma_queue[t].pop(0)
+        if op[0] == "commit":
+            # a commit arrives once this warp's earlier MMAs have finished; they run in order
+            op[1].arrive()
+            return
+        if op[0] == "S":
+            _, tt, k, j, idx = op
+            check(q_gen[0] == k, f"S({k}, {j}) of tile {tt} reads Q of unit {q_gen[0]}")
+            check(slot_gen[idx % slots] == idx, f"S reads slot holding {slot_gen[idx % slots]}, wants {idx}")
+            released.setdefault(idx, set()).add(tt)
+            prev = sbuf[tt]
+            check(prev is None or (tt,) + prev[1:] in s_read, f"S({k}, {j}) overwrites unread {prev}")
+            sbuf[tt] = ("S", k, j)
+            s_reads_pending[0] -= 1
+        else:
+            _, tt, k, j, idx, h, first = op
+            check(slot_gen[idx % slots] == idx, f"P·V reads slot holding {slot_gen[idx % slots]}, wants {idx}")
+            check(preg[tt][h] == ("P", k, j), f"P·V({k}, {j}) half {h} reads {preg[tt][h]}")
+            if h == 1:
+                released.setdefault(idx, set()).add(tt)
+                pv_blocks[tt] += 1
+            st = o_state[tt]
+            if first:
+                check(st[0] is None or (tt, st[0]) in o_read, f"unit {k} overwrites O of unit {st[0]} before its epilogue")
+                st[0], st[1] = k, 0
+            check(st[0] == k, f"P·V of unit {k} onto O of unit {st[0]}")
+            st[1] += 1
+            st[2] -= 1
+
+    def land():
+        cp = tma.pop(rng.randrange(len(tma)))
+        if cp[0] == "q":
+            k = cp[1]
+            check(k == 0 or q_gen[0] == k - 1, "Q reload out of order")
+            check(s_reads_pending[0] == 0, f"Q of unit {k} lands while S MMAs still read unit {q_gen[0]}")
+            q_gen[0] = k
+            spans = units[k][0]
+            s_reads_pending[0] = sum(max(0, s[1] - s[0]) for s in spans)
+            q_full.arrive()
+            return
+        _, s, n = cp
+        if n >= slots:
+            check(released.get(n - slots, set()) == {0, 1},
+                  f"load {n} overwrites load {n - slots} (released by {released.get(n - slots)})")
+        slot_gen[s] = n
+        full[s].arrive()
+
+    agents = {"producer": producer(), "mma0": mma_warp(0), "mma1": mma_warp(1),
+              "smx0": softmax(0), "smx1": softmax(1)}
+    pending = {n: None for n in agents}
+    finished = set()
+
+    def ready(name):
+        req = pending[name]
+        if req is None or req[0] == "step":
+            return True
+        _, bar, target = req
+        check(target - 1 <= bar.done <= target,
+              f"{name} waits for {target} phases of {bar.name}, which has {bar.done}: parity alias")
+        return bar.done == target
+
+    steps = 0
+    while True:
+        steps += 1
+        check(steps < 500_000, "runaway")
+        choices = [("agent", n) for n in agents if n not in finished and ready(n)]
+        choices += [("mma", t) for t in range(2) if mma_queue[t]]
+        if tma:
+            choices.append(("tma", None))
+        if not choices:
+            check(len(finished) == len(agents), f"deadlock: {pending}")
+            break
+        kind, x = rng.choice(choices)
+        if kind == "mma":
+            run_mma(x)
+        elif kind == "tma":
+            land()
+        else:
+            try:
+                pending[x] = next(agents[x])
+            except StopIteration:
+                pending[x] = None
+                finished.add(x)
+    return True
+
+
+@pytest.mark.parametrize("slots", [4, 8])
+def test_protocol_holds_under_random_schedules(slots):
+    rng = random.Random(slots)
+    for trial in range(250):
+        units = make_units(rng)
+        simulate(units, slots, seed=trial)
+
+
+@pytest.mark.parametrize("mutant", ["producer_skips_q_free", "mma_skips_s_free", "mma_skips_p_half",
+                                    "mma_skips_p_full", "softmax_skips_pv_done"])
+def test_mutants_are_caught(mutant):
+    rng = random.Random(7)
+    caught = False
+    for trial in range(400):
+        units = make_units(rng)
+        try:
+            simulate(units, 4, seed=trial, mutant=mutant)
+        except ProtocolError:
+            caught = True
+            break
+    assert caught, mutant
