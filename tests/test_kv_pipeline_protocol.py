@@ -23,28 +23,7 @@ import random
 
 import pytest
 
-
-class Bar:
-    """mbarrier: `count` arrivals complete a phase; `done` counts completed phases."""
-
-    def __init__(self, name, count):
-        self.name, self.count, self.pending, self.done = name, count, count, 0
-
-    def arrive(self):
-        self.pending -= 1
-        assert self.pending >= 0, self.name
-        if self.pending == 0:
-            self.done += 1
-            self.pending = self.count
-
-
-class ProtocolError(AssertionError):
-    pass
-
-
-def check(cond, msg):
-    if not cond:
-        raise ProtocolError(msg)
+from protocol_model import STEP, Bar, CopyEngine, InOrderQueue, ProtocolError, check, run, wait
 
 
 def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
@@ -71,26 +50,22 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
     o_count = [0]                      # P·V products accumulated in O
     o_pending = [0]                    # P·V issued but not finished
     xdata = {}
+    copies = CopyEngine(lambda cp: land_copy(cp))       # copies issued, landing in any order
+    mma_queue = InOrderQueue(lambda op: run_mma_op(op))  # the MMA warp's operations, in issue order
 
-    mma_queue = []                     # the tensor core's in-order queue: ops and commits
-    tma_inflight = []                  # copies issued, landing in any order
-
-    def wait(bar, target):
-        """Parity wait for `target` completed phases (the phase target - 1)."""
-        return ("wait", bar, target)
 
     # ------------------------------------------------------------------ roles
     def producer():
         if nb == 0:
             return
-        tma_inflight.append(("q",))
+        copies.issue(("q",))
         n = 0
         for _ in range(nb):
             for _kv in range(2):
                 s = n % slots
                 if mutant != "producer_skips_empty":
                     yield wait(empty[s], n // slots)
-                tma_inflight.append(("kv", s, n))
+                copies.issue(("kv", s, n))
                 n += 1
 
     def mma_warp():
@@ -103,9 +78,9 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             s = kidx % slots
             yield wait(full[s], kidx // slots + 1)
             b = 0 if dec else jj & 1
-            mma_queue.append(("S", jj, s, b))
-            mma_queue.append(("commit", s_full[b]))
-            mma_queue.append(("commit", empty[s]))
+            mma_queue.push(("S", jj, s, b))
+            mma_queue.commit(s_full[b])
+            mma_queue.commit(empty[s])
 
         def issue_pv(jj):
             vidx = 2 * jj + 1
@@ -114,10 +89,10 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             b = 0 if dec else jj & 1
             if mutant != "mma_skips_p_full":
                 yield wait(p_full[b], (jj + 1) if dec else (jj >> 1) + 1)
-            mma_queue.append(("PV", jj, s, b))
+            mma_queue.push(("PV", jj, s, b))
             o_pending[0] += 1
-            mma_queue.append(("commit", pv_done[b]))
-            mma_queue.append(("commit", empty[s]))
+            mma_queue.commit(pv_done[b])
+            mma_queue.commit(empty[s])
 
         yield from issue_s(0)
         if dec:
@@ -134,7 +109,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
                 yield from issue_pv(jj)
                 if jj + 2 < nb:
                     yield from issue_s(jj + 2)
-        mma_queue.append(("commit", o_full))
+        mma_queue.commit(o_full)
 
     def softmax(part):
         def exchange(n):
@@ -151,7 +126,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             s_read.add((jj, part))
             if dec:
                 s_free.arrive()
-            yield ("step",)
+            yield STEP
             if parts > 1:
                 yield from exchange(jj)
             if dec and jj >= 1 and mutant != "softmax_skips_pv_done":
@@ -162,14 +137,14 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
                 preg[0] = ("P", jj)
             else:
                 sbuf[b][part] = ("P", jj)  # over this part's own scores
-            yield ("step",)
+            yield STEP
             if jj > 0 and rng.random() < rescale_p:
                 bp = 0 if dec else (jj - 1) & 1
                 yield wait(pv_done[bp], jj if dec else ((jj - 1) >> 1) + 1)
                 check(o_pending[0] == 0 and o_count[0] == jj,
                       f"O rescaled at block {jj} with {o_pending[0]} P·V in flight, {o_count[0]} done")
             p_full[b].arrive()
-            yield ("step",)
+            yield STEP
         if nb > 0:
             yield wait(o_full, 1)
         if parts > 1:
@@ -177,11 +152,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
         check(o_count[0] == nb and o_pending[0] == 0, f"epilogue reads O after {o_count[0]} of {nb} P·V")
 
     # ------------------------------------------------------------- engines
-    def run_mma_op():
-        op = mma_queue.pop(0)
-        if op[0] == "commit":
-            op[1].arrive()
-            return
+    def run_mma_op(op):
         kind, jj, s, b = op
         if kind == "S":
             check(slot_gen[s] == 2 * jj, f"S({jj}) reads slot {s} holding load {slot_gen[s]}")
@@ -205,8 +176,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             o_count[0] += 1
             o_pending[0] -= 1
 
-    def land_copy():
-        cp = tma_inflight.pop(rng.randrange(len(tma_inflight)))
+    def land_copy(cp):
         if cp[0] == "q":
             q_full.arrive()
             return
@@ -220,41 +190,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
     agents = {"producer": producer(), "mma": mma_warp()}
     for pt in range(parts):
         agents[f"softmax{pt}"] = softmax(pt)
-    pending = {name: None for name in agents}
-    finished = set()
-
-    def ready(name):
-        req = pending[name]
-        if req is None or req[0] == "step":
-            return True
-        _, bar, target = req
-        check(target - 1 <= bar.done <= target,
-              f"{name} waits for {target} phases of {bar.name}, which has {bar.done}: parity alias")
-        return bar.done == target
-
-    steps = 0
-    while True:
-        steps += 1
-        check(steps < 200_000, "runaway")
-        choices = [("agent", n) for n in agents if n not in finished and ready(n)]
-        if mma_queue:
-            choices.append(("mma", None))
-        if tma_inflight:
-            choices.append(("tma", None))
-        if not choices:
-            check(len(finished) == len(agents), f"deadlock: waiting {pending}")
-            break
-        kind, name = rng.choice(choices)
-        if kind == "mma":
-            run_mma_op()
-        elif kind == "tma":
-            land_copy()
-        else:
-            try:
-                pending[name] = next(agents[name])
-            except StopIteration:
-                pending[name] = None
-                finished.add(name)
+    run(agents, [copies, mma_queue], rng)
     return True
 
 

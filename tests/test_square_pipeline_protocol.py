@@ -27,28 +27,9 @@ import random
 
 import pytest
 
+from protocol_model import STEP, Bar, CopyEngine, InOrderQueue, ProtocolError, check, run, wait
+
 KBM = KBN = 128
-
-
-class Bar:
-    def __init__(self, name, count):
-        self.name, self.count, self.pending, self.done = name, count, count, 0
-
-    def arrive(self):
-        self.pending -= 1
-        assert self.pending >= 0, self.name
-        if self.pending == 0:
-            self.done += 1
-            self.pending = self.count
-
-
-class ProtocolError(AssertionError):
-    pass
-
-
-def check(cond, msg):
-    if not cond:
-        raise ProtocolError(msg)
 
 
 def tile_span(L, causal, wl, row0):
@@ -102,23 +83,21 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
     o_state = [[None, 0, 0], [None, 0, 0]]  # per tile: unit, P·V halves done, P·V halves in flight
     o_read = set()                      # (t, k): epilogue done
     pv_blocks = [0, 0]                  # blocks whose P·V (both halves) has run, per tile
-    mma_queue = [[], []]                # per MMA warp, in issue order (one tensor core, two queues)
-    tma = []
-
-    def wait(bar, target):
-        return ("wait", bar, target)
+    # per MMA warp, in issue order (one tensor core, two queues); copies land in any order
+    mma_queue = [InOrderQueue(lambda op: run_mma(op)), InOrderQueue(lambda op: run_mma(op))]
+    copies = CopyEngine(lambda cp: land(cp))
 
     def producer():
         it = 0
         for k, (spans, lo, hi) in enumerate(units):
             if mutant != "producer_skips_q_free":
                 yield wait(q_free, k)
-            tma.append(("q", k))
+            copies.issue(("q", k))
             for j in range(lo, hi):
                 for kv in range(2):
                     s = it % slots
                     yield wait(empty[s], it // slots)
-                    tma.append(("kv", s, it))
+                    copies.issue(("kv", s, it))
                     it += 1
 
     def mma_warp(t):
@@ -149,10 +128,10 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                     yield wait(full[idx % slots], idx // slots + 1)
                     if ns > 0 and mutant != "mma_skips_s_free":
                         yield wait(s_free[t], ns)
-                    q.append(("S", t, k, j, idx))
-                    q.append(("commit", s_full[t]))
+                    q.push(("S", t, k, j, idx))
+                    q.commit(s_full[t])
                     ns += 1
-                    q.append(("commit", empty[idx % slots]))
+                    q.commit(empty[idx % slots])
 
                 def pv_block(j, first):
                     nonlocal p_cnt
@@ -162,28 +141,28 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                         yield wait(p_half[t], p_cnt + 1)
                     if first:
                         yield wait(o_free[t], o_cnt)
-                    q.append(("PV", t, k, j, idx, 0, first))
+                    q.push(("PV", t, k, j, idx, 0, first))
                     o_state[t][2] += 1
                     if mutant != "mma_skips_p_full":
                         yield wait(p_full[t], p_cnt + 1)
-                    q.append(("PV", t, k, j, idx, 1, False))
+                    q.push(("PV", t, k, j, idx, 1, False))
                     o_state[t][2] += 1
                     p_cnt += 1
-                    q.append(("commit", pv_done[t]))
-                    q.append(("commit", empty[idx % slots]))
+                    q.commit(pv_done[t])
+                    q.commit(empty[idx % slots])
 
                 yield from s_block(j_lo)
                 for j in range(j_lo, j_hi):
                     if j + 1 < j_hi:
                         yield from s_block(j + 1)
                     yield from pv_block(j, j == j_lo)
-                q.append(("commit", o_full[t]))
+                q.commit(o_full[t])
                 o_cnt += 1
             for j in range(j_hi, hi):
                 yield from skip(j)
             it = it0 + 2 * (hi - lo)
-            q.append(("commit", q_free))
-        q.append(("commit", drain))
+            q.commit(q_free)
+        q.commit(drain)
         yield wait(drain, 1)
 
     def softmax(t):
@@ -197,7 +176,7 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                 check(sbuf[t] == ("S", k, j), f"tile {t} reads {sbuf[t]} for S({k}, {j})")
                 s_read.add((t, k, j))
                 s_free[t].arrive()
-                yield ("step",)
+                yield STEP
                 rescale = j != slo and rng.random() < rescale_p
                 if s_cnt > 0 and mutant != "softmax_skips_pv_done":
                     yield wait(pv_done[t], s_cnt)
@@ -209,10 +188,10 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                     check(o_state[t][0] == k and o_state[t][1] == 2 * (j - slo),
                           f"tile {t} rescales O holding {o_state[t]} at block {j}")
                 p_half[t].arrive()
-                yield ("step",)
+                yield STEP
                 preg[t][1] = ("P", k, j)
                 p_full[t].arrive()
-                yield ("step",)
+                yield STEP
                 s_cnt += 1
             yield wait(o_full[t], o_cnt + 1)
             check(o_state[t][0] == k and o_state[t][1] == 2 * (shi - slo) and o_state[t][2] == 0,
@@ -221,12 +200,7 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
             o_free[t].arrive()
             o_cnt += 1
 
-    def run_mma(t):
-        op = mma_queue[t].pop(0)
-        if op[0] == "commit":
-            # a commit arrives once this warp's earlier MMAs have finished; they run in order
-            op[1].arrive()
-            return
+    def run_mma(op):
         if op[0] == "S":
             _, tt, k, j, idx = op
             check(q_gen[0] == k, f"S({k}, {j}) of tile {tt} reads Q of unit {q_gen[0]}")
@@ -251,8 +225,7 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
             st[1] += 1
             st[2] -= 1
 
-    def land():
-        cp = tma.pop(rng.randrange(len(tma)))
+    def land(cp):
         if cp[0] == "q":
             k = cp[1]
             check(k == 0 or q_gen[0] == k - 1, "Q reload out of order")
@@ -271,40 +244,7 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
 
     agents = {"producer": producer(), "mma0": mma_warp(0), "mma1": mma_warp(1),
               "smx0": softmax(0), "smx1": softmax(1)}
-    pending = {n: None for n in agents}
-    finished = set()
-
-    def ready(name):
-        req = pending[name]
-        if req is None or req[0] == "step":
-            return True
-        _, bar, target = req
-        check(target - 1 <= bar.done <= target,
-              f"{name} waits for {target} phases of {bar.name}, which has {bar.done}: parity alias")
-        return bar.done == target
-
-    steps = 0
-    while True:
-        steps += 1
-        check(steps < 500_000, "runaway")
-        choices = [("agent", n) for n in agents if n not in finished and ready(n)]
-        choices += [("mma", t) for t in range(2) if mma_queue[t]]
-        if tma:
-            choices.append(("tma", None))
-        if not choices:
-            check(len(finished) == len(agents), f"deadlock: {pending}")
-            break
-        kind, x = rng.choice(choices)
-        if kind == "mma":
-            run_mma(x)
-        elif kind == "tma":
-            land()
-        else:
-            try:
-                pending[x] = next(agents[x])
-            except StopIteration:
-                pending[x] = None
-                finished.add(x)
+    run(agents, [copies] + mma_queue, rng)
     return True
 
 
