@@ -139,7 +139,7 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                     yield wait(full[idx % slots], idx // slots + 1)
                     if mutant != "mma_skips_p_half":
                         yield wait(p_half[t], p_cnt + 1)
-                    if first:
+                    if first and mutant != "mma_skips_o_free":
                         yield wait(o_free[t], o_cnt)
                     q.push(("PV", t, k, j, idx, 0, first))
                     o_state[t][2] += 1
@@ -269,3 +269,10 @@ def test_mutants_are_caught(mutant):
             caught = True
             break
     assert caught, mutant
+
+
+def test_o_free_wait_is_implied():
+    """Without the MMA warp's o_free wait no schedule breaks the protocol."""
+    rng = random.Random(11)
+    for trial in range(300):
+        simulate(make_units(rng), 4, seed=trial, mutant="mma_skips_o_free")
