@@ -205,6 +205,10 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
     *abort_flag = 0u;                                                                          \
     fence_mbar_init();                                                                         \
   }                                                                                            \
+  /* launched as a programmatic dependent: the kernels before it on the stream have */         \
+  /* completed and their writes are visible past this point (no-op otherwise); TMEM */        \
+  /* is allocated only after it, so no CTA holds TMEM while it waits on another kernel */      \
+  asm volatile("griddepcontrol.wait;" ::: "memory");                                           \
   if (warp == kMmaWarp) {                                                                      \
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);                                                \
     tmem_relinquish();                                                                         \
@@ -213,9 +217,6 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
   __syncthreads();                                                                             \
   tc_fence_after();                                                                            \
   const uint32_t tmem_base = *tmem_slot;                                                       \
-  /* launched as a programmatic dependent: the kernels before it on the stream have */         \
-  /* completed and their writes are visible past this point (no-op otherwise) */               \
-  asm volatile("griddepcontrol.wait;" ::: "memory");                                           \
   WaitCtl wc;                                                                                  \
   wc.abort_flag = abort_flag;                                                                  \
   wc.status = p.status;                                                                        \

@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_vt);
   }
+  // Launched as a programmatic dependent of the V transpose: past this point Vᵀ (and
+  // everything before it on the stream) is complete and visible. TMEM is allocated
+  // only after it, so this CTA never holds TMEM while it waits on another kernel.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -181,9 +185,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Launched as a programmatic dependent of the V transpose: Vᵀ (and everything
-  // before it on the stream) is complete and visible past this point.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   WaitCtl wc;
   wc.abort_flag = abort_flag;

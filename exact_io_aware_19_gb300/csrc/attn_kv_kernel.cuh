@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Prologue: shared memory, TMEM and the tensor maps only (no global memory), so
-  // it may overlap the previous kernel on the stream.
+  // Prologue: shared memory and the tensor maps only (no global memory, no TMEM),
+  // so it may overlap the previous kernel on the stream.
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full(s), 1);
@@ -269,6 +269,12 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
   }
+  // Launched as a programmatic dependent: past this point the previous kernel's
+  // writes (Q, K, V, the page table, a merge still reading this workspace) are
+  // complete and visible. TMEM is allocated only after it, so this CTA never holds
+  // TMEM while it waits on a kernel that may still need some. A no-op for an
+  // ordinary launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -277,10 +283,6 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Launched as a programmatic dependent: the previous kernel's writes (Q, K, V, the
-  // page table, a merge still reading this workspace) are complete and visible past
-  // this point. A no-op for an ordinary launch.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const KvItem it = kv_item<PAGED>(p);
   const int nblocks = max(0, it.hi - it.lo);
 
