@@ -25,7 +25,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["attn_fwd", "attn_fwd_into", "workspace_size", "attn_fwd_kv", "attn_fwd_kv_into",
+__all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_noalloc", "workspace_size", "attn_fwd_kv",
+           "attn_fwd_kv_into",
            "attn_fwd_kv_paged", "attn_fwd_window", "attn_fwd_fp8", "attn_bwd",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
@@ -62,6 +63,8 @@ def _bind(lib):
     p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.attn_fwd.restype = i
     lib.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p, sz, p]
+    lib.attn_fwd_noalloc.restype = i
+    lib.attn_fwd_noalloc.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p]
     lib.attn_fwd_workspace_size.restype = sz
     lib.attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.attn_fwd_kv.restype = i
@@ -207,6 +210,24 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
                         int(bool(causal)), int(window_left), float(scale), dt, out,
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
+    _check(code)
+
+
+def attn_fwd_noalloc(q, k, v, o, lse, causal=False, window_left=-1, scale=None, stream=None) -> None:
+    """attn_fwd_into without a workspace: the C entry point of the same name keeps its
+    status word in library-owned device memory, so neither this call nor the library
+    allocates anything (for callers inside an allocator or memory-pool callback).
+    Writes ``o`` (q's dtype or float32) and ``lse`` (float32 [B, Hq, L] or None)."""
+    lib = load_library()
+    (B, L, Lk, Hq, Hkv, d), dt, out = _check_tensors(q, k, v, o, lse)
+    if Lk != L:
+        raise ValueError("k and v must have q's sequence length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
+                                int(bool(causal)), int(window_left), float(scale), dt, out,
+                                _stream_handle(stream))
     _check(code)
 
 

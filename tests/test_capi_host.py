@@ -106,6 +106,18 @@ def test_python_binding_rejects_cpu_tensors():
         ex.attn_fwd(q, q, q)
 
 
+def test_python_noalloc_binding_checks_arguments():
+    """The no-allocation binding validates like attn_fwd_into (nothing reaches the GPU)."""
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.float16)
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 1, 8, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        ex.attn_fwd_noalloc(q, q, q, o, lse)
+    assert "attn_fwd_noalloc" in ex.__all__
+    lib = ex.load_library()
+    assert lib.attn_fwd_noalloc.argtypes is not None and len(lib.attn_fwd_noalloc.argtypes) == 16
+
+
 # --- decode-shaped entry points ----------------------------------------------------------
 
 def test_kv_workspace_size(lib):
