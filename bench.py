@@ -212,6 +212,8 @@ def reference_arm(args, world, rank):
     w = WORKLOAD
     q, k, v = si.make_qkv(w)
     per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    if args.ref_step_seconds is not None:  # a shorter sample per step (the host tests)
+        per_step = args.ref_step_seconds
     for s in range(args.warmup):
         oracle_sample(w, per_step, seed=100 + s, q=q, k=k, v=v)
     flops, secs, rows, thr = 0.0, 0.0, 0, 1
@@ -584,6 +586,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="reference arm: seconds of oracle work per step (default: sized so the run "
+                         "takes about 150 s)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     world, rank, local = dist_setup(args.gpus)
