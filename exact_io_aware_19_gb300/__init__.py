@@ -100,7 +100,7 @@ def _bind(lib):
     lib.attn_debug_wait_probe.restype = i
     lib.attn_debug_wait_probe.argtypes = [p, sz, ctypes.c_uint64, p]
     lib.attn_debug_exp2.restype = i
-    lib.attn_debug_exp2.argtypes = [p, p, p, p, i, p]
+    lib.attn_debug_exp2.argtypes = [p, p, p, i, p]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i]
     lib.attn_last_error_detail.restype = ctypes.c_char_p
@@ -445,16 +445,16 @@ def set_wait_limit_ns(limit_ns: int) -> None:
 
 
 def debug_exp2(x: torch.Tensor, with_f16: bool = False):
-    """2^x by the kernel's polynomial path and by MUFU ex2 (and, with ``with_f16``, by
-    the packed fp16 MUFU path) for a CUDA float32 tensor."""
+    """2^x by the fp32 MUFU instruction (and, with ``with_f16``, by the packed fp16
+    one on arguments rounded to fp16) for a CUDA float32 tensor."""
     lib = load_library()
     x = x.contiguous()
-    yp, ym = torch.empty_like(x), torch.empty_like(x)
+    ym = torch.empty_like(x)
     yh = torch.empty_like(x) if with_f16 else None
-    _check(lib.attn_debug_exp2(x.data_ptr(), yp.data_ptr(), ym.data_ptr(),
+    _check(lib.attn_debug_exp2(x.data_ptr(), ym.data_ptr(),
                                yh.data_ptr() if yh is not None else None, x.numel(),
                                _stream_handle(None)))
-    return (yp, ym, yh) if with_f16 else (yp, ym)
+    return (ym, yh) if with_f16 else ym
 
 
 def debug_wait_probe(workspace: torch.Tensor, limit_ns: int, stream=None) -> None:

@@ -43,35 +43,8 @@ def _inputs():
         glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "attn.h"), __file__]
 
 
-STAMP = os.path.join(BUILD, "flags.txt")
-
-
-def _defines():
-    """Tuning defines taken from the environment: EX19_POLY_PAIRS (pairs of every 8
-    softmax columns whose exp2 runs on the FMA-pipe polynomial; default 0),
-    EX19_SEPARATE_P (d = 64 fp16 keeps P in its own TMEM columns; default 1),
-    EX19_SOFTMAX_F2 (paired fp32 FMA / adds in the softmax; default 1),
-    EX19_MAX3 (3-input max instruction in the row max; default 1),
-    EX19_SUSPEND_NS (sleep hint of the mbarrier polls in ns; default 1e6, 0 = none),
-    EX19_TRACE (CTA 0 records a clock64 timeline of its first unit in the workspace; default 0),
-    EX19_ONEPASS (the softmax reads S from TMEM once instead of twice; default 1),
-    EX19_SPIN (bounded waits spin on mbarrier.test_wait instead of try_wait; default 0),
-    EX19_EXP_F16X2 (fp16: packed fp16 exponentials, two per MUFU operation; default 1),
-    EX19_PV_HALVES (separate P: P handed to the P·V MMAs in two 64-key halves; default 1)."""
-    out = []
-    for name in ("EX19_POLY_PAIRS", "EX19_SEPARATE_P", "EX19_SOFTMAX_F2", "EX19_MAX3",
-                 "EX19_SUSPEND_NS",
-                 "EX19_TRACE", "EX19_ONEPASS", "EX19_SPIN", "EX19_PV_HALVES",
-                 "EX19_EXP_F16X2"):
-        if os.environ.get(name):
-            out.append("-D%s=%d" % (name, int(os.environ[name])))
-    return out
-
-
 def up_to_date() -> bool:
-    if not os.path.exists(LIB) or not os.path.exists(STAMP):
-        return False
-    if open(STAMP).read() != " ".join(_defines()):
+    if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(p) <= t for p in _inputs())
@@ -83,7 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    extra = (["-Xptxas", "-v"] if verbose else []) + _defines()
+    extra = ["-Xptxas", "-v"] if verbose else []
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
@@ -104,8 +77,6 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
-    with open(STAMP, "w") as fh:
-        fh.write(" ".join(_defines()))
     return LIB
 
 

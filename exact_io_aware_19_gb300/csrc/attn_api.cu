@@ -17,11 +17,8 @@
 
 namespace {
 
-#ifndef EX19_TRACE
-#define EX19_TRACE 0
-#endif
-// status word (16 B), padded; trace builds append the timeline probe buffer
-constexpr size_t kWorkspaceBytes = EX19_TRACE ? 256 + 16384 : 256;
+// status word (16 B), padded to 256 bytes
+constexpr size_t kWorkspaceBytes = 256;
 constexpr unsigned long long kDefaultWaitLimitNs = 4000000000ull;
 constexpr int kUnitRows = 256;           // query rows per kernel work unit
 
@@ -452,19 +449,27 @@ namespace ex19 {
 // Lets other translation units of the library set the detail string that
 // attn_last_error_detail() returns to the calling thread.
 void set_last_error_detail(const std::string& msg) { g_detail = msg; }
-}  // namespace ex19
 
-extern "C" {
-
-size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal, int window_left) {
-  if (check_shape(B, L, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
-  return kWorkspaceBytes;
+// The current device, if it is a compute capability 10.3 device; otherwise the
+// status attn_fwd returns for it (with its detail).
+attn_status_t current_sm103_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  DeviceInfo info;
+  if (!device_info(*dev, &info, &e)) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (info.major != 10 || info.minor != 3)
+    return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
+                                          std::to_string(info.major) + "." +
+                                          std::to_string(info.minor));
+  return ATTN_OK;
 }
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+// attn_fwd, optionally clearing the first `clear_status_bytes` of the workspace on
+// the call's stream once every argument has been validated (attn_fwd passes 0).
+attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int L, int Hq, int Hkv, int d, int causal, int window_left, float scale,
                        attn_dtype_t dtype, attn_out_t out_dtype, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, size_t clear_status_bytes) {
   g_detail.clear();
   attn_status_t st = check_shape(B, L, Hq, Hkv, d, causal, window_left);
   if (st != ATTN_OK) return st;
@@ -496,6 +501,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   for (int i = 0; i < 6; ++i)
     if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
       return fail(ATTN_ERR_INVALID_ARG, why);
+  if (clear_status_bytes > 0) {  // the caller's status word starts at zero (after validation)
+    e = cudaMemsetAsync(workspace, 0, clear_status_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("clearing the status word", e);
+  }
 
   const bool bf16 = dtype == ATTN_BF16;
   const bool out_f32 = out_dtype == ATTN_OUT_FP32;
@@ -538,14 +547,28 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.units_per_bh = (L + kUnitRows - 1) / kUnitRows;
   p.num_units = num_units;
   p.wait_limit_ns = g_wait_limit_ns.load();
-  p.trace = EX19_TRACE ? reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + 256)
-                       : nullptr;
   a.grid = p.num_units < info.sms ? p.num_units : info.sms;
   a.stream = static_cast<cudaStream_t>(stream);
 
   e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
+}
+}  // namespace ex19
+
+extern "C" {
+
+size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal, int window_left) {
+  if (check_shape(B, L, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
+  return kWorkspaceBytes;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int L, int Hq, int Hkv, int d, int causal, int window_left, float scale,
+                       attn_dtype_t dtype, attn_out_t out_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return ex19::fwd_impl(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, scale, dtype,
+                        out_dtype, workspace, workspace_bytes, stream, 0);
 }
 
 attn_status_t attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -896,12 +919,11 @@ attn_status_t attn_debug_wait_probe(void* workspace, size_t workspace_bytes, uin
   return ATTN_OK;
 }
 
-attn_status_t attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
-                              void* stream) {
+attn_status_t attn_debug_exp2(const float* x, float* y_mufu, float* y_f16, int n, void* stream) {
   g_detail.clear();
   if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be >= 0");
   if (n == 0) return ATTN_OK;
-  if (!x || !y_poly || !y_mufu) return fail(ATTN_ERR_INVALID_ARG, "pointers must be non-null");
+  if (!x || !y_mufu) return fail(ATTN_ERR_INVALID_ARG, "pointers must be non-null");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
@@ -910,12 +932,12 @@ attn_status_t attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, floa
   if (info.major != 10 || info.minor != 3)
     return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300)");
   std::string why;
-  const void* ptrs[4] = {x, y_poly, y_mufu, y_f16};
-  const char* names[4] = {"x", "y_poly", "y_mufu", "y_f16"};
-  for (int i = 0; i < 4; ++i)
+  const void* ptrs[3] = {x, y_mufu, y_f16};
+  const char* names[3] = {"x", "y_mufu", "y_f16"};
+  for (int i = 0; i < 3; ++i)
     if (ptrs[i] && !is_device_ptr(ptrs[i], dev, &why, names[i]))
       return fail(ATTN_ERR_INVALID_ARG, why);
-  e = ex19::launch_exp2_probe(x, y_poly, y_mufu, y_f16, n, static_cast<cudaStream_t>(stream));
+  e = ex19::launch_exp2_probe(x, y_mufu, y_f16, n, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("exp2 probe launch", e);
   return ATTN_OK;
 }

@@ -220,7 +220,7 @@ __device__ __forceinline__ void tmem_ld2_x64(uint32_t ta, uint32_t (&ra)[64], ui
   WaitCtl wc;                                                                                  \
   wc.abort_flag = abort_flag;                                                                  \
   wc.status = p.status;                                                                        \
-  wc.limit_ns = p.wait_limit_ns;                                                               \
+  wc.set_limit(p.wait_limit_ns);                                                               \
   wc.unit = blockIdx.x;
 
 #define EX19_BWD_TEARDOWN()            \
@@ -361,7 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
         }
       }
-      if (!ok) {
+      // Whether or not this CTA aborted, the copies issued last may still be in
+      // flight (another role can abort after this loop has ended, and then nothing
+      // consumes them): let them land before the CTA can exit.
+      {
         for (uint32_t back = 1; back <= S && back <= n; ++back) {
           const uint32_t m = n - back;
           mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrain);
@@ -597,7 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
         }
       }
-      if (!ok) {
+      // Whether or not this CTA aborted, the copies issued last may still be in
+      // flight (another role can abort after this loop has ended, and then nothing
+      // consumes them): let them land before the CTA can exit.
+      {
         for (uint32_t back = 1; back <= S && back <= n; ++back) {
           const uint32_t m = n - back;
           mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrain);

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   WaitCtl wc;
   wc.abort_flag = abort_flag;
   wc.status = p.status;
-  wc.limit_ns = p.wait_limit_ns;
+  wc.set_limit(p.wait_limit_ns);
   wc.unit = blockIdx.x;
 
   if (warp == kProducerWarp) {
@@ -212,7 +212,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           ++n;
         }
       }
-      if (!ok) {
+      // Whether or not this CTA aborted, the copies issued last may still be in
+      // flight (another role can abort after this loop has ended, and then nothing
+      // consumes them): let them land before the CTA can exit.
+      {
         for (uint32_t back = 1; back <= S && back <= n; ++back) {
           const uint32_t m = n - back;
           mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrainLoads);

@@ -13,16 +13,19 @@
 //     share one stream of K/V blocks of 128 keys.
 //   * warp 8   (producer): TMA loads of the Q tiles and of K_j, V_j into a ring of
 //              shared-memory slots (128-byte swizzle), signalled by mbarriers.
-//   * warp 9   (MMA): one thread issues tcgen05.mma. S_t = Q_t K_jᵀ goes to TMEM
-//              (fp32, 128 columns per tile); O_t += P_t V_j reads P_t from TMEM
-//              (16-bit, aliased over S_t) and V_j from shared memory. MMAs of the
-//              two tiles are interleaved so one tile's softmax overlaps the other
-//              tile's MMAs.
+//   * warps 9, 10 (MMA, tile 0 / tile 1): each warp runs its issue loop
+//              warp-uniformly and one lane, picked by elect.sync, issues each
+//              tcgen05.mma. S_t = Q_t K_jᵀ goes to TMEM (fp32, 128 columns per
+//              tile); O_t += P_t V_j reads P_t from TMEM (16-bit; in columns of its
+//              own at d = 64 fp16, aliased over S_t otherwise) and V_j from shared
+//              memory. One issuer per tile, so one tile's softmax overlaps the
+//              other tile's MMAs and neither tile's MMAs queue behind the other's.
 //   * warps 0-3 / 4-7 (softmax, tile 0 / tile 1): one thread per query row (TMEM
 //              lane). Loads its row of S, masks boundary blocks, keeps the running
 //              max m (base-2 units) and sum l, writes P = 2^(x - m) back to TMEM,
-//              rescales its O row when m grows by more than 2^8, and at the end of
-//              the unit writes O / l and LSE.
+//              rescales its O row when m grows by more than a threshold (2^1 with
+//              packed fp16 exponentials, 2^8 otherwise), and at the end of the unit
+//              writes O / l and LSE.
 //   * Every wait is bounded (globaltimer); a wait that runs out records a timeout
 //     in the status word and every role leaves its loop, so the CTA still frees
 //     its TMEM and exits.
@@ -49,28 +52,7 @@ constexpr int kThreads = 352;        // 8 softmax warps + producer warp + 2 MMA 
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;          // warps 9 and 10: MMA issuers of tile 0 and tile 1
 constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..)
-constexpr float kRescaleThreshold = 8.0f;
-#ifndef EX19_SEPARATE_P
-#define EX19_SEPARATE_P 1  // d = 64 fp16: P in its own TMEM columns (S released early)
-#endif
-#ifndef EX19_SOFTMAX_F2
-#define EX19_SOFTMAX_F2 1  // softmax FMA / adds as paired fp32 (sm_100+ float2 builtins)
-#endif
-#ifndef EX19_TRACE
-#define EX19_TRACE 0  // 1: CTA 0 stamps clock64 at each step of its first unit (debug)
-#endif
-#ifndef EX19_EXP_F16X2
-#define EX19_EXP_F16X2 1  // fp16: exponentials two at a time on packed fp16 arguments
-#endif
-#ifndef EX19_ONEPASS
-#define EX19_ONEPASS 1  // S read from TMEM once (1) or twice, max then exponentials (0)
-#endif
-#ifndef EX19_PV_HALVES
-#define EX19_PV_HALVES 1  // separate P: hand P to the P·V MMAs in two 64-key halves (1) or whole (0)
-#endif
-#ifndef EX19_POLY_PAIRS
-#define EX19_POLY_PAIRS 0  // exp2 polynomial offload: pairs out of every 8 (0 = all on MUFU)
-#endif  // log2 units: rescale O only when m grows > 2^8
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows > 2^8
 
 // Wait sites (for the status word): role << 16 | site
 enum : uint32_t {
@@ -98,16 +80,6 @@ struct Geometry {
   static constexpr int kSmemUsed = kOffMisc + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
 };
-
-// Timeline probe (trace builds): u64 slots [softmax tile 0 | tile 1 | MMA | producer],
-// kTraceBlocks blocks each, kTraceEv events per block.
-constexpr int kTraceBlocks = 48, kTraceEv = 10;
-__device__ __forceinline__ void trace_mark(const FwdParams& p, int role, int k, int jr, int ev) {
-#if EX19_TRACE
-  if (p.trace != nullptr && blockIdx.x == 0 && k == 0 && jr >= 0 && jr < kTraceBlocks)
-    p.trace[(role * kTraceBlocks + jr) * kTraceEv + ev] = clock64();
-#endif
-}
 
 // Rows and key blocks of one query tile of a unit.
 struct TileSpan {
@@ -173,22 +145,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // bf16 P is split into hi + lo halves (two P·V MMAs) so that rounding P to 8
   // significant bits does not dominate the output error; fp16 P has 11 bits.
   constexpr bool kSplitP = BF16;
-  // Of every 8 column pairs, this many take exp2 from the FMA-pipe polynomial
-  // instead of MUFU (fp16 only: the bf16 path keeps P to ~16 bits).
-  constexpr int kPolyPairs = BF16 ? 0 : EX19_POLY_PAIRS;
   // Packed fp16 exponentials (fp16 inputs): x is rounded to fp16 before 2^x, so x
   // must stay small where P is large; the reference max is then moved whenever
   // the row max grows by more than 2^1 instead of 2^8.
-  constexpr bool kF16Exp = !BF16 && (EX19_EXP_F16X2 != 0);
+  constexpr bool kF16Exp = !BF16;
   constexpr float kThresh = kF16Exp ? 1.0f : kRescaleThreshold;
   // TMEM columns. With P over S (d = 128, or bf16 whose split P needs 128 columns):
   // S_t = [128t, 128t+128), P_t aliased over S_t, O_t = [256+128t, ...). With a
   // separate P region (d = 64 fp16): S_t = [128t, ...), P_t = [256+64t, 256+64t+64),
   // O_t = [384+64t, 384+64t+64) — all 512 columns.
-  constexpr bool kSeparateP = (D == 64) && !BF16 && (EX19_SEPARATE_P != 0);
+  constexpr bool kSeparateP = (D == 64) && !BF16;
   // Separate P: the softmax releases the first 64 keys of P (p_half) before it
   // computes the rest, and the first four P·V MMAs run under that second half.
-  constexpr bool kHalves = kSeparateP && (EX19_PV_HALVES != 0) && (EX19_ONEPASS != 0);
+  constexpr bool kHalves = kSeparateP;
   constexpr uint32_t kColS0 = 0, kStrideS = 128;
   constexpr uint32_t kColP0 = kSeparateP ? 256 : 0, kStrideP = kSeparateP ? 64 : 128;
   constexpr uint32_t kColO0 = kSeparateP ? 384 : 256, kStrideO = kSeparateP ? 64 : 128;
@@ -257,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   WaitCtl wc;
   wc.abort_flag = abort_flag;
   wc.status = p.status;
-  wc.limit_ns = p.wait_limit_ns;
+  wc.set_limit(p.wait_limit_ns);
   wc.unit = 0;
 
   if (warp == kProducerWarp) {
@@ -283,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++q_cnt;
         for (int j = u.lo; ok && j < u.hi; ++j) {
-          trace_mark(p, 3, k, j - u.lo, 0);
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t slot = it % S;
             ok = mbar_wait_bounded(bar_empty(slot), ((it / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
@@ -294,18 +262,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
                           c * 64, u.g, j * kBN, u.b);
             ++it;
-            trace_mark(p, 3, k, j - u.lo, 1 + kv);
           }
         }
       }
-      if (!ok) {
-        // Let the copies already in flight land before the CTA can exit.
-        for (uint32_t back = 1; back <= S && back <= it; ++back) {
-          const uint32_t n = it - back;
-          mbar_wait_drain(bar_full(n % S), (n / S) & 1u, wc, kSiteDrainLoads);
-        }
-        if (q_cnt > 0) mbar_wait_drain(bar_q_full, (q_cnt - 1) & 1u, wc, kSiteDrainLoads);
+      // Whether or not this CTA aborted, the copies issued last may still be in
+      // flight (another role can abort after this loop has ended, and then nothing
+      // consumes them): let them land before the CTA can exit.
+      for (uint32_t back = 1; back <= S && back <= it; ++back) {
+        const uint32_t n = it - back;
+        mbar_wait_drain(bar_full(n % S), (n / S) & 1u, wc, kSiteDrainLoads);
       }
+      if (q_cnt > 0) mbar_wait_drain(bar_q_full, (q_cnt - 1) & 1u, wc, kSiteDrainLoads);
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------- MMA issuers, one per tile
@@ -430,11 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           ok = s_block(j_lo);
           for (int j = j_lo; ok && j < j_hi; ++j) {
-            if (t == 0) trace_mark(p, 2, k, j - u.lo, 0);
             if (j + 1 < j_hi && !(ok = s_block(j + 1))) break;
-            if (t == 0) trace_mark(p, 2, k, j - u.lo, 1);
             ok = pv_block(j);
-            if (t == 0) trace_mark(p, 2, k, j - u.lo, 3);
           }
         } else {
           // P over S: PV_t(j-1) is issued before S_t(j), which overwrites the
@@ -484,12 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = span.row0 + r_in_tile;
       float m_ref = -INFINITY;  // reference max (base-2 units) the P values are relative to
       float l = 0.f;            // running sum of P
-      const bool tr = EX19_TRACE && quarter == 0 && lane == 0;
       for (int j = span.lo; j < span.hi; ++j) {
-        const int jr = j - span.lo;
-        if (tr) trace_mark(p, t, k, jr, 0);
         ok = mbar_wait_warp(bar_s_full(t), s_cnt & 1u, wc, kSiteSmxSFull);
-        if (tr) trace_mark(p, t, k, jr, 1);
         if (!ok) break;
         tc_fence_after();
         const int key0 = j * kBN;
@@ -510,17 +470,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool rescale = false;
         bool stop = false;
         // The block body, instantiated twice: blocks that cross no mask boundary
-        // (almost all of them) carry no per-element selects at all. S is read from
-        // TMEM twice: all 128 columns for the row maximum, then 64 at a time for the
-        // exponentials, which keeps the live registers of a thread well under 168.
+        // (almost all of them) carry no per-element selects at all.
         auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
           constexpr bool M = decltype(masked_tag)::value;
-#if EX19_ONEPASS
           // One TMEM read of S (128 columns). S is released right away, the row
           // maximum and the exponentials both work from these registers.
           uint32_t sr[128];
           tmem_ld_x128(tS, sr);
-          if (tr) trace_mark(p, t, k, jr, 2);
           if constexpr (kSeparateP) {  // S is in registers: the next S MMA may overwrite it
             tc_fence_before();
             mbar_arrive(bar_s_free(t));
@@ -541,7 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               mx = row_max128(sv);
           }
-          if (tr) trace_mark(p, t, k, jr, 3);
           const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
           if (bm > m_ref + kThresh) {
             alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
@@ -574,14 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           };
-          if (tr) trace_mark(p, t, k, jr, 4);
-#if EX19_SOFTMAX_F2
           const float2 c2 = make_float2(Cs, Cs);
           const float2 nmu2 = make_float2(-mu, -mu);
           float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#else
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
-#endif
           // P in 32-column chunks of 16 packed registers, stored to TMEM (P hi at
           // column c/2 of the P region; split P keeps each 64-key half h as
           // [hi 32 columns | lo 32 columns] at column 64h).
@@ -612,13 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                   const __half2 s2 = __hadd2(*reinterpret_cast<__half2*>(&prev),
                                              *reinterpret_cast<__half2*>(&pp));
-#if EX19_SOFTMAX_F2
                   acc[(c >> 2) & 1] = __fadd2_rn(acc[(c >> 2) & 1], __half22float2(s2));
-#else
-                  const float2 f = __half22float2(s2);
-                  acc[(c >> 1) & 3] += f.x;
-                  acc[((c >> 1) + 1) & 3] += f.y;
-#endif
                 }
               }
               tmem_st_x16(tP + (c0 >> 1), pk);
@@ -630,36 +574,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mbar_arrive(bar_p_half(t));
                 }
               }
-              if (tr && (c0 & 32)) trace_mark(p, t, k, jr, 5 + (c0 >> 6));
               continue;
             }
 #pragma unroll
             for (int c = c0; c < c0 + 32; c += 2) {
-#if EX19_SOFTMAX_F2
               const float2 x = __ffma2_rn(
                   make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nmu2);
               const float x0 = x.x, x1 = x.y;
-#else
-              const float x0 = fmaf(__uint_as_float(sr[c]), Cs, -mu);
-              const float x1 = fmaf(__uint_as_float(sr[c + 1]), Cs, -mu);
-#endif
-              float p0, p1;
-              if (kPolyPairs > 0 && ((c >> 1) & 7) < kPolyPairs) {
-                exp2_poly_pair(x0, x1, p0, p1);  // on the FMA/ALU pipes
-              } else {
-                p0 = ex2_approx(x0);  // on MUFU
-                p1 = ex2_approx(x1);
-              }
+              float p0 = ex2_approx(x0);
+              float p1 = ex2_approx(x1);
               if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
                 p0 = (c >= vis_lo && c < vis_hi) ? p0 : 0.f;
                 p1 = (c + 1 >= vis_lo && c + 1 < vis_hi) ? p1 : 0.f;
               }
-#if EX19_SOFTMAX_F2
               acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
-#else
-              acc[c & 3] += p0;
-              acc[(c + 1) & 3] += p1;
-#endif
               const uint32_t hi = pack2(p0, p1, BF16);
               pk[(c - c0) >> 1] = hi;
               if constexpr (kSplitP)
@@ -681,129 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar_p_half(t));
               }
             }
-            if (tr && (c0 & 32)) trace_mark(p, t, k, jr, 5 + (c0 >> 6));
           }
-#else
-          float mx;  // max over visible columns of Cs·s / C (i.e. of ±s)
-          {
-            float m8[8];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t sr[64];
-              tmem_ld_x64(tS + 64 * h, sr);
-              float sv[64];
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                sv[c] = neg ? -__uint_as_float(sr[c]) : __uint_as_float(sr[c]);
-                if constexpr (M) {
-                  if (64 * h + c < vis_lo || 64 * h + c >= vis_hi) sv[c] = -INFINITY;
-                }
-              }
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float a = (h == 0) ? sv[i] : fmaxf(m8[i], sv[i]);
-#pragma unroll
-                for (int c = 8; c < 64; c += 8) a = fmaxf(a, sv[c + i]);
-                m8[i] = a;
-              }
-            }
-            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          }
-          const float bm = (mx == -INFINITY) ? -INFINITY : mx * C;
-          if (bm > m_ref + kThresh) {
-            alpha = ex2_approx(m_ref - bm);  // 0 when m_ref is -inf
-            m_ref = bm;
-            rescale = true;
-          }
-          const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-          if constexpr (kSeparateP) {
-            // P_t and O_t are read by this tile's previous P·V: wait until it is done.
-            if (s_cnt > 0) {
-              if (!mbar_wait_warp(bar_pv_done(t), (s_cnt - 1) & 1u, wc, kSiteSmxPvDone)) {
-                stop = true;
-                return;
-              }
-              tc_fence_after();
-            }
-          }
-          if (tr) trace_mark(p, t, k, jr, 4);
-#if EX19_SOFTMAX_F2
-          const float2 c2 = make_float2(Cs, Cs);
-          const float2 nmu2 = make_float2(-mu, -mu);
-          float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#else
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
-#endif
-          // Second pass, 64 columns at a time; P in 32-column chunks of 16 packed
-          // registers, stored to TMEM (P hi at column c/2 of the P region, P lo at
-          // 64 + c/2).
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t sr[64];
-            tmem_ld_x64(tS + 64 * h, sr);
-            if (tr) trace_mark(p, t, k, jr, 5 + 2 * h);
-            if constexpr (kSeparateP) {
-              if (h == 1) {  // S is fully in registers: the next S MMA may overwrite it
-                tc_fence_before();
-                mbar_arrive(bar_s_free(t));
-              }
-            }
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-              uint32_t pk[16];
-              uint32_t pk_lo[16];
-#pragma unroll
-              for (int c = c0; c < c0 + 32; c += 2) {
-                const int cc = 64 * h + c;  // column within the block
-#if EX19_SOFTMAX_F2
-                const float2 x = __ffma2_rn(
-                    make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nmu2);
-                const float x0 = x.x, x1 = x.y;
-#else
-                const float x0 = fmaf(__uint_as_float(sr[c]), Cs, -mu);
-                const float x1 = fmaf(__uint_as_float(sr[c + 1]), Cs, -mu);
-#endif
-                float p0, p1;
-                if (kPolyPairs > 0 && ((cc >> 1) & 7) < kPolyPairs) {
-                  exp2_poly_pair(x0, x1, p0, p1);  // on the FMA/ALU pipes
-                } else {
-                  p0 = ex2_approx(x0);  // on MUFU
-                  p1 = ex2_approx(x1);
-                }
-                if constexpr (M) {  // masked keys get exactly 0 (also when scale = 0)
-                  p0 = (cc >= vis_lo && cc < vis_hi) ? p0 : 0.f;
-                  p1 = (cc + 1 >= vis_lo && cc + 1 < vis_hi) ? p1 : 0.f;
-                }
-#if EX19_SOFTMAX_F2
-                acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
-#else
-                acc[c & 3] += p0;
-                acc[(c + 1) & 3] += p1;
-#endif
-                const uint32_t hi = pack2(p0, p1, BF16);
-                pk[(c - c0) >> 1] = hi;
-                if constexpr (kSplitP)
-                  pk_lo[(c - c0) >> 1] =
-                      pack2(p0 - low_as_float(hi, BF16), p1 - high_as_float(hi, BF16), BF16);
-              }
-              if constexpr (kSplitP) {
-                // P over S, half h: hi at columns 64h .. 64h+31, lo at 64h+32 .. 64h+63,
-                // i.e. inside the S columns this thread has already read.
-                tmem_st_x16(tP + 64 * h + (c0 >> 1), pk);
-                tmem_st_x16(tP + 64 * h + 32 + (c0 >> 1), pk_lo);
-              } else {
-                tmem_st_x16(tP + 32 * h + (c0 >> 1), pk);  // P at columns 0 .. 63
-              }
-            }
-            if (tr) trace_mark(p, t, k, jr, 6 + 2 * h);
-          }
-#endif
-#if EX19_SOFTMAX_F2
           const float rowsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-#else
-          const float rowsum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-#endif
           l = l * alpha + rowsum;
         };
         if (masked)
@@ -832,7 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar_p_full(t));
-        if (tr) trace_mark(p, t, k, jr, 9);
       }
       if (!ok) break;
       // ---- epilogue: O / l and LSE for this tile

@@ -130,22 +130,16 @@ struct KvItem {
   bool bad;    // paged: the sequence length is out of range (nothing is computed)
 };
 
-// Maximum of a 64-value half row: 8 independent chains (8 values each), then a tree.
+// Maximum of a 64-value half row: 8 independent chains (8 values each, 3-input
+// maxima), then a tree.
 __device__ __forceinline__ float row_max64(const float (&s)[64]) {
   float m[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-#if EX19_MAX3
     float a = max3f(s[i], s[8 + i], s[16 + i]);
     a = max3f(a, s[24 + i], s[32 + i]);
     a = max3f(a, s[40 + i], s[48 + i]);
     m[i] = fmaxf(a, s[56 + i]);
-#else
-    float a = s[i];
-#pragma unroll
-    for (int k = 8; k < 64; k += 8) a = fmaxf(a, s[k + i]);
-    m[i] = a;
-#endif
   }
   return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
@@ -289,7 +283,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
   WaitCtl wc;
   wc.abort_flag = abort_flag;
   wc.status = p.status;
-  wc.limit_ns = p.wait_limit_ns;
+  wc.set_limit(p.wait_limit_ns);
   wc.unit = blockIdx.x;
   if (it.bad) {
     // Nothing of this batch entry is computed or written; report it once per CTA.
@@ -364,8 +358,10 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
           }
         }
       }
-      if (!ok && lane == 0) {
-        // Let the copies already in flight land before the CTA can exit.
+      if (lane == 0) {
+        // Whether or not this CTA aborted, the copies issued last may still be in
+        // flight (another role can abort after this loop has ended, and then nothing
+        // consumes them): let them land before the CTA can exit.
         for (uint32_t back = 1; back <= S && back <= n; ++back) {
           const uint32_t m = n - back;
           mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrainLoads);

@@ -75,7 +75,7 @@ cudaError_t launch_fp8(bool out_f32, const Fp8LaunchArgs& a);
 // The backward pass: the D / LSE2 pass, the dQ kernel and the dK / dV kernel.
 cudaError_t launch_bwd(int d, bool bf16, bool out_f32, const BwdLaunchArgs& a);
 cudaError_t launch_wait_probe(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
-cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
+cudaError_t launch_exp2_probe(const float* x, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream);
 
 }  // namespace ex19

@@ -16,7 +16,6 @@ struct FwdParams {
   int units_per_bh;     // ceil(L / 256): 256-row work units per (batch, head)
   int num_units;        // B * Hq * units_per_bh
   unsigned long long wait_limit_ns;
-  unsigned long long* trace;  // timeline probe buffer (trace builds only), else null
 };
 
 }  // namespace ex19

@@ -19,38 +19,33 @@ __global__ void wait_probe_kernel(uint32_t* status, unsigned long long limit_ns)
   WaitCtl wc;
   wc.abort_flag = &abort_flag;
   wc.status = status;
-  wc.limit_ns = limit_ns;
+  wc.set_limit(limit_ns);
   wc.unit = 0;
   mbar_wait_warp(smem_u32(&bar), 0, wc, 0x50001);
 }
 
 
-// Element-wise 2^x by the polynomial path and by MUFU ex2, for accuracy tests.
-__global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n) {
+// Element-wise 2^x by the fp32 MUFU instruction and, when y_f16 is given, by the
+// packed fp16 one (arguments rounded to fp16 first), for accuracy tests.
+__global__ void exp2_probe_kernel(const float* x, float* y_mufu, float* y_f16, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (i >= n) return;
   const float a = x[i];
   const float b = (i + 1 < n) ? x[i + 1] : 0.f;
-  float p0, p1;
-  exp2_poly_pair(a, b, p0, p1);
-  y_poly[i] = p0;
   y_mufu[i] = ex2_approx(a);
-  if (y_f16 != nullptr) {  // the packed fp16 path: arguments rounded to fp16 first
+  if (y_f16 != nullptr) {
     __half2 h = __floats2half2_rn(a, b);
     const uint32_t r = ex2_f16x2(*reinterpret_cast<uint32_t*>(&h));
     y_f16[i] = __half2float(__ushort_as_half(static_cast<unsigned short>(r & 0xFFFFu)));
     if (i + 1 < n) y_f16[i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(r >> 16)));
   }
-  if (i + 1 < n) {
-    y_poly[i + 1] = p1;
-    y_mufu[i + 1] = ex2_approx(b);
-  }
+  if (i + 1 < n) y_mufu[i + 1] = ex2_approx(b);
 }
 
-cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, float* y_f16, int n,
+cudaError_t launch_exp2_probe(const float* x, float* y_mufu, float* y_f16, int n,
                               cudaStream_t stream) {
   const int pairs = (n + 1) / 2;
-  exp2_probe_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y_poly, y_mufu, y_f16, n);
+  exp2_probe_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y_mufu, y_f16, n);
   return cudaGetLastError();
 }
 

@@ -9,16 +9,12 @@
 
 #include "sm103_ptx.cuh"
 
-#ifndef EX19_MAX3
-#define EX19_MAX3 1  // row max with 3-input max.f32 (1) or two-input fmaxf (0)
-#endif
-
 namespace ex19 {
 
-// Maximum of a 128-value row: 8 independent chains (16 values each), then a tree.
+// Maximum of a 128-value row: 8 independent chains (16 values each, 3-input
+// maxima), then a tree.
 __device__ __forceinline__ float row_max128(const float (&s)[128]) {
   float m[8];
-#if EX19_MAX3
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     float a = max3f(s[i], s[8 + i], s[16 + i]);
@@ -27,16 +23,6 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
     m[i] = fmaxf(a, s[120 + i]);
   }
   return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
-#else
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float a = s[i];
-#pragma unroll
-    for (int k = 8; k < 128; k += 8) a = fmaxf(a, s[k + i]);
-    m[i] = a;
-  }
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-#endif
 }
 
 // Minimum of a 128-value row (used when the scale is negative).

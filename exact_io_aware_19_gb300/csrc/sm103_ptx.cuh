@@ -9,8 +9,6 @@
 #include <cstdint>
 #include <cuda.h>
 
-#include "exp2_poly.h"
-
 namespace ex19 {
 
 // ---------------------------------------------------------------- status words
@@ -59,8 +57,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe (never suspends): used by the MMA issuer, which polls several
-// barriers in turn and must not sleep on one while another is ready.
+// Non-blocking probe (never suspends): used instead of the potentially blocking
+// try_wait when the wait limit is shorter than kMaxSuspendNs.
 __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -76,26 +74,25 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
 // Probe with a suspend-time hint: a thread whose phase is not complete sleeps in
 // hardware until the phase completes or `hint_ns` passes, instead of spinning and
 // taking issue slots from the warps that do the work.
-#ifndef EX19_SPIN
-#define EX19_SPIN 0  // 1: bounded waits spin on the non-blocking test instead of try_wait
-#endif
-#ifndef EX19_SUSPEND_NS
-#define EX19_SUSPEND_NS 1000000  // 1 ms: also the worst-case reaction time to an abort (0: no hint)
-#endif
-__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity) {
-#if EX19_SUSPEND_NS == 0
-  return mbar_test(bar, parity);
-#endif
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(EX19_SUSPEND_NS))
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
+
+// Longest single sleep of a waiting thread (1 ms): also the worst-case time a role
+// takes to notice that another role of its CTA has aborted.
+constexpr uint64_t kMaxSuspendNs = 1000000ull;
+// Waits that drain copies and MMAs already issued (after an abort) run for at least
+// this long (1 s), whatever the configured limit: those operations always complete,
+// and the CTA must not free its shared memory or TMEM while they are in flight.
+constexpr uint64_t kDrainFloorNs = 1000000000ull;
 
 // Shared control block of one CTA for bounded waits.
 struct WaitCtl {
@@ -103,6 +100,19 @@ struct WaitCtl {
   uint32_t* status;               // global status word (may be null)
   uint64_t limit_ns;              // per-wait limit
   uint32_t unit;                  // current work unit, for the report
+  uint32_t hint_ns;               // sleep hint of one poll: min(limit, kMaxSuspendNs)
+  uint64_t drain_ns;              // limit of drain waits: max(limit, kDrainFloorNs)
+  // Limits shorter than kMaxSuspendNs: every probe is non-blocking, so a wait runs
+  // out as soon as it has waited for longer than the limit. (A potentially blocking
+  // try_wait may sleep in hardware until its phase completes, for a time the
+  // hardware chooses, before the limit is ever looked at.)
+  bool poll_only;
+  __device__ __forceinline__ void set_limit(uint64_t ns) {
+    limit_ns = ns;
+    hint_ns = static_cast<uint32_t>(ns < kMaxSuspendNs ? ns : kMaxSuspendNs);
+    drain_ns = ns > kDrainFloorNs ? ns : kDrainFloorNs;
+    poll_only = ns < kMaxSuspendNs;
+  }
 };
 
 __device__ __forceinline__ void record_error(const WaitCtl& c, uint32_t code, uint32_t where) {
@@ -119,18 +129,17 @@ __device__ __forceinline__ void record_error(const WaitCtl& c, uint32_t code, ui
 
 // Slow path of a bounded wait: polls until phase `parity` of `bar` completes, the
 // limit runs out (recording a timeout) or, when `honor_abort`, another role of
-// the CTA has aborted. Returns true only when the phase completed.
+// the CTA has aborted. Returns true only when the phase completed. The sleep hint
+// never exceeds the limit, so a short limit times out as soon as a wait has to wait.
+// Drain waits (`honor_abort` false) use at least kDrainFloorNs.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                             uint32_t where, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = honor_abort ? c.limit_ns : c.drain_ns;
   while (true) {
-#if EX19_SPIN
-    if (mbar_poll(bar, parity)) return true;  // pure spin: no suspension at all
-#else
-    if (mbar_test_sleep(bar, parity)) return true;
-#endif
+    if (c.poll_only ? mbar_poll(bar, parity) : mbar_test_sleep(bar, parity, c.hint_ns)) return true;
     if (honor_abort && *c.abort_flag) return false;
-    if (globaltimer_ns() - t0 > c.limit_ns) {
+    if (globaltimer_ns() - t0 >= limit) {
       record_error(c, kStatusTimeout, where);
       return false;
     }
@@ -140,7 +149,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 // Waits for phase `parity` of `bar`; false (never an endless wait) on timeout or abort.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                                   uint32_t where) {
-  if (mbar_test(bar, parity)) return true;
+  if (c.poll_only ? mbar_poll(bar, parity) : mbar_test(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, c, where, true);
 }
 
@@ -148,7 +157,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // finish before the CTA releases its TMEM and exits.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                                 uint32_t where) {
-  if (mbar_test(bar, parity)) return true;
+  if (c.poll_only ? mbar_poll(bar, parity) : mbar_test(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, c, where, false);
 }
 
@@ -361,50 +370,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// Packed pairs of fp32 (one 64-bit register) and the sm_100+ paired FMA / add.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-// 2^x0, 2^x1 on the FMA and ALU pipes instead of MUFU: x = j + f with j = rint(x)
-// (1.5·2^23 rounding trick) and f in [-1/2, 1/2]; 2^f from the fitted polynomial
-// of exp2_poly.h; j is added to the exponent field. Inputs are clamped to
-// [-125, +inf) so the result stays a normal number (or a negligible 2^-125).
-__device__ __forceinline__ void exp2_poly_pair(float x0, float x1, float& y0, float& y1) {
-  x0 = fmaxf(x0, -125.f);
-  x1 = fmaxf(x1, -125.f);
-  const uint64_t xx = f2_pack(x0, x1);
-  const uint64_t t = f2_add(xx, f2_pack(12582912.f, 12582912.f));
-  const uint64_t jf = f2_add(t, f2_pack(-12582912.f, -12582912.f));
-  const uint64_t f = f2_fma(jf, f2_pack(-1.f, -1.f), xx);
-  uint64_t p = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
-  p = f2_fma(p, f, f2_pack(kExp2C1, kExp2C1));
-  p = f2_fma(p, f, f2_pack(kExp2C0, kExp2C0));
-  float t0, t1, p0, p1;
-  f2_unpack(t, t0, t1);
-  f2_unpack(p, p0, p1);
-  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
 // Two exponentials in one MUFU operation: (2^a, 2^b) for a packed pair of fp16

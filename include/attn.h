@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 typedef enum {
     ATTN_OK = 0,
@@ -182,9 +182,14 @@ attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void 
  *   - Problems needing more scratch than 256 bytes return ATTN_ERR_WORKSPACE (none
  *     do today).
  *   - All calls on a device share the array, and each call clears its status word
- *     first: calls that overlap on the GPU (other streams, other threads) race.
+ *     (after its arguments are validated: a rejected call enqueues nothing): calls
+ *     that overlap on the GPU (other streams, other threads) race.
  *   - The first call on a device looks up the array's address (and may load the
- *     library's device code); make it before any stream capture starts.
+ *     library's device code); make it before any stream capture starts. A device
+ *     reset (cudaDeviceReset) invalidates that address: the first call in the new
+ *     context looks it up again, and the same rule applies to it.
+ *   - On a device other than compute capability 10.3 the call returns
+ *     ATTN_ERR_UNSUPPORTED, as attn_fwd does.
  *   - A device-side timeout is recorded only in that shared word, which no entry
  *     point reads; use attn_fwd with a workspace when that report is needed.
  */
@@ -289,7 +294,12 @@ int attn_get_path_policy(void);
  * Sets the limit, in nanoseconds, of every device-side wait in kernels launched
  * afterwards by this process (default 4e9 = 4 s; 0 restores the default). A wait
  * that runs out records ATTN_ERR_TIMEOUT in the workspace and makes every role of
- * the kernel stop and release its resources.
+ * the kernel stop, let the copies and MMAs it already issued complete (these drain
+ * waits run for at least 1 s whatever the limit), free its tensor memory and exit.
+ * Limits below 1 ms make every wait poll without sleeping in hardware, so that a
+ * wait runs out as soon as it has lasted longer than the limit: a limit of a few
+ * nanoseconds makes a kernel time out at its first wait that has to wait at all
+ * (used by the tests of the timeout path; no fault is involved).
  */
 void attn_set_wait_limit_ns(uint64_t limit_ns);
 
@@ -303,15 +313,12 @@ attn_status_t attn_debug_wait_probe(void *workspace, size_t workspace_bytes,
                                     uint64_t limit_ns, void *stream);
 
 /*
- * Evaluates 2^x[i] for i < n with the exp2 paths of the attention kernel: the
- * FMA-pipe polynomial (y_poly), the fp32 MUFU instruction (y_mufu) and, when
- * y_f16 is not NULL, the packed fp16 MUFU instruction on arguments rounded to
- * fp16 (y_f16, widened back to float). Device float32 arrays; used by the
- * accuracy tests. The polynomial (degree 3, fitted by fit_exp2_poly.py) is valid
- * for x <= 128; inputs below -125 are clamped to -125.
+ * Evaluates 2^x[i] for i < n with the exp2 paths of the attention kernels: the
+ * fp32 MUFU instruction (y_mufu) and, when y_f16 is not NULL, the packed fp16 MUFU
+ * instruction on arguments rounded to fp16 (y_f16, widened back to float). Device
+ * float32 arrays; used by the accuracy tests.
  */
-attn_status_t attn_debug_exp2(const float *x, float *y_poly, float *y_mufu, float *y_f16, int n,
-                              void *stream);
+attn_status_t attn_debug_exp2(const float *x, float *y_mufu, float *y_f16, int n, void *stream);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status_t s);

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(ex.library_path())
     missing = [n for n in declared_functions() if not hasattr(raw, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert lib.attn_abi_version() == 2
+    assert lib.attn_abi_version() == 3
 
 
 def test_status_strings(lib):

@@ -49,6 +49,44 @@ def test_scale_values(scale, kernel_path):
         compare(q, k, v, "fp16", causal, -1, scale, label=f"scale={scale} causal={causal}")
 
 
+def _planted_max_growth(L, seed, sign=1.0):
+    """fp16 d=64 inputs whose row maxima jump at planted keys: every even row's query
+    is the same direction u, odd rows point the other way (their maxima stay put),
+    and key rows 5, 150 and 330 are u scaled by 4, 20 and 40 (scores up to about 50,
+    jumps of 2.9 and 3.6 in base-2 units at scale 1/8). Key 150 lies in the first
+    64-key half of block 1, key 330 in the second half of block 2."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.where(torch.rand(64, generator=g) < 0.5, -0.125, 0.125)  # |u|^2 = 1
+    q = torch.randn(1, L, 2, 64, generator=g) * 0.1
+    k = torch.randn(1, L, 2, 64, generator=g) * 0.1
+    v = torch.randn(1, L, 2, 64, generator=g)
+    rows = torch.arange(L)
+    q += sign * torch.where(rows % 2 == 0, 1.0, -0.01)[None, :, None, None] * u
+    for key, c in ((5, 4.0), (150, 20.0), (330, 40.0)):
+        if key < L:
+            k[0, key] = c * u
+    return q.half(), k.half(), v.half()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_planted_max_growth_square_kernel(causal):
+    """The square kernel's online maximum against planted score jumps of 2.9 and 3.6
+    (base-2 units) inside later key blocks, at different key positions of a block, with
+    rows that jump and rows that do not in one warp (the O rescale is per row); also
+    with a negative scale."""
+    import exact_io_aware_19_gb300 as ex
+    old = ex.set_path_policy(ex.PATH_SQUARE)
+    try:
+        for L in (512, 700):
+            q, k, v = _planted_max_growth(L, seed=L)
+            compare(q, k, v, "fp16", causal, -1, 0.125, label=f"planted L={L} causal={causal}")
+            q, k, v = _planted_max_growth(L, seed=L + 1, sign=-1.0)
+            compare(q, k, v, "fp16", causal, -1, -0.125,
+                    label=f"planted L={L} causal={causal} negative scale")
+    finally:
+        ex.set_path_policy(old)
+
+
 def test_gqa_group_sizes(kernel_path):
     for hq, hkv in [(8, 8), (8, 4), (8, 2), (8, 1)]:
         q, k, v = si.random_qkv(1, 513, hq, hkv, 128, dtype="bf16", seed=hq * 10 + hkv)
@@ -166,24 +204,18 @@ def test_wrong_device_type_rejected():
         ex.attn_fwd(q, q, q)
 
 
-def test_exp2_polynomial_error_bound():
-    """The FMA-pipe exp2 (fitted degree-3 polynomial + exponent insertion) stays within
-    its fitted relative-error bound against float64 2^x, and MUFU ex2 stays near 2^x."""
-    import re
+def test_exp2_mufu_accuracy():
+    """The fp32 MUFU ex2 the softmax uses stays within 1e-6 relative of 2^x, and far
+    below the normal range it gives a tiny non-negative number, never inf or nan."""
     import exact_io_aware_19_gb300 as ex
-    hdr = open(ex.__file__.replace("__init__.py", "csrc/exp2_poly.h")).read()
-    bound = float(re.search(r"kExp2PolyMaxRelErr = ([0-9.e+-]+)f", hdr).group(1))
     x = torch.cat([torch.linspace(-124.0, 8.0, 1 << 20),
                    torch.tensor([0.0, -0.5, 0.5, 1.0, -1.0])])
-    yp, ym = ex.debug_exp2(x.cuda())
+    ym = ex.debug_exp2(x.cuda())
     ref = torch.exp2(x.double())
-    rel_p = ((yp.double().cpu() - ref) / ref).abs().max().item()
     rel_m = ((ym.double().cpu() - ref) / ref).abs().max().item()
-    assert rel_p <= bound * 1.05 + 2e-7, (rel_p, bound)
     assert rel_m <= 1e-6
-    # clamping: far below the range gives a tiny positive number, never inf/nan
-    yp, _ = ex.debug_exp2(torch.tensor([-1000.0, -200.0, -126.0], device="cuda"))
-    assert torch.isfinite(yp).all() and (yp >= 0).all() and (yp < 1e-37).all()
+    ym = ex.debug_exp2(torch.tensor([-1000.0, -200.0, -126.0], device="cuda"))
+    assert torch.isfinite(ym).all() and (ym >= 0).all() and (ym < 1e-37).all()
 
 
 def test_exp2_f16x2_accuracy():
@@ -192,7 +224,7 @@ def test_exp2_f16x2_accuracy():
     absolute error within the fp16 subnormal spacing 2^-24 below that."""
     import exact_io_aware_19_gb300 as ex
     x = torch.linspace(-30.0, 1.0, 1 << 16).half().float()  # exactly representable
-    _, _, yh = ex.debug_exp2(x.cuda(), with_f16=True)
+    _, yh = ex.debug_exp2(x.cuda(), with_f16=True)
     ref = torch.exp2(x.double())
     got = yh.double().cpu()
     normal = x >= -14.0
