@@ -15,15 +15,19 @@
 //   * a problem whose workspace need exceeds 256 bytes is rejected with
 //     ATTN_ERR_WORKSPACE (no shape needs more today);
 //   * all calls on a device share the one array. Each call clears the status word
-//     at its start (on the call's stream), so calls that overlap on the GPU — on
-//     different streams, or from different threads — race on it; serialise them;
-//   * the first call on each device looks up the array's device address with
-//     cudaGetSymbolAddress (loading this file's module if needed). Make that first
-//     call before any stream capture begins;
+//     (on the call's stream, after its arguments are validated), so calls that
+//     overlap on the GPU — on different streams, or from different threads — race
+//     on it; serialise them;
+//   * the first call on each device, and the first after that device's context was
+//     destroyed and created again (cudaDeviceReset), looks up the array's device
+//     address with cudaGetSymbolAddress (loading this file's module if needed).
+//     Make that first call before any stream capture begins;
 //   * a device-side timeout is recorded in this shared status word, which no
 //     other entry point reads; callers that need that report should use attn_fwd
 //     with their own workspace and attn_fwd_sync_status.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 #include <string>
@@ -32,6 +36,11 @@
 
 namespace ex19 {
 void set_last_error_detail(const std::string& msg);  // defined in attn_api.cu
+attn_status_t current_sm103_device(int* dev);        // defined in attn_api.cu
+attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int L, int Hq, int Hkv, int d, int causal, int window_left, float scale,
+                       attn_dtype_t dtype, attn_out_t out_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream, size_t clear_status_bytes);
 }
 
 namespace {
@@ -42,24 +51,66 @@ constexpr size_t kStatusWordBytes = 16;
 // The scratch of attn_fwd_noalloc (holds the kernel's status word).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on device `dev`, looked up once per device
-// with that device current (the caller of attn_fwd_noalloc made it current).
+// Driver calls that identify the current context (cuCtxGetId gives an id that is
+// never reused within the process, so a context created again after a reset gets
+// a new one).
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+  static std::once_flag once;
+  static CtxFns fns;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return fns;
+}
+
+// Id of the calling thread's current context, or 0 when there is none (or the
+// driver cannot say).
+unsigned long long current_ctx_id() {
+  const CtxFns& f = ctx_fns();
+  if (f.get_current == nullptr || f.get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  return f.get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_noalloc_scratch on device `dev` (current), cached per device
+// and context: a context destroyed and created again (cudaDeviceReset) may load
+// the module at another address, so a new context id triggers a new lookup.
 void* scratch_on_device(int dev, cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   if (dev < 0 || dev >= 64) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  const unsigned long long id = current_ctx_id();
+  if (addr[dev] == nullptr || id == 0 || id != ctx_of[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) {
+      cudaGetLastError();  // leave no sticky error behind for unrelated calls
+      addr[dev] = nullptr;
       *err = e;
       return nullptr;
     }
     addr[dev] = p;
+    // the lookup made the primary context current if none was
+    ctx_of[dev] = (id != 0) ? id : current_ctx_id();
   }
   *err = cudaSuccess;
   return addr[dev];
@@ -86,20 +137,17 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
     return ATTN_ERR_WORKSPACE;
   }
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  void* scratch = (e == cudaSuccess) ? scratch_on_device(dev, &e) : nullptr;
+  const attn_status_t st = ex19::current_sm103_device(&dev);  // no image for other devices
+  if (st != ATTN_OK) return st;
+  cudaError_t e = cudaSuccess;
+  void* scratch = scratch_on_device(dev, &e);
   if (scratch == nullptr) {
     ex19::set_last_error_detail(std::string("locating the no-allocation scratch: ") +
                                 cudaGetErrorName(e));
     return ATTN_ERR_CUDA;
   }
-  // The status word must start at zero (the kernel records only the first error).
-  e = cudaMemsetAsync(scratch, 0, kStatusWordBytes, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    ex19::set_last_error_detail(std::string("clearing the scratch status word: ") +
-                                cudaGetErrorName(e));
-    return ATTN_ERR_CUDA;
-  }
-  return attn_fwd(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, scale, dtype,
-                  out_dtype, scratch, kNoAllocScratchBytes, stream);
+  // The status word must start at zero (the kernel records only the first error);
+  // attn_fwd's checks run first, so a rejected call enqueues nothing.
+  return ex19::fwd_impl(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, scale, dtype,
+                        out_dtype, scratch, kNoAllocScratchBytes, stream, kStatusWordBytes);
 }

@@ -63,3 +63,43 @@ def test_noalloc_rejects_bad_arguments_without_launching():
     assert _noalloc(lib, z, z, z, z, lse, False, 5, 0.125, False) == 2  # window needs causal
     z96 = torch.zeros(1, 16, 1, 96, dtype=torch.float16, device="cuda")
     assert _noalloc(lib, z96, z96, z96, z96, lse, True, -1, 0.125, False) == 2  # d = 96
+
+
+def test_noalloc_rejects_bad_values_after_the_scratch_lookup():
+    """Shapes that pass the scratch-size check but values that attn_fwd rejects: the
+    call returns attn_fwd's code (nothing is enqueued before validation), and the next
+    valid call still gives attn_fwd's bits."""
+    lib = ex.load_library()
+    q, k, v = si.random_qkv(1, 300, 2, 2, 64, dtype="fp16", seed=5, device="cuda")
+    o_ref, lse_ref = ex.attn_fwd(q, k, v, causal=True, scale=0.125)
+    ex.sync_status()
+    o, lse = torch.empty_like(o_ref), torch.empty_like(lse_ref)
+    assert _noalloc(lib, q, k, v, o, lse, True, -1, float("inf"), False) == 1  # scale not finite
+    assert _noalloc(lib, q, k, v, o, lse, True, -1, float("nan"), False) == 1
+    f = lib.attn_fwd_noalloc
+    stream = torch.cuda.current_stream().cuda_stream
+    assert f(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, lse.data_ptr(), 1, 300, 2, 2, 64, 1,
+             -1, 0.125, 0, 0, stream) == 1  # null o
+    assert f(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 300, 2, 2,
+             64, 1, -1, 0.125, 7, 0, stream) == 1  # bad dtype
+    assert f(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 300, 2, 2,
+             64, 1, -1, 0.125, 0, 5, stream) == 1  # bad out_dtype
+    assert _noalloc(lib, q, k, v, o, lse, True, -1, 0.125, False) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+def test_noalloc_python_binding_matches_attn_fwd():
+    """The Python binding of the same name (argument marshalling only) on two calls in
+    a row, against attn_fwd through its own workspace."""
+    q, k, v = si.random_qkv(2, 640, 8, 2, 128, dtype="bf16", seed=9, device="cuda")
+    o_ref, lse_ref = ex.attn_fwd(q, k, v, causal=True, window_left=200, scale=None)
+    ex.sync_status()
+    for _ in range(2):
+        o = torch.full_like(o_ref, float("nan"))
+        lse = torch.full_like(lse_ref, float("nan"))
+        ex.attn_fwd_noalloc(q, k, v, o, lse, causal=True, window_left=200)
+        torch.cuda.synchronize()
+        d_o = (o.double() - o_ref.double()).abs()
+        assert d_o.max().item() <= MAX_ABS_O and d_o.mean().item() <= MEAN_ABS_O
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
