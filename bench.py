@@ -59,7 +59,7 @@ TRAFFIC_BY_SOURCE = {
 
 
 KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "row_ops.cuh", "sm103_ptx.cuh", "tmem_io.cuh",
-                  "attn_params.h", "exp2_poly.h", "attn_fwd_d64.cu", "attn_fwd_d128.cu")
+                  "attn_params.h", "attn_fwd_d64.cu", "attn_fwd_d128.cu")
 
 
 def kernel_source_hash() -> str:
@@ -77,6 +77,51 @@ def measured_peaks():
         with open(path) as f:
             return json.load(f), "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def loglog_slope(xs, ys):
+    """Least-squares slope of log(y) against log(x)."""
+    lx, ly = np.log(np.asarray(xs, dtype=np.float64)), np.log(np.asarray(ys, dtype=np.float64))
+    lx -= lx.mean()
+    return float(np.dot(lx, ly - ly.mean()) / np.dot(lx, lx))
+
+
+def time_launches(fn, flush, stream, reps: int, warm: int = 1):
+    """Median CUDA-event time (ms) of ``fn()`` on ``stream``, L2 flushed before each
+    launch outside the events; the first ``warm`` launches are not counted."""
+    times = []
+    for r in range(warm + reps):
+        flush.fill_(float(r))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if r >= warm:
+            times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def mm_rate(dtype, dev, n: int = 8192, reps: int = 10):
+    """Best torch.mm rate (TFLOP/s) of an n x n x n product in ``dtype`` (fp32 accumulate),
+    CUDA events, after a warm-up: the same-run tensor-peak check beside the divisor."""
+    a = torch.randn(n, n, device=dev).to(dtype)
+    b = torch.randn(n, n, device=dev).to(dtype)
+    c = torch.empty(n, n, device=dev, dtype=dtype)
+    for _ in range(3):
+        torch.mm(a, b, out=c)
+    best = float("inf")
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.mm(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b, c
+    return 2.0 * n ** 3 / best / 1e9
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -339,35 +384,133 @@ def ours_arm(args, world, rank, local):
     d2h = sum(t.numel() * t.element_size() for t in outs[0])
     assert torch.equal(outs[(args.steps - 1) % 2][1], lse.cpu()), "end-to-end LSE differs"
     ex.sync_status()
-    del bufs
+    # the same on one stream, nothing overlapped: upload, attention, download per step
+    qb, kb, vb, ob, lb = bufs[1]
 
-    # ---- the rest of the sweep (one timed launch each after a warm-up launch)
-    sweep = {}
+    def serial_step():
+        qb.copy_(qp, non_blocking=True)
+        kb.copy_(kp, non_blocking=True)
+        vb.copy_(vp, non_blocking=True)
+        ex.attn_fwd_into(qb, kb, vb, ob, lb, causal=w.causal, window_left=w.window_left,
+                         scale=w.scale, stream=stream)
+        outs[0][0].copy_(ob, non_blocking=True)
+        outs[0][1].copy_(lb, non_blocking=True)
+
+    for _ in range(2):
+        serial_step()
+    torch.cuda.synchronize(dev)
+    dist_barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        serial_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_serial_ms = dist_max(world, e0.elapsed_time(e1) / args.steps)
+    assert torch.equal(outs[0][1], lse.cpu()), "single-stream end-to-end LSE differs"
+    ex.sync_status()
+    del bufs, qb, kb, vb, ob, lb
+
+    # ---- the rest of the sweep (median of 5 launches each, after a warm-up launch)
+    sweep, sweep_slopes = {}, {}
     if not args.no_sweep:
         for L in si.SWEEP_LENGTHS[:-1]:
             ws = w.with_length(L)
             qs, ks, vs = (t.to(dev) for t in si.make_qkv(ws))
             os_ = torch.empty_like(qs)
             ls_ = torch.empty(1, ws.Hq, L, dtype=torch.float32, device=dev)
-            times = []
-            for r in range(4):
-                flush.fill_(0.0)
-                a = torch.cuda.Event(enable_timing=True)
-                bb = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                ex.attn_fwd_into(qs, ks, vs, os_, ls_, causal=True, scale=ws.scale)
-                bb.record(stream)
-                torch.cuda.synchronize(dev)
-                if r:
-                    times.append(a.elapsed_time(bb))
-            t = statistics.median(times)
-            sweep[str(L)] = {"ms": t, "tflops": ws.algorithmic_flop() / t / 1e9}
-        sweep[str(w.L)] = {"ms": ms, "tflops": flop / ms / 1e9}
+            torch.cuda.synchronize(dev)
+            base = torch.cuda.memory_allocated(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            t = time_launches(lambda: ex.attn_fwd_into(qs, ks, vs, os_, ls_, causal=True,
+                                                       scale=ws.scale), flush, stream, reps=5)
+            extra = torch.cuda.max_memory_allocated(dev) - base
+            held = sum(x.numel() * x.element_size() for x in (qs, ks, vs, os_, ls_))
+            sweep[str(L)] = {"ms": t, "tflops": ws.algorithmic_flop() / t / 1e9,
+                             "frac_of_tensor_peak": ws.algorithmic_flop() / t / 1e9 /
+                             float(measured_peaks()[0]["bf16_tflops"]),
+                             "peak_hbm_bytes": held + extra, "library_extra_bytes": extra}
+            del qs, ks, vs, os_, ls_
+        held = sum(x.numel() * x.element_size() for x in (q, k, v, o, lse))
+        sweep[str(w.L)] = {"ms": ms, "tflops": flop / ms / 1e9,
+                           "frac_of_tensor_peak": flop / ms / 1e9 /
+                           float(measured_peaks()[0]["bf16_tflops"]),
+                           "peak_hbm_bytes": held + (peak_hbm - base_alloc),
+                           "library_extra_bytes": peak_hbm - base_alloc}
         ex.sync_status()
+        Ls = sorted(int(x) for x in sweep)
+        sweep_slopes = {
+            "time_vs_L": loglog_slope(Ls, [sweep[str(x)]["ms"] for x in Ls]),
+            "time_vs_L_from_16k": loglog_slope([x for x in Ls if x >= 16384],
+                                               [sweep[str(x)]["ms"] for x in Ls if x >= 16384]),
+            "peak_hbm_vs_L": loglog_slope(Ls, [sweep[str(x)]["peak_hbm_bytes"] for x in Ls]),
+            "method": "least-squares slope of log(ms) and log(peak HBM bytes) against log(L) "
+                      "(the spec page's stage 4: time ~ L^2, memory ~ L)"}
+
+    # ---- every other configuration of the pages' workloads, one line each
+    peaks, src = measured_peaks()
+    configs = {}
+    if not args.no_configs:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        two_sided = si.WINDOW_B4_H16_D128
+        cases = [(si.CAUSAL_B1_H4_L2048_D64, None), (si.NONCAUSAL_B2_H8_D64_L512, None),
+                 (si.NONCAUSAL_B2_H8_D64_L2048, None), (si.CAUSAL_GQA_B1_H32_KV8_D128, None),
+                 (si.WINDOW_B4_H16_D128, None), (two_sided, (256, 256))]
+        for wc, both in cases:
+            qc, kc, vc = (x.to(dev) for x in si.make_qkv(wc))
+            oc = torch.empty_like(qc)
+            lc = torch.empty(wc.B, wc.Hq, wc.L, dtype=torch.float32, device=dev)
+            if both is None:
+                name = wc.name
+                flop_c = wc.algorithmic_flop()
+
+                def call():
+                    ex.attn_fwd_into(qc, kc, vc, oc, lc, causal=wc.causal,
+                                     window_left=wc.window_left, scale=wc.scale)
+                units = wc.B * wc.Hq * ((wc.L + 255) // 256)
+                few = units <= sms if wc.causal else 2 * units <= sms
+                kernel = "one-tile (128 rows per CTA)" if few else "persistent two-tile"
+            else:
+                name = f"window{both[0]}_{both[1]}_b{wc.B}_h{wc.Hq}_d{wc.d}_{wc.dtype}_L{wc.L}"
+                i = np.arange(wc.L, dtype=np.int64)
+                pairs = int(np.sum(np.minimum(wc.L - 1, i + both[1]) - np.maximum(0, i - both[0])
+                                   + 1))
+                flop_c = 4.0 * wc.d * pairs * wc.B * wc.Hq
+
+                def call():
+                    ex.attn_fwd_window(qc, kc, vc, both[0], both[1], scale=wc.scale)
+                kernel = "one-tile (attn_fwd_window)"
+            torch.cuda.synchronize(dev)
+            base = torch.cuda.memory_allocated(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            reps = 10 if flop_c < 1e13 else 5
+            t = time_launches(call, flush, stream, reps=reps, warm=2)
+            ex.sync_status()
+            extra = torch.cuda.max_memory_allocated(dev) - base
+            held = sum(x.numel() * x.element_size() for x in (qc, kc, vc, oc, lc))
+            tf = flop_c / t / 1e9
+            gbs = wc.algorithmic_bytes() / (t * 1e-3) / 1e9
+            configs[name] = {
+                "ms": t, "tflops": tf, "frac_of_tensor_peak": tf / float(peaks["bf16_tflops"]),
+                "algorithmic_flop": flop_c, "algorithmic_bytes": wc.algorithmic_bytes(),
+                "GB/s": gbs, "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
+                "roofline_frac": max(tf / float(peaks["bf16_tflops"]),
+                                     gbs / float(peaks["hbm_gbs"])),
+                "peak_hbm_bytes": held + extra, "library_extra_bytes": extra,
+                "kernel": kernel, "dtype": wc.dtype,
+                "timing": f"median of {reps} launches, L2 flushed before each (outside the events)"}
+            del qc, kc, vc, oc, lc
+        torch.cuda.empty_cache()
+
+    # ---- the same-run tensor rate of torch.mm (cuBLAS), beside the measured divisor
+    mm = {}
+    if not args.no_configs:
+        mm = {"fp16_tflops": mm_rate(torch.float16, dev), "bf16_tflops": mm_rate(torch.bfloat16, dev),
+              "shape": "8192 x 8192 x 8192, best of 10, CUDA events",
+              "note": "reported only; the roofline divides by MEASURED_PEAKS.json bf16_tflops"}
+        torch.cuda.empty_cache()
 
     # ---- decode-shaped forward (split-KV + merge): HBM-bound, one line per workload
     decode = {}
-    peaks, src = measured_peaks()
     if not args.no_decode:
         for wd in (si.DECODE_GQA_B1_H32_KV8_D128, si.DECODE_B1_H4_D64):
             qd, kd, vd = si.make_qkv_decode(wd, device=dev)
@@ -558,13 +701,20 @@ def ours_arm(args, world, rank, local):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
                     "pipeline": "two device buffer sets; step i+1's upload and step i-1's "
-                                "download (own streams) overlap step i's attention"},
+                                "download (own streams) overlap step i's attention",
+                    "single_stream": {"value": flop * world / e2e_serial_ms / 1e9, "unit": UNIT,
+                                      "ms_per_step": e2e_serial_ms,
+                                      "pipeline": "one stream: upload, attention, download in "
+                                                  "turn, nothing overlapped"}},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "peak_hbm_bytes": peak_hbm - base_alloc + sum(
                 t.numel() * t.element_size() for t in (q, k, v, o, lse)),
             "library_extra_bytes": peak_hbm - base_alloc,
             "sweep": sweep,
+            "sweep_slopes": sweep_slopes,
+            "configs": configs,
+            "tensor_rate_same_run": mm,
             "decode": decode,
             "fp8": fp8,
             "backward": backward,
@@ -585,6 +735,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration lines and the same-run torch.mm rate")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="reference arm: seconds of oracle work per step (default: sized so the run "
