@@ -466,10 +466,16 @@ def ours_arm(args, world, rank, local):
                 def call():
                     ex.attn_fwd_into(qc, kc, vc, oc, lc, causal=wc.causal,
                                      window_left=wc.window_left, scale=wc.scale)
+                # the library's automatic choice (attn_set_path_policy in attn.h)
                 units = wc.B * wc.Hq * ((wc.L + 255) // 256)
                 few = units <= sms if wc.causal else 2 * units <= sms
-                kernel = "one-tile (128 rows per CTA)" if few else "persistent two-tile"
+                span = min(wc.L, wc.window_left + 128) if wc.window_left >= 0 else wc.L
+                tiles_win = (wc.d == 128 or wc.dtype == "bf16") and \
+                    4.0 * wc.B * wc.Hkv * span * wc.d <= 192 * 2 ** 20
+                kernel = "one-tile (128 rows per CTA)" if (few or tiles_win) else "persistent two-tile"
             else:
+                del oc, lc  # attn_fwd_window allocates its outputs (counted in the peak below)
+                oc = lc = torch.empty(0, device=dev)
                 name = f"window{both[0]}_{both[1]}_b{wc.B}_h{wc.Hq}_d{wc.d}_{wc.dtype}_L{wc.L}"
                 i = np.arange(wc.L, dtype=np.int64)
                 pairs = int(np.sum(np.minimum(wc.L - 1, i + both[1]) - np.maximum(0, i - both[0])

@@ -250,6 +250,25 @@ def test_auto_path_choice_causal_one_unit_per_sm():
         assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (causal, L)
 
 
+def test_auto_path_choice_d128_by_kv_size():
+    """d = 128 (P over S in the two-tile kernel): AUTO takes the one-tile kernel while
+    the K/V its keys span fit in 192 MiB (here 2x8x8192 rows, 64 MiB), the two-tile
+    kernel beyond that (1x8x65536 with no window, 256 MiB), and the one-tile kernel
+    again when a left window bounds the span. AUTO gives the chosen kernel's bits."""
+    import exact_io_aware_19_gb300 as ex
+    for B, L, causal, wl, pick in ((2, 8192, True, -1, ex.PATH_TILES),
+                                   (1, 65536, True, -1, ex.PATH_SQUARE),
+                                   (1, 65536, True, 1000, ex.PATH_TILES)):
+        q, k, v = si.random_qkv(B, L, 16, 8, 128, dtype="bf16", seed=L + B, device="cuda")
+        assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
+        o_auto, l_auto = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, out_fp32=True)
+        ex.set_path_policy(pick)
+        o_p, l_p = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, out_fp32=True)
+        ex.set_path_policy(ex.PATH_AUTO)
+        assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (B, L, wl)
+        del q, k, v, o_auto, o_p
+
+
 def test_auto_path_choice():
     """AUTO takes the one-tile kernel exactly when the problem has at most half as many
     256-row units as SMs (causal: at most as many); both kernels agree to rounding."""
