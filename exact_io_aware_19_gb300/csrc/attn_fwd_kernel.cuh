@@ -135,6 +135,22 @@ __device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
 
 __device__ __forceinline__ bool has_block(const TileSpan& s, int j) { return j >= s.lo && j < s.hi; }
 
+// The key blocks [a, b) of a tile's span [lo, hi) that cross no mask boundary:
+// every key visible to every row of the tile (no ragged tail, wholly below the
+// causal diagonal, wholly inside the left window). Blocks [lo, a) and [b, hi) are
+// the masked ones: the window's first blocks and the diagonal or tail block.
+__device__ __forceinline__ void unmasked_blocks(const FwdParams& p, const TileSpan& s, int& a, int& b) {
+  a = s.lo;
+  if (p.window_left >= 0) {  // key0 >= row0 + kBM - 1 - window_left
+    const int first = s.row0 + kBM - 1 - p.window_left;
+    if (first > 0) a = max(a, (first + kBN - 1) / kBN);
+  }
+  b = min(s.hi, p.L / kBN);  // key0 + kBN <= L
+  if (p.causal) b = min(b, (s.row0 >= kBN - 1) ? (s.row0 - (kBN - 1)) / kBN + 1 : 0);  // key0 + kBN - 1 <= row0
+  a = min(a, s.hi);
+  b = max(b, a);
+}
+
 template <int D, bool BF16, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -448,15 +464,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = span.row0 + r_in_tile;
       float m_ref = -INFINITY;  // reference max (base-2 units) the P values are relative to
       float l = 0.f;            // running sum of P
-      for (int j = span.lo; j < span.hi; ++j) {
-        ok = mbar_wait_warp(bar_s_full(t), s_cnt & 1u, wc, kSiteSmxSFull);
-        if (!ok) break;
+      // One key block; false when a wait gave up. Blocks that cross a mask boundary
+      // run the masked instantiation in loops of their own before and after the
+      // unmasked middle, so the hot loop holds one block body only (its code size
+      // measurably matters: the masked body in the same loop cost 7 %).
+      auto one_block = [&](int j, auto masked_tag) __attribute__((always_inline)) -> bool {
+        constexpr bool masked = decltype(masked_tag)::value;
+        if (!mbar_wait_warp(bar_s_full(t), s_cnt & 1u, wc, kSiteSmxSFull)) return false;
         tc_fence_after();
         const int key0 = j * kBN;
-        const bool masked = (key0 + kBN > p.L) || (p.causal && key0 + kBN - 1 > span.row0) ||
-                            (p.window_left >= 0 && key0 < span.row0 + kBM - 1 - p.window_left);
         int vis_lo = 0, vis_hi = kBN;  // visible columns of this row: [vis_lo, vis_hi)
-        if (masked) {
+        if constexpr (masked) {
           int hi_key = p.L;
           if (p.causal) hi_key = min(hi_key, row + 1);
           int lo_key = (p.window_left >= 0) ? row - p.window_left : 0;
@@ -613,14 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float rowsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
           l = l * alpha + rowsum;
         };
-        if (masked)
-          block_body(std::true_type{});
-        else
-          block_body(std::false_type{});
-        if (stop) {
-          ok = false;
-          break;
-        }
+        block_body(masked_tag);
+        if (stop) return false;
         ++s_cnt;
         // O rescale. The previous P·V of this tile is complete: with P over S,
         // S_t(j) was issued after it and s_full tracks all earlier MMAs; with a
@@ -639,6 +651,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar_p_full(t));
+        return true;
+      };
+      int ja, jb;
+      unmasked_blocks(p, span, ja, jb);
+      // the masked prefix, the unmasked middle (a tight loop of its own), the masked
+      // suffix; one instance of each block body
+      for (int j = span.lo; ok && j < span.hi;) {
+        if (j >= ja && j < jb) {
+          for (; ok && j < jb; ++j) ok = one_block(j, std::false_type{});
+        } else {
+          ok = one_block(j, std::true_type{});
+          ++j;
+        }
       }
       if (!ok) break;
       // ---- epilogue: O / l and LSE for this tile

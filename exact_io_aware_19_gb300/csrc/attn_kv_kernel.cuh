@@ -506,21 +506,23 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       other = xbuf[(b * 2 + (ch ^ 1)) * kBM + rho];
       return true;
     };
-    for (int jj = 0; jj < nblocks; ++jj) {
+    // One key block (jj-th of this CTA); false when a wait gave up. Blocks that cross
+    // a mask boundary run the masked instantiation outside the unmasked middle's own
+    // tight loop, so the hot loop holds one block body only.
+    auto one_block = [&](int jj, auto masked_tag) __attribute__((always_inline)) -> bool {
+      constexpr bool masked = decltype(masked_tag)::value;
       const int j = it.lo + jj;
       const uint32_t buf = DEC ? 0u : (jj & 1);
-      ok = mbar_wait_warp(bar_s_full(buf), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc, kSiteSmxSFull);
-      if (!ok) break;
+      if (!mbar_wait_warp(bar_s_full(buf), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc, kSiteSmxSFull))
+        return false;
       tc_fence_after();
       // S of this block, then P over the scores this thread has read (DEC: P in its
       // own columns)
       const uint32_t tS = tmem_base + lane_off + (DEC ? 0u : 128u * buf);
       const uint32_t tP = DEC ? tmem_base + lane_off + R::kColP : tS;
       const int key0 = j * kBN;
-      const bool masked = (key0 + kBN > Lk) || (wr >= 0 && key0 + kBN - 1 > pos_min + wr) ||
-                          (p.window_left >= 0 && key0 < pos_max - p.window_left);
       int vis_lo = 0, vis_hi = kBN;  // visible columns of this row: [vis_lo, vis_hi)
-      if (masked) {
+      if constexpr (masked) {
         const int hi_key = (wr >= 0) ? min(Lk, pos + wr + 1) : Lk;
         const int lo_key = (p.window_left >= 0) ? pos - p.window_left : 0;
         vis_hi = max(0, min(kBN, hi_key - key0));
@@ -639,22 +641,14 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         }
         l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
       };
-      if (masked)
-        block_body(std::true_type{});
-      else
-        block_body(std::false_type{});
-      if (stop) {
-        ok = false;
-        break;
-      }
+      block_body(masked_tag);
+      if (stop) return false;
       // O rescale (this thread's columns) once the previous P·V, which accumulates
       // into O, is complete; the first block's P·V overwrites O.
       if (__any_sync(0xffffffffu, rescale && jj > 0)) {
         if (!mbar_wait_warp(bar_pv_done(DEC ? 0 : ((jj - 1) & 1)),
-                            DEC ? ((jj - 1) & 1u) : (((jj - 1) >> 1) & 1u), wc, kSiteSmxPvDone)) {
-          ok = false;
-          break;
-        }
+                            DEC ? ((jj - 1) & 1u) : (((jj - 1) >> 1) & 1u), wc, kSiteSmxPvDone))
+          return false;
         tc_fence_after();
         const float a = (rescale && jj > 0) ? alpha : 1.f;
 #pragma unroll
@@ -669,6 +663,31 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p_full(buf));
+      return true;
+    };
+    {
+      // Blocks [ja, jb) of this CTA cross no mask boundary: every key visible at
+      // every position of the tile (no ragged end, wholly inside both windows).
+      int ja = 0, jb = nblocks;
+      if (p.window_left >= 0) {  // key0 >= pos_max - window_left
+        const int first = pos_max - p.window_left;
+        if (first > 0) ja = max(ja, (first + kBN - 1) / kBN - it.lo);
+      }
+      jb = min(jb, Lk / kBN - it.lo);  // key0 + kBN <= Lk
+      if (wr >= 0) {                   // key0 + kBN - 1 <= pos_min + wr
+        const int last = pos_min + wr - (kBN - 1);
+        jb = min(jb, last >= 0 ? last / kBN + 1 - it.lo : 0);
+      }
+      ja = min(max(ja, 0), nblocks);
+      jb = max(jb, ja);
+      for (int jj = 0; ok && jj < nblocks;) {
+        if (jj >= ja && jj < jb) {
+          for (; ok && jj < jb; ++jj) ok = one_block(jj, std::false_type{});
+        } else {
+          ok = one_block(jj, std::true_type{});
+          ++jj;
+        }
+      }
     }
     if (ok && nblocks > 0) {
       ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteSmxOFull);
