@@ -470,7 +470,7 @@ def ours_arm(args, world, rank, local):
                 units = wc.B * wc.Hq * ((wc.L + 255) // 256)
                 few = units <= sms if wc.causal else 2 * units <= sms
                 span = min(wc.L, wc.window_left + 128) if wc.window_left >= 0 else wc.L
-                tiles_win = (wc.d == 128 or wc.dtype == "bf16") and \
+                tiles_win = (wc.d == 128 or wc.dtype == "bf16") and wc.window_left >= 0 and \
                     4.0 * wc.B * wc.Hkv * span * wc.d <= 192 * 2 ** 20
                 kernel = "one-tile (128 rows per CTA)" if (few or tiles_win) else "persistent two-tile"
             else:

@@ -519,16 +519,17 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   // 97 µs; at twice that the persistent kernel's throughput wins).
   // With d = 128 or bf16 the persistent kernel keeps P over S, so a tile's next S
   // product waits for its P·V; the one-tile kernel double-buffers S and runs two
-  // softmax threads per row, and wins while the K/V its CTAs stream together stays
-  // near L2 (it reads each K/V block for 128 rows, not 256): measured on one GB300,
-  // GQA 32/8 d = 128 causal L = 16384 2.16 against 2.45 ms, window 4096 4x16x32768
-  // 4.83 against 5.54 ms, but causal L = 131072 (512 MiB of K/V) 163 against 159 ms.
+  // softmax threads per row. Under a left window (a few dozen key blocks per tile,
+  // two of them masked) it wins while the K/V its keys span stays near L2 (it
+  // reads each K/V block for 128 rows, not 256): measured on one GB300, window 4096
+  // 4x16x32768 d = 128 bf16 4.83 against 4.99 ms; causal without a window the
+  // persistent kernel wins (GQA 32/8 d = 128 L = 16384 2.03 against 2.16 ms).
   const int policy = g_path_policy.load();
   const bool few_units = causal ? num_units <= info.sms : 2 * num_units <= info.sms;
   const bool p_over_s = (d == 128) || bf16;
   const int kv_span = (window_left >= 0) ? std::min(L, window_left + 128) : L;
   const double kv_bytes = 4.0 * B * Hkv * static_cast<double>(kv_span) * d;  // K and V, 2 B each
-  const bool tiles_win = p_over_s && kv_bytes <= 192.0 * 1024 * 1024;
+  const bool tiles_win = p_over_s && window_left >= 0 && kv_bytes <= 192.0 * 1024 * 1024;
   if (policy == ATTN_PATH_TILES ||
       (policy == ATTN_PATH_AUTO && (few_units || tiles_win) && Hq / Hkv <= 128))
     return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, -1, scale,

@@ -299,18 +299,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float Cs = neg ? -C : C;
     float m_ref = -INFINITY;  // reference max (base-2 units)
     bool ok = true;
-    for (int jj = 0; jj < nblocks; ++jj) {
+    // One key block (jj-th of this CTA); false when a wait gave up. Blocks that cross
+    // a mask boundary run the masked instantiation outside the unmasked middle's own
+    // tight loop, so the hot loop holds one block body only.
+    auto one_block = [&](int jj, auto masked_tag) __attribute__((always_inline)) -> bool {
+      constexpr bool masked = decltype(masked_tag)::value;
       const int j = blk_lo + jj;
       const uint32_t buf = jj & 1;
-      ok = mbar_wait_warp(bar_s_full, jj & 1u, wc, kSiteSmxSFull);
-      if (!ok) break;
+      if (!mbar_wait_warp(bar_s_full, jj & 1u, wc, kSiteSmxSFull)) return false;
       tc_fence_after();
       const uint32_t tS = tmem_base + lane_off + kColS;
       const int key0 = j * kBN;
-      const bool masked = (key0 + kBN > L) || (wr >= 0 && key0 + kBN - 1 > pos_min + wr) ||
-                          (p.window_left >= 0 && key0 < pos_max - p.window_left);
       int vis_lo = 0, vis_hi = kBN;
-      if (masked) {
+      if constexpr (masked) {
         const int hi_key = (wr >= 0) ? min(L, qi + wr + 1) : L;
         const int lo_key = (p.window_left >= 0) ? qi - p.window_left : 0;
         vis_hi = max(0, min(kBN, hi_key - key0));
@@ -386,20 +387,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         fence_proxy_async_shared();  // P is read by the tensor core (async proxy)
       };
-      if (masked)
-        block_body(std::true_type{});
-      else
-        block_body(std::false_type{});
-      if (stop) {
-        ok = false;
-        break;
-      }
+      block_body(masked_tag);
+      if (stop) return false;
       // O rescale once the previous P·V is complete; the first block's P·V overwrites O.
       if (__any_sync(0xffffffffu, rescale && jj > 0)) {
-        if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone))
+          return false;
         tc_fence_after();
         const float a = (rescale && jj > 0) ? alpha : 1.f;
 #pragma unroll
@@ -421,6 +414,30 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_before();
       mbar_arrive(bar_p_full(buf));
+      return true;
+    };
+    {
+      // Blocks [ja, jb) of this CTA cross no mask boundary (the one-tile kernel's rule).
+      int ja = 0, jb = nblocks;
+      if (p.window_left >= 0) {  // key0 >= pos_max - window_left
+        const int first = pos_max - p.window_left;
+        if (first > 0) ja = max(ja, (first + kBN - 1) / kBN - blk_lo);
+      }
+      jb = min(jb, L / kBN - blk_lo);  // key0 + kBN <= L
+      if (wr >= 0) {                   // key0 + kBN - 1 <= pos_min + wr
+        const int last = pos_min + wr - (kBN - 1);
+        jb = min(jb, last >= 0 ? last / kBN + 1 - blk_lo : 0);
+      }
+      ja = min(max(ja, 0), nblocks);
+      jb = max(jb, ja);
+      for (int jj = 0; ok && jj < nblocks;) {
+        if (jj >= ja && jj < jb) {
+          for (; ok && jj < jb; ++jj) ok = one_block(jj, std::false_type{});
+        } else {
+          ok = one_block(jj, std::true_type{});
+          ++jj;
+        }
+      }
     }
     if (ok && nblocks > 0) {
       ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteSmxOFull);

@@ -280,10 +280,9 @@ attn_status_t attn_fwd_kv_paged(const void *q, const void *k_cache, const void *
  *   ATTN_PATH_AUTO    the persistent two-tile kernel (256 query rows per work unit),
  *                     unless the problem has at most half as many such units as the
  *                     device has SMs (causal: at most as many), or it has d = 128 or
- *                     bf16 inputs and the K/V rows its keys span (B * Hkv * L, or
- *                     B * Hkv * (window_left + 128) with a window) take at most
- *                     192 MiB; then the one-tile kernel (128 rows per CTA, the
- *                     longest tiles first).
+ *                     bf16 inputs and a left window whose K/V rows
+ *                     (B * Hkv * (window_left + 128)) take at most 192 MiB; then the
+ *                     one-tile kernel (128 rows per CTA, the longest tiles first).
  *   ATTN_PATH_SQUARE  always the persistent two-tile kernel.
  *   ATTN_PATH_TILES   always the one-tile kernel (attn_fwd_kv's with Lq = Lk and one
  *                     key split).

@@ -250,13 +250,13 @@ def test_auto_path_choice_causal_one_unit_per_sm():
         assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (causal, L)
 
 
-def test_auto_path_choice_d128_by_kv_size():
-    """d = 128 (P over S in the two-tile kernel): AUTO takes the one-tile kernel while
-    the K/V its keys span fit in 192 MiB (here 2x8x8192 rows, 64 MiB), the two-tile
-    kernel beyond that (1x8x65536 with no window, 256 MiB), and the one-tile kernel
-    again when a left window bounds the span. AUTO gives the chosen kernel's bits."""
+def test_auto_path_choice_d128_window():
+    """d = 128 (P over S in the two-tile kernel): AUTO takes the one-tile kernel under
+    a left window whose K/V span fits in 192 MiB, the two-tile kernel for causal
+    attention without a window (at any length with more units than SMs). AUTO gives
+    the chosen kernel's bits."""
     import exact_io_aware_19_gb300 as ex
-    for B, L, causal, wl, pick in ((2, 8192, True, -1, ex.PATH_TILES),
+    for B, L, causal, wl, pick in ((2, 8192, True, -1, ex.PATH_SQUARE),
                                    (1, 65536, True, -1, ex.PATH_SQUARE),
                                    (1, 65536, True, 1000, ex.PATH_TILES)):
         q, k, v = si.random_qkv(B, L, 16, 8, 128, dtype="bf16", seed=L + B, device="cuda")
