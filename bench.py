@@ -733,6 +733,59 @@ def ours_arm(args, world, rank, local):
     return result
 
 
+def profile_case(name: str, reps: int) -> None:
+    """Runs one named workload ``reps`` times, untimed, on cuda:0 and prints ``ok NAME``.
+
+    The launches and inputs are those of the bench's own measurements (same seeded
+    generators), so that an ncu capture of ``bench.py --case NAME`` covers a bench kernel
+    on its workload, or on a shortened copy of it that a ``--set full`` capture finishes.
+    """
+    import dataclasses
+    import torch
+    import exact_io_aware_19_gb300 as ex
+    dev = "cuda"
+    fwd = {"c1": si.CAUSAL_B1_H4_L2048_D64, "c2a": si.NONCAUSAL_B2_H8_D64_L512,
+           "c2b": si.NONCAUSAL_B2_H8_D64_L2048, "c3": si.CAUSAL_SWEEP_B1_H4_D64,
+           "c3_16k": si.CAUSAL_SWEEP_B1_H4_D64.with_length(16384),
+           "c3_32k": si.CAUSAL_SWEEP_B1_H4_D64.with_length(32768),
+           "c4": si.CAUSAL_GQA_B1_H32_KV8_D128,
+           "c4_16k": si.CAUSAL_GQA_B1_H32_KV8_D128.with_length(16384),
+           "c5": si.WINDOW_B4_H16_D128, "c5_b1": dataclasses.replace(si.WINDOW_B4_H16_D128, B=1)}
+    for L in si.SWEEP_LENGTHS:
+        fwd[f"sweep{L}"] = si.CAUSAL_SWEEP_B1_H4_D64.with_length(L)
+    if name in fwd:
+        w = fwd[name]
+        q, k, v = si.make_qkv(w, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            ex.attn_fwd_into(q, k, v, o, lse, causal=w.causal, window_left=w.window_left,
+                             scale=w.scale)
+    elif name == "bwd":  # the backward line's shape: causal 4 heads d = 64 fp16, L = 16384
+        w = si.CAUSAL_SWEEP_B1_H4_D64.with_length(16384)
+        q, k, v = si.make_qkv(w, device=dev)
+        do = torch.randn(q.shape, generator=torch.Generator().manual_seed(1010)).to(q.dtype).to(dev)
+        o, lse = ex.attn_fwd(q, k, v, causal=True, scale=w.scale)
+        for _ in range(reps):
+            ex.attn_bwd(q, k, v, o, lse, do, causal=True, scale=w.scale)
+    elif name == "fp8":  # the FP8 line's shape: 2 x 4096 x 32 x 64 e4m3, non-causal
+        g8 = torch.Generator().manual_seed(1009)
+        q8, k8, v8 = (torch.randn(2, 4096, 32, 64, generator=g8).to(torch.float8_e4m3fn).to(dev)
+                      for _ in range(3))
+        for _ in range(reps):
+            ex.attn_fwd_fp8(q8, k8, v8)
+    elif name in ("decode_gqa", "decode64"):
+        wd = si.DECODE_GQA_B1_H32_KV8_D128 if name == "decode_gqa" else si.DECODE_B1_H4_D64
+        qd, kd, vd = si.make_qkv_decode(wd, device=dev)
+        for _ in range(reps):
+            ex.attn_fwd_kv(qd, kd, vd, causal=True, scale=wd.scale)
+    else:
+        raise SystemExit(f"unknown case {name!r}")
+    ex.sync_status()
+    torch.cuda.synchronize()
+    print("ok", name, flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -748,7 +801,15 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="reference arm: seconds of oracle work per step (default: sized so the run "
                          "takes about 150 s)")
+    ap.add_argument("--case", default=None,
+                    help="run one named workload --reps times, untimed, and exit (for ncu "
+                         "captures): c1 c2a c2b c3 c3_16k c3_32k c4 c4_16k c5 c5_b1 sweepL bwd "
+                         "fp8 decode_gqa decode64")
+    ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
+    if args.case is not None:
+        profile_case(args.case, args.reps)
+        return
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     world, rank, local = dist_setup(args.gpus)
     try:
