@@ -470,10 +470,12 @@ def ours_arm(args, world, rank, local):
                 # the library's automatic choice (attn_set_path_policy in attn.h)
                 units = wc.B * wc.Hq * ((wc.L + 255) // 256)
                 few = units <= sms if wc.causal else 2 * units <= sms
-                span = min(wc.L, wc.window_left + 128) if wc.window_left >= 0 else wc.L
-                tiles_win = (wc.d == 128 or wc.dtype == "bf16") and wc.window_left >= 0 and \
-                    4.0 * wc.B * wc.Hkv * span * wc.d <= 192 * 2 ** 20
-                kernel = "one-tile (128 rows per CTA)" if (few or tiles_win) else "persistent two-tile"
+                # (the default workspace is the full one: bf16 runs the fp16 copy of V,
+                # whose one P·V product per block makes the two-tile kernel the faster one
+                # under a window too)
+                kernel = "one-tile (128 rows per CTA)" if few else "persistent two-tile"
+                if wc.dtype == "bf16":
+                    kernel += " after the fp16 copy of V (two conversion kernels)"
             else:
                 del oc, lc  # attn_fwd_window allocates its outputs (counted in the peak below)
                 oc = lc = torch.empty(0, device=dev)

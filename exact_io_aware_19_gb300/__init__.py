@@ -65,8 +65,10 @@ def _bind(lib):
     lib.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p, sz, p]
     lib.attn_fwd_noalloc.restype = i
     lib.attn_fwd_noalloc.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_float, i, i, p]
+    lib.attn_debug_v16_exponent.restype = i
+    lib.attn_debug_v16_exponent.argtypes = [ctypes.c_uint32]
     lib.attn_fwd_workspace_size.restype = sz
-    lib.attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
     lib.attn_fwd_kv.restype = i
     lib.attn_fwd_kv.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, ctypes.c_float, i, i, i,
                                 p, sz, p]
@@ -141,9 +143,12 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"q, k, v must be float16 or bfloat16, got {t.dtype}")
 
 
-def workspace_size(B, L, Hq, Hkv, d, causal=False, window_left=-1) -> int:
+def workspace_size(B, L, Hq, Hkv, d, causal=False, window_left=-1, dtype="fp16") -> int:
+    """attn_fwd's workspace bytes: 256 for fp16; for bf16 also the fp16 copy of V
+    (a smaller bf16 workspace of at least 256 bytes runs the split-weight path)."""
+    code = {"fp16": FP16, "bf16": BF16, torch.float16: FP16, torch.bfloat16: BF16}[dtype]
     return int(load_library().attn_fwd_workspace_size(B, L, Hq, Hkv, d, int(bool(causal)),
-                                                      int(window_left)))
+                                                      int(window_left), code))
 
 
 def _default_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
@@ -204,7 +209,8 @@ def attn_fwd_into(q, k, v, o, lse, causal=False, window_left=-1, scale=None,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if workspace is None:  # a given workspace's size is checked by the library
-        workspace = _default_workspace(q.device, workspace_size(B, L, Hq, Hkv, d, causal, window_left))
+        workspace = _default_workspace(q.device, workspace_size(B, L, Hq, Hkv, d, causal, window_left,
+                                                                q.dtype))
     code = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                         lse.data_ptr() if lse is not None else None, B, L, Hq, Hkv, d,
                         int(bool(causal)), int(window_left), float(scale), dt, out,

@@ -14,6 +14,7 @@
 
 #include "attn.h"
 #include "attn_launch.h"
+#include "vscale.cuh"
 
 namespace {
 
@@ -195,6 +196,14 @@ attn_status_t check_shape(int B, int L, int Hq, int Hkv, int d, int causal, int 
   const long long rows = (long long)B * Hq * L;
   if (rows >= (1LL << 31)) return fail(ATTN_ERR_INVALID_ARG, "B * Hq * L must be < 2^31");
   return ATTN_OK;
+}
+
+// attn_fwd's workspace: the status word; with bfloat16 inputs also the heads' largest
+// |v| ([B, Hkv] u32, padded to 256 bytes) and the fp16 copy of V ([B, L, Hkv, d]).
+size_t fwd_vmax_bytes(int B, int Hkv) { return ((size_t)B * Hkv * 4 + 255) / 256 * 256; }
+size_t fwd_workspace_bytes(int B, int L, int Hkv, int d, attn_dtype_t dtype) {
+  if (dtype != ATTN_BF16) return kWorkspaceBytes;
+  return kWorkspaceBytes + fwd_vmax_bytes(B, Hkv) + (size_t)2 * B * L * Hkv * d;
 }
 
 // ---------------------------------------------------------------- decode shapes
@@ -401,7 +410,8 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
 attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int L, int Hq, int Hkv, int d, int causal,
                                   int window_left, int window_right, float scale, bool bf16,
-                                  bool out_f32, void* workspace, void* stream) {
+                                  bool out_f32, void* workspace, void* stream,
+                                  const void* v16 = nullptr, const uint32_t* vmax = nullptr) {
   const KvPlan plan = kv_plan(B, L, L, Hq, Hkv, causal, window_left);
   if (plan.group > 128)
     return fail(ATTN_ERR_UNSUPPORTED, "at most 128 query heads may share one K/V head");
@@ -409,7 +419,8 @@ attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, v
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why, plan.group, plan.q_per_tile) ||
       !make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) ||
-      !make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why))
+      !(v16 ? make_tensor_map(&tm_v, v16, false, B, L, Hkv, d, &why)
+            : make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why)))
     return fail(ATTN_ERR_CUDA, why);
   ex19::KvLaunchArgs a = {};
   a.tm_q = &tm_q;
@@ -421,6 +432,7 @@ attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, v
   p.status = static_cast<uint32_t*>(workspace);
   p.o_part = nullptr;
   p.lse_part = nullptr;
+  p.vmax = vmax;
   p.B = B;
   p.Lq = L;
   p.Lk = L;
@@ -438,7 +450,15 @@ attn_status_t launch_square_as_kv(const void* q, const void* k, const void* v, v
   p.wait_limit_ns = g_wait_limit_ns.load();
   a.grid = plan.items;
   a.stream = static_cast<cudaStream_t>(stream);
-  cudaError_t e = ex19::launch_kv(d, bf16, out_f32, a);
+  cudaError_t e = cudaSuccess;
+  if (v16) {
+    e = ex19::launch_v_to_f16(v, const_cast<void*>(v16), const_cast<uint32_t*>(vmax), B, L, Hkv, d,
+                              a.stream);
+    if (e != cudaSuccess) return cuda_fail("the fp16 copy of V", e);
+    e = ex19::launch_kv_pv16(d, out_f32, a);
+  } else {
+    e = ex19::launch_kv(d, bf16, out_f32, a);
+  }
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
 }
@@ -508,6 +528,16 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
 
   const bool bf16 = dtype == ATTN_BF16;
   const bool out_f32 = out_dtype == ATTN_OUT_FP32;
+  // bfloat16 inputs with the full workspace: P·V in fp16 against a per-head scaled
+  // fp16 copy of V (one product per key block instead of the split P's two). A
+  // workspace of only the status word (attn_fwd_noalloc's) keeps the split P.
+  const bool pv16 = bf16 && workspace_bytes >= fwd_workspace_bytes(B, L, Hkv, d, dtype);
+  uint32_t* vmax = nullptr;
+  void* v16 = nullptr;
+  if (pv16) {  // written by launch_v_to_f16 right before the attention kernel
+    vmax = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kWorkspaceBytes);
+    v16 = static_cast<char*>(workspace) + kWorkspaceBytes + fwd_vmax_bytes(B, Hkv);
+  }
   const int num_units = B * Hq * ((L + kUnitRows - 1) / kUnitRows);
   // Problems with at most half as many 256-row units as SMs leave most SMs idle in
   // the persistent two-tile kernel; the one-tile kernel (the decode-shaped path with
@@ -517,30 +547,33 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   // another); the one-tile kernel starts the longest tiles first and spreads the
   // rest, which wins up to one unit per SM (measured at L = 8192, 4 heads: 72 against
   // 97 µs; at twice that the persistent kernel's throughput wins).
-  // With d = 128 or bf16 the persistent kernel keeps P over S, so a tile's next S
-  // product waits for its P·V; the one-tile kernel double-buffers S and runs two
-  // softmax threads per row. Under a left window (a few dozen key blocks per tile,
-  // two of them masked) it wins while the K/V its keys span stays near L2 (it
-  // reads each K/V block for 128 rows, not 256): measured on one GB300, window 4096
-  // 4x16x32768 d = 128 bf16 4.83 against 4.99 ms; causal without a window the
-  // persistent kernel wins (GQA 32/8 d = 128 L = 16384 2.03 against 2.16 ms).
+  // With the split bf16 P (two P·V products per block) the persistent kernel keeps P
+  // over S, so a tile's next S product waits for both; the one-tile kernel
+  // double-buffers S and runs two softmax threads per row. Under a left window (a few
+  // dozen key blocks per tile, two of them masked) it wins while the K/V its keys
+  // span stays near L2 (it reads each K/V block for 128 rows, not 256): measured on
+  // one GB300, window 4096 4x16x32768 d = 128 bf16 4.83 against 4.99 ms; causal
+  // without a window the persistent kernel wins (GQA 32/8 d = 128 L = 16384 2.03
+  // against 2.16 ms). With fp16 P (one P·V product) the persistent kernel wins both
+  // (3.60 against 4.14 ms, 1.55 against 1.69 ms).
   const int policy = g_path_policy.load();
   const bool few_units = causal ? num_units <= info.sms : 2 * num_units <= info.sms;
-  const bool p_over_s = (d == 128) || bf16;
+  const bool split_p = bf16 && !pv16;
   const int kv_span = (window_left >= 0) ? std::min(L, window_left + 128) : L;
   const double kv_bytes = 4.0 * B * Hkv * static_cast<double>(kv_span) * d;  // K and V, 2 B each
-  const bool tiles_win = p_over_s && window_left >= 0 && kv_bytes <= 192.0 * 1024 * 1024;
+  const bool tiles_win = split_p && window_left >= 0 && kv_bytes <= 192.0 * 1024 * 1024;
   if (policy == ATTN_PATH_TILES ||
       (policy == ATTN_PATH_AUTO && (few_units || tiles_win) && Hq / Hkv <= 128))
     return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, -1, scale,
-                               bf16, out_f32, workspace, stream);
+                               bf16, out_f32, workspace, stream, v16, vmax);
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_tensor_map(&tm_q, q, bf16, B, L, Hq, d, &why) ||
       !make_tensor_map(&tm_k, k, bf16, B, L, Hkv, d, &why) ||
-      !make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why))
+      !(pv16 ? make_tensor_map(&tm_v, v16, false, B, L, Hkv, d, &why)
+             : make_tensor_map(&tm_v, v, bf16, B, L, Hkv, d, &why)))
     return fail(ATTN_ERR_CUDA, why);
 
-  ex19::LaunchArgs a;
+  ex19::LaunchArgs a = {};
   a.tm_q = &tm_q;
   a.tm_k = &tm_k;
   a.tm_v = &tm_v;
@@ -548,6 +581,7 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   p.o = o;
   p.lse = lse;
   p.status = static_cast<uint32_t*>(workspace);
+  p.vmax = vmax;
   p.B = B;
   p.L = L;
   p.Hq = Hq;
@@ -562,7 +596,12 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   a.grid = p.num_units < info.sms ? p.num_units : info.sms;
   a.stream = static_cast<cudaStream_t>(stream);
 
-  e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
+  if (pv16) {
+    e = ex19::launch_v_to_f16(v, v16, vmax, B, L, Hkv, d, a.stream);
+    if (e != cudaSuccess) return cuda_fail("the fp16 copy of V", e);
+    e = ex19::launch_fwd_pv16(d, out_f32, a);
+  } else
+    e = (d == 64) ? ex19::launch_fwd_d64(bf16, out_f32, a) : ex19::launch_fwd_d128(bf16, out_f32, a);
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return ATTN_OK;
 }
@@ -570,9 +609,11 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
 
 extern "C" {
 
-size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal, int window_left) {
+size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal, int window_left,
+                               attn_dtype_t dtype) {
   if (check_shape(B, L, Hq, Hkv, d, causal, window_left) != ATTN_OK) return 0;
-  return kWorkspaceBytes;
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return 0;
+  return fwd_workspace_bytes(B, L, Hkv, d, dtype);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -930,6 +971,8 @@ attn_status_t attn_debug_wait_probe(void* workspace, size_t workspace_bytes, uin
   if (e != cudaSuccess) return cuda_fail("probe launch", e);
   return ATTN_OK;
 }
+
+int attn_debug_v16_exponent(uint32_t absmax_bits) { return ex19::v16_exponent(absmax_bits); }
 
 attn_status_t attn_debug_exp2(const float* x, float* y_mufu, float* y_f16, int n, void* stream) {
   g_detail.clear();

@@ -69,6 +69,7 @@
 #include "row_ops.cuh"
 #include "sm103_ptx.cuh"
 #include "tmem_io.cuh"
+#include "vscale.cuh"
 
 namespace ex19 {
 namespace kv {
@@ -197,7 +198,9 @@ __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   return it;
 }
 
-template <int D, bool BF16, bool OUT_F32, bool PAGED, bool DEC>
+// PV16 (bf16 inputs only): V is the call's fp16 copy scaled per (batch, K/V head)
+// by 2^e (vscale.cuh), P is fp16 and P·V one fp16 product; the output is scaled back.
+template <int D, bool BF16, bool OUT_F32, bool PAGED, bool DEC, bool PV16 = false>
 __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     attn_kv_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -210,8 +213,9 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
   constexpr uint32_t kTmemCols = R::kTmemCols;
   constexpr uint32_t kColO = R::kColO;
   constexpr int S = G::kSlots;
-  constexpr bool kSplitP = BF16;  // bf16 P as hi + lo halves (two P·V MMAs)
-  constexpr bool kF16Exp = !BF16;  // fp16: exponentials on packed fp16 pairs
+  static_assert(!PV16 || (BF16 && !PAGED), "the fp16 copy of V is for dense bfloat16 inputs");
+  constexpr bool kSplitP = BF16 && !PV16;  // bf16 P as hi + lo halves (two P·V MMAs)
+  constexpr bool kF16Exp = !BF16;  // fp16 inputs: exponentials on packed fp16 pairs
   constexpr float kThresh = kF16Exp ? 1.0f : 8.0f;  // log2 units of max growth before a rescale
 
   extern __shared__ uint8_t smem_raw[];
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     // ------------------------------------------------------------- MMA issuer
     if (nblocks > 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32acc(BF16, kBM, kBN, false);
-      constexpr uint32_t idesc_o = idesc_f16_f32acc(BF16, kBM, D, true);
+      constexpr uint32_t idesc_o = idesc_f16_f32acc(kSplitP, kBM, D, true);
       const uint64_t dq = sdesc_sw128(sQ, 16, 1024);               // Q tile, K-major
       const uint64_t dk = sdesc_sw128(sKV, 16, 1024);              // K slots, K-major
       const uint64_t dv = sdesc_sw128(sKV, G::kChunkBytes, 1024);  // V slots, MN-major
@@ -618,7 +622,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
                 p1 = (cg + 1 >= vis_lo && cg + 1 < vis_hi) ? p1 : 0.f;
               }
               acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], make_float2(p0, p1));
-              const uint32_t hi = pack2(p0, p1, BF16);
+              const uint32_t hi = pack2(p0, p1, kSplitP);  // bf16 halves or fp16 P
               pk[(c - c0) >> 1] = hi;
               if constexpr (kSplitP)
                 pk_lo[(c - c0) >> 1] =
@@ -705,7 +709,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       // ---- epilogue: O / l and the log-sum-exp of this row over this split; each
       // half of the row writes its half of the O columns
       const bool have = nblocks > 0;
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      if constexpr (PV16) inv_l *= exp2_int(-v16_exponent(p.vmax[it.b * p.Hkv + it.g]));
       const size_t row = (static_cast<size_t>(it.b) * p.Hq + h) * p.Lq + qi;  // LSE index
       const bool partial = p.splits > 1;
       const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;

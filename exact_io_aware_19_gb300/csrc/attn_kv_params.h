@@ -11,6 +11,7 @@ struct KvParams {
   uint32_t* status;     // 4 x u32 status word in the workspace
   float* o_part;        // [splits, B*Hq*Lq, D] float32 partial outputs (splits > 1), else null
   float* lse_part;      // [splits, B*Hq*Lq] partial log2-sum-exp (splits > 1), else null
+  const uint32_t* vmax; // [B, Hkv] largest finite |v| (bf16 bits) of the fp16 copy of V, or null
   int B, Lq, Lk, Hq, Hkv;
   int group;            // Hq / Hkv: query heads that read one K/V head
   int causal;           // 0 / 1

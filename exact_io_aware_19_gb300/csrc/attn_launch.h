@@ -56,8 +56,18 @@ struct BwdLaunchArgs {
 // Each returns the CUDA error of configuring / enqueuing the kernel.
 cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
+// bfloat16 inputs with the fp16 copy of V (a.tm_v over it, a.p.vmax set).
+cudaError_t launch_fwd_pv16(int d, bool out_f32, const LaunchArgs& a);
+// The fp16 copy of a bfloat16 V [B, L, Hkv, d] with one power-of-two scale per
+// (batch, K/V head): clears vmax [B * Hkv], writes the heads' largest finite |v|
+// there, then v16 (the same layout as v). Three operations on `stream`.
+cudaError_t launch_v_to_f16(const void* v, void* v16, uint32_t* vmax, int B, int L, int Hkv,
+                            int d, cudaStream_t stream);
 // The decode-shaped forward (and, when p.splits > 1, its merge kernel).
 cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
+// The one-tile kernel for attn_fwd on bfloat16 inputs with the fp16 copy of V (one
+// key split; a.tm_v over the copy, a.p.vmax set).
+cudaError_t launch_kv_pv16(int d, bool out_f32, const KvLaunchArgs& a);
 // The one-tile kernel's decode mode (one softmax warp, two CTAs per SM): fp16 at
 // d = 64 with at most 32 rows per tile (q_per_tile * group). Its split count targets
 // two CTAs per SM (kv_decode_shape: the same rule without the dtype, which the split

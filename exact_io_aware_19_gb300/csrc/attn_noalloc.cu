@@ -13,7 +13,8 @@
 //   * the array is kNoAllocScratchBytes = 256 bytes; every GPU that loads this
 //     library holds it until the process exits;
 //   * a problem whose workspace need exceeds 256 bytes is rejected with
-//     ATTN_ERR_WORKSPACE (no shape needs more today);
+//     ATTN_ERR_WORKSPACE (no shape needs more: bfloat16 inputs run attn_fwd's
+//     split-weight path, which makes no copy of V);
 //   * all calls on a device share the one array. Each call clears the status word
 //     (on the call's stream, after its arguments are validated), so calls that
 //     overlap on the GPU — on different streams, or from different threads — race
@@ -123,7 +124,10 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
                                           int causal, int window_left, float scale,
                                           attn_dtype_t dtype, attn_out_t out_dtype,
                                           void* stream) {
-  const size_t need = attn_fwd_workspace_size(B, L, Hq, Hkv, d, causal, window_left);
+  // The least workspace attn_fwd accepts (the status word; fp16's full size). With
+  // bfloat16 inputs so small a workspace runs the split-weight path, which needs no
+  // copy of V.
+  const size_t need = attn_fwd_workspace_size(B, L, Hq, Hkv, d, causal, window_left, ATTN_FP16);
   if (need == 0) {
     // An invalid shape: attn_fwd reports it (and its detail) before touching memory.
     return attn_fwd(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, scale, dtype,

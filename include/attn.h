@@ -9,7 +9,8 @@
  * described in "What is memory-efficient attention for long context on 8x H100?"
  * (aivaro.ru, answers 650), section 2: Q/K/V are processed in blocks held on chip
  * with an online softmax, so the L x L score matrix never reaches HBM and the extra
- * memory is O(L·d) (only inputs, outputs and a fixed-size workspace).
+ * memory is O(L·d) (inputs, outputs and a workspace: a fixed 256 bytes for fp16
+ * inputs, a copy of V for bfloat16 inputs).
  *
  * For batch b, query head h, row i, with g = h / (Hq / Hkv) and the visible keys
  *   J_i = { j < L : (causal => j <= i) and (window_left >= 0 => j >= i - window_left) }:
@@ -24,7 +25,8 @@
  * All pointers passed to attn_fwd are DEVICE pointers of the current CUDA device.
  *
  * Asynchrony. attn_fwd enqueues one kernel on `stream` (a cudaStream_t; NULL = the
- * legacy default stream) and returns without synchronising. Argument errors are
+ * legacy default stream; with bfloat16 inputs and the full workspace, first a memset
+ * and two kernels that write the fp16 copy of V) and returns without synchronising. Argument errors are
  * returned before anything is enqueued. Errors detected on the device (a bounded
  * wait that ran out) are recorded in the workspace status word and reported by
  * attn_fwd_sync_status.
@@ -54,7 +56,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 typedef enum {
     ATTN_OK = 0,
@@ -76,12 +78,22 @@ typedef enum {
 } attn_out_t;
 
 /*
- * Bytes of device workspace attn_fwd needs for this problem (a status word; the
- * size does not depend on the problem today, but callers should query it).
- * Returns 0 for sizes attn_fwd would reject.
+ * Bytes of device workspace attn_fwd needs for this problem. fp16: 256 (a status
+ * word). bfloat16: 256 + (4·B·Hkv rounded up to 256) + 2·B·L·Hkv·d, the status word,
+ * then per (batch, K/V head) the largest finite |v| and an fp16 copy of V scaled by
+ * a power of two per (batch, K/V head), so that the attention weights enter the P·V
+ * product as fp16 (11 significant bits) in one product per key block; the scale is
+ * undone on the output. Every bfloat16 value of V whose scaled magnitude is at least
+ * 2^-17 is copied exactly (the largest scaled |v| is in [2^14, 2^15)); smaller ones,
+ * below 2^-31 of their head's largest |v|, round to the nearest multiple of 2^-24.
+ * attn_fwd also accepts a bfloat16 call with a workspace of at least 256 bytes but
+ * less than this: it then splits the weights into two bfloat16 parts (hi + lo) and
+ * runs two P·V products per key block instead, with the same accuracy bound and
+ * about 1.4x the time at d = 128 (this is what attn_fwd_noalloc runs).
+ * Returns 0 for sizes or a dtype attn_fwd would reject.
  */
 size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
-                               int window_left);
+                               int window_left, attn_dtype_t dtype);
 
 /*
  * Attention forward (see the header comment for the definition).
@@ -94,8 +106,9 @@ size_t attn_fwd_workspace_size(int B, int L, int Hq, int Hkv, int d, int causal,
  *   causal      0 or 1 (causal: key j visible from query i only when j <= i)
  *   window_left -1 for none, or w >= 0 (keys i-w .. i); requires causal = 1
  *   scale       finite multiplier of q·k (1/sqrt(d) is the usual choice)
- *   workspace   device pointer, 16-byte aligned, >= attn_fwd_workspace_size bytes;
- *               must not be used by another call that is still running
+ *   workspace   device pointer, 16-byte aligned, >= attn_fwd_workspace_size bytes
+ *               (bfloat16: >= 256 bytes, see attn_fwd_workspace_size); must not be used
+ *               by another call that is still running
  *   stream      cudaStream_t to enqueue on
  * Returns ATTN_OK when the kernel was enqueued; otherwise nothing was enqueued and
  * the outputs are untouched. Requires a device of compute capability 10.3.
@@ -157,8 +170,9 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
  *   J_i = { j < L : (window_left >= 0 => j >= i - window_left) and
  *                   (window_right >= 0 => j <= i + window_right) },
  * each bound -1 for none: (-1, 0) is causal attention, (-1, -1) full attention.
- * Other arguments, layouts, workspace (attn_fwd_workspace_size) and errors as for
- * attn_fwd; at most 128 query heads per K/V head. It runs on the one-tile kernel
+ * Other arguments, layouts and errors as for attn_fwd; the workspace is at least 256
+ * bytes (the status word; bfloat16 inputs run the split-weight path, without a copy
+ * of V); at most 128 query heads per K/V head. It runs on the one-tile kernel
  * (ATTN_PATH_TILES below): a band of a few hundred keys per row is little work per
  * query tile, which that kernel spreads over one CTA per 128-row tile.
  */
@@ -180,7 +194,8 @@ attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void 
  * library keeps until the process exits. Arguments and results are those of
  * attn_fwd. Rules:
  *   - Problems needing more scratch than 256 bytes return ATTN_ERR_WORKSPACE (none
- *     do today).
+ *     do: bfloat16 inputs run the split-weight path of attn_fwd, which makes no copy
+ *     of V; see attn_fwd_workspace_size).
  *   - All calls on a device share the array, and each call clears its status word
  *     (after its arguments are validated: a rejected call enqueues nothing): calls
  *     that overlap on the GPU (other streams, other threads) race.
@@ -321,6 +336,15 @@ attn_status_t attn_debug_wait_probe(void *workspace, size_t workspace_bytes,
  * float32 arrays; used by the accuracy tests.
  */
 attn_status_t attn_debug_exp2(const float *x, float *y_mufu, float *y_f16, int n, void *stream);
+
+/*
+ * The power-of-two exponent e of the fp16 copy of a bfloat16 V (see
+ * attn_fwd_workspace_size) for a head whose largest finite |v| has the bfloat16 bit
+ * pattern `absmax_bits` (sign clear): the kernels scale that head's V by 2^e and its
+ * output by 2^-e. Host arithmetic only (the device runs the same function); used by
+ * the tests.
+ */
+int attn_debug_v16_exponent(uint32_t absmax_bits);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status_t s);

@@ -29,11 +29,11 @@ def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
     return 0.5 * 2.0 ** (e - mant)
 
 
-def gpu_run(q, k, v, causal, wl, scale, out_fp32):
+def gpu_run(q, k, v, causal, wl, scale, out_fp32, workspace=None):
     import exact_io_aware_19_gb300 as ex
     o, lse = ex.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, window_left=wl,
-                         scale=scale, out_fp32=out_fp32)
-    ex.sync_status()
+                         scale=scale, out_fp32=out_fp32, workspace=workspace)
+    ex.sync_status(workspace)
     return o, lse
 
 
@@ -59,14 +59,16 @@ def gather_rows(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, rows: np.ndarray):
     return o, lse
 
 
-def compare(q, k, v, dtype, causal, wl, scale, rows=None, label=""):
+def compare(q, k, v, dtype, causal, wl, scale, rows=None, label="", workspace=None):
     """Run GPU (float32 and in-dtype output) and oracle; assert the tolerances.
+    ``workspace`` (a CUDA uint8 tensor) replaces the default one: a bf16 call with
+    less than attn_fwd_workspace_size bytes runs the split-weight path.
 
     Returns a dict of error statistics.
     """
     rows, o_ref, lse_ref = oracle_rows(q, k, v, dtype, causal, wl, scale, rows)
-    o32, lse = gpu_run(q, k, v, causal, wl, scale, out_fp32=True)
-    o16, lse16 = gpu_run(q, k, v, causal, wl, scale, out_fp32=False)
+    o32, lse = gpu_run(q, k, v, causal, wl, scale, out_fp32=True, workspace=workspace)
+    o16, lse16 = gpu_run(q, k, v, causal, wl, scale, out_fp32=False, workspace=workspace)
     g32, glse = gather_rows(o32, lse, rows)
     g16, _ = gather_rows(o16, lse16, rows)
     assert np.isfinite(g32).all() and np.isfinite(glse).all(), f"{label}: non-finite output"

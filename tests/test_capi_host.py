@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(ex.library_path())
     missing = [n for n in declared_functions() if not hasattr(raw, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert lib.attn_abi_version() == 3
+    assert lib.attn_abi_version() == 4
 
 
 def test_status_strings(lib):
@@ -52,12 +52,60 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    assert lib.attn_fwd_workspace_size(1, 131072, 4, 4, 64, 1, -1) == 256
-    assert lib.attn_fwd_workspace_size(1, 1, 32, 8, 128, 1, 4096) == 256
+    FP16, BF16 = 0, 1
+    assert lib.attn_fwd_workspace_size(1, 131072, 4, 4, 64, 1, -1, FP16) == 256
+    assert lib.attn_fwd_workspace_size(1, 1, 32, 8, 128, 1, 4096, FP16) == 256
+    # bf16: status word, the heads' largest |v| (padded to 256 bytes), the fp16 copy of V
+    assert lib.attn_fwd_workspace_size(1, 131072, 32, 8, 128, 1, -1, BF16) == \
+        256 + 256 + 2 * 131072 * 8 * 128
+    assert lib.attn_fwd_workspace_size(4, 32768, 16, 16, 128, 1, 4096, BF16) == \
+        256 + 256 + 2 * 4 * 32768 * 16 * 128
+    assert lib.attn_fwd_workspace_size(3, 100, 200, 100, 64, 0, -1, BF16) == \
+        256 + 1280 + 2 * 3 * 100 * 100 * 64  # 4 * 300 bytes of maxima -> 1280
+    assert lib.attn_fwd_workspace_size(1, 16, 4, 4, 64, 1, -1, 2) == 0  # no such dtype
     for bad in [(0, 16, 4, 4, 64, 1, -1), (1, 0, 4, 4, 64, 1, -1), (1, 16, 3, 2, 64, 1, -1),
                 (1, 16, 4, 4, 96, 1, -1), (1, 16, 4, 4, 64, 0, 5), (1, 16, 4, 4, 64, 1, -2),
                 (1, 16, 4, 4, 64, 2, -1), (1 << 16, 1 << 16, 1, 1, 64, 0, -1)]:
-        assert lib.attn_fwd_workspace_size(*bad) == 0, bad
+        for dt in (FP16, BF16):
+            assert lib.attn_fwd_workspace_size(*bad, dt) == 0, bad
+
+
+def _bf16_value(bits):
+    return float(torch.tensor([bits << 16], dtype=torch.int32).view(torch.float32))
+
+
+def test_v16_exponent_puts_each_head_maximum_in_2e14_2e15(lib):
+    """The fp16 copy of a bfloat16 V: for every finite bf16 maximum m, m·2^e lies in
+    [2^14, 2^15) (largest fp16 value 65504 < 2^16), unless 2^e would leave the normal
+    floats (e = 126 then, m·2^126 < 2^14); e and -e stay in [-126, 126]."""
+    assert lib.attn_debug_v16_exponent(0) == 0  # an all-zero head
+    for bits in range(1, 0x7F80):
+        e = lib.attn_debug_v16_exponent(bits)
+        m = _bf16_value(bits)
+        assert -126 <= e <= 126, (hex(bits), e)
+        scaled = m * 2.0 ** e
+        if e < 126:
+            assert 2.0 ** 14 <= scaled < 2.0 ** 15, (hex(bits), e, scaled)
+        else:
+            assert scaled < 2.0 ** 15, (hex(bits), e, scaled)
+            assert m < 2.0 ** -111, (hex(bits), m)
+
+
+def test_v16_copy_is_exact_above_2e_minus_17():
+    """Every bfloat16 value v with |v| <= m has 8 significant bits, so fp16(v·2^e) is
+    v·2^e exactly whenever |v·2^e| >= 2^-17; below, the error is at most 2^-25 (half
+    the fp16 subnormal spacing), i.e. under 2^-39 of the head's maximum."""
+    import numpy as np
+    allbits = np.arange(0, 0x7F80, dtype=np.uint32)
+    vals = (allbits << 16).view(np.float32).astype(np.float64)
+    for e in (-113, -20, 0, 7, 14, 40, 126):
+        scaled = vals * 2.0 ** e
+        keep = scaled < 2.0 ** 15
+        x = scaled[keep]
+        h = x.astype(np.float16).astype(np.float64)
+        exact = x >= 2.0 ** -17
+        assert (h[exact] == x[exact]).all(), e
+        assert (np.abs(h - x)[~exact] <= 2.0 ** -25).all(), e
 
 
 A = 1 << 20  # a fake, 16-byte aligned address; never dereferenced

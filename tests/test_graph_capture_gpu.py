@@ -64,3 +64,28 @@ def test_attn_fwd_graph_replay():
         o_ref, l_ref = ex.attn_fwd(q, k, v, causal=True, scale=1 / math.sqrt(64))
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), seed
     ex.sync_status(ws)
+
+
+def test_attn_fwd_bf16_copy_of_v_graph_replay():
+    """bf16 with the full workspace: the capture holds the memset and the two kernels
+    that write the fp16 copy of V, then the attention kernel; a replay with new V gives
+    the direct call's bits (the copy is rewritten from the new V)."""
+    import exact_io_aware_19_gb300 as ex
+    B, L, H, Hkv, d = 1, 1500, 8, 2, 128
+    q, k, v = si.random_qkv(B, L, H, Hkv, d, dtype="bf16", seed=31, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, L, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(ex.workspace_size(B, L, H, Hkv, d, True, -1, "bf16"), dtype=torch.uint8,
+                     device="cuda")
+    g = _capture(lambda: ex.attn_fwd_into(q, k, v, o, lse, causal=True, workspace=ws,
+                                          stream=torch.cuda.current_stream()))
+    ws_ref = torch.zeros_like(ws)
+    for seed in (32, 33):
+        qn, kn, vn = si.random_qkv(B, L, H, Hkv, d, dtype="bf16", seed=seed, device="cuda")
+        q.copy_(qn), k.copy_(kn), v.copy_(vn * 2.0 ** (seed - 40))  # another scale per replay
+        g.replay()
+        torch.cuda.synchronize()
+        o_ref, l_ref = ex.attn_fwd(q, k, v, causal=True, workspace=ws_ref)
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), seed
+    ex.sync_status(ws)
+    ex.sync_status(ws_ref)

@@ -63,7 +63,10 @@ def test_square_problem_matches_the_square_kernel():
     import exact_io_aware_19_gb300 as ex
     q, k, v = si.random_qkv(2, 513, 4, 2, 128, dtype="bf16", seed=17, device="cuda")
     compare_kv(q.cpu(), k.cpu(), v.cpu(), "bf16", True, -1, 0.09, num_splits=2, label="square")
-    o1, l1 = ex.attn_fwd(q, k, v, causal=True, scale=0.09, out_fp32=True)
+    # attn_fwd with a status-word-sized workspace: the split bf16 weights, as here
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    o1, l1 = ex.attn_fwd(q, k, v, causal=True, scale=0.09, out_fp32=True, workspace=ws)
+    ex.sync_status(ws)
     o2, l2 = ex.attn_fwd_kv(q, k, v, causal=True, scale=0.09, out_fp32=True, num_splits=1)
     assert (o1 - o2).abs().max().item() < 2e-3 and (l1 - l2).abs().max().item() < 1e-4
 

@@ -251,21 +251,27 @@ def test_auto_path_choice_causal_one_unit_per_sm():
 
 
 def test_auto_path_choice_d128_window():
-    """d = 128 (P over S in the two-tile kernel): AUTO takes the one-tile kernel under
-    a left window whose K/V span fits in 192 MiB, the two-tile kernel for causal
-    attention without a window (at any length with more units than SMs). AUTO gives
-    the chosen kernel's bits."""
+    """d = 128 bf16. With the full workspace (fp16 weights against the fp16 copy of V,
+    one P·V product) AUTO takes the two-tile kernel, window or not. With a 256-byte
+    workspace (the split weights, P over S in the two-tile kernel) it takes the
+    one-tile kernel under a left window whose K/V span fits in 192 MiB, the two-tile
+    kernel for causal attention without a window. AUTO gives the chosen kernel's bits."""
     import exact_io_aware_19_gb300 as ex
-    for B, L, causal, wl, pick in ((2, 8192, True, -1, ex.PATH_SQUARE),
-                                   (1, 65536, True, -1, ex.PATH_SQUARE),
-                                   (1, 65536, True, 1000, ex.PATH_TILES)):
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for B, L, causal, wl, ws, pick in ((2, 8192, True, -1, small, ex.PATH_SQUARE),
+                                       (1, 65536, True, -1, small, ex.PATH_SQUARE),
+                                       (1, 65536, True, 1000, small, ex.PATH_TILES),
+                                       (1, 65536, True, 1000, None, ex.PATH_SQUARE),
+                                       (2, 8192, True, -1, None, ex.PATH_SQUARE)):
         q, k, v = si.random_qkv(B, L, 16, 8, 128, dtype="bf16", seed=L + B, device="cuda")
         assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
-        o_auto, l_auto = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, out_fp32=True)
+        o_auto, l_auto = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, out_fp32=True,
+                                     workspace=ws)
         ex.set_path_policy(pick)
-        o_p, l_p = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, out_fp32=True)
+        o_p, l_p = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, out_fp32=True, workspace=ws)
         ex.set_path_policy(ex.PATH_AUTO)
-        assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (B, L, wl)
+        ex.sync_status(ws)
+        assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (B, L, wl, ws is None)
         del q, k, v, o_auto, o_p
 
 

@@ -40,9 +40,12 @@ def test_noalloc_matches_attn_fwd_twice(shape):
     lib = ex.load_library()
     scale = 1.0 / math.sqrt(d)
     q, k, v = si.random_qkv(B, L, Hq, Hkv, d, dtype=dt, seed=L + d, device="cuda")
+    # attn_fwd with a status-word-sized workspace runs the kernel the no-allocation
+    # call runs (bf16: the split weights, no copy of V)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     o_ref, lse_ref = ex.attn_fwd(q, k, v, causal=causal, window_left=wl, scale=scale,
-                                 out_fp32=out_fp32)
-    ex.sync_status()
+                                 out_fp32=out_fp32, workspace=ws)
+    ex.sync_status(ws)
     for _ in range(2):
         o = torch.full_like(o_ref, float("nan"))
         lse = torch.full_like(lse_ref, float("nan"))
@@ -93,8 +96,9 @@ def test_noalloc_python_binding_matches_attn_fwd():
     """The Python binding of the same name (argument marshalling only) on two calls in
     a row, against attn_fwd through its own workspace."""
     q, k, v = si.random_qkv(2, 640, 8, 2, 128, dtype="bf16", seed=9, device="cuda")
-    o_ref, lse_ref = ex.attn_fwd(q, k, v, causal=True, window_left=200, scale=None)
-    ex.sync_status()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")  # the same (split-weight) kernel
+    o_ref, lse_ref = ex.attn_fwd(q, k, v, causal=True, window_left=200, scale=None, workspace=ws)
+    ex.sync_status(ws)
     for _ in range(2):
         o = torch.full_like(o_ref, float("nan"))
         lse = torch.full_like(lse_ref, float("nan"))
