@@ -250,11 +250,11 @@ KvPlan kv_plan(int B, int Lq, int Lk, int Hq, int Hkv, int causal, int window_le
   return k;
 }
 
-// Splits that fill the SMs with one wave of CTAs (two per SM for the one-tile
-// kernel's decode mode: d = 64 with at most 32 rows per tile), keeping at least 2 key
-// blocks per split and at most kKvMaxSplits.
+// Splits that fill the SMs with one wave of CTAs (for items of at most 32 rows, the
+// keys-on-lanes kernel's CTAs per SM: two at d = 64), keeping at least 2 key blocks
+// per split and at most kKvMaxSplits.
 int kv_auto_splits(const KvPlan& k, int sms, int d) {
-  const int ctas = ex19::kv_decode_shape(d, k.q_per_tile, k.group) ? 2 * sms : sms;
+  const int ctas = ex19::kv_keys_shape(k.q_per_tile, k.group) ? ex19::kv_keys_ctas_per_sm(d) * sms : sms;
   int s = std::max(1, ctas / std::max(1, k.items));
   s = std::min(s, std::max(1, k.max_blocks / 2));
   return std::min(s, kKvMaxSplits);

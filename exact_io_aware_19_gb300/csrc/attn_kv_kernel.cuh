@@ -49,13 +49,8 @@
 //     32 / (128 / page_size) blocks, loaded a window ahead, and lane pp issues page
 //     pp's copies, so neither page-table latency nor a serial issue of small boxes
 //     paces the stream.
-//   * Decode mode (DEC; fp16, d = 64, at most 32 valid rows per tile, as in one new
-//     token per sequence): the tile's rows fit one softmax warp, so the CTA has 3
-//     warps (softmax, producer, MMA), one S buffer with P in its own 64 columns and
-//     O (256 TMEM columns) and 5 ring slots (96 KiB), and two CTAs share an SM: two
-//     softmax chains per SM instead of one, for a shape whose time per key block is
-//     one row's softmax latency. S(j + 1) is issued once the softmax has read S(j)
-//     into registers (s_free); the softmax writes P(j) after P·V(j − 1) is done.
+//   * Items of at most 32 query rows (a decode step) run the keys-on-lanes kernel of
+//     attn_kv_keys_kernel.cuh instead, with the same items, splits and partials.
 //   * Every wait is bounded; a timeout sets the status word and all roles leave.
 #pragma once
 #include <cuda.h>
@@ -77,19 +72,16 @@ namespace kv {
 constexpr int kBM = 128;             // rows per tile (= TMEM lanes)
 constexpr int kBN = 128;             // keys per K/V block
 
-// Warp roles and TMEM columns of the two modes.
-template <bool DEC>
+// Warp roles and TMEM columns.
 struct KvRoles {
-  static constexpr int kSmxWarps = DEC ? 1 : 8;               // softmax warps (32 rows each)
-  static constexpr int kHalves = DEC ? 1 : 2;                  // softmax threads per row
+  static constexpr int kSmxWarps = 8;                          // softmax warps (two per lane quarter)
+  static constexpr int kHalves = 2;                            // softmax threads per row
   static constexpr int kThreads = 32 * (kSmxWarps + 2);        // + producer warp + MMA warp
   static constexpr int kProducerWarp = kSmxWarps;
   static constexpr int kMmaWarp = kSmxWarps + 1;
-  static constexpr uint32_t kTmemCols = DEC ? 256 : 512;
-  // DEC: S [0,128), P [128,192), O [192,256); else S0 [0,128), S1 [128,256) with P
-  // over them, O [256, 256 + D)
-  static constexpr uint32_t kColP = 128;
-  static constexpr uint32_t kColO = DEC ? 192 : 256;
+  static constexpr uint32_t kTmemCols = 512;
+  // S0 [0,128), S1 [128,256) with P over them, O [256, 256 + D)
+  static constexpr uint32_t kColO = 256;
 };
 
 enum : uint32_t {
@@ -102,22 +94,22 @@ enum : uint32_t {
   kSiteBadSeqLen = 0x90001,  // a paged sequence length outside [Lq, max_seq_len]
 };
 
-template <int D, bool DEC = false>
+template <int D>
 struct KvGeometry {
   static constexpr int kChunks = D / 64;          // 128-byte swizzle boxes per row
   static constexpr int kChunkBytes = kBM * 128;   // one box column of a 128-row tile
   static constexpr int kTileBytes = kBM * D * 2;  // a 128-row tile of Q, K or V
-  static constexpr int kSlots = DEC ? 5 : (D == 64) ? 8 : 5;
+  static constexpr int kSlots = (D == 64) ? 8 : 5;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-  // barriers: full[S], empty[S], q_full, s_full[2] (DEC: s_full, s_free), p_full[2],
-  // pv_done[2], o_full, drain, exchange[4 warp pairs][2 buffers]
+  // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full,
+  // drain, exchange[4 warp pairs][2 buffers]
   static constexpr int kNumBars = 2 * kSlots + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   // the two halves of a row trade one float per round: [2 buffers][2 halves][128 rows]
   static constexpr int kOffX = kOffMisc + 16;
-  static constexpr int kXBytes = DEC ? 0 : 2 * 2 * kBM * 4;
+  static constexpr int kXBytes = 2 * 2 * kBM * 4;
   static constexpr int kSmemUsed = kOffX + kXBytes;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
 };
@@ -198,16 +190,114 @@ __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   return it;
 }
 
+// The TMA producer warp of the one-tile kernels: the Q tile of the work item, then K_j
+// and V_j of its blocks [it.lo, it.hi) into a ring of S slots of 128 keys × D (slot s
+// at sKV + s·128·D·2; its full barrier at bars + 8s, its empty barrier at bars +
+// 8(S + s)); q_full at bars + 16S. Q chunk c (64 columns) lands at sQ + c·q_chunk_bytes.
+// The whole warp calls it (the paged producer uses every lane).
+template <bool PAGED, int D>
+__device__ __forceinline__ void kv_produce(const KvParams& p, const KvItem& it, int nblocks,
+                                           const CUtensorMap* tm_q_, const CUtensorMap* tm_k_,
+                                           const CUtensorMap* tm_v_, uint32_t sQ,
+                                           uint32_t q_chunk_bytes, uint32_t sKV, int S,
+                                           uint32_t bars, const WaitCtl& wc, int lane) {
+  constexpr int kChunks = D / 64;
+  constexpr int kTileBytes = kBM * D * 2;
+  constexpr int kChunkBytes = kBM * 128;
+  auto bar_full = [&](uint32_t s) { return bars + 8u * s; };
+  auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
+  const uint32_t bar_q_full = bars + 8u * (2 * S);
+  const CUtensorMap& tm_q = *tm_q_;
+  const CUtensorMap& tm_k = *tm_k_;
+  const CUtensorMap& tm_v = *tm_v_;
+  if (nblocks > 0) {
+    if (lane == 0) {
+      // The Q box is {64, group, q_per_tile, 1}; rows past Lq are zero-filled and
+      // still counted in the transaction bytes.
+      mbar_arrive_expect_tx(bar_q_full, kChunks * 128u * p.group * p.q_per_tile);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(sQ + c * q_chunk_bytes, &tm_q, bar_q_full, c * 64, it.g * p.group, it.i0,
+                    it.b);
+    }
+    uint32_t n = 0;
+    bool ok = true;
+    if constexpr (PAGED) {
+      // The whole warp runs the loop: its 32 lanes hold the physical rows of the
+      // pages of a window of W = 32 / P blocks (P = 128 / page_size pages per block),
+      // and the next window's page-table loads are issued when the current window
+      // starts, so they land long before they are needed (a table read per block,
+      // right before its TMA, put an L2 round trip under load on every block).
+      // Lane 0 takes each page's row by shuffle and issues the copies.
+      const int P = kBN / p.page_size;
+      const int W = 32 / P;
+      const int oob_row = p.num_pages * p.page_size;  // past the cache: zero-filled
+      auto fetch = [&](int j0) -> int {  // this lane's page of the window starting at j0
+        const int jb = j0 + lane / P, lp = jb * P + lane % P;  // block, logical page
+        int phys = -1;
+        if (jb < it.hi && lp * p.page_size < it.Lk)
+          phys = p.block_table[static_cast<size_t>(it.b) * p.max_pages + lp];
+        return (phys >= 0 && phys < p.num_pages) ? phys * p.page_size : oob_row;
+      };
+      int cur = fetch(it.lo), nxt = oob_row;
+      for (int j = it.lo; ok && j < it.hi; ++j) {
+        const int jw = (j - it.lo) % W;
+        if (jw == 0) nxt = fetch(j + W);
+        for (int kv = 0; ok && kv < 2; ++kv) {
+          const uint32_t slot = n % S;
+          ok = mbar_wait_warp(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(bar_full(slot), kTileBytes);
+          __syncwarp();  // the transaction count is set before any copy can complete
+          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+          // lane pp < P copies page pp of this block: one box of page_size rows
+          const int row = __shfl_sync(0xffffffffu, cur, jw * P + (lane % P));
+          if (lane < P) {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(sKV + slot * kTileBytes + c * kChunkBytes + lane * p.page_size * 128,
+                          tm, bar_full(slot), c * 64, it.g, row, 0);
+          }
+          ++n;
+        }
+        if (jw == W - 1) cur = nxt;
+      }
+    } else if (lane == 0) {
+      for (int j = it.lo; ok && j < it.hi; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t slot = n % S;
+          ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_full(slot), kTileBytes);
+          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(sKV + slot * kTileBytes + c * kChunkBytes, tm, bar_full(slot),
+                        c * 64, it.g, j * kBN, it.b);
+          ++n;
+        }
+      }
+    }
+    if (lane == 0) {
+      // Whether or not this CTA aborted, the copies issued last may still be in
+      // flight (another role can abort after this loop has ended, and then nothing
+      // consumes them): let them land before the CTA can exit.
+      for (uint32_t back = 1; back <= S && back <= n; ++back) {
+        const uint32_t m = n - back;
+        mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrainLoads);
+      }
+      mbar_wait_drain(bar_q_full, 0, wc, kSiteDrainLoads);
+    }
+  }
+}
+
 // PV16 (bf16 inputs only): V is the call's fp16 copy scaled per (batch, K/V head)
 // by 2^e (vscale.cuh), P is fp16 and P·V one fp16 product; the output is scaled back.
-template <int D, bool BF16, bool OUT_F32, bool PAGED, bool DEC, bool PV16 = false>
-__global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
+template <int D, bool BF16, bool OUT_F32, bool PAGED, bool PV16 = false>
+__global__ void __launch_bounds__(KvRoles::kThreads, 1)
     attn_kv_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const KvParams p) {
-  static_assert(!DEC || (D == 64 && !BF16), "decode mode: fp16, d = 64 (P in 64 TMEM columns)");
-  using G = KvGeometry<D, DEC>;
-  using R = KvRoles<DEC>;
+  using G = KvGeometry<D>;
+  using R = KvRoles;
   constexpr int kProducerWarp = R::kProducerWarp;
   constexpr int kMmaWarp = R::kMmaWarp;
   constexpr uint32_t kTmemCols = R::kTmemCols;
@@ -229,7 +319,6 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
   auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
   const uint32_t bar_q_full = bars + 8u * (2 * S);
   auto bar_s_full = [&](uint32_t b) { return bars + 8u * (2 * S + 1 + b); };
-  const uint32_t bar_s_free = bar_s_full(1);  // DEC: the softmax has read S
   auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 3 + b); };
   auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
   const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
@@ -251,7 +340,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     }
     mbar_init(bar_q_full, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s_full(b), (DEC && b == 1) ? R::kSmxWarps * 32 : 1);  // DEC: s_free
+      mbar_init(bar_s_full(b), 1);
       mbar_init(bar_p_full(b), R::kSmxWarps * 32);
       mbar_init(bar_pv_done(b), 1);
     }
@@ -296,83 +385,8 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (nblocks > 0) {
-      if (lane == 0) {
-        // The Q box is {64, group, q_per_tile, 1}; rows past Lq are zero-filled and
-        // still counted in the transaction bytes.
-        mbar_arrive_expect_tx(bar_q_full, G::kChunks * 128u * p.group * p.q_per_tile);
-        for (int c = 0; c < G::kChunks; ++c)
-          tma_load_4d(sQ + c * G::kChunkBytes, &tm_q, bar_q_full, c * 64, it.g * p.group, it.i0,
-                      it.b);
-      }
-      uint32_t n = 0;
-      bool ok = true;
-      if constexpr (PAGED) {
-        // The whole warp runs the loop: its 32 lanes hold the physical rows of the
-        // pages of a window of W = 32 / P blocks (P = 128 / page_size pages per block),
-        // and the next window's page-table loads are issued when the current window
-        // starts, so they land long before they are needed (a table read per block,
-        // right before its TMA, put an L2 round trip under load on every block).
-        // Lane 0 takes each page's row by shuffle and issues the copies.
-        const int P = kBN / p.page_size;
-        const int W = 32 / P;
-        const int oob_row = p.num_pages * p.page_size;  // past the cache: zero-filled
-        auto fetch = [&](int j0) -> int {  // this lane's page of the window starting at j0
-          const int jb = j0 + lane / P, lp = jb * P + lane % P;  // block, logical page
-          int phys = -1;
-          if (jb < it.hi && lp * p.page_size < it.Lk)
-            phys = p.block_table[static_cast<size_t>(it.b) * p.max_pages + lp];
-          return (phys >= 0 && phys < p.num_pages) ? phys * p.page_size : oob_row;
-        };
-        int cur = fetch(it.lo), nxt = oob_row;
-        for (int j = it.lo; ok && j < it.hi; ++j) {
-          const int jw = (j - it.lo) % W;
-          if (jw == 0) nxt = fetch(j + W);
-          for (int kv = 0; ok && kv < 2; ++kv) {
-            const uint32_t slot = n % S;
-            ok = mbar_wait_warp(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
-            __syncwarp();  // the transaction count is set before any copy can complete
-            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-            // lane pp < P copies page pp of this block: one box of page_size rows
-            const int row = __shfl_sync(0xffffffffu, cur, jw * P + (lane % P));
-            if (lane < P) {
-#pragma unroll
-              for (int c = 0; c < G::kChunks; ++c)
-                tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes + lane * p.page_size * 128,
-                            tm, bar_full(slot), c * 64, it.g, row, 0);
-            }
-            ++n;
-          }
-          if (jw == W - 1) cur = nxt;
-        }
-      } else if (lane == 0) {
-        for (int j = it.lo; ok && j < it.hi; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const uint32_t slot = n % S;
-            ok = mbar_wait_bounded(bar_empty(slot), ((n / S) & 1u) ^ 1u, wc, kSiteProdEmpty);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bar_full(slot), G::kTileBytes);
-            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-            for (int c = 0; c < G::kChunks; ++c)
-              tma_load_4d(sKV + slot * G::kTileBytes + c * G::kChunkBytes, tm, bar_full(slot),
-                          c * 64, it.g, j * kBN, it.b);
-            ++n;
-          }
-        }
-      }
-      if (lane == 0) {
-        // Whether or not this CTA aborted, the copies issued last may still be in
-        // flight (another role can abort after this loop has ended, and then nothing
-        // consumes them): let them land before the CTA can exit.
-        for (uint32_t back = 1; back <= S && back <= n; ++back) {
-          const uint32_t m = n - back;
-          mbar_wait_drain(bar_full(m % S), (m / S) & 1u, wc, kSiteDrainLoads);
-        }
-        mbar_wait_drain(bar_q_full, 0, wc, kSiteDrainLoads);
-      }
-    }
+    kv_produce<PAGED, D>(p, it, nblocks, &tm_q, &tm_k, &tm_v, sQ, G::kChunkBytes, sKV, S, bars, wc,
+                         lane);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (nblocks > 0) {
@@ -389,14 +403,14 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
         const uint32_t kidx = 2u * jj;
         if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull)) return false;
         tc_fence_after();
-        const uint32_t mS = tmem_base + (DEC ? 0u : 128u * (jj & 1));
+        const uint32_t mS = tmem_base + 128u * (jj & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
           mma_ss_elect(mS, dq + (off >> 4), dk + ((slot_of(kidx) * G::kTileBytes + off) >> 4),
                        idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit_elect(bar_s_full(DEC ? 0 : (jj & 1)));
+        mma_commit_elect(bar_s_full(jj & 1));
         mma_commit_elect(bar_empty(slot_of(kidx)));
         return true;
       };
@@ -418,17 +432,17 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
             __syncwarp();
           }
         }
-        if (!mbar_wait_warp(bar_p_full(DEC ? 0 : (jj & 1)), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc,
+        if (!mbar_wait_warp(bar_p_full(jj & 1), (jj >> 1) & 1u, wc,
                             kSiteMmaPFull))
           return false;
         tc_fence_after();
-        const uint32_t mP = tmem_base + (DEC ? R::kColP : 128u * (jj & 1));
+        const uint32_t mP = tmem_base + 128u * (jj & 1);
         const uint64_t dvs = dv + ((slot_of(vidx) * G::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          // keys 16 kk .. 16 kk + 15: DEC P is packed from column 0; otherwise each
+          // keys 16 kk .. 16 kk + 15: each
           // 64-key half h sits at column 64 h (bf16: hi there, lo 32 columns on)
-          const uint32_t pcol = DEC ? kk * 8 : (kk >> 2) * 64 + (kk & 3) * 8;
+          const uint32_t pcol = (kk >> 2) * 64 + (kk & 3) * 8;
           mma_ts_elect(mO, mP + pcol, dvs + ((kk * 2048) >> 4), idesc_o,
                        (jj == 0 && kk == 0) ? 0u : 1u);
         }
@@ -439,7 +453,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
             mma_ts_elect(mO, mP + pcol, dvs + ((kk * 2048) >> 4), idesc_o, 1u);
           }
         }
-        mma_commit_elect(bar_pv_done(DEC ? 0 : (jj & 1)));
+        mma_commit_elect(bar_pv_done(jj & 1));
         mma_commit_elect(bar_empty(slot_of(vidx)));
         return true;
       };
@@ -447,24 +461,10 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       if (ok) {
         tc_fence_after();
         ok = issue_s(0);
-        if constexpr (DEC) {
-          // one S buffer: S(jj + 1) once the softmax holds S(jj) in registers
-          for (int jj = 0; ok && jj < nblocks; ++jj) {
-            if (jj + 1 < nblocks) {
-              ok = mbar_wait_warp(bar_s_free, jj & 1u, wc, kSiteMmaPFull);
-              if (ok) {
-                tc_fence_after();
-                ok = issue_s(jj + 1);
-              }
-            }
-            if (ok) ok = issue_pv(jj);
-          }
-        } else {
-          if (ok && nblocks > 1) ok = issue_s(1);
-          for (int jj = 0; ok && jj < nblocks; ++jj) {
-            ok = issue_pv(jj);
-            if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
-          }
+        if (ok && nblocks > 1) ok = issue_s(1);
+        for (int jj = 0; ok && jj < nblocks; ++jj) {
+          ok = issue_pv(jj);
+          if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
         }
         if (ok) mma_commit_elect(bar_o_full);
       }
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     constexpr int kCols = kBN / kHalves;  // scores of a block per softmax thread
     constexpr int kOCols = D / kHalves;   // O columns this thread rescales and writes
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
-    const int ch = warp >> 2;             // key half of this warp (0 in DEC)
+    const int ch = warp >> 2;             // key half of this warp
     const int col0 = ch * kCols;          // first score column of this thread
     const int rho = quarter * 32 + lane;  // row of the tile
     const bool row_ok = !it.bad && rho < (it.i1 - it.i0) * p.group;
@@ -516,14 +516,13 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
     auto one_block = [&](int jj, auto masked_tag) __attribute__((always_inline)) -> bool {
       constexpr bool masked = decltype(masked_tag)::value;
       const int j = it.lo + jj;
-      const uint32_t buf = DEC ? 0u : (jj & 1);
-      if (!mbar_wait_warp(bar_s_full(buf), DEC ? (jj & 1u) : ((jj >> 1) & 1u), wc, kSiteSmxSFull))
+      const uint32_t buf = jj & 1;
+      if (!mbar_wait_warp(bar_s_full(buf), (jj >> 1) & 1u, wc, kSiteSmxSFull))
         return false;
       tc_fence_after();
-      // S of this block, then P over the scores this thread has read (DEC: P in its
-      // own columns)
-      const uint32_t tS = tmem_base + lane_off + (DEC ? 0u : 128u * buf);
-      const uint32_t tP = DEC ? tmem_base + lane_off + R::kColP : tS;
+      // S of this block, then P over the scores this thread has read
+      const uint32_t tS = tmem_base + lane_off + 128u * buf;
+      const uint32_t tP = tS;
       const int key0 = j * kBN;
       int vis_lo = 0, vis_hi = kBN;  // visible columns of this row: [vis_lo, vis_hi)
       if constexpr (masked) {
@@ -538,14 +537,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       auto block_body = [&](auto masked_tag) __attribute__((always_inline)) {
         constexpr bool M = decltype(masked_tag)::value;
         uint32_t sr[kCols];
-        if constexpr (kCols == 128)
-          tmem_ld_x128(tS, sr);
-        else
-          tmem_ld_x64(tS + col0, sr);
-        if constexpr (DEC) {
-          tc_fence_before();
-          mbar_arrive(bar_s_free);  // the S buffer may take S(jj + 1)
-        }
+        tmem_ld_x64(tS + col0, sr);
         if constexpr (M) {  // masked keys: -inf for the max (+inf for the min), p = 0 below
           const uint32_t fill = neg ? 0x7f800000u : 0xff800000u;
 #pragma unroll
@@ -557,10 +549,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
           float sv[kCols];
 #pragma unroll
           for (int c = 0; c < kCols; ++c) sv[c] = __uint_as_float(sr[c]);
-          if constexpr (kCols == 128)
-            mx = neg ? -row_min128(sv) : row_max128(sv);
-          else
-            mx = neg ? -row_min64(sv) : row_max64(sv);
+          mx = neg ? -row_min64(sv) : row_max64(sv);
         }
         if constexpr (kHalves == 2) {
           // the row max over both halves, combined in the same order by both
@@ -578,15 +567,6 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
           rescale = true;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-        if constexpr (DEC) {  // the P columns were read by P·V(jj - 1)
-          if (jj >= 1) {
-            if (!mbar_wait_warp(bar_pv_done(0), (jj - 1) & 1u, wc, kSiteSmxPvDone)) {
-              stop = true;
-              return;
-            }
-            tc_fence_after();
-          }
-        }
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c0 = 0; c0 < kCols; c0 += 32) {
@@ -630,15 +610,13 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
             }
           }
           // P of keys [64 hh, 64 hh + 64) at column 64 hh, over scores this thread has
-          // already read (DEC: packed from column 0 of its own region); split P keeps
+          // already read; split P keeps
           // [hi 32 columns | lo 32 columns] there.
           const int cb = col0 + c0;  // first key of this chunk
           if constexpr (kSplitP) {
             const int hh = cb >> 6, cl = cb & 63;
             tmem_st_x16(tP + 64 * hh + (cl >> 1), pk);
             tmem_st_x16(tP + 64 * hh + 32 + (cl >> 1), pk_lo);
-          } else if constexpr (DEC) {
-            tmem_st_x16(tP + (cb >> 1), pk);
           } else {
             tmem_st_x16(tP + 64 * (cb >> 6) + ((cb & 63) >> 1), pk);
           }
@@ -650,8 +628,7 @@ __global__ void __launch_bounds__(KvRoles<DEC>::kThreads, DEC ? 2 : 1)
       // O rescale (this thread's columns) once the previous P·V, which accumulates
       // into O, is complete; the first block's P·V overwrites O.
       if (__any_sync(0xffffffffu, rescale && jj > 0)) {
-        if (!mbar_wait_warp(bar_pv_done(DEC ? 0 : ((jj - 1) & 1)),
-                            DEC ? ((jj - 1) & 1u) : (((jj - 1) >> 1) & 1u), wc, kSiteSmxPvDone))
+        if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone))
           return false;
         tc_fence_after();
         const float a = (rescale && jj > 0) ? alpha : 1.f;

@@ -1,0 +1,457 @@
+// attn_kv_keys_kernel.cuh — the decode-shaped forward with the keys of a block on the
+// TMEM lanes, for work items of at most 32 query rows (a few new tokens, times the
+// query heads that share one K/V head).
+//
+// It computes what attn_kv_sm103_kernel computes for the same item (the last Lq
+// positions of an Lk-long sequence, the same masks, key splits and partial outputs),
+// the generation step that "What is memory-efficient attention for long context on
+// 8x H100?" (section 1) names as bound by reading the whole KV cache. With only a few
+// rows the row-per-lane layout leaves one thread to walk 128 scores per block while
+// the rest of the warp idles; here the products are transposed so that each thread
+// owns one key:
+//   * S^T = K_j · Q^T: M = 128 keys (TMEM lanes), N = 16 or 32 query rows (columns).
+//     A = the K slot (K-major), B = the Q tile (K-major, 32 rows).
+//   * O^T += V_j^T · P^T: M = 128 (the d dimension; at d = 64 the second half of M
+//     reads unrelated shared memory and those accumulator lanes are never read),
+//     N = the query rows. A = the V slot read MN-major (the same layout the TMA
+//     writes), B = P^T written by the softmax threads into shared memory in the
+//     K-major 128-byte-swizzled layout. bf16 P is split into hi + lo operands (two
+//     products) as in the other kernels; fp16 P is not.
+//   * warps 0-3 (softmax, thread t = key t of the block): one score per query row per
+//     block. All rows share one reference max per row (the weights of one product
+//     must): a block whose scores exceed it by more than 2^8 is detected by a vote of
+//     the four warps (a named barrier per block) and takes a slow path that reduces
+//     the block maximum over all keys, moves the reference and rescales O^T and the
+//     per-thread sums l. The sums are per thread and meet once, in the epilogue.
+//   * warp 4 (producer): kv_produce, the ring of K/V slots of the one-tile kernel.
+//   * warp 5 (MMA): O^T += V^T P^T(j) once P(j) is in shared memory, then S^T(j+2)
+//     (two S buffers, two P buffers). Two orderings need no barrier of their own:
+//     S^T(j+2) overwrites S^T(j) only after P·V(j) waited for P(j), which every
+//     warp writes after reading S^T(j); and the commit of S^T(j) (s_full) tracks
+//     P·V(j-2), issued before it, so a warp that has S^T(j) may overwrite P(j-2).
+//   * Every wait is bounded; the four softmax warps leave the block loop together
+//     (an abort bit rides on the per-block vote), so the named barriers never wait
+//     for a warp that has left.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "attn_kv_kernel.cuh"
+
+namespace ex19 {
+namespace kv {
+
+constexpr int kKeysRowsMax = 32;  // query rows per work item
+constexpr int kKeysThreads = 192;  // 4 softmax warps + producer + MMA
+constexpr int kKeysProducerWarp = 4;
+constexpr int kKeysMmaWarp = 5;
+constexpr uint32_t kKeysTmemCols = 128;  // S^T buffers [0, 32) and [32, 64), O^T [64, 96)
+
+enum : uint32_t {
+  kSiteKeysMmaKFull = 0xA0001, kSiteKeysMmaVFull = 0xA0002, kSiteKeysMmaPFull = 0xA0003,
+  kSiteKeysMmaQFull = 0xA0005, kSiteKeysMmaDrain = 0xA0006,
+  kSiteKeysSmxSFull = 0xB0001, kSiteKeysSmxPvDone = 0xB0003, kSiteKeysSmxOFull = 0xB0004,
+};
+
+template <int D>
+struct KeysGeometry {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kBM * D * 2;             // 128 keys of K or V
+  static constexpr int kChunkBytes = kBM * 128;              // 64 columns of such a tile
+  static constexpr int kRowChunkBytes = kKeysRowsMax * 128;  // 64 columns of 32 rows
+  static constexpr int kPBytes = 2 * kRowChunkBytes;         // P^T of one block: 128 keys x 32 rows
+  static constexpr int kSlots = (D == 64) ? 4 : 5;
+  static constexpr int kCtasPerSm = (D == 64) ? 2 : 1;
+  // The ring first, then P: at d = 64 the O^T product's second M half reads the 16 KiB
+  // after a V slot, which for the last slot is the P region.
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffP = kOffKV + kSlots * kTileBytes;  // [buffer 2][part 2 (hi, lo)]
+  static constexpr int kOffQ = kOffP + 4 * kPBytes;
+  static constexpr int kOffBar = kOffQ + kChunks * kRowChunkBytes;
+  // full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full, drain
+  static constexpr int kNumBars = 2 * kSlots + 9;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag, votes [2][4] bytes
+  static constexpr int kOffRed = kOffMisc + 16;            // [2][4 warps][32 rows] block maxima
+  static constexpr int kOffLsum = kOffRed + 2 * 4 * kKeysRowsMax * 4;  // [4 warps][32 rows] sums
+  static constexpr int kSmemUsed = kOffLsum + 4 * kKeysRowsMax * 4;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// NQ: the query rows a work item may have (1, 8 or 32; the products use N = max(NQ, 16)).
+template <int D, bool BF16, bool PAGED, int NQ>
+__global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
+    attn_kv_keys_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const KvParams p, int out_f32) {
+  static_assert(NQ == 1 || NQ == 8 || NQ == 32, "rows per item");
+  using G = KeysGeometry<D>;
+  constexpr int S = G::kSlots;
+  constexpr int kN = NQ < 16 ? 16 : NQ;  // N of both products
+  constexpr bool kSplitP = BF16;         // bf16 P as hi + lo operands
+  constexpr float kThresh = 8.0f;        // log2 units of max growth before a rescale
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sKV = sbase + G::kOffKV;
+  const uint32_t sP = sbase + G::kOffP;
+  const uint32_t sQ = sbase + G::kOffQ;
+  const uint32_t bars = sbase + G::kOffBar;
+  auto bar_full = [&](uint32_t s) { return bars + 8u * s; };
+  auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
+  const uint32_t bar_q_full = bars + 8u * (2 * S);
+  auto bar_s_full = [&](uint32_t b) { return bars + 8u * (2 * S + 1 + b); };
+  auto bar_p_full = [&](uint32_t b) { return bars + 8u * (2 * S + 3 + b); };
+  auto bar_pv_done = [&](uint32_t b) { return bars + 8u * (2 * S + 5 + b); };
+  const uint32_t bar_o_full = bars + 8u * (2 * S + 7);
+  const uint32_t bar_drain = bars + 8u * (2 * S + 8);
+  auto p_buf = [&](uint32_t b, int part) { return sP + (2u * b + part) * G::kPBytes; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
+  volatile uint8_t* votes = smem + G::kOffMisc + 8;  // [2 buffers][4 warps]
+  float* red = reinterpret_cast<float*>(smem + G::kOffRed);
+  float* lsum = reinterpret_cast<float*>(smem + G::kOffLsum);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_q_full, 1);
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(bar_s_full(b), 1);
+      mbar_init(bar_p_full(b), 128);
+      mbar_init(bar_pv_done(b), 1);
+    }
+    mbar_init(bar_o_full, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kKeysProducerWarp && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  // A programmatic dependent launch: the previous kernel's writes are visible past
+  // this point; TMEM is allocated only after it (as in the one-tile kernel).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (warp == kKeysMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kKeysTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const KvItem it = kv_item<PAGED>(p);
+  const int nblocks = max(0, it.hi - it.lo);
+
+  WaitCtl wc;
+  wc.abort_flag = abort_flag;
+  wc.status = p.status;
+  wc.set_limit(p.wait_limit_ns);
+  wc.unit = blockIdx.x;
+  if (it.bad && threadIdx.x == 0) record_error(wc, kStatusInvalidArg, kSiteBadSeqLen);
+
+  if (warp == kKeysProducerWarp) {
+    kv_produce<PAGED, D>(p, it, nblocks, &tm_q, &tm_k, &tm_v, sQ, G::kRowChunkBytes, sKV, S, bars,
+                         wc, lane);
+  } else if (warp == kKeysMmaWarp) {
+    // ------------------------------------------------------------- MMA issuer
+    if (nblocks > 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32acc_ab(BF16, kBM, kN, false, false);
+      constexpr uint32_t idesc_o = idesc_f16_f32acc_ab(BF16, kBM, kN, true, false);
+      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);               // K slots as A, K-major
+      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);                // Q rows as B, K-major
+      const uint64_t dv = sdesc_sw128(sKV, G::kChunkBytes, 1024);   // V slots as A, MN-major
+      const uint32_t mO = tmem_base + 64;
+      auto slot_of = [&](uint32_t idx) { return idx % S; };
+      auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
+      // S^T(jj) = K_j · Q^T into buffer jj & 1 (S^T(jj - 2) has been read: see the
+      // header).
+      auto issue_s = [&](int jj) __attribute__((always_inline)) -> bool {
+        const uint32_t kidx = 2u * jj, b = jj & 1;
+        if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteKeysMmaKFull)) return false;
+        tc_fence_after();
+        const uint32_t mS = tmem_base + 32u * b;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * G::kRowChunkBytes + (kk & 3) * 32;
+          mma_ss_elect(mS, dk + ((slot_of(kidx) * G::kTileBytes + ka) >> 4), dq + (kb >> 4), idesc_s,
+                       kk > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(bar_s_full(b));
+        mma_commit_elect(bar_empty(slot_of(kidx)));
+        return true;
+      };
+      // O^T += V_j^T · P^T(jj) once P(jj) is in buffer jj & 1; releases V_j.
+      auto issue_pv = [&](int jj) __attribute__((always_inline)) -> bool {
+        const uint32_t vidx = 2u * jj + 1u, b = jj & 1;
+        if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteKeysMmaVFull)) return false;
+        if constexpr (PAGED) {
+          // Rows past the sequence in its last block: the part of a partial page the
+          // TMA did load holds arbitrary cache contents; make every such V row 0.
+          const int r0 = it.Lk - (it.lo + jj) * kBN;
+          if (r0 < kBN) {
+            const uint32_t base = sKV + slot_of(vidx) * G::kTileBytes;
+            for (int idx = lane; idx < (kBN - r0) * 8 * G::kChunks; idx += 32) {
+              const int c = idx / ((kBN - r0) * 8), rem = idx % ((kBN - r0) * 8);
+              st_shared_zero16(base + c * G::kChunkBytes + (r0 + rem / 8) * 128 + (rem % 8) * 16);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+          }
+        }
+        if (!mbar_wait_warp(bar_p_full(b), (jj >> 1) & 1u, wc, kSiteKeysMmaPFull)) return false;
+        tc_fence_after();
+        const uint64_t dvs = dv + ((slot_of(vidx) * G::kTileBytes) >> 4);
+#pragma unroll
+        for (int part = 0; part < (kSplitP ? 2 : 1); ++part) {
+          const uint64_t dp = sdesc_sw128(p_buf(b, part), 16, 1024);  // P^T rows as B, K-major
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint32_t kb = (kk >> 2) * G::kRowChunkBytes + (kk & 3) * 32;
+            mma_ss_elect(mO, dvs + ((kk * 2048) >> 4), dp + (kb >> 4), idesc_o,
+                         (jj == 0 && part == 0 && kk == 0) ? 0u : 1u);
+          }
+        }
+        mma_commit_elect(bar_pv_done(b));
+        mma_commit_elect(bar_empty(slot_of(vidx)));
+        return true;
+      };
+      bool ok = mbar_wait_warp(bar_q_full, 0, wc, kSiteKeysMmaQFull);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+        if (ok && nblocks > 1) ok = issue_s(1);
+        for (int jj = 0; ok && jj < nblocks; ++jj) {
+          ok = issue_pv(jj);
+          if (ok && jj + 2 < nblocks) ok = issue_s(jj + 2);
+        }
+        if (ok) mma_commit_elect(bar_o_full);
+      }
+    }
+    mma_commit_elect(bar_drain);
+    mbar_wait_drain(bar_drain, 0, wc, kSiteKeysMmaDrain);
+  } else {
+    // -------------------------------------------------------- softmax warps
+    const int t = threadIdx.x;  // key of the block, TMEM lane (and the d row of O^T)
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int rows = it.bad ? 0 : (it.i1 - it.i0) * p.group;  // valid query rows (<= NQ)
+    const int Lk = it.Lk;
+    const int off = Lk - p.Lq;
+    const int wr = right_bound(p);
+    const float C = p.score_log2;
+    const float Cs = (p.negate_scores != 0) ? -C : C;
+    float mref[NQ], l[NQ];
+#pragma unroll
+    for (int c = 0; c < NQ; ++c) {
+      mref[c] = -INFINITY;
+      l[c] = 0.f;
+    }
+    // the key-of-thread byte offset in a P^T operand (chunk of 64 keys, swizzled
+    // 16-byte granule of the row); the row part is added per row
+    const uint32_t p_key = static_cast<uint32_t>((t >> 6) * G::kRowChunkBytes + (t & 7) * 2);
+    const uint32_t p_gran = static_cast<uint32_t>((t & 63) >> 3);
+    bool ok = true;
+    // Blocks [ja, jb) cross no mask boundary (as in the one-tile kernel).
+    int ja = 0, jb = nblocks;
+    {
+      const int pos_min = off + it.i0, pos_max = off + it.i1 - 1;
+      if (p.window_left >= 0) {
+        const int first = pos_max - p.window_left;
+        if (first > 0) ja = max(ja, (first + kBN - 1) / kBN - it.lo);
+      }
+      jb = min(jb, Lk / kBN - it.lo);
+      if (wr >= 0) {
+        const int last = pos_min + wr - (kBN - 1);
+        jb = min(jb, last >= 0 ? last / kBN + 1 - it.lo : 0);
+      }
+      ja = min(max(ja, 0), nblocks);
+      jb = max(jb, ja);
+    }
+    for (int jj = 0; jj < nblocks; ++jj) {
+      const uint32_t b = jj & 1;
+      float x[NQ];
+      bool exceed = false;
+      if (ok) {
+        ok = mbar_wait_warp(bar_s_full(b), (jj >> 1) & 1u, wc, kSiteKeysSmxSFull);
+        if (ok) {
+          tc_fence_after();
+          uint32_t sr[NQ];
+          tmem_ld_n<NQ>(tmem_base + lane_off + 32u * b, sr);
+          const bool masked = jj < ja || jj >= jb;
+          const int key = (it.lo + jj) * kBN + t;
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) {
+            x[c] = __uint_as_float(sr[c]) * Cs;
+            bool vis = c < rows;
+            if (masked) {
+              const int pos = off + it.i0 + c / p.group;
+              vis = vis && key < Lk && (wr < 0 || key <= pos + wr) &&
+                    (p.window_left < 0 || key >= pos - p.window_left);
+            }
+            if (!vis) x[c] = -INFINITY;
+            exceed = exceed || x[c] > mref[c] + kThresh;
+          }
+        }
+      }
+      // the vote: bit 0 a score above the reference, bit 1 this warp stopped
+      const bool any = __any_sync(0xffffffffu, exceed);
+      if (lane == 0) votes[b * 4 + warp] = static_cast<uint8_t>((any ? 1u : 0u) | ((ok && !*abort_flag) ? 0u : 2u));
+      named_barrier(1, 128);
+      const uint32_t v4 = *reinterpret_cast<volatile uint32_t*>(votes + b * 4);
+      if (v4 & 0x02020202u) {
+        ok = false;
+        break;
+      }
+      if (v4 & 0x01010101u) {
+        // slow path: the block maximum of every row over all 128 keys
+        float* rb = red + b * 4 * kKeysRowsMax;
+#pragma unroll
+        for (int c = 0; c < NQ; ++c) {
+          const float m = warp_max(x[c]);
+          if (lane == 0) rb[warp * kKeysRowsMax + c] = m;
+        }
+        named_barrier(1, 128);
+        float alpha[NQ];
+        bool resc = false;
+#pragma unroll
+        for (int c = 0; c < NQ; ++c) {
+          const float bm = fmaxf(fmaxf(rb[c], rb[kKeysRowsMax + c]),
+                                 fmaxf(rb[2 * kKeysRowsMax + c], rb[3 * kKeysRowsMax + c]));
+          alpha[c] = 1.f;
+          if (bm > mref[c] + kThresh) {
+            alpha[c] = ex2_approx(mref[c] - bm);  // 0 when mref is -inf
+            mref[c] = bm;
+            resc = true;
+          }
+          l[c] *= alpha[c];
+        }
+        if (resc && jj > 0) {  // O^T lanes = d rows, columns = query rows
+          ok = mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteKeysSmxPvDone);
+          if (ok) {
+            tc_fence_after();
+            uint32_t orow[NQ];
+            tmem_ld_n<NQ>(tmem_base + lane_off + 64u, orow);
+#pragma unroll
+            for (int c = 0; c < NQ; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * alpha[c]);
+            tmem_st_n<NQ>(tmem_base + lane_off + 64u, orow);
+            tmem_st_wait();
+          }
+        }
+      }
+      if (!ok) continue;  // the next vote carries the stop
+      // P = 2^(x - m) for this key and every row; l per thread
+#pragma unroll
+      for (int c = 0; c < NQ; ++c) {
+        const float mu = (mref[c] == -INFINITY) ? 0.f : mref[c];
+        const float pv = ex2_approx(x[c] - mu);  // 0 for masked keys (x = -inf)
+        l[c] += pv;
+        if (c < rows) {
+          const uint32_t a = p_key + c * 128 + ((p_gran ^ (c & 7)) << 4);
+          if constexpr (kSplitP) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+            st_shared_u16(p_buf(b, 0) + a, __bfloat16_as_ushort(hi));
+            st_shared_u16(p_buf(b, 1) + a, __bfloat16_as_ushort(lo));
+          } else {
+            st_shared_u16(p_buf(b, 0) + a, __half_as_ushort(__float2half_rn(pv)));
+          }
+        }
+      }
+      fence_proxy_async_shared();
+      tc_fence_before();
+      mbar_arrive(bar_p_full(b));
+    }
+    // ---- epilogue: the row sums over the 128 key threads, then O / l and the LSE
+#pragma unroll
+    for (int c = 0; c < NQ; ++c) {
+      const float s = warp_sum(l[c]);
+      if (lane == 0) lsum[warp * kKeysRowsMax + c] = s;
+    }
+    if (ok && nblocks > 0) {
+      ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteKeysSmxOFull);
+      if (ok) tc_fence_after();
+    }
+    named_barrier(1, 128);
+    if (ok) {
+      float lt[NQ];
+#pragma unroll
+      for (int c = 0; c < NQ; ++c)
+        lt[c] = (lsum[c] + lsum[kKeysRowsMax + c]) + (lsum[2 * kKeysRowsMax + c] + lsum[3 * kKeysRowsMax + c]);
+      uint32_t orow[NQ];
+      if (nblocks > 0) {
+        tmem_ld_n<NQ>(tmem_base + lane_off + 64u, orow);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NQ; ++c) orow[c] = 0u;
+      }
+      const bool partial = p.splits > 1;
+      const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+#pragma unroll
+      for (int c = 0; c < NQ; ++c) {
+        if (c >= rows) continue;
+        const int qi = it.i0 + c / p.group;
+        const int h = it.g * p.group + c % p.group;
+        const size_t row = (static_cast<size_t>(it.b) * p.Hq + h) * p.Lq + qi;  // LSE index
+        const float inv_l = (lt[c] > 0.f) ? 1.f / lt[c] : 0.f;
+        if (t < D) {
+          const float o = __uint_as_float(orow[c]) * inv_l;
+          if (partial) {
+            p.o_part[(static_cast<size_t>(it.split) * nrows + row) * D + t] = o;
+          } else {
+            const size_t oi = ((static_cast<size_t>(it.b) * p.Lq + qi) * p.Hq + h) * D + t;
+            if (out_f32)
+              static_cast<float*>(p.o)[oi] = o;
+            else if constexpr (BF16)
+              static_cast<__nv_bfloat16*>(p.o)[oi] = __float2bfloat16_rn(o);
+            else
+              static_cast<__half*>(p.o)[oi] = __float2half_rn(o);
+          }
+        }
+        if (t == c) {
+          const float lse2 = (lt[c] > 0.f) ? mref[c] + lg2_approx(lt[c]) : -INFINITY;  // base 2
+          if (partial)
+            p.lse_part[static_cast<size_t>(it.split) * nrows + row] = lse2;
+          else if (p.lse != nullptr)
+            p.lse[row] = (lt[c] > 0.f) ? lse2 * 0.69314718055994531f : -INFINITY;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kKeysMmaWarp) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kKeysTmemCols);
+  }
+}
+
+}  // namespace kv
+}  // namespace ex19

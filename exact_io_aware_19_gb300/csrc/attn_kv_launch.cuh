@@ -9,11 +9,39 @@
 
 namespace ex19 {
 
-template <int D, bool BF16, bool OUT_F32, bool PAGED, bool DEC, bool PV16 = false>
+// The merge of a call's key splits (a programmatic dependent launch after the split
+// kernel): one CTA per row when the call has at most one row per SM (decode: many
+// splits per row), one warp per row otherwise.
+template <int D, bool BF16, bool OUT_F32>
+cudaError_t launch_kv_merge_t(const KvLaunchArgs& a) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
+  if (rows <= sms) {  // few rows (decode): one CTA per row
+    cfg.gridDim = dim3(static_cast<unsigned>(rows));
+    return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 8>, a.p);
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));  // many rows: one warp per row
+  return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 1>, a.p);
+}
+
+template <int D, bool BF16, bool OUT_F32, bool PAGED, bool PV16 = false>
 cudaError_t launch_kv_one(const KvLaunchArgs& a) {
-  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32, PAGED, DEC, PV16>;
+  auto kern = kv::attn_kv_sm103_kernel<D, BF16, OUT_F32, PAGED, PV16>;
   if (PV16 && a.p.splits != 1) return cudaErrorInvalidValue;  // attn_fwd's path: one key split
-  constexpr int smem = kv::KvGeometry<D, DEC>::kSmemBytes;
+  constexpr int smem = kv::KvGeometry<D>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -34,7 +62,7 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = a.grid;
-  cfg.blockDim = dim3(kv::KvRoles<DEC>::kThreads);
+  cfg.blockDim = dim3(kv::KvRoles::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
   cfg.attrs = attr;
@@ -44,17 +72,7 @@ cudaError_t launch_kv_one(const KvLaunchArgs& a) {
     return e;  // one key split (checked above): no merge
   } else {
     if (e != cudaSuccess || a.p.splits <= 1) return e;
-    const long long rows = static_cast<long long>(a.p.B) * a.p.Hq * a.p.Lq;
-    int sms = 148;  // `dev` is the current device (above)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    if (rows <= sms) {  // few rows (decode): one CTA per row
-      cfg.gridDim = dim3(static_cast<unsigned>(rows));
-      return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 8>, a.p);
-    }
-    cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));  // many rows: one warp per row
-    return cudaLaunchKernelEx(&cfg, kv::attn_kv_merge_kernel<D, BF16, OUT_F32, 1>, a.p);
+    return launch_kv_merge(D, BF16, OUT_F32, a);
   }
 }
 

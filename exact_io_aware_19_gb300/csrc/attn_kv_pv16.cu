@@ -6,10 +6,10 @@ namespace ex19 {
 
 cudaError_t launch_kv_pv16(int d, bool out_f32, const KvLaunchArgs& a) {
   if (d == 64)
-    return out_f32 ? launch_kv_one<64, true, true, false, false, true>(a)
-                   : launch_kv_one<64, true, false, false, false, true>(a);
-  return out_f32 ? launch_kv_one<128, true, true, false, false, true>(a)
-                 : launch_kv_one<128, true, false, false, false, true>(a);
+    return out_f32 ? launch_kv_one<64, true, true, false, true>(a)
+                   : launch_kv_one<64, true, false, false, true>(a);
+  return out_f32 ? launch_kv_one<128, true, true, false, true>(a)
+                 : launch_kv_one<128, true, false, false, true>(a);
 }
 
 }  // namespace ex19

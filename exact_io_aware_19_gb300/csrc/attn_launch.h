@@ -68,16 +68,13 @@ cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // The one-tile kernel for attn_fwd on bfloat16 inputs with the fp16 copy of V (one
 // key split; a.tm_v over the copy, a.p.vmax set).
 cudaError_t launch_kv_pv16(int d, bool out_f32, const KvLaunchArgs& a);
-// The one-tile kernel's decode mode (one softmax warp, two CTAs per SM): fp16 at
-// d = 64 with at most 32 rows per tile (q_per_tile * group). Its split count targets
-// two CTAs per SM (kv_decode_shape: the same rule without the dtype, which the split
-// count of attn_fwd_kv_num_splits cannot see).
-inline bool kv_decode_shape(int d, int q_per_tile, int group) {
-  return d == 64 && q_per_tile * group <= 32;
-}
-inline bool kv_decode_mode(int d, bool bf16, int q_per_tile, int group) {
-  return !bf16 && kv_decode_shape(d, q_per_tile, group);
-}
+// Work items of at most 32 query rows (q_per_tile * group) run the keys-on-lanes
+// kernel (attn_kv_keys_kernel.cuh), two CTAs per SM at d = 64 and one at d = 128.
+inline bool kv_keys_shape(int q_per_tile, int group) { return q_per_tile * group <= 32; }
+inline int kv_keys_ctas_per_sm(int d) { return d == 64 ? 2 : 1; }
+cudaError_t launch_kv_keys(int d, bool bf16, bool paged, bool out_f32, const KvLaunchArgs& a);
+// The merge of a.p.splits > 1 partial results into O and LSE.
+cudaError_t launch_kv_merge(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // The same over a paged K/V cache (a.p.block_table, seq_lens, page_size, ... set).
 cudaError_t launch_kv_paged(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // The float8 forward: the V transpose, then the attention kernel.

@@ -194,6 +194,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 // One float from shared memory.
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Barrier `id` (1..15) over the first `count` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
@@ -356,6 +365,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, int M, int N,
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with either operand's major-ness: A MN-major (bit 15) reads A[m][k] with m
+// contiguous (64-element segments `lbo` apart, 8-element groups of k `sbo` apart).
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc_ab(bool bf16, int M, int N, bool a_mn_major,
+                                                         bool b_mn_major) {
+  return idesc_f16_f32acc(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // -------------------------------------------------------------------- arithmetic

@@ -9,7 +9,7 @@ under random interleavings:
   * the MMA warp waits for K, V and P as the kernel does and issues S = Q Kᵀ and
     O += P V; the tensor core runs the MMAs of that one thread in issue order, and
     each commit arrives once every MMA issued before it has finished;
-  * the softmax parts (two per row, or one in decode mode) wait for S, trade their
+  * the softmax parts (two per row) wait for S, trade their
     row maxima (exchange rounds), write P, rescale O when the row max moved (after
     the previous P·V is done), release P and finally read O.
 
@@ -26,16 +26,15 @@ import pytest
 from protocol_model import STEP, Bar, CopyEngine, InOrderQueue, ProtocolError, check, run, wait
 
 
-def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
+def simulate(nb, slots, seed, rescale_p=0.3, mutant=None):
     """One CTA's run over `nb` key blocks. Raises ProtocolError on a violation."""
     rng = random.Random(seed)
-    parts = 1 if dec else 2
+    parts = 2
     full = [Bar(f"full{s}", 1) for s in range(slots)]
     empty = [Bar(f"empty{s}", 1) for s in range(slots)]
     q_full = Bar("q_full", 1)
-    nbuf = 1 if dec else 2
+    nbuf = 2
     s_full = [Bar(f"s_full{b}", 1) for b in range(nbuf)]
-    s_free = Bar("s_free", parts)  # decode mode only
     p_full = [Bar(f"p_full{b}", parts) for b in range(nbuf)]
     pv_done = [Bar(f"pv_done{b}", 1) for b in range(nbuf)]
     o_full = Bar("o_full", 1)
@@ -43,9 +42,8 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
 
     slot_gen = [None] * slots          # which load a ring slot holds
     consumed = set()                   # loads the MMAs have read
-    # TMEM contents: S buffers (tags per part: the key range each part owns), P region (decode)
+    # TMEM contents: S buffers (tags per part: the key range each part owns)
     sbuf = [[None] * parts for _ in range(nbuf)]
-    preg = [None]
     s_read = set()                     # (jj, part): the part has S(jj) in registers
     o_count = [0]                      # P·V products accumulated in O
     o_pending = [0]                    # P·V issued but not finished
@@ -77,7 +75,7 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             kidx = 2 * jj
             s = kidx % slots
             yield wait(full[s], kidx // slots + 1)
-            b = 0 if dec else jj & 1
+            b = jj & 1
             mma_queue.push(("S", jj, s, b))
             mma_queue.commit(s_full[b])
             mma_queue.commit(empty[s])
@@ -86,29 +84,21 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             vidx = 2 * jj + 1
             s = vidx % slots
             yield wait(full[s], vidx // slots + 1)
-            b = 0 if dec else jj & 1
+            b = jj & 1
             if mutant != "mma_skips_p_full":
-                yield wait(p_full[b], (jj + 1) if dec else (jj >> 1) + 1)
+                yield wait(p_full[b], (jj >> 1) + 1)
             mma_queue.push(("PV", jj, s, b))
             o_pending[0] += 1
             mma_queue.commit(pv_done[b])
             mma_queue.commit(empty[s])
 
         yield from issue_s(0)
-        if dec:
-            for jj in range(nb):
-                if jj + 1 < nb:
-                    if mutant != "mma_skips_s_free":
-                        yield wait(s_free, jj + 1)
-                    yield from issue_s(jj + 1)
-                yield from issue_pv(jj)
-        else:
-            if nb > 1:
-                yield from issue_s(1)
-            for jj in range(nb):
-                yield from issue_pv(jj)
-                if jj + 2 < nb:
-                    yield from issue_s(jj + 2)
+        if nb > 1:
+            yield from issue_s(1)
+        for jj in range(nb):
+            yield from issue_pv(jj)
+            if jj + 2 < nb:
+                yield from issue_s(jj + 2)
         mma_queue.commit(o_full)
 
     def softmax(part):
@@ -120,35 +110,24 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
                 check(xdata[(n & 1, o)] == (n, o), f"part {part} round {n} read {xdata[(n & 1, o)]}")
 
         for jj in range(nb):
-            b = 0 if dec else jj & 1
-            yield wait(s_full[b], (jj + 1) if dec else (jj >> 1) + 1)
+            b = jj & 1
+            yield wait(s_full[b], (jj >> 1) + 1)
             check(sbuf[b][part] == ("S", jj), f"part {part} reads {sbuf[b][part]} for S({jj})")
             s_read.add((jj, part))
-            if dec:
-                s_free.arrive()
             yield STEP
-            if parts > 1:
-                yield from exchange(jj)
-            if dec and jj >= 1 and mutant != "softmax_skips_pv_done":
-                yield wait(pv_done[0], jj)  # P·V(jj - 1) has read the P region
-            if dec:
-                check(o_pending[0] == 0 or preg[0] is None or o_count[0] >= jj,
-                      f"P({jj}) written while P·V({jj - 1}) may still read it")
-                preg[0] = ("P", jj)
-            else:
-                sbuf[b][part] = ("P", jj)  # over this part's own scores
+            yield from exchange(jj)
+            sbuf[b][part] = ("P", jj)  # over this part's own scores
             yield STEP
             if jj > 0 and rng.random() < rescale_p:
-                bp = 0 if dec else (jj - 1) & 1
-                yield wait(pv_done[bp], jj if dec else ((jj - 1) >> 1) + 1)
+                if mutant != "softmax_skips_pv_done":
+                    yield wait(pv_done[(jj - 1) & 1], ((jj - 1) >> 1) + 1)
                 check(o_pending[0] == 0 and o_count[0] == jj,
                       f"O rescaled at block {jj} with {o_pending[0]} P·V in flight, {o_count[0]} done")
             p_full[b].arrive()
             yield STEP
         if nb > 0:
             yield wait(o_full, 1)
-        if parts > 1:
-            yield from exchange(nb)
+        yield from exchange(nb)
         check(o_count[0] == nb and o_pending[0] == 0, f"epilogue reads O after {o_count[0]} of {nb} P·V")
 
     # ------------------------------------------------------------- engines
@@ -159,19 +138,13 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
             consumed.add(2 * jj)
             for pt in range(parts):
                 prev = sbuf[b][pt]
-                if dec:
-                    check(jj == 0 or (jj - 1, pt) in s_read, f"S({jj}) overwrites S({jj - 1}) before it is read")
-                else:
-                    check(prev is None or prev == ("P", jj - 2), f"S({jj}) overwrites {prev}")
+                check(prev is None or prev == ("P", jj - 2), f"S({jj}) overwrites {prev}")
                 sbuf[b][pt] = ("S", jj)
         else:
             check(slot_gen[s] == 2 * jj + 1, f"P·V({jj}) reads slot {s} holding load {slot_gen[s]}")
             consumed.add(2 * jj + 1)
-            if dec:
-                check(preg[0] == ("P", jj), f"P·V({jj}) reads {preg[0]}")
-            else:
-                for pt in range(parts):
-                    check(sbuf[b][pt] == ("P", jj), f"P·V({jj}) reads {sbuf[b][pt]} (part {pt})")
+            for pt in range(parts):
+                check(sbuf[b][pt] == ("P", jj), f"P·V({jj}) reads {sbuf[b][pt]} (part {pt})")
             check(o_count[0] == jj, f"P·V({jj}) onto O holding {o_count[0]} products")
             o_count[0] += 1
             o_pending[0] -= 1
@@ -194,22 +167,21 @@ def simulate(nb, slots, dec, seed, rescale_p=0.3, mutant=None):
     return True
 
 
-CASES = [(nb, slots, dec) for dec in (False, True) for slots in (5, 8) for nb in (0, 1, 2, 3, 5, 11)]
+CASES = [(nb, slots) for slots in (5, 8) for nb in (0, 1, 2, 3, 5, 11)]
 
 
-@pytest.mark.parametrize("nb,slots,dec", CASES)
-def test_protocol_holds_under_random_schedules(nb, slots, dec):
+@pytest.mark.parametrize("nb,slots", CASES)
+def test_protocol_holds_under_random_schedules(nb, slots):
     for seed in range(150):
-        simulate(nb, slots, dec, seed)
+        simulate(nb, slots, seed)
 
 
-@pytest.mark.parametrize("mutant,dec", [("producer_skips_empty", False), ("mma_skips_p_full", False),
-                                        ("mma_skips_s_free", True), ("softmax_skips_pv_done", True)])
-def test_mutants_are_caught(mutant, dec):
+@pytest.mark.parametrize("mutant", ["producer_skips_empty", "mma_skips_p_full", "softmax_skips_pv_done"])
+def test_mutants_are_caught(mutant):
     caught = False
     for seed in range(400):
         try:
-            simulate(6, 5, dec, seed, mutant=mutant)
+            simulate(6, 5, seed, mutant=mutant)
         except ProtocolError:
             caught = True
             break
