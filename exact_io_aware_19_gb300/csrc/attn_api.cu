@@ -250,12 +250,10 @@ KvPlan kv_plan(int B, int Lq, int Lk, int Hq, int Hkv, int causal, int window_le
   return k;
 }
 
-// Splits that fill the SMs with one wave of CTAs (for items of at most 32 rows, the
-// keys-on-lanes kernel's CTAs per SM: two at d = 64), keeping at least 2 key blocks
-// per split and at most kKvMaxSplits.
-int kv_auto_splits(const KvPlan& k, int sms, int d) {
-  const int ctas = ex19::kv_keys_shape(k.q_per_tile, k.group) ? ex19::kv_keys_ctas_per_sm(d) * sms : sms;
-  int s = std::max(1, ctas / std::max(1, k.items));
+// Splits that fill the SMs with one wave of CTAs (one per SM), keeping at least 2 key
+// blocks per split and at most kKvMaxSplits.
+int kv_auto_splits(const KvPlan& k, int sms) {
+  int s = std::max(1, sms / std::max(1, k.items));
   s = std::min(s, std::max(1, k.max_blocks / 2));
   return std::min(s, kKvMaxSplits);
 }
@@ -334,7 +332,7 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
     return fail(ATTN_ERR_UNSUPPORTED, "needs a compute capability 10.3 device (GB300), found " +
                                           std::to_string(info.major) + "." +
                                           std::to_string(info.minor));
-  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms, d);
+  const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms);
   if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits))
     return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
   if ((long long)plan.items * splits >= (1LL << 31))
@@ -884,7 +882,7 @@ int attn_fwd_kv_num_splits(int B, int Lq, int Lk, int Hq, int Hkv, int d, int ca
     fail(ATTN_ERR_CUDA, "no CUDA device");
     return 0;
   }
-  return kv_auto_splits(kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left), sms, d);
+  return kv_auto_splits(kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left), sms);
 }
 
 size_t attn_fwd_kv_workspace_size(int B, int Lq, int Lk, int Hq, int Hkv, int d, int causal,

@@ -69,9 +69,8 @@ cudaError_t launch_kv(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
 // key split; a.tm_v over the copy, a.p.vmax set).
 cudaError_t launch_kv_pv16(int d, bool out_f32, const KvLaunchArgs& a);
 // Work items of at most 32 query rows (q_per_tile * group) run the keys-on-lanes
-// kernel (attn_kv_keys_kernel.cuh), two CTAs per SM at d = 64 and one at d = 128.
+// kernel (attn_kv_keys_kernel.cuh), one CTA per SM.
 inline bool kv_keys_shape(int q_per_tile, int group) { return q_per_tile * group <= 32; }
-inline int kv_keys_ctas_per_sm(int d) { return d == 64 ? 2 : 1; }
 cudaError_t launch_kv_keys(int d, bool bf16, bool paged, bool out_f32, const KvLaunchArgs& a);
 // The merge of a.p.splits > 1 partial results into O and LSE.
 cudaError_t launch_kv_merge(int d, bool bf16, bool out_f32, const KvLaunchArgs& a);
