@@ -56,6 +56,7 @@ TRAFFIC_BY_SOURCE = {
     "560da211fd607b93": 876_527_360 + 64_404_224,  # P handed to the P·V MMAs in two halves
     "fd0fa8df494247a6": 875_117_312 + 63_871_232,  # 3-input max in the row max
     "eec2919036746b6b": 887_364_608 + 121_369_344,  # masked blocks outside the unmasked loop
+    "7b8d7e8882791981": 882_185_472 + 120_702_720,  # + the bf16 fp16-copy-of-V instantiations
 }
 
 
