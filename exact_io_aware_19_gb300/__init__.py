@@ -30,7 +30,7 @@ __all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_noalloc", "workspace_size", "a
            "attn_fwd_kv_paged", "attn_fwd_window", "attn_fwd_fp8", "attn_bwd",
            "kv_num_splits", "kv_workspace_size", "sync_status", "AttnError",
            "library_path", "load_library", "set_wait_limit_ns", "set_path_policy", "PATH_AUTO",
-           "PATH_SQUARE", "PATH_TILES", "debug_wait_probe", "debug_exp2",
+           "PATH_SQUARE", "PATH_TILES", "PATH_ALTERNATE", "debug_wait_probe", "debug_exp2",
            "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -434,11 +434,12 @@ def sync_status(workspace: Optional[torch.Tensor] = None, device=None, stream=No
     _check(lib.attn_fwd_sync_status(workspace.data_ptr(), _stream_handle(stream)))
 
 
-PATH_AUTO, PATH_SQUARE, PATH_TILES = 0, 1, 2
+PATH_AUTO, PATH_SQUARE, PATH_TILES, PATH_ALTERNATE = 0, 1, 2, 3
 
 
 def set_path_policy(policy: int) -> int:
-    """Choose attn_fwd's kernel process-wide (PATH_AUTO, PATH_SQUARE or PATH_TILES);
+    """Choose attn_fwd's kernel process-wide (PATH_AUTO, PATH_SQUARE, PATH_TILES or
+    PATH_ALTERNATE);
     returns the previous setting."""
     lib = load_library()
     old = int(lib.attn_get_path_policy())

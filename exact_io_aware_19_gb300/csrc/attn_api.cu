@@ -560,8 +560,23 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   const int kv_span = (window_left >= 0) ? std::min(L, window_left + 128) : L;
   const double kv_bytes = 4.0 * B * Hkv * static_cast<double>(kv_span) * d;  // K and V, 2 B each
   const bool tiles_win = split_p && window_left >= 0 && kv_bytes <= 192.0 * 1024 * 1024;
-  if (policy == ATTN_PATH_TILES ||
-      (policy == ATTN_PATH_AUTO && (few_units || tiles_win) && Hq / Hkv <= 128))
+  // The alternating mode (one 128-row tile per unit, the two pipelines on alternate
+  // key blocks) halves the longest tile's chain; its smaller units also balance the
+  // causal triangle better. Measured on one GB300 (causal 4 heads, fp16, d = 64, CUDA
+  // events, L2 flushed), against the kernel AUTO took before: L = 2048 27.7 -> 22.1 us,
+  // 4096 35.5 -> 31.4 us, 8192 61.1 -> 53.9 us, 16384 167 -> 164 us, 32768 585 ->
+  // 563 us, 65536 2.16 -> 2.11 ms; at 131072 8.26 against 8.41 ms (the two-tile units'
+  // shared K/V wins) and at L = 256 11 against 13 us. Non-causal tiles carry equal work,
+  // so there it wins only within one wave (2x8x512: 12.9 -> 11.9 us; 2x8x2048: 33.4
+  // against 36.4 us).
+  const bool alt_shape = !bf16 && d == 64;
+  const long long alt_units = static_cast<long long>(B) * Hq * ((L + 127) / 128);
+  const bool alt_auto = alt_shape && window_left < 0 && L >= 512 &&
+                        (causal ? alt_units <= 16LL * info.sms : alt_units <= info.sms);
+  const bool alt = alt_shape && (policy == ATTN_PATH_ALTERNATE || (policy == ATTN_PATH_AUTO && alt_auto));
+  if (!alt && (policy == ATTN_PATH_TILES ||
+               ((policy == ATTN_PATH_AUTO || policy == ATTN_PATH_ALTERNATE) && (few_units || tiles_win) &&
+                Hq / Hkv <= 128)))
     return launch_square_as_kv(q, k, v, o, lse, B, L, Hq, Hkv, d, causal, window_left, -1, scale,
                                bf16, out_f32, workspace, stream, v16, vmax);
   CUtensorMap tm_q, tm_k, tm_v;
@@ -588,13 +603,15 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   p.window_left = window_left;
   p.score_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f ? 1 : 0;
-  p.units_per_bh = (L + kUnitRows - 1) / kUnitRows;
-  p.num_units = num_units;
+  p.units_per_bh = alt ? (L + 127) / 128 : (L + kUnitRows - 1) / kUnitRows;
+  p.num_units = B * Hq * p.units_per_bh;
   p.wait_limit_ns = g_wait_limit_ns.load();
   a.grid = p.num_units < info.sms ? p.num_units : info.sms;
   a.stream = static_cast<cudaStream_t>(stream);
 
-  if (pv16) {
+  if (alt) {
+    e = ex19::launch_fwd_alt(out_f32, a);
+  } else if (pv16) {
     e = ex19::launch_v_to_f16(v, v16, vmax, B, L, Hkv, d, a.stream);
     if (e != cudaSuccess) return cuda_fail("the fp16 copy of V", e);
     e = ex19::launch_fwd_pv16(d, out_f32, a);
@@ -940,8 +957,10 @@ attn_status_t attn_fwd_sync_status(void* workspace, void* stream) {
 }
 
 void attn_set_path_policy(int policy) {
-  g_path_policy.store((policy == ATTN_PATH_SQUARE || policy == ATTN_PATH_TILES) ? policy
-                                                                               : ATTN_PATH_AUTO);
+  g_path_policy.store((policy == ATTN_PATH_SQUARE || policy == ATTN_PATH_TILES ||
+                       policy == ATTN_PATH_ALTERNATE)
+                          ? policy
+                          : ATTN_PATH_AUTO);
 }
 
 int attn_get_path_policy(void) { return g_path_policy.load(); }

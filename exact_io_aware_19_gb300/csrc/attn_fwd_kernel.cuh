@@ -26,6 +26,15 @@
 //              rescales its O row when m grows by more than a threshold (2^1 with
 //              packed fp16 exponentials, 2^8 otherwise), and at the end of the unit
 //              writes O / l and LSE.
+//   * Alternating mode (ALT, for small problems whose time is the longest row
+//     tile's chain of key blocks): a work unit is one 128-row tile, and both
+//     pipelines (MMA warp, softmax warps, TMEM columns) work on it, pipeline t
+//     taking the key blocks lo + t, lo + t + 2, ... with its own running max, sum
+//     and O. At the end tile 1's softmax warps hand their max and sum to tile 0's
+//     through shared memory, and tile 0's warps read O_1 from TMEM and write the
+//     combination (the merge of attention computed in parts: with m = max(m_0,
+//     m_1), O = (2^(m_0 - m) O_0 + 2^(m_1 - m) O_1) / (2^(m_0 - m) l_0 +
+//     2^(m_1 - m) l_1)). A tile's chain is half as long.
 //   * Every wait is bounded (globaltimer); a wait that runs out records a timeout
 //     in the status word and every role leaves its loop, so the CTA still frees
 //     its TMEM and exits.
@@ -75,10 +84,11 @@ struct Geometry {
   static constexpr int kOffKV = kTilesPerUnit * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   // barriers: full[S], empty[S], q_full, q_free, s_full[2], p_full[2], o_full[2], o_free[2],
-  // drain, s_free[2], pv_done[2], p_half[2]
-  static constexpr int kNumBars = 2 * kSlots + 17;
+  // drain, s_free[2], pv_done[2], p_half[2], merge_ready, merge_free (ALT)
+  static constexpr int kNumBars = 2 * kSlots + 19;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemUsed = kOffMisc + 16;
+  static constexpr int kOffXchg = kOffMisc + 16;           // ALT: [128 rows] (max, sum) of tile 1
+  static constexpr int kSmemUsed = kOffXchg + kBM * 8;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
 };
 
@@ -110,7 +120,9 @@ __device__ __forceinline__ TileSpan tile_span(const FwdParams& p, int row0) {
 }
 
 // k-th unit of this CTA. Ranks are dealt to CTAs in a snake order over a
-// heavy-first ranking (causal: the last row blocks see the most keys).
+// heavy-first ranking (causal: the last row blocks see the most keys). ALT: a unit
+// is one 128-row tile, given to both pipelines.
+template <bool ALT>
 __device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
   const int G = gridDim.x;
   const int c = blockIdx.x;
@@ -125,7 +137,7 @@ __device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
   u.lo = 0x7fffffff;
   u.hi = 0;
   for (int t = 0; t < kTilesPerUnit; ++t) {
-    u.t[t] = tile_span(p, mb * kUnitRows + t * kBM);
+    u.t[t] = tile_span(p, ALT ? mb * kBM : mb * kUnitRows + t * kBM);
     if (u.t[t].lo < u.t[t].hi) {
       u.lo = min(u.lo, u.t[t].lo);
       u.hi = max(u.hi, u.t[t].hi);
@@ -154,7 +166,7 @@ __device__ __forceinline__ void unmasked_blocks(const FwdParams& p, const TileSp
 
 // PV16 (bf16 inputs only): V is the call's fp16 copy scaled per (batch, K/V head)
 // by 2^e (vscale.cuh), P is fp16 and P·V one fp16 product; the output is scaled back.
-template <int D, bool BF16, bool OUT_F32, bool PV16 = false>
+template <int D, bool BF16, bool OUT_F32, bool PV16 = false, bool ALT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -186,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kColS0 = 0, kStrideS = 128;
   constexpr uint32_t kColP0 = kSeparateP ? 256 : 0, kStrideP = kSeparateP ? 64 : 128;
   constexpr uint32_t kColO0 = kSeparateP ? 384 : 256, kStrideO = kSeparateP ? 64 : 128;
+  static_assert(!ALT || kSeparateP, "the alternating mode is built for the separate-P layout");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -206,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_s_free = [&](int t) { return bars + 8u * (2 * S + 11 + t); };
   auto bar_pv_done = [&](int t) { return bars + 8u * (2 * S + 13 + t); };
   auto bar_p_half = [&](int t) { return bars + 8u * (2 * S + 15 + t); };
+  const uint32_t bar_merge_ready = bars + 8u * (2 * S + 17);  // ALT: tile 1's max and sum are written
+  const uint32_t bar_merge_free = bars + 8u * (2 * S + 18);   // ALT: tile 0 has read them and O_1
+  float2* xchg = reinterpret_cast<float2*>(smem + G::kOffXchg);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
 
@@ -231,6 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_pv_done(t), 1);
       mbar_init(bar_p_half(t), kBM);
     }
+    mbar_init(bar_merge_ready, kBM);
+    mbar_init(bar_merge_free, kBM);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -261,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_cnt = 0;   // Q loads issued
       bool ok = true;
       Unit u;
-      for (int k = 0; ok && unit_of(p, k, u); ++k) {
+      for (int k = 0; ok && unit_of<ALT>(p, k, u); ++k) {
         wc.unit = k;
         ok = mbar_wait_bounded(bar_q_free, (q_cnt & 1u) ^ 1u, wc, kSiteProdQFree);
         if (!ok) break;
@@ -351,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    for (int k = 0; ok && unit_of(p, k, u); ++k) {
+    for (int k = 0; ok && unit_of<ALT>(p, k, u); ++k) {
       wc.unit = k;
       ok = mbar_wait_warp(bar_q_full, q_cnt & 1u, wc, kSiteMmaQFull);
       ++q_cnt;
@@ -403,6 +421,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(bar_empty(slot_of(vidx)));
         return true;
       };
+      if constexpr (ALT) {
+        // This pipeline's blocks are lo + t, lo + t + 2, ...; the other pipeline's
+        // blocks between them are released in order (skip_block).
+        const int j_own = u.lo + t;
+        const bool own = j_own < u.hi;
+        auto s_block = [&](int j) __attribute__((always_inline)) -> bool {
+          const uint32_t kidx = kidx_of(j);
+          if (!mbar_wait_warp(bar_full(slot_of(kidx)), par_of(kidx), wc, kSiteMmaKFull)) return false;
+          if (ns > 0 && !mbar_wait_warp(bar_s_free(t), (ns - 1) & 1u, wc, kSiteMmaSFree)) return false;
+          tc_fence_after();
+          issue_s(slot_of(kidx));
+          mma_commit_elect(bar_empty(slot_of(kidx)));
+          return true;
+        };
+        for (int j = u.lo; ok && j < (own ? j_own : u.hi); ++j) ok = skip_block(j);
+        if (ok && own) {
+          ok = s_block(j_own);
+          for (int j = j_own; ok && j < u.hi; j += 2) {
+            if (j + 1 < u.hi && !(ok = skip_block(j + 1))) break;
+            if (j + 2 < u.hi && !(ok = s_block(j + 2))) break;
+            ok = pv_block(j);
+          }
+          if (ok) {
+            mma_commit_elect(bar_o_full(t));
+            ++o_cnt;
+          }
+        }
+        if (!ok) break;
+        it = it0 + 2u * (u.hi - u.lo);
+        mma_commit_elect(bar_q_free);
+        continue;
+      }
       for (int j = u.lo; ok && j < j_lo; ++j) ok = skip_block(j);
       if (ok && live) {
         if constexpr (kSeparateP) {
@@ -464,12 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem_base + lane_off + kColO0 + kStrideO * t;
     const float C = p.score_log2;
     uint32_t s_cnt = 0, o_cnt = 0;  // blocks / units this tile has processed (all units)
+    [[maybe_unused]] uint32_t o1_cnt = 0, m_cnt = 0;  // ALT: tile 1's O_1 handed over, merges done
     bool ok = true;
     Unit u;
-    for (int k = 0; ok && unit_of(p, k, u); ++k) {
+    for (int k = 0; ok && unit_of<ALT>(p, k, u); ++k) {
       wc.unit = k;
       const TileSpan span = (t == 0) ? u.t[0] : u.t[1];  // no dynamic index: stays in registers
-      if (span.lo >= span.hi) continue;
+      if (!ALT && span.lo >= span.hi) continue;
+      // this tile's first block, and the step between its blocks
+      const int j0 = ALT ? span.lo + t : span.lo;
+      constexpr int kStep = ALT ? 2 : 1;
       const int row = span.row0 + r_in_tile;
       float m_ref = -INFINITY;  // reference max (base-2 units) the P values are relative to
       float l = 0.f;            // running sum of P
@@ -544,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O rescale before the first half of this block's P·V (kHalves), once half
           // of the scores are consumed: 16 columns of O at a time.
           auto rescale_o_early = [&]() __attribute__((always_inline)) {
-            if (__any_sync(0xffffffffu, rescale && j != span.lo)) {
-              const float a = (rescale && j != span.lo) ? alpha : 1.f;
+            if (__any_sync(0xffffffffu, rescale && j != j0)) {
+              const float a = (rescale && j != j0) ? alpha : 1.f;
 #pragma unroll 1
               for (int c0 = 0; c0 < D; c0 += 16) {
                 uint32_t orow[16];
@@ -646,8 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O rescale. The previous P·V of this tile is complete: with P over S,
         // S_t(j) was issued after it and s_full tracks all earlier MMAs; with a
         // separate P region, pv_done was waited just above.
-        if (!kHalves && __any_sync(0xffffffffu, rescale && j != span.lo)) {
-          const float a = (rescale && j != span.lo) ? alpha : 1.f;
+        if (!kHalves && __any_sync(0xffffffffu, rescale && j != j0)) {
+          const float a = (rescale && j != j0) ? alpha : 1.f;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t orow[32];
@@ -666,19 +720,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       unmasked_blocks(p, span, ja, jb);
       // the masked prefix, the unmasked middle (a tight loop of its own), the masked
       // suffix; one instance of each block body
-      for (int j = span.lo; ok && j < span.hi;) {
+      for (int j = j0; ok && j < span.hi;) {
         if (j >= ja && j < jb) {
-          for (; ok && j < jb; ++j) ok = one_block(j, std::false_type{});
+          for (; ok && j < jb; j += kStep) ok = one_block(j, std::false_type{});
         } else {
           ok = one_block(j, std::true_type{});
-          ++j;
+          j += kStep;
         }
       }
       if (!ok) break;
+      if constexpr (ALT) {
+        if (t == 1) {
+          // hand this row's max and sum to tile 0, which reads O_1 from TMEM
+          if (m_cnt > 0 && !mbar_wait_warp(bar_merge_free, (m_cnt - 1) & 1u, wc, kSiteSmxOFull)) break;
+          xchg[r_in_tile] = make_float2(m_ref, l);
+          mbar_arrive(bar_merge_ready);
+          ++m_cnt;
+          continue;
+        }
+      }
       // ---- epilogue: O / l and LSE for this tile
       ok = mbar_wait_warp(bar_o_full(t), o_cnt & 1u, wc, kSiteSmxOFull);
       ++o_cnt;
       if (!ok) break;
+      [[maybe_unused]] bool live1 = false;
+      [[maybe_unused]] float w0 = 1.f, w1 = 0.f;
+      if constexpr (ALT) {
+        // combine with tile 1's part: its max and sum from shared memory, O_1 from TMEM
+        live1 = span.lo + 1 < span.hi;
+        if (!(ok = mbar_wait_warp(bar_merge_ready, m_cnt & 1u, wc, kSiteSmxOFull))) break;
+        if (live1) {
+          if (!(ok = mbar_wait_warp(bar_o_full(1), o1_cnt & 1u, wc, kSiteSmxOFull))) break;
+          ++o1_cnt;
+        }
+        const float2 ml1 = xchg[r_in_tile];
+        const float mm = fmaxf(m_ref, ml1.x);
+        w0 = (l > 0.f) ? ex2_approx(m_ref - mm) : 0.f;
+        w1 = (ml1.y > 0.f) ? ex2_approx(ml1.x - mm) : 0.f;
+        l = l * w0 + ml1.y * w1;
+        m_ref = mm;
+      }
       tc_fence_after();
       // Opaque copies: keep the compiler from hoisting the epilogue's 64-bit
       // addresses above the block loop, where they would hold registers the
@@ -693,6 +774,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t orow[32];
         tmem_ld_x32(tO + c0, orow);
+        if constexpr (ALT) {
+          uint32_t o1[32];
+          tmem_ld_x32(tO + kStrideO + c0, o1);  // O_1: the same lanes, tile 1's columns
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float a = __uint_as_float(orow[c]) * w0;
+            orow[c] = __float_as_uint(w1 > 0.f ? a + __uint_as_float(o1[c]) * w1 : a);
+          }
+        }
         if (live) {
           if constexpr (OUT_F32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_row + c0);
@@ -723,6 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(bar_o_free(t));
+      if constexpr (ALT) {
+        if (live1) mbar_arrive(bar_o_free(1));  // O_1 has been read
+        mbar_arrive(bar_merge_free);
+        ++m_cnt;
+      }
     }
   }
 

@@ -8,9 +8,9 @@
 
 namespace ex19 {
 
-template <int D, bool BF16, bool OUT_F32, bool PV16>
+template <int D, bool BF16, bool OUT_F32, bool PV16, bool ALT = false>
 cudaError_t launch_fwd_one(const LaunchArgs& a) {
-  auto kern = attn_fwd_sm103_kernel<D, BF16, OUT_F32, PV16>;
+  auto kern = attn_fwd_sm103_kernel<D, BF16, OUT_F32, PV16, ALT>;
   constexpr int smem = Geometry<D>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
   int dev = 0;

@@ -56,6 +56,9 @@ struct BwdLaunchArgs {
 // Each returns the CUDA error of configuring / enqueuing the kernel.
 cudaError_t launch_fwd_d64(bool bf16, bool out_f32, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool bf16, bool out_f32, const LaunchArgs& a);
+// The alternating mode (fp16, d = 64): one 128-row tile per work unit, both
+// pipelines on alternate key blocks (a.p.units_per_bh = ceil(L / 128)).
+cudaError_t launch_fwd_alt(bool out_f32, const LaunchArgs& a);
 // bfloat16 inputs with the fp16 copy of V (a.tm_v over it, a.p.vmax set).
 cudaError_t launch_fwd_pv16(int d, bool out_f32, const LaunchArgs& a);
 // The fp16 copy of a bfloat16 V [B, L, Hkv, d] with one power-of-two scale per

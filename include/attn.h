@@ -290,20 +290,30 @@ attn_status_t attn_fwd_kv_paged(const void *q, const void *k_cache, const void *
                                 size_t workspace_bytes, void *stream);
 
 /*
- * Which kernel attn_fwd (and attn_fwd_noalloc) uses, process-wide. Both compute the
+ * Which kernel attn_fwd (and attn_fwd_noalloc) uses, process-wide. All compute the
  * same result (up to rounding order); they differ in how the work is cut:
- *   ATTN_PATH_AUTO    the persistent two-tile kernel (256 query rows per work unit),
- *                     unless the problem has at most half as many such units as the
- *                     device has SMs (causal: at most as many), or it has d = 128 or
- *                     bf16 inputs and a left window whose K/V rows
- *                     (B * Hkv * (window_left + 128)) take at most 192 MiB; then the
- *                     one-tile kernel (128 rows per CTA, the longest tiles first).
- *   ATTN_PATH_SQUARE  always the persistent two-tile kernel.
- *   ATTN_PATH_TILES   always the one-tile kernel (attn_fwd_kv's with Lq = Lk and one
- *                     key split).
+ *   ATTN_PATH_AUTO       fp16, d = 64, no window, L >= 512: the alternating mode below
+ *                        when its units (B * Hq * ceil(L / 128)) number at most 16 per
+ *                        SM (causal) or one per SM (non-causal). Otherwise the
+ *                        persistent two-tile kernel (256 query rows per work unit),
+ *                        unless the problem has at most half as many such units as the
+ *                        device has SMs (causal: at most as many); then the one-tile
+ *                        kernel (128 rows per CTA, the longest tiles first). bfloat16
+ *                        inputs with a workspace too small for the copy of V (see
+ *                        attn_fwd_workspace_size) also take the one-tile kernel under a
+ *                        left window whose K/V rows (B * Hkv * (window_left + 128))
+ *                        take at most 192 MiB.
+ *   ATTN_PATH_SQUARE     always the persistent two-tile kernel.
+ *   ATTN_PATH_TILES      always the one-tile kernel (attn_fwd_kv's with Lq = Lk and one
+ *                        key split).
+ *   ATTN_PATH_ALTERNATE  the persistent kernel with one 128-row tile per work unit,
+ *                        its two pipelines taking alternate key blocks of that tile
+ *                        (each with its own running max, sum and O, combined at the
+ *                        end): the longest tile's chain of blocks is half as long.
+ *                        fp16 inputs with d = 64; other calls fall back to AUTO.
  * Any other value selects ATTN_PATH_AUTO. attn_get_path_policy returns the setting.
  */
-enum { ATTN_PATH_AUTO = 0, ATTN_PATH_SQUARE = 1, ATTN_PATH_TILES = 2 };
+enum { ATTN_PATH_AUTO = 0, ATTN_PATH_SQUARE = 1, ATTN_PATH_TILES = 2, ATTN_PATH_ALTERNATE = 3 };
 void attn_set_path_policy(int policy);
 int attn_get_path_policy(void);
 

@@ -217,7 +217,7 @@ def test_python_kv_binding_checks_shapes():
 
 def test_path_policy_round_trip(lib):
     old = lib.attn_get_path_policy()
-    for policy, want in [(1, 1), (2, 2), (0, 0), (7, 0), (-1, 0)]:
+    for policy, want in [(1, 1), (2, 2), (3, 3), (0, 0), (7, 0), (-1, 0)]:
         lib.attn_set_path_policy(policy)
         assert lib.attn_get_path_policy() == want
     lib.attn_set_path_policy(old)

@@ -234,20 +234,24 @@ def test_exp2_f16x2_accuracy():
 
 
 def test_auto_path_choice_causal_one_unit_per_sm():
-    """Causal problems with at most one 256-row unit per SM take the one-tile kernel
-    (128 units at L = 8192, 4 heads); a non-causal problem of the same size takes the
-    persistent kernel. AUTO gives exactly the chosen kernel's bits."""
+    """fp16 d = 64: a causal problem takes the alternating mode (L = 8192, 4 heads: 256
+    one-tile units); a non-causal one with more one-tile units than SMs takes the
+    persistent two-tile kernel; bf16 at d = 64 (no alternating mode), causal with at
+    most one 256-row unit per SM, takes the one-tile kernel. AUTO gives exactly the
+    chosen kernel's bits."""
     import exact_io_aware_19_gb300 as ex
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert 128 <= sms
-    for causal, B, L, H, pick in ((True, 1, 8192, 4, ex.PATH_TILES), (False, 2, 2048, 8, ex.PATH_SQUARE)):
-        q, k, v = si.random_qkv(B, L, H, H, 64, seed=L, device="cuda")
+    for causal, B, L, H, dt, pick in ((True, 1, 8192, 4, "fp16", ex.PATH_ALTERNATE),
+                                      (False, 2, 2048, 8, "fp16", ex.PATH_SQUARE),
+                                      (True, 1, 8192, 4, "bf16", ex.PATH_TILES)):
+        q, k, v = si.random_qkv(B, L, H, H, 64, dtype=dt, seed=L, device="cuda")
         assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
         o_auto, l_auto = ex.attn_fwd(q, k, v, causal=causal, out_fp32=True)
         ex.set_path_policy(pick)
         o_p, l_p = ex.attn_fwd(q, k, v, causal=causal, out_fp32=True)
         ex.set_path_policy(ex.PATH_AUTO)
-        assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (causal, L)
+        assert torch.equal(o_auto, o_p) and torch.equal(l_auto, l_p), (causal, L, dt)
 
 
 def test_auto_path_choice_d128_window():
@@ -276,16 +280,18 @@ def test_auto_path_choice_d128_window():
 
 
 def test_auto_path_choice():
-    """AUTO takes the one-tile kernel exactly when the problem has at most half as many
-    256-row units as SMs (causal: at most as many); both kernels agree to rounding."""
+    """The small causal workload (fp16, d = 64, L = 2048): AUTO takes the alternating
+    mode; the three kernels agree to rounding."""
     import exact_io_aware_19_gb300 as ex
     assert ex.set_path_policy(ex.PATH_AUTO) == ex.PATH_AUTO
     q, k, v = si.random_qkv(1, 2048, 4, 4, 64, seed=8, device="cuda")
     o_auto, l_auto = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
-    ex.set_path_policy(ex.PATH_TILES)
-    o_t, l_t = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
-    ex.set_path_policy(ex.PATH_SQUARE)
-    o_s, l_s = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
+    outs = {}
+    for name, pol in (("alt", ex.PATH_ALTERNATE), ("tiles", ex.PATH_TILES), ("square", ex.PATH_SQUARE)):
+        ex.set_path_policy(pol)
+        outs[name] = ex.attn_fwd(q, k, v, causal=True, out_fp32=True)
     ex.set_path_policy(ex.PATH_AUTO)
-    assert torch.equal(o_auto, o_t) and torch.equal(l_auto, l_t)  # 32 units: one-tile kernel
-    assert (o_t - o_s).abs().max().item() < 2e-3 and (l_t - l_s).abs().max().item() < 1e-4
+    assert torch.equal(o_auto, outs["alt"][0]) and torch.equal(l_auto, outs["alt"][1])
+    for name in ("tiles", "square"):
+        assert (outs[name][0] - o_auto).abs().max().item() < 2e-3, name
+        assert (outs[name][1] - l_auto).abs().max().item() < 1e-3, name

@@ -18,6 +18,12 @@ and masks (causal, left window, ragged tails, a second tile past the end):
     P·V of a unit waits for the previous unit's epilogue, an O rescale happens
     with no P·V in flight.
 
+The alternating mode (ALT) is modelled too: a unit is one tile whose key blocks the
+two pipelines take in turn (pipeline t: lo + t, lo + t + 2, ...); tile 1's softmax
+hands its max and sum over (merge_ready, after merge_free for the previous unit) and
+tile 0's reads O_1 once tile 1's last P·V is done (o_full of tile 1), then releases
+O_1 for tile 1's next unit (o_free of tile 1).
+
 Mutants with one wait removed must be caught. (Removing the MMA warp's o_free
 wait is not among them: the model shows it is implied, since the first P·V of a
 unit also waits for that unit's first P, which the softmax writes only after its
@@ -43,14 +49,15 @@ def tile_span(L, causal, wl, row0):
     return (lo, hi)
 
 
-def make_units(rng):
+def make_units(rng, alt=False):
     L = rng.randrange(1, 1700)
     causal = rng.random() < 0.7
     wl = rng.choice([-1, -1, 0, 100, 300]) if causal else -1
-    n_units = (L + 2 * KBM - 1) // (2 * KBM)
+    rows = KBM if alt else 2 * KBM
+    n_units = (L + rows - 1) // rows
     units = []
     for mb in range(n_units):
-        t = [tile_span(L, causal, wl, mb * 2 * KBM + i * KBM) for i in range(2)]
+        t = [tile_span(L, causal, wl, mb * KBM if alt else mb * 2 * KBM + i * KBM) for i in range(2)]
         live = [s for s in t if s[0] < s[1]]
         assert live, "the first tile of a unit is always inside the sequence"
         units.append((t, min(s[0] for s in live), max(s[1] for s in live)))
@@ -59,8 +66,10 @@ def make_units(rng):
     return mine
 
 
-def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
+def simulate(units, slots, seed, rescale_p=0.3, mutant=None, alt=False):
     rng = random.Random(seed)
+    merge_ready, merge_free = Bar("merge_ready", 1), Bar("merge_free", 1)
+    xchg = [None]                       # ALT: the unit whose tile-1 max and sum are in shared memory
     full = [Bar(f"full{s}", 1) for s in range(slots)]
     empty = [Bar(f"empty{s}", 2) for s in range(slots)]  # one release per tile
     q_full, q_free = Bar("q_full", 1), Bar("q_free", 2)
@@ -119,6 +128,53 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                     released.setdefault(idx, set()).add(t)
                     empty[idx % slots].arrive()
 
+            def s_block(j):
+                nonlocal ns
+                idx = kidx(j)
+                yield wait(full[idx % slots], idx // slots + 1)
+                if ns > 0 and mutant != "mma_skips_s_free":
+                    yield wait(s_free[t], ns)
+                q.push(("S", t, k, j, idx))
+                q.commit(s_full[t])
+                ns += 1
+                q.commit(empty[idx % slots])
+
+            def pv_block(j, first):
+                nonlocal p_cnt
+                idx = kidx(j) + 1
+                yield wait(full[idx % slots], idx // slots + 1)
+                if mutant != "mma_skips_p_half":
+                    yield wait(p_half[t], p_cnt + 1)
+                if first and mutant != "mma_skips_o_free":
+                    yield wait(o_free[t], o_cnt)
+                q.push(("PV", t, k, j, idx, 0, first))
+                o_state[t][2] += 1
+                if mutant != "mma_skips_p_full":
+                    yield wait(p_full[t], p_cnt + 1)
+                q.push(("PV", t, k, j, idx, 1, False))
+                o_state[t][2] += 1
+                p_cnt += 1
+                q.commit(pv_done[t])
+                q.commit(empty[idx % slots])
+
+            if alt:
+                j_own = lo + t
+                own = j_own < hi
+                for j in range(lo, j_own if own else hi):
+                    yield from skip(j)
+                if own:
+                    yield from s_block(j_own)
+                    for j in range(j_own, hi, 2):
+                        if j + 1 < hi:
+                            yield from skip(j + 1)
+                        if j + 2 < hi:
+                            yield from s_block(j + 2)
+                        yield from pv_block(j, j == j_own)
+                    q.commit(o_full[t])
+                    o_cnt += 1
+                it = it0 + 2 * (hi - lo)
+                q.commit(q_free)
+                continue
             for j in range(lo, j_lo):
                 yield from skip(j)
             if live:
@@ -166,18 +222,20 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
         yield wait(drain, 1)
 
     def softmax(t):
-        s_cnt = o_cnt = 0
+        s_cnt = o_cnt = o1_cnt = m_cnt = 0
         for k, (spans, lo, hi) in enumerate(units):
             slo, shi = spans[t]
             if slo >= shi:
                 continue
-            for j in range(slo, shi):
+            j0, step = (slo + t, 2) if alt else (slo, 1)
+            own_done = 0
+            for j in range(j0, shi, step):
                 yield wait(s_full[t], s_cnt + 1)
                 check(sbuf[t] == ("S", k, j), f"tile {t} reads {sbuf[t]} for S({k}, {j})")
                 s_read.add((t, k, j))
                 s_free[t].arrive()
                 yield STEP
-                rescale = j != slo and rng.random() < rescale_p
+                rescale = j != j0 and rng.random() < rescale_p
                 if s_cnt > 0 and mutant != "softmax_skips_pv_done":
                     yield wait(pv_done[t], s_cnt)
                 # the previous block's P·V has read both halves of P
@@ -185,7 +243,7 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                 preg[t][0] = ("P", k, j)
                 if rescale:
                     check(o_state[t][2] == 0, f"tile {t} rescales O with a P·V in flight")
-                    check(o_state[t][0] == k and o_state[t][1] == 2 * (j - slo),
+                    check(o_state[t][0] == k and o_state[t][1] == 2 * own_done,
                           f"tile {t} rescales O holding {o_state[t]} at block {j}")
                 p_half[t].arrive()
                 yield STEP
@@ -193,12 +251,38 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
                 p_full[t].arrive()
                 yield STEP
                 s_cnt += 1
+                own_done += 1
+            if alt and t == 1:
+                # hand max and sum over; O_1 stays in TMEM for tile 0
+                if m_cnt > 0 and mutant != "alt_skips_merge_free":
+                    yield wait(merge_free, m_cnt)
+                xchg[0] = k
+                merge_ready.arrive()
+                m_cnt += 1
+                continue
             yield wait(o_full[t], o_cnt + 1)
-            check(o_state[t][0] == k and o_state[t][1] == 2 * (shi - slo) and o_state[t][2] == 0,
+            check(o_state[t][0] == k and o_state[t][1] == 2 * own_done and o_state[t][2] == 0,
                   f"tile {t} epilogue reads O {o_state[t]} for unit {k}")
+            if alt:
+                n1 = len(range(slo + 1, shi, 2))
+                if mutant != "alt_skips_merge_ready":
+                    yield wait(merge_ready, m_cnt + 1)
+                check(xchg[0] == k, f"tile 0 merges unit {k} with tile 1's values of unit {xchg[0]}")
+                if n1 > 0:
+                    if mutant != "alt_skips_o_full1":
+                        yield wait(o_full[1], o1_cnt + 1)
+                    o1_cnt += 1
+                    check(o_state[1][0] == k and o_state[1][1] == 2 * n1 and o_state[1][2] == 0,
+                          f"tile 0 reads O_1 {o_state[1]} for unit {k}")
+                    o_read.add((1, k))
             o_read.add((t, k))
             o_free[t].arrive()
             o_cnt += 1
+            if alt:
+                if n1 > 0:
+                    o_free[1].arrive()
+                merge_free.arrive()
+                m_cnt += 1
 
     def run_mma(op):
         if op[0] == "S":
@@ -232,7 +316,10 @@ def simulate(units, slots, seed, rescale_p=0.3, mutant=None):
             check(s_reads_pending[0] == 0, f"Q of unit {k} lands while S MMAs still read unit {q_gen[0]}")
             q_gen[0] = k
             spans = units[k][0]
-            s_reads_pending[0] = sum(max(0, s[1] - s[0]) for s in spans)
+            if alt:
+                s_reads_pending[0] = max(0, spans[0][1] - spans[0][0])
+            else:
+                s_reads_pending[0] = sum(max(0, s[1] - s[0]) for s in spans)
             q_full.arrive()
             return
         _, s, n = cp
@@ -276,3 +363,24 @@ def test_o_free_wait_is_implied():
     rng = random.Random(11)
     for trial in range(300):
         simulate(make_units(rng), 4, seed=trial, mutant="mma_skips_o_free")
+
+
+@pytest.mark.parametrize("slots", [4, 8])
+def test_alternating_protocol_holds_under_random_schedules(slots):
+    rng = random.Random(100 + slots)
+    for trial in range(250):
+        simulate(make_units(rng, alt=True), slots, seed=trial, alt=True)
+
+
+@pytest.mark.parametrize("mutant", ["alt_skips_merge_free", "alt_skips_merge_ready", "alt_skips_o_full1",
+                                    "mma_skips_p_half", "softmax_skips_pv_done"])
+def test_alternating_mutants_are_caught(mutant):
+    rng = random.Random(17)
+    caught = False
+    for trial in range(600):
+        try:
+            simulate(make_units(rng, alt=True), 4, seed=trial, mutant=mutant, alt=True)
+        except ProtocolError:
+            caught = True
+            break
+    assert caught, mutant
