@@ -58,6 +58,7 @@ TRAFFIC_BY_SOURCE = {
     "eec2919036746b6b": 887_364_608 + 121_369_344,  # masked blocks outside the unmasked loop
     "7b8d7e8882791981": 882_185_472 + 120_702_720,  # + the bf16 fp16-copy-of-V instantiations
     "1b6bfdd889851ddf": 884_794_880 + 119_256_576,  # + the alternating mode (barriers, exchange)
+    "244f03d03a58a5d8": 911_313_920 + 117_537_280,  # dynamic unit scheduling (unit queue)
 }
 
 
@@ -478,7 +479,7 @@ def ours_arm(args, world, rank, local):
                 kernel = "one-tile (128 rows per CTA)" if few else "persistent two-tile"
                 alt_units = wc.B * wc.Hq * ((wc.L + 127) // 128)
                 if wc.dtype == "fp16" and wc.d == 64 and wc.window_left < 0 and wc.L >= 512 and \
-                        (alt_units <= 16 * sms if wc.causal else alt_units <= sms):
+                        (alt_units <= 8 * sms if wc.causal else alt_units <= sms):
                     kernel = "persistent, one 128-row tile per unit, pipelines on alternate key blocks"
                 if wc.dtype == "bf16":
                     kernel += " after the fp16 copy of V (two conversion kernels)"

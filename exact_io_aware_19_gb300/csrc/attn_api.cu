@@ -18,8 +18,10 @@
 
 namespace {
 
-// status word (16 B), padded to 256 bytes
+// status word (16 B) and the persistent kernel's unit counter (at byte 64), padded to
+// 256 bytes
 constexpr size_t kWorkspaceBytes = 256;
+constexpr size_t kSchedOffset = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 4000000000ull;
 constexpr int kUnitRows = 256;           // query rows per kernel work unit
 
@@ -563,16 +565,18 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   // The alternating mode (one 128-row tile per unit, the two pipelines on alternate
   // key blocks) halves the longest tile's chain; its smaller units also balance the
   // causal triangle better. Measured on one GB300 (causal 4 heads, fp16, d = 64, CUDA
-  // events, L2 flushed), against the kernel AUTO took before: L = 2048 27.7 -> 22.1 us,
-  // 4096 35.5 -> 31.4 us, 8192 61.1 -> 53.9 us, 16384 167 -> 164 us, 32768 585 ->
-  // 563 us, 65536 2.16 -> 2.11 ms; at 131072 8.26 against 8.41 ms (the two-tile units'
-  // shared K/V wins) and at L = 256 11 against 13 us. Non-causal tiles carry equal work,
-  // so there it wins only within one wave (2x8x512: 12.9 -> 11.9 us; 2x8x2048: 33.4
+  // events, L2 flushed), against the one-tile kernel below one unit per SM and the
+  // two-tile kernel with dynamic scheduling above: L = 2048 27.7 -> 22.1 us, 4096 35.5
+  // -> 31.4 us, 8192 90 (61 on the one-tile kernel) -> 52 us, 16384 171 -> 164 us,
+  // 32768 equal (0.56 ms); the two-tile kernel wins at 65536 (2.07 against 2.15 ms)
+  // and 131072 (7.95 against 8.41 ms: its units share each K/V block between two
+  // tiles), and at L = 256 (11 against 13 us). Non-causal tiles carry equal work, so
+  // there it wins only within one wave (2x8x512: 12.9 -> 11.9 us; 2x8x2048: 33.4
   // against 36.4 us).
   const bool alt_shape = !bf16 && d == 64;
   const long long alt_units = static_cast<long long>(B) * Hq * ((L + 127) / 128);
   const bool alt_auto = alt_shape && window_left < 0 && L >= 512 &&
-                        (causal ? alt_units <= 16LL * info.sms : alt_units <= info.sms);
+                        (causal ? alt_units <= 8LL * info.sms : alt_units <= info.sms);
   const bool alt = alt_shape && (policy == ATTN_PATH_ALTERNATE || (policy == ATTN_PATH_AUTO && alt_auto));
   if (!alt && (policy == ATTN_PATH_TILES ||
                ((policy == ATTN_PATH_AUTO || policy == ATTN_PATH_ALTERNATE) && (few_units || tiles_win) &&
@@ -608,6 +612,18 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, flo
   p.wait_limit_ns = g_wait_limit_ns.load();
   a.grid = p.num_units < info.sms ? p.num_units : info.sms;
   a.stream = static_cast<cudaStream_t>(stream);
+  // More two-tile units than CTAs: the CTAs take units from a counter in the
+  // workspace (bytes 64..67, cleared here on the stream) instead of a static deal, so
+  // that SMs that run faster take more of them (causal 4 heads d = 64 L = 131072:
+  // 8.28 -> 7.93 ms; GQA d = 128 L = 16384 1.51 -> 1.48 ms; window 4096 3.67 -> 3.59
+  // ms). The alternating mode keeps the static deal, which measured better for it
+  // (L = 65536: 2.11 against 2.17 ms).
+  if (!alt && p.num_units > a.grid) {
+    uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kSchedOffset);
+    e = cudaMemsetAsync(counter, 0, sizeof(uint32_t), a.stream);
+    if (e != cudaSuccess) return cuda_fail("clearing the unit counter", e);
+    p.sched = counter;
+  }
 
   if (alt) {
     e = ex19::launch_fwd_alt(out_f32, a);

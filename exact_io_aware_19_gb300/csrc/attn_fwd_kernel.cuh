@@ -35,6 +35,13 @@
 //     combination (the merge of attention computed in parts: with m = max(m_0,
 //     m_1), O = (2^(m_0 - m) O_0 + 2^(m_1 - m) O_1) / (2^(m_0 - m) l_0 +
 //     2^(m_1 - m) l_1)). A tile's chain is half as long.
+//   * Dynamic scheduling (when the call gives a counter, p.sched): the producer
+//     takes the next unit rank from a global atomic counter when it starts a unit
+//     and passes it to the MMA and softmax warps through a 4-entry queue in shared
+//     memory. Ranks stay heaviest first; a CTA on a faster SM simply takes more
+//     units, so the grid ends within about one small unit of the mean (a static deal
+//     left CTAs finishing from 7.9 to 8.6 ms on one causal L = 131072 call, the same
+//     units running up to 18 % slower on some SMs).
 //   * Every wait is bounded (globaltimer); a wait that runs out records a timeout
 //     in the status word and every role leaves its loop, so the CTA still frees
 //     its TMEM and exits.
@@ -71,8 +78,11 @@ enum : uint32_t {
   kSiteMmaPFull = 0x20004, kSiteMmaOFree = 0x20005, kSiteMmaDrain = 0x20006,
   kSiteMmaSFree = 0x20007,
   kSiteSmxSFull = 0x30001, kSiteSmxOFull = 0x30002, kSiteSmxPvDone = 0x30003,
-  kSiteDrainLoads = 0x40001,
+  kSiteDrainLoads = 0x40001, kSiteUnitQueue = 0x40002,
 };
+
+constexpr int kUnitQueue = 4;  // dynamic scheduling: unit ranks in flight between the roles
+constexpr int kUnitReaders = 2 + 8;  // the MMA warps and the softmax warps read each entry
 
 template <int D>
 struct Geometry {
@@ -84,11 +94,13 @@ struct Geometry {
   static constexpr int kOffKV = kTilesPerUnit * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   // barriers: full[S], empty[S], q_full, q_free, s_full[2], p_full[2], o_full[2], o_free[2],
-  // drain, s_free[2], pv_done[2], p_half[2], merge_ready, merge_free (ALT)
-  static constexpr int kNumBars = 2 * kSlots + 19;
+  // drain, s_free[2], pv_done[2], p_half[2], merge_ready, merge_free (ALT),
+  // unit queue full[4], empty[4] (dynamic scheduling)
+  static constexpr int kNumBars = 2 * kSlots + 19 + 2 * kUnitQueue;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kOffXchg = kOffMisc + 16;           // ALT: [128 rows] (max, sum) of tile 1
-  static constexpr int kSmemUsed = kOffXchg + kBM * 8;
+  static constexpr int kOffUq = kOffXchg + kBM * 8;        // unit queue: [4] unit ranks
+  static constexpr int kSmemUsed = kOffUq + kUnitQueue * 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;     // slack to align the base to 1024
 };
 
@@ -122,12 +134,9 @@ __device__ __forceinline__ TileSpan tile_span(const FwdParams& p, int row0) {
 // k-th unit of this CTA. Ranks are dealt to CTAs in a snake order over a
 // heavy-first ranking (causal: the last row blocks see the most keys). ALT: a unit
 // is one 128-row tile, given to both pipelines.
+// The unit of rank r (rank 0 = the heaviest).
 template <bool ALT>
-__device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
-  const long long r = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  if (r >= p.num_units) return false;
+__device__ __forceinline__ void unit_from_rank(const FwdParams& p, long long r, Unit& u) {
   const int BH = p.B * p.Hq;
   const int mb = p.units_per_bh - 1 - static_cast<int>(r / BH);
   const int bh = static_cast<int>(r % BH);
@@ -143,6 +152,15 @@ __device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
       u.hi = max(u.hi, u.t[t].hi);
     }
   }
+}
+
+template <bool ALT>
+__device__ __forceinline__ bool unit_of(const FwdParams& p, int k, Unit& u) {
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  const long long r = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (r >= p.num_units) return false;
+  unit_from_rank<ALT>(p, r, u);
   return true;
 }
 
@@ -222,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_merge_ready = bars + 8u * (2 * S + 17);  // ALT: tile 1's max and sum are written
   const uint32_t bar_merge_free = bars + 8u * (2 * S + 18);   // ALT: tile 0 has read them and O_1
   float2* xchg = reinterpret_cast<float2*>(smem + G::kOffXchg);
+  auto bar_uq_full = [&](int i) { return bars + 8u * (2 * S + 19 + i); };
+  auto bar_uq_empty = [&](int i) { return bars + 8u * (2 * S + 19 + kUnitQueue + i); };
+  volatile int* uq = reinterpret_cast<volatile int*>(smem + G::kOffUq);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 4);
 
@@ -249,6 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_merge_ready, kBM);
     mbar_init(bar_merge_free, kBM);
+    for (int i = 0; i < kUnitQueue; ++i) {
+      mbar_init(bar_uq_full(i), 1);
+      mbar_init(bar_uq_empty(i), kUnitReaders);
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -271,6 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   wc.status = p.status;
   wc.set_limit(p.wait_limit_ns);
   wc.unit = 0;
+  // The k-th unit of a reading warp (MMA or softmax): from the static deal, or from
+  // the producer's queue entry k (false at the end of the work, or when the wait
+  // gave up: `ok` is cleared then).
+  auto next_unit = [&](int k, Unit& uu, bool& ok) -> bool {
+    if (p.sched == nullptr) return unit_of<ALT>(p, k, uu);
+    const int slot = k & (kUnitQueue - 1);
+    if (!mbar_wait_warp(bar_uq_full(slot), (k / kUnitQueue) & 1u, wc, kSiteUnitQueue)) {
+      ok = false;
+      return false;
+    }
+    const int r = uq[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_uq_empty(slot));
+    if (r < 0) return false;
+    unit_from_rank<ALT>(p, r, uu);
+    return true;
+  };
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -279,7 +321,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_cnt = 0;   // Q loads issued
       bool ok = true;
       Unit u;
-      for (int k = 0; ok && unit_of<ALT>(p, k, u); ++k) {
+      // The producer's k-th unit: static, or the next rank of the global counter,
+      // published in queue entry k for the other roles (-1: no more work).
+      auto take_unit = [&](int k, Unit& uu) -> bool {
+        if (p.sched == nullptr) return unit_of<ALT>(p, k, uu);
+        const int slot = k & (kUnitQueue - 1);
+        if (k >= kUnitQueue &&
+            !mbar_wait_bounded(bar_uq_empty(slot), ((k / kUnitQueue) - 1) & 1u, wc, kSiteUnitQueue)) {
+          ok = false;
+          return false;
+        }
+        const unsigned r = atomicAdd(p.sched, 1u);
+        const int rank = (r < static_cast<unsigned>(p.num_units)) ? static_cast<int>(r) : -1;
+        uq[slot] = rank;
+        mbar_arrive(bar_uq_full(slot));
+        if (rank < 0) return false;
+        unit_from_rank<ALT>(p, rank, uu);
+        return true;
+      };
+      for (int k = 0; ok && take_unit(k, u); ++k) {
         wc.unit = k;
         ok = mbar_wait_bounded(bar_q_free, (q_cnt & 1u) ^ 1u, wc, kSiteProdQFree);
         if (!ok) break;
@@ -369,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    for (int k = 0; ok && unit_of<ALT>(p, k, u); ++k) {
+    for (int k = 0; ok && next_unit(k, u, ok); ++k) {
       wc.unit = k;
       ok = mbar_wait_warp(bar_q_full, q_cnt & 1u, wc, kSiteMmaQFull);
       ++q_cnt;
@@ -517,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     [[maybe_unused]] uint32_t o1_cnt = 0, m_cnt = 0;  // ALT: tile 1's O_1 handed over, merges done
     bool ok = true;
     Unit u;
-    for (int k = 0; ok && unit_of<ALT>(p, k, u); ++k) {
+    for (int k = 0; ok && next_unit(k, u, ok); ++k) {
       wc.unit = k;
       const TileSpan span = (t == 0) ? u.t[0] : u.t[1];  // no dynamic index: stays in registers
       if (!ALT && span.lo >= span.hi) continue;

@@ -9,6 +9,7 @@ struct FwdParams {
   float* lse;           // [B, Hq, L] or null
   uint32_t* status;     // 4 x u32 status word in the workspace, or null
   const uint32_t* vmax; // [B, Hkv] largest finite |v| (bf16 bits) of the fp16 copy of V, or null
+  uint32_t* sched;      // dynamic scheduling: a zeroed counter of unit ranks taken, or null (static)
   int B, L, Hq, Hkv;
   int causal;           // 0 / 1
   int window_left;      // -1 or >= 0

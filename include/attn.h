@@ -79,7 +79,8 @@ typedef enum {
 
 /*
  * Bytes of device workspace attn_fwd needs for this problem. fp16: 256 (a status
- * word). bfloat16: 256 + (4·B·Hkv rounded up to 256) + 2·B·L·Hkv·d, the status word,
+ * word and, from byte 64, the persistent kernel's unit counter, cleared by each call
+ * that uses it). bfloat16: 256 + (4·B·Hkv rounded up to 256) + 2·B·L·Hkv·d, the status word,
  * then per (batch, K/V head) the largest finite |v| and an fp16 copy of V scaled by
  * a power of two per (batch, K/V head), so that the attention weights enter the P·V
  * product as fp16 (11 significant bits) in one product per key block; the scale is
@@ -293,7 +294,7 @@ attn_status_t attn_fwd_kv_paged(const void *q, const void *k_cache, const void *
  * Which kernel attn_fwd (and attn_fwd_noalloc) uses, process-wide. All compute the
  * same result (up to rounding order); they differ in how the work is cut:
  *   ATTN_PATH_AUTO       fp16, d = 64, no window, L >= 512: the alternating mode below
- *                        when its units (B * Hq * ceil(L / 128)) number at most 16 per
+ *                        when its units (B * Hq * ceil(L / 128)) number at most 8 per
  *                        SM (causal) or one per SM (non-causal). Otherwise the
  *                        persistent two-tile kernel (256 query rows per work unit),
  *                        unless the problem has at most half as many such units as the

@@ -384,3 +384,79 @@ def test_alternating_mutants_are_caught(mutant):
             caught = True
             break
     assert caught, mutant
+
+
+def simulate_unit_queue(n_units, readers, seed, depth=4, mutant=None):
+    """The dynamic schedule's hand-over inside one CTA: the producer takes ranks from a
+    counter shared with other CTAs (here: a random number of ranks go elsewhere
+    between takes) and writes each into queue entry k mod depth (uq_full), after every
+    reader has released the entry's previous use (uq_empty); each reader waits for
+    entry k, copies it and releases it. A rank past the end is written as -1 and ends
+    everyone's loop. Readers must see the producer's ranks, in order, each once."""
+    rng = random.Random(seed)
+    full = [Bar(f"uq_full{i}", 1) for i in range(depth)]
+    empty = [Bar(f"uq_empty{i}", readers) for i in range(depth)]
+    q = [None] * depth
+    counter = [0]
+    taken = []
+    seen = {r: [] for r in range(readers)}
+
+    def producer():
+        k = 0
+        while True:
+            slot = k % depth
+            if k >= depth and mutant != "producer_skips_uq_empty":
+                yield wait(empty[slot], k // depth)
+            counter[0] += rng.randrange(0, 3)  # other CTAs' takes
+            r = counter[0]
+            counter[0] += 1
+            rank = r if r < n_units else -1
+            check(q[slot] is None or q[slot][1] == "read", f"entry {slot} overwritten before every reader read it")
+            q[slot] = (rank, "fresh", set())
+            full[slot].arrive()
+            if rank < 0:
+                return
+            taken.append(rank)
+            k += 1
+            yield STEP
+
+    def reader(i):
+        k = 0
+        while True:
+            slot = k % depth
+            yield wait(full[slot], k // depth + 1)
+            rank, _, who = q[slot]
+            who.add(i)
+            if len(who) == readers:
+                q[slot] = (rank, "read", who)
+            empty[slot].arrive()
+            if rank < 0:
+                return
+            seen[i].append(rank)
+            k += 1
+            yield STEP
+
+    agents = {"producer": producer()}
+    for i in range(readers):
+        agents[f"reader{i}"] = reader(i)
+    run(agents, [], rng)
+    for i in range(readers):
+        check(seen[i] == taken, f"reader {i} saw {seen[i]}, the producer took {taken}")
+    return True
+
+
+@pytest.mark.parametrize("n_units", [0, 1, 3, 9, 40])
+def test_unit_queue_hand_over(n_units):
+    for seed in range(200):
+        simulate_unit_queue(n_units, readers=10, seed=seed)
+
+
+def test_unit_queue_mutant_is_caught():
+    caught = False
+    for seed in range(400):
+        try:
+            simulate_unit_queue(20, readers=10, seed=seed, mutant="producer_skips_uq_empty")
+        except ProtocolError:
+            caught = True
+            break
+    assert caught
