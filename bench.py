@@ -17,7 +17,7 @@ no runnable code) on a bounded row sample of the same workload.
 
 The line also carries, outside the timed region, the rest of the length sweep and a
 ``decode`` object: the decode-shaped forward (one new query against 128k cached
-keys, split-KV plus merge) timed with CUDA events and reported against the measured
+keys, split-KV with the splits merged inside the kernel) timed with CUDA events and reported against the measured
 HBM bandwidth, since reading the KV cache is its bound ("What is memory-efficient
 attention for long context on 8x H100?", section 1).
 """
@@ -525,7 +525,7 @@ def ours_arm(args, world, rank, local):
               "note": "reported only; the roofline divides by MEASURED_PEAKS.json bf16_tflops"}
         torch.cuda.empty_cache()
 
-    # ---- decode-shaped forward (split-KV + merge): HBM-bound, one line per workload
+    # ---- decode-shaped forward (split-KV, merged in the kernel): HBM-bound, one line per workload
     decode = {}
     if not args.no_decode:
         for wd in (si.DECODE_GQA_B1_H32_KV8_D128, si.DECODE_B1_H4_D64):
@@ -573,7 +573,7 @@ def ours_arm(args, world, rank, local):
             decode[wd.name] = {"us": t * 1e3, "GB/s": gbs, "splits": splits,
                                "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
                                "algorithmic_bytes": wd.algorithmic_bytes(),
-                               "launches_per_call": 2 if splits > 1 else 1,
+                               "launches_per_call": 1,  # items of <= 32 rows: the kernel merges its splits
                                "timing": f"{per_rep} calls back to back between CUDA events, "
                                          "per-call mean (median of 6)",
                                "us_single_call": statistics.median(single) * 1e3}
@@ -620,7 +620,7 @@ def ours_arm(args, world, rank, local):
         decode[wd.name + "_paged16"] = {
             "us": t * 1e3, "GB/s": gbs, "splits": splits,
             "frac_of_hbm": gbs / float(peaks["hbm_gbs"]), "algorithmic_bytes": pbytes,
-            "launches_per_call": 2 if splits > 1 else 1,
+            "launches_per_call": 1,  # items of <= 32 rows: the kernel merges its splits
             "timing": f"{per_rep} calls back to back between CUDA events, per-call mean "
                       "(median of 6)",
             "layout": "K/V cache in 16-token pages, pages in shuffled order"}

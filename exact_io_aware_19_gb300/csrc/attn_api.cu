@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -260,11 +261,27 @@ int kv_auto_splits(const KvPlan& k, int sms) {
   return std::min(s, kKvMaxSplits);
 }
 
-size_t kv_workspace_bytes(int B, int Lq, int Hq, int d, int splits) {
+// The decode workspace: the status word, then (splits > 1) the partial LSEs, the
+// partial outputs and one merge ticket (8 bytes) per work item.
+size_t kv_lse_part_bytes(size_t rows, int splits) { return ((size_t)splits * rows * 4 + 255) / 256 * 256; }
+
+size_t kv_workspace_bytes(int B, int Lq, int Hq, int d, int splits, int items) {
   if (splits <= 1) return kWorkspaceBytes;
   const size_t rows = (size_t)B * Hq * Lq;
-  const size_t lse_bytes = ((size_t)splits * rows * 4 + 255) / 256 * 256;
-  return kWorkspaceBytes + lse_bytes + (size_t)splits * rows * d * 4;
+  const size_t ticket_bytes = ((size_t)items * 8 + 255) / 256 * 256;
+  return kWorkspaceBytes + kv_lse_part_bytes(rows, splits) + (size_t)splits * rows * d * 4 + ticket_bytes;
+}
+
+// The tag of a call's merge tickets (kept in bits 9 and up of a ticket word). Each call
+// takes the next value of a process-wide counter that starts from the wall clock in
+// microseconds, so a tag differs from those of earlier calls and, with all but
+// negligible probability, from whatever a fresh workspace holds.
+unsigned long long next_ticket_base() {
+  static std::atomic<unsigned long long> next{static_cast<unsigned long long>(
+      std::chrono::duration_cast<std::chrono::microseconds>(
+          std::chrono::system_clock::now().time_since_epoch()).count())};
+  const unsigned long long tag = next.fetch_add(1) & ((1ull << 55) - 1);
+  return tag << 9;
 }
 
 int current_sms(int* sms) {
@@ -322,7 +339,7 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
   if (!workspace) return fail(ATTN_ERR_WORKSPACE, "workspace must be non-null");
   if (!aligned(workspace, 16)) return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned");
   const KvPlan plan = kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left);
-  if (num_splits > 0 && workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, num_splits))
+  if (num_splits > 0 && workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, num_splits, plan.items))
     return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
 
   int dev = 0;
@@ -335,7 +352,7 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
                                           std::to_string(info.major) + "." +
                                           std::to_string(info.minor));
   const int splits = num_splits ? num_splits : kv_auto_splits(plan, info.sms);
-  if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits))
+  if (workspace_bytes < kv_workspace_bytes(B, Lq, Hq, d, splits, plan.items))
     return fail(ATTN_ERR_WORKSPACE, "workspace smaller than attn_fwd_kv_workspace_size()");
   if ((long long)plan.items * splits >= (1LL << 31))
     return fail(ATTN_ERR_INVALID_ARG, "too many work items");
@@ -372,8 +389,11 @@ attn_status_t kv_run(const void* q, const void* k, const void* v, void* o, float
   const size_t rows = (size_t)B * Hq * Lq;
   if (splits > 1) {
     char* base = static_cast<char*>(workspace) + kWorkspaceBytes;
+    const size_t lse_bytes = kv_lse_part_bytes(rows, splits);
     p.lse_part = reinterpret_cast<float*>(base);
-    p.o_part = reinterpret_cast<float*>(base + ((size_t)splits * rows * 4 + 255) / 256 * 256);
+    p.o_part = reinterpret_cast<float*>(base + lse_bytes);
+    p.tickets = reinterpret_cast<unsigned long long*>(base + lse_bytes + (size_t)splits * rows * d * 4);
+    p.ticket_base = next_ticket_base();
   }
   p.B = B;
   p.Lq = Lq;
@@ -926,7 +946,8 @@ size_t attn_fwd_kv_workspace_size(int B, int Lq, int Lk, int Hq, int Hkv, int d,
     num_splits = attn_fwd_kv_num_splits(B, Lq, Lk, Hq, Hkv, d, causal, window_left);
     if (num_splits == 0) return 0;
   }
-  return kv_workspace_bytes(B, Lq, Hq, d, num_splits);
+  return kv_workspace_bytes(B, Lq, Hq, d, num_splits,
+                            kv_plan(B, Lq, Lk, Hq, Hkv, causal, window_left).items);
 }
 
 attn_status_t attn_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,

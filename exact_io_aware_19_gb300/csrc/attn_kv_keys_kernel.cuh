@@ -32,6 +32,18 @@
 //   * Every wait is bounded; the four softmax warps leave the block loop together
 //     (an abort bit rides on the per-block vote), so the named barriers never wait
 //     for a warp that has left.
+//   * Key splits (splits > 1) of items of at most 8 rows are combined by their
+//     log-sum-exp inside this kernel, by whichever CTA of a work item stores its
+//     partial result last; no CTA waits for another (32-row items leave their
+//     partial results to the merge kernel). Each item has a 64-bit ticket in the workspace holding the call's
+//     tag (bits 9 and up, a new value per call) and a count (bits 0-8). At its start
+//     a CTA claims the ticket for this call (a compare-and-swap that replaces a word
+//     with another tag, whatever an earlier call or a fresh workspace left there, by
+//     tag << 9); after storing its partial O and LSE (and a fence) it adds 1. The CTA
+//     whose add returns splits - 1 reads every split's partial result back from L2,
+//     writes the item's O and LSE, and resets the count to 0 (so a graph replay with
+//     the same tag starts from a claimed, empty ticket). Every CTA adds exactly once,
+//     on error paths too.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,6 +67,7 @@ enum : uint32_t {
   kSiteKeysMmaKFull = 0xA0001, kSiteKeysMmaVFull = 0xA0002, kSiteKeysMmaPFull = 0xA0003,
   kSiteKeysMmaQFull = 0xA0005, kSiteKeysMmaDrain = 0xA0006,
   kSiteKeysSmxSFull = 0xB0001, kSiteKeysSmxPvDone = 0xB0003, kSiteKeysSmxOFull = 0xB0004,
+  kSiteKeysTicket = 0xB0005,
 };
 
 template <int D>
@@ -76,8 +89,9 @@ struct KeysGeometry {
   static constexpr int kOffBar = kOffQ + kChunks * kRowChunkBytes;
   // full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], o_full, drain
   static constexpr int kNumBars = 2 * kSlots + 9;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag, votes [2][4] bytes
-  static constexpr int kOffRed = kOffMisc + 16;            // [2][4 warps][32 rows] block maxima
+  // tmem base, abort flag, votes [2][4] bytes, the last-CTA flag of the merge
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffRed = kOffMisc + 32;            // [2][4 warps][32 rows] block maxima
   static constexpr int kOffLsum = kOffRed + 2 * 4 * kKeysRowsMax * 4;  // [4 warps][32 rows] sums
   static constexpr int kSmemUsed = kOffLsum + 4 * kKeysRowsMax * 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -95,6 +109,112 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The merge of a work item's key splits by the last of its CTAs (the 128 softmax
+// threads; every split's partial result is in L2). Row r of the item:
+// O = sum_s w_s O_s and LSE = m + log2(L) (base 2, stored as ln), with
+// w_s = 2^(lse_s - m) / L, L = sum_s 2^(lse_s - m), m = max_s lse_s ("What is
+// memory-efficient attention for long context on 8x H100?", section 4: attention in
+// parts, combined by the log-sum-exp). An empty split (lse = -inf, O = 0) has weight
+// 0; a row with no visible key gets O = 0 and LSE = -inf.
+// The item's output is cut into 16-byte quads (rows x D/4). With at most 128 quads,
+// `slots` = 128 / quads threads share a quad and take every slots-th split; each
+// thread loads all of its splits' LSEs and O quads at once (a reload from L2 costs
+// about a microsecond, so the merge is one round trip), folds them in with a running
+// maximum, and the slots of a quad meet in shared memory in slot order (the result
+// does not depend on which CTA merges). With more quads each thread takes quads
+// t, t + 128, ... alone. `scratch` holds 6 floats per (slot, quad).
+template <int D, bool BF16>
+__device__ __forceinline__ void keys_merge_splits(const KvParams& p, const KvItem& it, int rows,
+                                                  int t, float* scratch, int out_f32) {
+  constexpr int kQuads = D / 4;
+  constexpr int kPer = 24;  // splits of one thread in flight at once
+  const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  const int S = p.splits;
+  const int nq = rows * kQuads;
+  const int slots = (nq < 128) ? 128 / nq : 1;
+  for (int base = 0; base < nq; base += 128 / slots) {
+    const int qd = base + t % (128 / slots), slot = t / (128 / slots);
+    const bool live = qd < nq && slot < slots;
+    const int r = qd / kQuads, c4 = qd % kQuads;
+    const int qi = it.i0 + r / p.group;
+    const int h = it.g * p.group + r % p.group;
+    const size_t row = (static_cast<size_t>(it.b) * p.Hq + h) * p.Lq + qi;
+    float m = -INFINITY, l = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = slot; live && s0 < S; s0 += slots * kPer) {
+      float ls[kPer];
+      float4 ov[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int sp = s0 + u * slots;
+        ls[u] = -INFINITY;
+        ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (sp < S) {
+          ls[u] = __ldcg(p.lse_part + static_cast<size_t>(sp) * nrows + row);
+          ov[u] = __ldcg(reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(sp) * nrows + row) * D) + c4);
+        }
+      }
+      float mc = m;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) mc = fmaxf(mc, ls[u]);
+      if (mc != -INFINITY) {
+        const float f = exp2f(m - mc);  // 0 while m is -inf
+        l *= f;
+        a = make_float4(a.x * f, a.y * f, a.z * f, a.w * f);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const float w = exp2f(ls[u] - mc);  // 0 for an empty split
+          l += w;
+          a = make_float4(fmaf(w, ov[u].x, a.x), fmaf(w, ov[u].y, a.y), fmaf(w, ov[u].z, a.z),
+                          fmaf(w, ov[u].w, a.w));
+        }
+        m = mc;
+      }
+    }
+    if (slots > 1) {  // uniform: the slots of a quad meet in shared memory
+      float* mine = scratch + 6 * (slot * nq + qd);
+      if (live && slot > 0) {
+        mine[0] = m;
+        mine[1] = l;
+        mine[2] = a.x;
+        mine[3] = a.y;
+        mine[4] = a.z;
+        mine[5] = a.w;
+      }
+      named_barrier(1, 128);
+      if (live && slot == 0) {
+        for (int o = 1; o < slots; ++o) {
+          const float* q = scratch + 6 * (o * nq + qd);
+          const float mm = fmaxf(m, q[0]);
+          if (mm != -INFINITY) {
+            const float f1 = exp2f(m - mm), f2 = exp2f(q[0] - mm);
+            l = l * f1 + q[1] * f2;
+            a = make_float4(a.x * f1 + q[2] * f2, a.y * f1 + q[3] * f2, a.z * f1 + q[4] * f2,
+                            a.w * f1 + q[5] * f2);
+            m = mm;
+          }
+        }
+      }
+    }
+    if (live && slot == 0) {
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float o4[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+      const size_t oi = ((static_cast<size_t>(it.b) * p.Lq + qi) * p.Hq + h) * D + 4 * c4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (out_f32)
+          static_cast<float*>(p.o)[oi + j] = o4[j];
+        else if constexpr (BF16)
+          static_cast<__nv_bfloat16*>(p.o)[oi + j] = __float2bfloat16_rn(o4[j]);
+        else
+          static_cast<__half*>(p.o)[oi + j] = __float2half_rn(o4[j]);
+      }
+      if (c4 == 0 && p.lse != nullptr)
+        p.lse[row] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+}
+
 // NQ: the query rows a work item may have (1, 8 or 32; the products use N = max(NQ, 16)).
 template <int D, bool BF16, bool PAGED, int NQ>
 __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
@@ -107,6 +227,7 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
   constexpr int kN = NQ < 16 ? 16 : NQ;  // N of both products
   constexpr bool kSplitP = BF16;         // bf16 P as hi + lo operands
   constexpr float kThresh = 8.0f;        // log2 units of max growth before a rescale
+  constexpr bool kSelfMerge = NQ <= 8;   // key splits merged by the item's last CTA
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -168,6 +289,16 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
   const uint32_t tmem_base = *tmem_slot;
   const KvItem it = kv_item<PAGED>(p);
   const int nblocks = max(0, it.hi - it.lo);
+  volatile uint32_t* merge_flag = reinterpret_cast<volatile uint32_t*>(smem + G::kOffMisc + 16);
+  // items of at most 8 rows merge their splits here; 32-row items leave it to the
+  // merge kernel launched after this one
+  unsigned long long* ticket =
+      (kSelfMerge && p.splits > 1) ? p.tickets + blockIdx.x / p.splits : nullptr;
+  if (ticket != nullptr && threadIdx.x == 0) {
+    // claim the item's ticket for this call (the same thread adds to it at the end)
+    const unsigned long long w = __ldcg(ticket);
+    if ((w & ~511ull) != p.ticket_base) atomicCAS(ticket, w, p.ticket_base);
+  }
 
   WaitCtl wc;
   wc.abort_flag = abort_flag;
@@ -441,6 +572,28 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
           else if (p.lse != nullptr)
             p.lse[row] = (lt[c] > 0.f) ? lse2 * 0.69314718055994531f : -INFINITY;
         }
+      }
+    }
+    if (ticket != nullptr) {
+      // ---- the split merge: this CTA's partial result is stored; take a ticket
+      __threadfence();  // each thread's partial stores, before the add below
+      named_barrier(1, 128);
+      if (t == 0) {
+        const unsigned long long prev = atomicAdd(ticket, 1ull);
+        const unsigned long long n = prev & 511ull;  // CTAs of the item that added before
+        uint32_t last = 0u;
+        if ((prev & ~511ull) != p.ticket_base || n >= static_cast<unsigned long long>(p.splits)) {
+          record_error(wc, kStatusWorkspace, kSiteKeysTicket);  // another call shares the workspace
+        } else if (n + 1 == static_cast<unsigned long long>(p.splits)) {
+          last = 1u;
+          atomicExch(ticket, p.ticket_base);  // empty again, for a replay with this tag
+        }
+        *merge_flag = last;
+      }
+      named_barrier(1, 128);
+      if (*merge_flag != 0u) {  // uniform over the 128 threads (the merge has barriers)
+        __threadfence();  // the other CTAs' partial results, after their adds
+        keys_merge_splits<D, BF16>(p, it, rows, t, reinterpret_cast<float*>(smem + G::kOffKV), out_f32);
       }
     }
   }

@@ -33,8 +33,12 @@ cudaError_t launch_keys_one(bool out_f32, const KvLaunchArgs& a) {
   cfg.stream = a.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // With key splits, items of at most 8 rows merge them in the kernel (the last CTA
+  // of each item; the tickets must be in the workspace), so this is the call's only
+  // launch; 32-row items are merged by the merge kernel after it.
+  if (NQ <= 8 && a.p.splits > 1 && a.p.tickets == nullptr) return cudaErrorInvalidValue;
   e = cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_v, a.p, out_f32 ? 1 : 0);
-  if (e != cudaSuccess || a.p.splits <= 1) return e;
+  if (e != cudaSuccess || NQ <= 8 || a.p.splits <= 1) return e;
   return launch_kv_merge(D, BF16, out_f32, a);
 }
 

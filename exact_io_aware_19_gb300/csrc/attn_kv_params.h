@@ -12,6 +12,10 @@ struct KvParams {
   float* o_part;        // [splits, B*Hq*Lq, D] float32 partial outputs (splits > 1), else null
   float* lse_part;      // [splits, B*Hq*Lq] partial log2-sum-exp (splits > 1), else null
   const uint32_t* vmax; // [B, Hkv] largest finite |v| (bf16 bits) of the fp16 copy of V, or null
+  // Merge tickets of the keys-on-lanes kernel (splits > 1): one 64-bit word per work
+  // item, (call tag << 9) | CTAs of the item that have stored their partial result.
+  unsigned long long* tickets;
+  unsigned long long ticket_base;  // this call's tag << 9 (low 9 bits zero)
   int B, Lq, Lk, Hq, Hkv;
   int group;            // Hq / Hkv: query heads that read one K/V head
   int causal;           // 0 / 1

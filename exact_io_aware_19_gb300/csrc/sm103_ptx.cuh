@@ -14,7 +14,7 @@ namespace ex19 {
 // ---------------------------------------------------------------- status words
 // The device status word (in the caller's workspace): [0] = attn_status_t code of
 // the first error, [1] = where it happened (role << 16 | site), [2] = CTA, [3] = unit.
-enum : uint32_t { kStatusInvalidArg = 1, kStatusTimeout = 5 };  // attn_status_t codes
+enum : uint32_t { kStatusInvalidArg = 1, kStatusWorkspace = 3, kStatusTimeout = 5 };  // attn_status_t codes
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

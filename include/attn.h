@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 typedef enum {
     ATTN_OK = 0,
@@ -235,8 +235,14 @@ attn_status_t attn_fwd_noalloc(const void *q, const void *k, const void *v, void
  *   Hq / Hkv    at most 128 (the query heads of one K/V head share a 128-row tile)
  *   num_splits  0 = the library's choice (attn_fwd_kv_num_splits), else 1..256
  *   workspace   >= attn_fwd_kv_workspace_size(..., num_splits) bytes: a status word
- *               and, when splits > 1, the float32 partial results
- * Enqueues one kernel, plus a merge kernel when splits > 1, on `stream`.
+ *               and, when splits > 1, the float32 partial results and an 8-byte
+ *               merge ticket per work item. The tickets need no initialisation:
+ *               each call tags them with a value of its own (a fresh workspace is
+ *               fine, and so is one used before by any call of this library).
+ * Enqueues one kernel on `stream` when a work item has at most 8 query rows
+ * (Lq * Hq / Hkv <= 8, a decode step): with splits > 1 the last CTA of each work
+ * item to finish combines the splits' partial results itself. Larger items add a
+ * merge kernel when splits > 1.
  *
  * attn_fwd_kv_num_splits returns the split count attn_fwd_kv uses for num_splits
  * = 0 on the current device (0 for rejected sizes or no device);

@@ -89,7 +89,8 @@ def compare(q, k, v, dtype, causal, wl, scale, rows=None, label="", workspace=No
     return stats
 
 
-def compare_kv(q, k, v, dtype, causal, wl, scale, num_splits=0, rows=None, label=""):
+def compare_kv(q, k, v, dtype, causal, wl, scale, num_splits=0, rows=None, label="",
+               workspace=None):
     """Decode-shaped parity: attn_fwd_kv (float32 and in-dtype output) against the
     oracle's decode rows, with the tolerances above. Returns error statistics."""
     import exact_io_aware_19_gb300 as ex
@@ -101,10 +102,10 @@ def compare_kv(q, k, v, dtype, causal, wl, scale, num_splits=0, rows=None, label
                                       wl, scale, rows)
     qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
     o32, lse = ex.attn_fwd_kv(qc, kc, vc, causal=causal, window_left=wl, scale=scale,
-                              out_fp32=True, num_splits=num_splits)
+                              out_fp32=True, num_splits=num_splits, workspace=workspace)
     o16, lse16 = ex.attn_fwd_kv(qc, kc, vc, causal=causal, window_left=wl, scale=scale,
-                                out_fp32=False, num_splits=num_splits)
-    ex.sync_status()
+                                out_fp32=False, num_splits=num_splits, workspace=workspace)
+    ex.sync_status(workspace)
     g32, glse = gather_rows(o32, lse, rows)
     g16, _ = gather_rows(o16, lse16, rows)
     assert np.isfinite(g32).all() and np.isfinite(glse).all(), f"{label}: non-finite output"

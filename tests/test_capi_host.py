@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(ex.library_path())
     missing = [n for n in declared_functions() if not hasattr(raw, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert lib.attn_abi_version() == 4
+    assert lib.attn_abi_version() == 5
 
 
 def test_status_strings(lib):
@@ -172,8 +172,15 @@ def test_kv_workspace_size(lib):
     # one split: the status word only
     assert lib.attn_fwd_kv_workspace_size(1, 1, 131072, 32, 8, 128, 1, -1, 1) == 256
     # four splits of 32 rows of d = 128: status + LSE parts (512 B, 256-aligned) + O parts
+    # + one 8-byte merge ticket per work item (8 items: 256 B after alignment)
     assert lib.attn_fwd_kv_workspace_size(1, 1, 131072, 32, 8, 128, 1, -1, 4) == \
-        256 + 512 + 4 * 32 * 128 * 4
+        256 + 512 + 4 * 32 * 128 * 4 + 256
+    # 3 x 4 items of 5 rows, 7 splits: LSE parts 7 * 60 * 4 = 1680 -> 1792
+    assert lib.attn_fwd_kv_workspace_size(3, 5, 4096, 4, 4, 64, 1, -1, 7) == \
+        256 + 1792 + 7 * 60 * 64 * 4 + 256
+    # 640 one-row items, 2 splits: 5120 B of tickets
+    assert lib.attn_fwd_kv_workspace_size(40, 1, 4096, 16, 16, 64, 1, -1, 2) == \
+        256 + 5120 + 2 * 640 * 64 * 4 + 5120
     for bad in [(1, 0, 16, 4, 4, 64, 1, -1, 1), (1, 17, 16, 4, 4, 64, 1, -1, 1),
                 (1, 1, 16, 4, 4, 96, 1, -1, 1), (1, 1, 16, 256, 1, 64, 1, -1, 1),
                 (1, 1, 16, 4, 4, 64, 0, 3, 1), (1, 1, 16, 4, 4, 64, 1, -1, -1),

@@ -49,6 +49,32 @@ def test_more_splits_than_key_blocks():
         compare_kv(q, k, v, "bf16", True, -1, 0.09, num_splits=splits, label=f"splits={splits}")
 
 
+def test_split_merge_on_an_uninitialised_workspace():
+    """Decode items (at most 32 rows) merge their key splits inside the kernel, by the
+    last CTA of each item, counted on a ticket per item in the workspace. The tickets
+    need no initialisation: a workspace of random bytes (status word zeroed) gives
+    oracle parity on its first and later calls, and each call leaves every ticket as
+    its tag << 9 (a zero count, one tag for all items)."""
+    import exact_io_aware_19_gb300 as ex
+    for hq, hkv, d, dtype in ((4, 4, 64, "fp16"), (32, 8, 128, "bf16"), (8, 2, 64, "bf16")):
+        q, k, v = si.random_qkv_decode(1, 1, 4096, hq, hkv, d, dtype=dtype, seed=hq + d)
+        for splits in (2, 7, 32):
+            n = ex.kv_workspace_size(1, 1, 4096, hq, hkv, d, True, -1, splits)
+            g = torch.Generator().manual_seed(splits * 100 + d)
+            ws = torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8)
+            ws[:16] = 0  # the status word
+            ws = ws.cuda()
+            for rep in range(2):
+                compare_kv(q, k, v, dtype, True, -1, 1 / math.sqrt(d), num_splits=splits,
+                           workspace=ws, label=f"heads={hq}/{hkv} d={d} splits={splits} call {rep}")
+            rows = hq  # B * Hq * Lq
+            lse_bytes = (splits * rows * 4 + 255) // 256 * 256
+            off = 256 + lse_bytes + splits * rows * d * 4
+            tickets = ws[off:off + 8 * hkv].cpu().numpy().view(np.uint64)
+            assert (tickets & np.uint64(511) == 0).all(), tickets
+            assert len(set(tickets.tolist())) == 1 and tickets[0] != 0, tickets
+
+
 def test_many_row_tiles():
     """Lq spanning several 128-row tiles (group 1: 128 queries per tile; group 4: 32)."""
     for hq, hkv in [(2, 2), (8, 2)]:
