@@ -282,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
   }
+  // A programmatic dependent launch: the prologue above touches only shared memory;
+  // the previous kernel's writes are visible past this point, and TMEM is allocated
+  // only after it (a kernel before this one may still hold TMEM on this SM).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();

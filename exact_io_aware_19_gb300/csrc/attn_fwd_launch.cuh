@@ -22,8 +22,20 @@ cudaError_t launch_fwd_one(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<a.grid, kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, a.p);
-  return cudaGetLastError();
+  // A programmatic dependent launch (as the decode kernels): the kernel may start its
+  // prologue while the previous kernel on the stream finishes, and waits for it
+  // (griddepcontrol.wait) before touching global memory or TMEM.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = a.grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_v, a.p);
 }
 
 }  // namespace ex19

@@ -31,8 +31,8 @@
  * wait that ran out) are recorded in the workspace status word and reported by
  * attn_fwd_sync_status.
  *
- * Launch order. The decode-shaped, FP8 and backward calls launch their kernels as
- * programmatic dependents (programmatic stream serialization): a kernel may begin
+ * Launch order. Every call launches its attention kernels as programmatic
+ * dependents (programmatic stream serialization): a kernel may begin
  * its prologue (barrier setup, tensor-map prefetch) while the previous kernel on the
  * stream finishes, and waits for that kernel's completion and memory
  * (griddepcontrol.wait) before it allocates tensor memory or touches global memory.
