@@ -64,6 +64,7 @@ TRAFFIC_BY_SOURCE = {
     "7b8d7e8882791981": 882_185_472 + 120_702_720,  # + the bf16 fp16-copy-of-V instantiations
     "1b6bfdd889851ddf": 884_794_880 + 119_256_576,  # + the alternating mode (barriers, exchange)
     "244f03d03a58a5d8": 911_313_920 + 117_537_280,  # dynamic unit scheduling (unit queue)
+    "e53bbaffdccf3333": 901_356_032 + 115_490_304,  # programmatic dependent launch
 }
 
 

@@ -62,6 +62,7 @@ constexpr int kKeysThreads = 192;  // 4 softmax warps + producer + MMA
 constexpr int kKeysProducerWarp = 4;
 constexpr int kKeysMmaWarp = 5;
 constexpr uint32_t kKeysTmemCols = 128;  // S^T buffers [0, 32) and [32, 64), O^T [64, 96)
+constexpr int kKeysPrefetchBlocks = 4;    // key blocks brought into L2 before the grid wait
 
 enum : uint32_t {
   kSiteKeysMmaKFull = 0xA0001, kSiteKeysMmaVFull = 0xA0002, kSiteKeysMmaPFull = 0xA0003,
@@ -275,6 +276,19 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if constexpr (!PAGED) {
+      // The first blocks of this CTA's keys, into L2 while the kernel before this one
+      // ends (each CTA of the previous decode call lets this grid start once its
+      // block loop is done). A prefetch is only a hint: what the loads read after
+      // griddepcontrol.wait below is the memory as that kernel left it, since its
+      // writes reach L2 too. The work item of a dense cache needs no global read.
+      const KvItem it0 = kv_item<false>(p);
+      for (int j = it0.lo; j < min(it0.hi, it0.lo + kKeysPrefetchBlocks); ++j)
+        for (int c = 0; c < D / 64; ++c) {
+          tma_prefetch_l2_4d(&tm_k, c * 64, it0.g, j * kBN, it0.b);
+          tma_prefetch_l2_4d(&tm_v, c * 64, it0.g, j * kBN, it0.b);
+        }
+    }
   }
   // A programmatic dependent launch: the previous kernel's writes are visible past
   // this point; TMEM is allocated only after it (as in the one-tile kernel).
@@ -529,6 +543,10 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
       ok = mbar_wait_warp(bar_o_full, 0, wc, kSiteKeysSmxOFull);
       if (ok) tc_fence_after();
     }
+    // This CTA has read all of its keys: the next kernel on the stream may start (its
+    // CTAs still wait for this grid's end before touching global memory or TMEM).
+    // Not when a merge kernel follows (it measured slower launched early).
+    if constexpr (kSelfMerge) asm volatile("griddepcontrol.launch_dependents;");
     named_barrier(1, 128);
     if (ok) {
       float lt[NQ];
