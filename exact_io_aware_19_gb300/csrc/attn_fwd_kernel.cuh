@@ -82,6 +82,7 @@ enum : uint32_t {
 };
 
 constexpr int kUnitQueue = 4;  // dynamic scheduling: unit ranks in flight between the roles
+constexpr int kPrefetchBlocks = 4;  // key blocks of the first unit brought into L2 before the grid wait
 constexpr int kUnitReaders = 2 + 8;  // the MMA warps and the softmax warps read each entry
 
 template <int D>
@@ -281,6 +282,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    Unit u0;
+    if (p.sched == nullptr && unit_of<ALT>(p, 0, u0)) {
+      // With the static deal the first unit is known here: its Q tiles and first key
+      // blocks go to L2 while the kernel before this one ends (the previous call's
+      // CTAs let this grid start once their loads are issued). A prefetch is only a
+      // hint; the loads after griddepcontrol.wait read what that kernel left.
+      for (int t = 0; t < kTilesPerUnit; ++t)
+        if (u0.t[t].lo < u0.t[t].hi)
+          for (int c = 0; c < G::kChunks; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, u0.h, u0.t[t].row0, u0.b);
+      for (int j = u0.lo; j < min(u0.hi, u0.lo + kPrefetchBlocks); ++j)
+        for (int c = 0; c < G::kChunks; ++c) {
+          tma_prefetch_l2_4d(&tm_k, c * 64, u0.g, j * kBN, u0.b);
+          tma_prefetch_l2_4d(&tm_v, c * 64, u0.g, j * kBN, u0.b);
+        }
+    }
   }
   // A programmatic dependent launch: the prologue above touches only shared memory;
   // the previous kernel's writes are visible past this point, and TMEM is allocated
@@ -372,6 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Every load of this CTA is issued: the next kernel on the stream may start (its
+      // CTAs still wait for this grid's end before touching global memory or TMEM).
+      asm volatile("griddepcontrol.launch_dependents;");
       // Whether or not this CTA aborted, the copies issued last may still be in
       // flight (another role can abort after this loop has ended, and then nothing
       // consumes them): let them land before the CTA can exit.
