@@ -65,6 +65,7 @@ TRAFFIC_BY_SOURCE = {
     "1b6bfdd889851ddf": 884_794_880 + 119_256_576,  # + the alternating mode (barriers, exchange)
     "244f03d03a58a5d8": 911_313_920 + 117_537_280,  # dynamic unit scheduling (unit queue)
     "e53bbaffdccf3333": 901_356_032 + 115_490_304,  # programmatic dependent launch
+    "19bf902c5ff94d12": 907_726_080 + 117_001_472,  # + L2 prefetch before the grid wait, early trigger
 }
 
 
