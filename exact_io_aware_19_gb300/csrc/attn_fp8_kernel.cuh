@@ -89,10 +89,9 @@ struct Fp8Geometry {
 
 // Two e4m3 values (low byte: the pair's first element) of a packed fp16 pair.
 __device__ __forceinline__ uint32_t e4m3x2_of_half2(uint32_t h2) {
-  __half2_raw r;
-  r.x = static_cast<unsigned short>(h2 & 0xFFFFu);
-  r.y = static_cast<unsigned short>(h2 >> 16);
-  return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return static_cast<uint32_t>(r);
 }
 
 template <bool OUT_F32>
