@@ -240,7 +240,10 @@ attn_status_t attn_fwd_noalloc(const void *q, const void *k, const void *v, void
  *               and, when splits > 1, the float32 partial results and an 8-byte
  *               merge ticket per work item. The tickets need no initialisation:
  *               each call tags them with a value of its own (a fresh workspace is
- *               fine, and so is one used before by any call of this library).
+ *               fine, and so is one used before by any call of this library). A
+ *               ticket found carrying another call's tag at the merge (two calls
+ *               running at once on one workspace) is recorded in the status word as
+ *               ATTN_ERR_WORKSPACE.
  * Enqueues one kernel on `stream` when a work item has at most 8 query rows
  * (Lq * Hq / Hkv <= 8, a decode step): with splits > 1 the last CTA of each work
  * item to finish combines the splits' partial results itself. Larger items add a
