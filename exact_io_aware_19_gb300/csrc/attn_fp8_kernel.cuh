@@ -18,7 +18,7 @@
 // the O rescale scales it together with O.
 //
 // GB300 mapping (one CTA per 128-row tile, two CTAs per SM so that one CTA's
-// softmax fills the other's waits; 256 TMEM columns and ~101 KiB of shared memory
+// softmax fills the other's waits; 256 TMEM columns and ~69 KiB of shared memory
 // each):
 //   * Q and K tiles: TMA boxes of 64 bytes (64 e4m3) per row, 64-byte swizzle.
 //   * V is read as Vᵀ (keys contiguous), written by attn_fp8_transpose_v into the
@@ -27,10 +27,11 @@
 //   * warp 4 (producer) streams K_j and Vᵀ_j into a ring of 10 KiB slots; warp 5
 //     (MMA) issues S(j) into the TMEM S buffer, S(j + 1) as soon as the softmax
 //     has read S(j) into registers (s_free), then O += P(j) Vᵀ(j) with P read
-//     from shared memory buffer j mod 2.
-//   * warps 0-3 (softmax): one thread per row; P' is converted to e4m3 and stored
-//     in the 128-byte-swizzle layout (16-byte chunk c of row r at chunk c ^ (r % 8)),
-//     then made visible to the tensor core (fence.proxy.async) before p_full.
+//     from TMEM (the A operand of a TS MMA: 8 columns of 4 e4m3 per K = 32).
+//   * warps 0-3 (softmax): one thread per row; P' is converted to e4m3, packed four
+//     keys to a 32-bit word and stored to the row's TMEM lane (32 columns) once the
+//     P·V of the previous block, which read the one P' buffer, is done (pv_done;
+//     s_full does not imply it, since S(j) is issued before P·V(j - 1)).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,9 +56,10 @@ constexpr int kThreads = 192;        // 4 softmax warps + producer warp + MMA wa
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kON = 80;              // P·V columns: O (64) and the normaliser (16 copies)
-constexpr uint32_t kTmemCols = 256;  // S [0,128), O and l' [128, 208)
+constexpr uint32_t kTmemCols = 256;  // S [0,128), O and l' [128, 208), P' [224, 256)
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 224;      // P' of a block: 128 e4m3 per row, 4 per 32-bit column
 constexpr int kPOffset = 7;          // P' = 2^(x - m + 7): at most 2^8 with the rescale threshold 1
 
 enum : uint32_t {
@@ -75,11 +77,9 @@ struct Fp8Geometry {
   static constexpr int kOnesBytes = (kON - kD) * 128;  // rows of ones after Vᵀ_j
   static constexpr int kSlotBytes = kTileBytes + kOnesBytes;  // 10 KiB, 1 KiB aligned
   static constexpr int kSlots = 6;                // even: K_j in even slots, Vᵀ_j in odd
-  static constexpr int kPBytes = kBM * kBN;       // 16 KiB: 128 rows x 128 bytes
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 8192;
-  static constexpr int kOffP = kOffKV + kSlots * kSlotBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffKV + kSlots * kSlotBytes;
   // barriers: full[S], empty[S], q_full, s_full, s_free, p_full[2], pv_done[2], o_full, drain
   static constexpr int kNumBars = 2 * kSlots + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -109,7 +109,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + G::kOffQ;
   const uint32_t sKV = sbase + G::kOffKV;
-  const uint32_t sP = sbase + G::kOffP;
   const uint32_t bars = sbase + G::kOffBar;
   auto bar_full = [&](uint32_t s) { return bars + 8u * s; };
   auto bar_empty = [&](uint32_t s) { return bars + 8u * (S + s); };
@@ -230,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint64_t dq = sdesc_swizzled(sQ, 16, 512, 4);      // 64-byte rows, 64-byte swizzle
       const uint64_t dk = sdesc_swizzled(sKV, 16, 512, 4);
       const uint64_t dvt = sdesc_swizzled(sKV, 16, 1024, 2);   // 128-byte rows, 128-byte swizzle
-      const uint64_t dp = sdesc_swizzled(sP, 16, 1024, 2);
       const uint32_t mO = tmem_base + kColO;
       auto slot_of = [&](uint32_t idx) { return idx % S; };
       auto par_of = [&](uint32_t idx) { return (idx / S) & 1u; };
@@ -248,18 +246,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_commit_elect(bar_empty(slot_of(kidx)));
         return true;
       };
-      // [O | l'] (+)= P(jj) · [V_j | 1] with P from shared-memory buffer jj & 1 and
-      // Vᵀ_j and the ones from its slot (four MMAs of K = 32 keys); releases Vᵀ_j.
+      // [O | l'] (+)= P(jj) · [V_j | 1] with P from TMEM (8 columns per MMA of K = 32
+      // keys) and Vᵀ_j and the ones from its slot (four MMAs); releases Vᵀ_j.
       auto issue_pv = [&](int jj) __attribute__((always_inline)) -> bool {
         const uint32_t vidx = 2u * jj + 1u;
         if (!mbar_wait_warp(bar_full(slot_of(vidx)), par_of(vidx), wc, kSiteMmaVFull)) return false;
         if (!mbar_wait_warp(bar_p_full(jj & 1), (jj >> 1) & 1u, wc, kSiteMmaPFull)) return false;
         tc_fence_after();
-        const uint64_t dps = dp + (((jj & 1) * G::kPBytes) >> 4);
         const uint64_t dvs = dvt + ((slot_of(vidx) * G::kSlotBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 32; ++kk)
-          mma_ss_f8_elect(mO, dps + (kk * 32 >> 4), dvs + (kk * 32 >> 4), idesc_o,
+          mma_ts_f8_elect(mO, tmem_base + kColP + 8 * kk, dvs + (kk * 32 >> 4), idesc_o,
                           (jj == 0 && kk == 0) ? 0u : 1u);
         mma_commit_elect(bar_pv_done(jj & 1));
         mma_commit_elect(bar_empty(slot_of(vidx)));
@@ -347,24 +344,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         // x - m + 7 with the reference max of this block
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
         const float nmu = static_cast<float>(kPOffset) - mu;
-        // P buffer `buf` was read by P·V(jj - 2): wait until that MMA is done.
-        if (jj >= 2) {
-          if (!mbar_wait_warp(bar_pv_done(buf), ((jj - 2) >> 1) & 1u, wc, kSiteSmxPvDone)) {
+        // The one P' buffer was read by P·V(jj - 1) (issued after S(jj), so s_full
+        // does not cover it): wait until that MMA is done before storing P'(jj).
+        if (jj >= 1) {
+          if (!mbar_wait_warp(bar_pv_done((jj - 1) & 1), ((jj - 1) >> 1) & 1u, wc, kSiteSmxPvDone)) {
             stop = true;
             return;
           }
           tc_fence_after();
         }
-        const uint32_t prow = sP + buf * G::kPBytes + rho * 128;
+        // P' of the row to its TMEM lane: key k in byte k mod 4 of column k / 4, stored
+        // 32 keys (8 columns) at a time so that few words are live at once.
 #pragma unroll
-        for (int q16 = 0; q16 < 8; ++q16) {  // 16 keys = one 16-byte chunk of the row
-          uint32_t w[4];
+        for (int q32 = 0; q32 < 4; ++q32) {
+          uint32_t w[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {  // 4 keys per 32-bit word
+          for (int u = 0; u < 8; ++u) {  // 4 keys per 32-bit word
             uint32_t e2[2];
 #pragma unroll
             for (int v2 = 0; v2 < 2; ++v2) {
-              const int c = q16 * 16 + u * 4 + v2 * 2;
+              const int c = q32 * 32 + u * 4 + v2 * 2;
               const float2 xx = __ffma2_rn(
                   make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
                   make_float2(Cs, Cs), make_float2(nmu, nmu));
@@ -379,12 +378,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             w[u] = e2[0] | (e2[1] << 16);
           }
-          const uint32_t addr = prow + ((q16 ^ (rho & 7)) << 4);  // 128-byte swizzle
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
-                       "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
+          tmem_st_x8(tmem_base + lane_off + kColP + 8 * q32, w);
         }
-        fence_proxy_async_shared();  // P is read by the tensor core (async proxy)
+        tmem_st_wait();
       };
       block_body(masked_tag);
       if (stop) return false;

@@ -1,14 +1,13 @@
 """Host-side model of the float8 kernel's barrier protocol (no GPU).
 
 attn_fp8_sm103_kernel keeps one S buffer in TMEM (the next S is issued once the
-softmax holds the current one in registers: s_free) and two P buffers in shared
-memory (P(j) goes to buffer j mod 2 once the P·V of block j - 2 has read it). The
-model replays the producer, the MMA warp (in-order MMAs, commits after them), the
-copies landing in any order and the softmax, and checks for deadlock, parity
-aliasing and stale data; mutants with one wait removed must be caught. The
-softmax's wait for the P·V of block j - 2 before it writes P(j) is not among them:
-the model shows it is implied, since S(j) is issued after that P·V and its commit
-(s_full) arrives only once every earlier MMA has run.
+softmax holds the current one in registers: s_free) and one P' buffer in TMEM, the A
+operand of the P·V MMA (P(j) is stored once the P·V of block j - 1 has read it:
+pv_done). The model replays the producer, the MMA warp (in-order MMAs, commits after
+them), the copies landing in any order and the softmax, and checks for deadlock,
+parity aliasing and stale data; mutants with one wait removed must be caught,
+including the softmax's wait for P·V(j - 1): S(j) is issued before that P·V, so its
+commit (s_full) does not cover it.
 """
 import pytest
 
@@ -29,7 +28,7 @@ def simulate_fp8(nb, slots, seed, rescale_p=0.3, mutant=None):
     q_in = [False]
     sbuf = [None]
     s_read = set()
-    pbuf = [None, None]
+    pbuf = [None]
     o = {"done": 0, "inflight": 0}
 
     def land(cp):
@@ -51,7 +50,7 @@ def simulate_fp8(nb, slots, seed, rescale_p=0.3, mutant=None):
             read.add(2 * jj)
         else:
             check(slot_gen[(2 * jj + 1) % slots] == 2 * jj + 1, f"P·V({jj}) reads the wrong Vᵀ")
-            check(pbuf[jj & 1] == jj, f"P·V({jj}) reads P of block {pbuf[jj & 1]}")
+            check(pbuf[0] == jj, f"P·V({jj}) reads P of block {pbuf[0]}")
             check(o["done"] == jj, f"P·V({jj}) onto O holding {o['done']} products")
             o["done"] += 1
             o["inflight"] -= 1
@@ -106,10 +105,10 @@ def simulate_fp8(nb, slots, seed, rescale_p=0.3, mutant=None):
             s_read.add(jj)
             s_free.arrive()
             yield STEP
-            if jj >= 2 and mutant != "softmax_skips_pv_done":
-                yield wait(pv_done[jj & 1], ((jj - 2) >> 1) + 1)
-            check(jj < 2 or o["done"] >= jj - 1, f"P({jj}) overwrites P({jj - 2}) before its P·V ran")
-            pbuf[jj & 1] = jj
+            if jj >= 1 and mutant != "softmax_skips_pv_done":
+                yield wait(pv_done[(jj - 1) & 1], ((jj - 1) >> 1) + 1)
+            check(jj < 1 or o["done"] >= jj, f"P({jj}) overwrites P({jj - 1}) before its P·V ran")
+            pbuf[0] = jj
             yield STEP
             if jj > 0 and rng.random() < rescale_p:
                 yield wait(pv_done[(jj - 1) & 1], ((jj - 1) >> 1) + 1)
@@ -130,7 +129,8 @@ def test_fp8_protocol(nb, slots):
         simulate_fp8(nb, slots, seed)
 
 
-@pytest.mark.parametrize("mutant", ["producer_skips_empty", "mma_skips_p_full", "mma_skips_s_free"])
+@pytest.mark.parametrize("mutant", ["producer_skips_empty", "mma_skips_p_full", "mma_skips_s_free",
+                                    "softmax_skips_pv_done"])
 def test_fp8_mutants_are_caught(mutant):
     """A removed wait that matters shows up as a protocol violation."""
     found = False
@@ -141,9 +141,3 @@ def test_fp8_mutants_are_caught(mutant):
             found = True
             break
     assert found, mutant
-
-
-def test_fp8_pv_done_before_p_is_implied():
-    """Without the softmax's P·V(j - 2) wait no schedule breaks the protocol."""
-    for seed in range(400):
-        simulate_fp8(6, 6, seed, mutant="softmax_skips_pv_done")
