@@ -119,16 +119,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 // 0; a row with no visible key gets O = 0 and LSE = -inf.
 // The item's output is cut into 16-byte quads (rows x D/4). With at most 128 quads,
 // `slots` = 128 / quads threads share a quad and take every slots-th split; each
-// thread loads all of its splits' LSEs and O quads at once (a reload from L2 costs
-// about a microsecond, so the merge is one round trip), folds them in with a running
-// maximum, and the slots of a quad meet in shared memory in slot order (the result
-// does not depend on which CTA merges). With more quads each thread takes quads
+// thread loads up to kPer of its splits' LSEs and O quads at once (a reload from L2
+// costs about a microsecond, so a merge of a call's splits is one or two round
+// trips), folds them in with a running maximum, and the slots of a quad meet in
+// shared memory in slot order (the result does not depend on which CTA merges). With more quads each thread takes quads
 // t, t + 128, ... alone. `scratch` holds 6 floats per (slot, quad).
-template <int D, bool BF16>
+template <int D, bool BF16, int kPer>
 __device__ __forceinline__ void keys_merge_splits(const KvParams& p, const KvItem& it, int rows,
                                                   int t, float* scratch, int out_f32) {
   constexpr int kQuads = D / 4;
-  constexpr int kPer = 24;  // splits of one thread in flight at once
   const size_t nrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
   const int S = p.splits;
   const int nq = rows * kQuads;
@@ -611,7 +610,11 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
       named_barrier(1, 128);
       if (*merge_flag != 0u) {  // uniform over the 128 threads (the merge has barriers)
         __threadfence();  // the other CTAs' partial results, after their adds
-        keys_merge_splits<D, BF16>(p, it, rows, t, reinterpret_cast<float*>(smem + G::kOffKV), out_f32);
+        // kPer: splits of one thread in flight at once. A one-row item shares each
+        // column quad among 128 / (D / 4) threads (8 at d = 64: 64 splits in one round
+        // trip with 8 each), and the smaller body is fetched faster (the merge code
+        // runs cold: once per call, on one CTA).
+        keys_merge_splits<D, BF16, (NQ == 1 ? 8 : 24)>(p, it, rows, t, reinterpret_cast<float*>(smem + G::kOffKV), out_f32);
       }
     }
   }
