@@ -87,10 +87,10 @@ struct Fp8Geometry {
   static constexpr int kSmemBytes = kSmemUsed + 1024;
 };
 
-// Two e4m3 values (low byte: the pair's first element) of a packed fp16 pair.
-__device__ __forceinline__ uint32_t e4m3x2_of_half2(uint32_t h2) {
+// Two e4m3 values of two fp32 weights (low byte: the first), rounded to nearest.
+__device__ __forceinline__ uint32_t e4m3x2_of_f32(float first, float second) {
   unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
   return static_cast<uint32_t>(r);
 }
 
@@ -101,7 +101,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                           const __grid_constant__ CUtensorMap tm_vt, const KvParams p) {
   using G = Fp8Geometry;
   constexpr int S = G::kSlots;
-  constexpr float kThresh = 1.0f;  // fp16 exponent arguments: move the reference max by > 2^1
+  // move the reference max when a score exceeds it by more than 2^1: P' stays at most
+  // 2^(1 + kPOffset) = 256, inside e4m3's range (448)
+  constexpr float kThresh = 1.0f;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -367,14 +369,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               const float2 xx = __ffma2_rn(
                   make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
                   make_float2(Cs, Cs), make_float2(nmu, nmu));
-              __half2 xh = __floats2half2_rn(xx.x, xx.y);
-              uint32_t pp = ex2_f16x2(*reinterpret_cast<uint32_t*>(&xh));
-              if constexpr (M) {
-                const uint32_t keep = ((c >= vis_lo && c < vis_hi) ? 0x0000FFFFu : 0u) |
-                                      ((c + 1 >= vis_lo && c + 1 < vis_hi) ? 0xFFFF0000u : 0u);
-                pp &= keep;
+              // fp32 exponentials and one conversion per pair (converting the
+              // arguments to fp16 pairs for a packed exponential measured slower: a
+              // second conversion on the ALU pipe, the busiest one here)
+              float p0 = ex2_approx(xx.x), p1 = ex2_approx(xx.y);
+              if constexpr (M) {  // masked keys get exactly 0
+                p0 = (c >= vis_lo && c < vis_hi) ? p0 : 0.f;
+                p1 = (c + 1 >= vis_lo && c + 1 < vis_hi) ? p1 : 0.f;
               }
-              e2[v2] = e4m3x2_of_half2(pp);
+              e2[v2] = e4m3x2_of_f32(p0, p1);
             }
             w[u] = e2[0] | (e2[1] << 16);
           }
