@@ -190,6 +190,21 @@ __device__ __forceinline__ KvItem kv_item(const KvParams& p) {
   return it;
 }
 
+// Asks for the first `nblk` key blocks of a dense-cache work item (K and V) in L2,
+// before griddepcontrol.wait: a prefetch is only a hint, so the loads after the wait
+// still read what the kernels before this one left (their stores reach L2 as well).
+// The work item of a dense cache needs no global read.
+template <int D>
+__device__ __forceinline__ void kv_prefetch_first_blocks(const KvParams& p, const CUtensorMap* tm_k,
+                                                         const CUtensorMap* tm_v, int nblk) {
+  const KvItem it0 = kv_item<false>(p);
+  for (int j = it0.lo; j < min(it0.hi, it0.lo + nblk); ++j)
+    for (int c = 0; c < D / 64; ++c) {
+      tma_prefetch_l2_4d(tm_k, c * 64, it0.g, j * kBN, it0.b);
+      tma_prefetch_l2_4d(tm_v, c * 64, it0.g, j * kBN, it0.b);
+    }
+}
+
 // The TMA producer warp of the one-tile kernels: the Q tile of the work item, then K_j
 // and V_j of its blocks [it.lo, it.hi) into a ring of S slots of 128 keys × D (slot s
 // at sKV + s·128·D·2; its full barrier at bars + 8s, its empty barrier at bars +
@@ -355,6 +370,7 @@ __global__ void __launch_bounds__(KvRoles::kThreads, 1)
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if constexpr (!PAGED && !kSplitP) kv_prefetch_first_blocks<D>(p, &tm_k, &tm_v, 4);
   }
   // Launched as a programmatic dependent: past this point the previous kernel's
   // writes (Q, K, V, the page table, a merge still reading this workspace) are
@@ -387,6 +403,10 @@ __global__ void __launch_bounds__(KvRoles::kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     kv_produce<PAGED, D>(p, it, nblocks, &tm_q, &tm_k, &tm_v, sQ, G::kChunkBytes, sKV, S, bars, wc,
                          lane);
+    // Every load of this CTA has landed: the next kernel on the stream may start (its
+    // CTAs still wait for this grid's end before touching global memory or TMEM).
+    // Not when a merge kernel follows (it measured slower launched early).
+    if (p.splits <= 1 && lane == 0) asm volatile("griddepcontrol.launch_dependents;");
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (nblocks > 0) {

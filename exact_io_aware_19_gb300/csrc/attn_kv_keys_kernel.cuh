@@ -275,19 +275,10 @@ __global__ void __launch_bounds__(kKeysThreads, KeysGeometry<D>::kCtasPerSm)
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
-    if constexpr (!PAGED) {
-      // The first blocks of this CTA's keys, into L2 while the kernel before this one
-      // ends (each CTA of the previous decode call lets this grid start once its
-      // block loop is done). A prefetch is only a hint: what the loads read after
-      // griddepcontrol.wait below is the memory as that kernel left it, since its
-      // writes reach L2 too. The work item of a dense cache needs no global read.
-      const KvItem it0 = kv_item<false>(p);
-      for (int j = it0.lo; j < min(it0.hi, it0.lo + kKeysPrefetchBlocks); ++j)
-        for (int c = 0; c < D / 64; ++c) {
-          tma_prefetch_l2_4d(&tm_k, c * 64, it0.g, j * kBN, it0.b);
-          tma_prefetch_l2_4d(&tm_v, c * 64, it0.g, j * kBN, it0.b);
-        }
-    }
+    // The first blocks of this CTA's keys, into L2 while the kernel before this one
+    // ends (each CTA of the previous decode call lets this grid start once its block
+    // loop is done).
+    if constexpr (!PAGED) kv_prefetch_first_blocks<D>(p, &tm_k, &tm_v, kKeysPrefetchBlocks);
   }
   // A programmatic dependent launch: the previous kernel's writes are visible past
   // this point; TMEM is allocated only after it (as in the one-tile kernel).
