@@ -68,6 +68,7 @@ TRAFFIC_BY_SOURCE = {
     "19bf902c5ff94d12": 907_726_080 + 117_001_472,  # + L2 prefetch before the grid wait, early trigger
     "027137e139ce0dc7": 912_837_376 + 116_481_024,  # same kernel; a TS fp8 MMA helper in sm103_ptx.cuh
     "56b118326dd964dc": 910_098_176 + 116_838_912,  # same kernel; unused helpers removed
+    "6050973771769e54": 911_374_592 + 117_136_640,  # same kernel; launch order in the header comment
 }
 
 

@@ -42,6 +42,11 @@
 //     units, so the grid ends within about one small unit of the mean (a static deal
 //     left CTAs finishing from 7.9 to 8.6 ms on one causal L = 131072 call, the same
 //     units running up to 18 % slower on some SMs).
+//   * Launch order: a programmatic dependent launch. The prologue touches shared
+//     memory only (with the static deal the producer also asks for its first
+//     unit's tiles in L2, a hint), then griddepcontrol.wait precedes the TMEM
+//     allocation and every global access; once the producer has issued its last
+//     load, the CTA lets the next kernel on the stream start.
 //   * Every wait is bounded (globaltimer); a wait that runs out records a timeout
 //     in the status word and every role leaves its loop, so the CTA still frees
 //     its TMEM and exits.
