@@ -36,9 +36,12 @@
  * its prologue (barrier setup, tensor-map prefetch) while the previous kernel on the
  * stream finishes, and waits for that kernel's completion and memory
  * (griddepcontrol.wait) before it allocates tensor memory or touches global memory.
- * Stream order is kept for every buffer. The decode kernel of attn_fwd_kv (dense cache)
- * also asks for the first key blocks of its cache in L2 before that wait: a prefetch
- * hint, so what it computes with is still the cache as the earlier kernels left it.
+ * Stream order is kept for every buffer. The kernels of attn_fwd_kv on a dense cache,
+ * and attn_fwd's kernel when it deals its units statically (small problems), also
+ * ask for their first tiles in L2 before that wait: a prefetch hint, so what they
+ * compute with is still the memory as the earlier kernels left it. Once a kernel has
+ * issued its last loads it lets the next kernel on the stream start its prologue
+ * (except when a merge kernel of the same call follows).
  *
  * Graphs. Every entry point may be captured into a CUDA graph (stream capture): the
  * capture records the kernels with the call's pointers and sizes, so a replay
