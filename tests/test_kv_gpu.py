@@ -75,6 +75,18 @@ def test_split_merge_on_an_uninitialised_workspace():
             assert len(set(tickets.tolist())) == 1 and tickets[0] != 0, tickets
 
 
+@pytest.mark.parametrize("splits", [5, 64, 256])
+def test_in_kernel_merge_of_many_splits(splits):
+    """One-row items (Hq = Hkv, d = 64) merge up to 256 splits inside the decode kernel:
+    eight threads per column quad, 8 splits each per round trip, so 256 splits take
+    four rounds; with 313 key blocks some of the 256 splits are empty. Two batch entries
+    and two query positions per entry (two-row items) cover the other item shape."""
+    for Lq in (1, 2):
+        q, k, v = si.random_qkv_decode(2, Lq, 40000, 4, 4, 64, dtype="fp16", seed=splits + Lq)
+        compare_kv(q, k, v, "fp16", True, -1, 0.125, num_splits=splits,
+                   label=f"Lq={Lq} splits={splits}")
+
+
 def test_many_row_tiles():
     """Lq spanning several 128-row tiles (group 1: 128 queries per tile; group 4: 32)."""
     for hq, hkv in [(2, 2), (8, 2)]:
