@@ -45,3 +45,30 @@ def test_chained_calls_equal_synchronised_calls(L):
         for i, (a, b) in enumerate(zip(got, ref)):
             assert torch.equal(a, b), (L, rep, i)
     ex.sync_status()
+
+
+def test_chained_bf16_calls_through_the_copy_of_v():
+    """bf16 inputs (the fp16 copy of V written by two conversion kernels before each
+    attention kernel), d = 128 and GQA: each call's O is the next call's V."""
+    import exact_io_aware_19_gb300 as ex
+    q, k, v = si.random_qkv(1, 1536, 8, 2, 128, dtype="bf16", seed=431, device="cuda")
+
+    def chain(sync):
+        outs = []
+        vv = v
+        for _ in range(3):
+            o, lse = ex.attn_fwd(q, k, vv, causal=True)
+            outs += [o, lse]
+            if sync:
+                torch.cuda.synchronize()
+            vv = o[:, :, ::4].contiguous()  # [1, L, 2, 128]: the next call's V
+        torch.cuda.synchronize()
+        return [x.clone() for x in outs]
+
+    ref = chain(True)
+    for rep in range(3):
+        got = chain(False)
+        for i, (a, b) in enumerate(zip(got, ref)):
+            assert torch.equal(a, b), (rep, i)
+    ex.sync_status()
+
